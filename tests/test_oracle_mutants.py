@@ -1,0 +1,61 @@
+"""The pins must catch plausible mistakes in the oracle.
+
+Each mutant is a copy of the oracle's C source with one planted mistake (a sign,
+a dropped term, a wrong index, a transposed operand, an off-by-one), built with
+gcc into a temporary directory.  Every mutant must fail at least one pin.  The
+mistakes are planted only in these temporary copies, on the CPU.
+"""
+import os
+
+import pytest
+
+import oracle
+import oracle_pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "moe_oracle.c")
+
+MUTANTS = {
+    "softmax_sign": ("pt[e] = exp(l[e] - m) / s;", "pt[e] = exp(m - l[e]) / s;"),
+    "lse_drops_max": ("lse[t] = m + log(s);", "lse[t] = log(s);"),
+    "tie_to_higher_index": ("return (a->e < b->e) ? -1 : (a->e > b->e);",
+                            "return (a->e > b->e) ? -1 : (a->e < b->e);"),
+    "no_renormalise": ("gates[(size_t)t * k + s2] = pt[it[s2]] / denom;",
+                       "gates[(size_t)t * k + s2] = pt[it[s2]];"),
+    "bias_ignored": ("ord[e].key = pt[e] + (sel_bias ? (double)sel_bias[e] : 0.0);",
+                     "ord[e].key = pt[e];"),
+    "gap_wrong_index": ("ord[k - 1].key - ord[k].key", "ord[0].key - ord[k].key"),
+    "offset_dropped": ("if (offset) acc += (double)offset[e];", "(void)offset;"),
+    "capacity_floor": ("return (int64_t)ceil(", "return (int64_t)floor("),
+    "capacity_without_k": ("c * (double)k * (double)T", "c * (double)T"),
+    "capacity_off_by_one": ("kept_counts[e] < C", "kept_counts[e] <= C"),
+    "offsets_from_precap_counts": ("offsets[e + 1] = offsets[e] + kept_counts[e];",
+                                   "offsets[e + 1] = offsets[e] + counts[e];"),
+    "silu_sign": ("return z / (1.0 + exp(-z));", "return z / (1.0 + exp(z));"),
+    "gate_up_swapped": ("h[j] = silu(a) * b;", "h[j] = a * silu(b);"),
+    "w2_transposed": ("bf16_val(w2[(size_t)o * Mw + j])", "bf16_val(w2[(size_t)j * d + o])"),
+    "dropped_pairs_added": ("if (dropped[pq]) continue;", "if (0) continue;"),
+    "shared_not_added": ("for (int o = 0; o < d; ++o) yt[o] += tmp[o];",
+                         "for (int o = 0; o < d; ++o) yt[o] += 0.0 * tmp[o];"),
+    "zloss_not_squared": ("sz += lse[t] * lse[t];", "sz += lse[t];"),
+    "f_over_T": ("(double)counts[e] / ((double)k * (double)T)", "(double)counts[e] / (double)T"),
+    "balance_without_E": ("*L_bal = lambda * (double)E * sfp;", "*L_bal = lambda * sfp;"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation anchor for {name} not unique/found"
+    msrc = tmp_path / "moe_oracle_mut.c"
+    msrc.write_text(src.replace(old, new))
+    lib_path = str(tmp_path / "libmut.so")
+    oracle.build(str(msrc), lib_path)
+    lib = oracle.load(lib_path)
+    failed = []
+    for pin in oracle_pins.ALL_PINS:
+        try:
+            pin(lib)
+        except AssertionError:
+            failed.append(pin.__name__)
+    assert failed, f"mutant {name} passed every pin"
