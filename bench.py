@@ -1,0 +1,414 @@
+#!/usr/bin/env python
+"""Benchmark of the MoE layer forward on B300 (tokens/s; grouped-FFN TFLOP/s
+against the bf16 tensor roofline; memory stages against the HBM roofline).
+
+One step = one whole layer forward (router, permute, grouped SwiGLU FFN with
+shared experts, combine, losses) over one batch of seeded synthetic tokens,
+through the C ABI (moe_layer_forward).  Default workload: the Mixtral-shaped
+layer (T=4096, d=4096, E=8, k=2, M=14336, dropless).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the fp64 CPU oracle, timed on host cores
+
+Under torchrun (N > 1) every rank runs an independent replica of the workload
+(the layer shards by independent batches; there is no data-path exchange);
+rank 0 prints one JSON line with the max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer fwd tokens/s and grouped-FFN TFLOP/s (% bf16 roofline), 1×B300"
+FLUSH_BYTES = 256 << 20
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="mixtral")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--cpu-budget-s", type=float, default=15.0,
+                    help="target seconds of oracle work for the CPU baseline sample")
+    return ap.parse_args(argv)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            p = json.load(fh)
+        return {k: float(p[k]) for k in FALLBACK_PEAKS}, "measured (MEASURED_PEAKS.json)"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# --------------------------------------------------------------------------- #
+# algorithmic work                                                             #
+# --------------------------------------------------------------------------- #
+def algorithmic_work(w, R: int):
+    """FLOPs of the two grouped projections and bytes of the memory stages.
+
+    gemm_swiglu: 2 * (R * d * 2M + T * d * 2Ms)   gemm_down: 2 * (R * M * d + T * Ms * d)
+    router  bytes: x (T d 2) + W_r (E d 2) + ids/gates (T k 8)
+    scatter bytes: x read once (T d 2) + rows written (R d 2) + slot rows/drop mask (T k 5)
+                   + row->token (R 4)
+    combine bytes: rows read (R d 2) + shared rows (T d 2 if shared) + y (T d 2)
+                   + slot rows/gates (T k 8)
+    """
+    T, d, M, E, k, Ms = w.T, w.d, w.M, w.E, w.k, w.Ms
+    f1 = 2.0 * (R * d * 2 * M + T * d * 2 * Ms)
+    f2 = 2.0 * (R * M * d + T * Ms * d)
+    b_router = T * d * 2 + E * d * 2 + T * k * 8
+    b_scatter = T * d * 2 + R * d * 2 + T * k * 5 + R * 4
+    b_combine = R * d * 2 + (T * d * 2 if Ms else 0) + T * d * 2 + T * k * 8
+    return {"gemm_swiglu": f1, "gemm_down": f2}, {"router": b_router, "scatter": b_scatter,
+                                                  "combine": b_combine}
+
+
+def workload_desc(w):
+    cap = f"capacity c={w.capacity_factor}" if w.capacity_factor > 0 else "dropless"
+    sh = f", {w.n_shared} shared" if w.n_shared else ""
+    return (f"{w.name}: T={w.T} d={w.d} E={w.E} k={w.k} M={w.M}{sh}, {cap}, "
+            f"offsets={w.offsets}, sel_bias={w.sel_bias}")
+
+
+# --------------------------------------------------------------------------- #
+# clocks                                                                       #
+# --------------------------------------------------------------------------- #
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self, device_index: int, enabled: bool = True):
+        self.proc = None
+        self.enabled = enabled
+        self.idx = device_index
+        self.path = None
+
+    def __enter__(self):
+        if not self.enabled:
+            return self
+        out_dir = os.path.join(ROOT, "gpurun_out")
+        os.makedirs(out_dir, exist_ok=True)
+        self.path = os.path.join(out_dir, f"clocks_rank{self.idx}.csv")
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={CLOCK_FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.fh,
+                stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or self.path is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["not sampled"]}
+        rows = []
+        with open(self.path) as fh:
+            for line in fh:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        pw = [num(r[3]) for r in rows if num(r[3]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4)
+                          if r[5 + i].lower().startswith("active")})
+        busy = [s for s in sm if s is not None]
+        return {"sm_mhz": statistics.median(busy) if busy else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(pw) if pw else None,
+                "samples": len(rows), "reasons": reasons}
+
+
+# --------------------------------------------------------------------------- #
+# oracle timing (CPU baseline and the reference arm)                           #
+# --------------------------------------------------------------------------- #
+def _host_inputs(inp):
+    import synth
+    u = synth.to_u16
+    return dict(x=u(inp.x), wr=u(inp.wr), w1=u(inp.w1), w3=u(inp.w3), w2=u(inp.w2),
+                ws1=u(inp.ws1), ws3=u(inp.ws3), ws2=u(inp.ws2),
+                off=None if inp.offset is None else inp.offset.cpu().numpy(),
+                bias=None if inp.sel_bias is None else inp.sel_bias.cpu().numpy())
+
+
+def oracle_tokens(w, h, start: int, n: int):
+    """The oracle's full layer on tokens [start, start+n) of the workload, as a
+    batch of n tokens; returns wall seconds."""
+    import oracle
+    x = h["x"][start:start + n]
+    t0 = time.perf_counter()
+    oracle.layer_forward(x, h["wr"], h["w1"], h["w3"], h["w2"], w.k, offset=h["off"],
+                         sel_bias=h["bias"], ws1=h["ws1"], ws3=h["ws3"], ws2=h["ws2"],
+                         capacity_factor=w.capacity_factor, lam=w.balance_coef)
+    return time.perf_counter() - t0
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(w, inp, budget_s: float):
+    """Times the oracle as it stands on a bounded sample of the workload."""
+    import oracle
+    oracle.load()
+    h = _host_inputs(inp)
+    cores = cpu_cores()
+    probe_n = min(w.T, cores)
+    t_probe = oracle_tokens(w, h, 0, probe_n)             # also the warm-up
+    per_round = max(t_probe, 1e-3)
+    rounds = max(1, int(budget_s / per_round))
+    n = min(w.T, probe_n * rounds)
+    t = oracle_tokens(w, h, 0, n)
+    threads = min(cores, n)
+    return {"value": n / t, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"first {n} tokens of the workload run through the fp64 oracle layer "
+                      f"as one batch of {n} (router, dispatch, experts, combine, losses); "
+                      f"{t:.1f} s wall, OpenMP over tokens"}
+
+
+def run_reference(args, w):
+    """Reference arm: the oracle on host cores (rank 0 only)."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import synth
+    import oracle
+    oracle.load()
+    inp = synth.make_inputs(w, "cpu")
+    h = _host_inputs(inp)
+    cores = cpu_cores()
+    t1 = oracle_tokens(w, h, 0, min(w.T, cores))
+    per_tok_round = max(t1, 1e-3)
+    budget = 150.0 / max(1, args.steps + args.warmup)     # whole run within a few minutes
+    n = max(1, min(w.T, int(min(w.T, cores) * max(1.0, budget / per_tok_round))))
+    if t1 > budget:
+        n = max(1, min(cores, int(min(w.T, cores) * budget / t1)))
+    for i in range(args.warmup):
+        oracle_tokens(w, h, 0, n)
+    times = [oracle_tokens(w, h, (i * n) % max(1, w.T - n + 1), n) for i in range(args.steps)]
+    ms = 1000.0 * statistics.mean(times)
+    value = n / (ms / 1000.0)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+            "config": {"workload": workload_desc(w), "T": w.T, "d": w.d, "E": w.E, "k": w.k,
+                       "M": w.M, "n_shared": w.n_shared,
+                       "capacity_factor": w.capacity_factor,
+                       "step": f"{n} tokens through the oracle layer"},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": min(cores, n),
+                             "kind": "oracle",
+                             "sample": f"{n} tokens per step (fp64 oracle, OpenMP over tokens)"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# --------------------------------------------------------------------------- #
+# our arm                                                                      #
+# --------------------------------------------------------------------------- #
+def run_ours(args, w):
+    import torch
+    import torch.distributed as dist
+
+    import synth
+    import top_routing_expert_lb_b300 as moe
+    from top_routing_expert_lb_b300 import build as mbuild
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0:
+        mbuild.ensure_built()
+    if world > 1:
+        dist.barrier()
+
+    inp = synth.make_inputs(w, dev)
+    shape = moe.Shape.of(w.T, w.d, w.M, w.E, w.k, w.n_shared, w.capacity_factor,
+                         w.balance_coef)
+    layer = moe.MoELayer(shape, inp.wr, inp.w1, inp.w3, inp.w2, inp.ws1, inp.ws3, inp.ws2,
+                         inp.offset, inp.sel_bias, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    for _ in range(args.warmup):
+        layer.forward(inp.x)
+    torch.cuda.synchronize(dev)
+    if moe.moe_check_status(layer.ws) != 0:
+        raise RuntimeError("device wait timed out during warm-up")
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    launches0 = moe.moe_launch_count()
+    moe.moe_profile_enable(True)
+    with ClockSampler(local, enabled=not args.no_clocks) as clk:
+        for i in range(args.steps):
+            flush.zero_()                                  # evict L2 between steps
+            starts[i].record(stream)
+            layer.forward(inp.x)
+            ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+    moe.moe_profile_enable(False)
+    prof = moe.moe_profile_collect()
+    launches = moe.moe_launch_count() - launches0
+    if world > 1:
+        dist.barrier()
+    if moe.moe_check_status(layer.ws) != 0:
+        raise RuntimeError("device wait timed out during the timed steps")
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms = statistics.mean(step_ms)
+    if world > 1:
+        t = torch.tensor([ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    per_kernel = {}
+    for name, t in prof:
+        per_kernel.setdefault(name, []).append(t)
+    kern_ms = {k: statistics.mean(v) for k, v in per_kernel.items()}
+    kern_n = {k: len(v) for k, v in per_kernel.items()}
+
+    R = int(w.T * w.k - int(layer.drop_mask.sum().item())) if w.k else 0
+    flops, bytes_ = algorithmic_work(w, R)
+    peaks, peak_src = load_peaks()
+    ffn_ms = kern_ms.get("gemm_swiglu", 0.0) + kern_ms.get("gemm_down", 0.0)
+    ffn_tflops = (flops["gemm_swiglu"] + flops["gemm_down"]) / (ffn_ms * 1e-3) / 1e12
+    dom = "gemm_swiglu"
+    ach = flops[dom] / (kern_ms[dom] * 1e-3) / 1e12
+    stage_gbs = {k: bytes_[k] / (kern_ms[k] * 1e-3) / 1e9 for k in bytes_ if k in kern_ms}
+
+    # end to end: host tokens in, host output and losses out, through the C ABI
+    e2e = None
+    if not args.no_e2e:
+        x_host = inp.x.cpu().pin_memory()
+        y_host = torch.empty_like(x_host).pin_memory()
+        losses_host = torch.empty(2, dtype=torch.float32).pin_memory()
+        x_dev = torch.empty_like(inp.x)
+        y_dev = torch.empty_like(inp.x)
+        n_e2e = max(3, min(args.steps, 20))
+
+        def e2e_step():
+            moe.moe_layer_forward_host(layer.shape, x_host, x_dev, layer.w_router,
+                                       layer.logit_offset, layer.sel_bias, layer.w13, layer.w2,
+                                       layer.w13_shared, layer.w2_shared, y_dev, y_host,
+                                       losses_host, layer.ids, layer.gates, layer.counts,
+                                       layer.drop_mask, layer.f, layer.P, layer.losses[0:1],
+                                       layer.losses[1:2], layer.ws)
+        for _ in range(2):
+            e2e_step()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(n_e2e)]
+        for a, b in ev:
+            flush.zero_()
+            a.record(stream)
+            e2e_step()
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+        if world > 1:
+            t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e = {"value": world * w.T / (e2e_ms * 1e-3), "unit": "tokens/s",
+               "ms_per_step": e2e_ms, "h2d_bytes_per_step": w.T * w.d * 2,
+               "d2h_bytes_per_step": w.T * w.d * 2 + 8,
+               "path": "moe_layer_forward_host (pinned host x in, y and losses out)"}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, inp, args.cpu_budget_s)
+
+    if rank != 0:
+        return 0
+    line = {
+        "metric": METRIC, "value": world * w.T / (ms * 1e-3), "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic: seeded N(0,1) tokens, random-init N(0,0.02) weights",
+        "config": {"workload": workload_desc(w), "T": w.T, "d": w.d, "E": w.E, "k": w.k,
+                   "M": w.M, "n_shared": w.n_shared, "capacity_factor": w.capacity_factor,
+                   "rows_computed": R,
+                   "l2": f"flushed: {FLUSH_BYTES >> 20} MiB written before every timed step",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "ffn_tflops": ffn_tflops,
+        "ffn_frac_of_bf16_peak": ffn_tflops / peaks["bf16_tflops"],
+        "kernel_ms": kern_ms, "kernel_launches_timed": kern_n,
+        "stage_gbs": stage_gbs,
+        "stage_frac_of_hbm": {k: v / peaks["hbm_gbs"] for k, v in stage_gbs.items()},
+        "roofline": {"bound": "tensor", "kernel": dom, "achieved": ach,
+                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": ach / peaks["bf16_tflops"], "traffic": None,
+                     "peak_source": f"bf16_tflops burst, {peak_src}",
+                     "frac_of_sustained": ach / peaks["bf16_tflops_sustained"],
+                     "algorithmic_flops_per_launch": flops[dom]},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    import synth
+    w = synth.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,225 @@
+/*
+ * moe.h - C ABI of libmoe_b300.so: the forward pass of one top-k routed
+ * Mixture-of-Experts FFN layer on one NVIDIA B300 (sm_103a).
+ *
+ * The layer ("MoE：条件计算与路由", llm-knowledge-atlas notes 04-04, core formula
+ * and §7 Eqs.(1)-(3)):
+ *
+ *     y(x) = sum_{e in S(x)} g~_e(x) E_e(x)  +  Ys(x)
+ *     p    = softmax(W_r x + o)              router, max-subtracted softmax
+ *     S    = TopK_e(p_e + b_e, k)            b_e: optional ALF-LB selection bias
+ *     g~_e = p_e / sum_{j in S} p_j          renormalised gates (unbiased p)
+ *     E_e(x) = W2_e (SiLU(W1_e x) * W3_e x)  SwiGLU expert ("深入理解 MoE" §10.2)
+ *     Ys   = shared experts, width n_shared*M, gate 1 (CSDN note, DeepseekV3MoE)
+ *
+ * with optional capacity C = ceil(c k T / E) ("MoE：条件计算与路由" §3), pairs
+ * beyond C per expert dropped in token-major (t, slot) order, and the side
+ * outputs f_e, P_e, L_bal = lambda E sum_e f_e P_e and the z-loss
+ * L_z = (1/T) sum_t (log sum_e exp l_te)^2 ("MOE大模型对比篇" §2.1, §2.2).
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers owned by the caller, unless a
+ *     parameter says "host".  The library never allocates device memory; the
+ *     scratch it needs is the caller's workspace (moe_workspace_size).
+ *   - bf16 tensors are passed as uint16_t bit patterns.  Layouts are
+ *     row-major; weights are [out][in] (nn.Linear layout, K-major).
+ *   - Every call enqueues work on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream) and returns without synchronising, except where stated.
+ *   - Every device pointer must be 16-byte aligned; the workspace 256-byte.
+ *   - Return value: MOE_OK or a negative MOE_ERR_* code.  Arguments are checked
+ *     on the host before anything is enqueued; on an error nothing is
+ *     enqueued.  MOE_ERR_CUDA reports a failed launch.  Device-side waits are
+ *     bounded; a wait that runs out records MOE_ERR_TIMEOUT in the workspace,
+ *     read back by moe_check_status.
+ *   - Determinism: for fixed inputs every output is bitwise reproducible (all
+ *     reductions run in a fixed order; no floating-point atomics).
+ */
+#ifndef MOE_B300_H
+#define MOE_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_OK 0
+#define MOE_ERR_INVALID_ARG (-1)  /* null/misaligned pointer, bad size, k > E ...  */
+#define MOE_ERR_UNSUPPORTED (-2)  /* shape outside the supported limits below       */
+#define MOE_ERR_CUDA (-3)         /* a CUDA runtime/driver call failed              */
+#define MOE_ERR_TIMEOUT (-4)      /* a bounded device wait ran out                  */
+#define MOE_ERR_WORKSPACE (-5)    /* workspace smaller than moe_workspace_size      */
+
+/* Supported limits (MOE_ERR_UNSUPPORTED outside them):
+ *   1 <= E <= 256;  0 <= k <= min(E, 8);  0 <= T <= 2^24;  d % 64 == 0,
+ *   64 <= d <= 16384;  M % 128 == 0, 128 <= M <= 32768;  0 <= n_shared <= 8.  */
+#define MOE_MAX_EXPERTS 256
+#define MOE_MAX_TOPK 8
+
+/* Layer shape.
+ *   T  tokens;  d  model width;  M  expert intermediate width;
+ *   E  routed experts;  k  experts per token;  n_shared  shared experts,
+ *      fused into one SwiGLU MLP of width Ms = n_shared * M;
+ *   capacity_factor  c; <= 0 means dropless, otherwise C = ceil(c*k*T/E)
+ *      evaluated in double precision;
+ *   balance_coef  lambda of the balance loss (0.01 is customary);
+ *   flags  must be 0 (reserved for routing variants).                          */
+typedef struct moe_shape {
+    int32_t T, d, M, E, k, n_shared;
+    float capacity_factor;
+    float balance_coef;
+    uint32_t flags;
+} moe_shape_t;
+
+/* Error text for a MOE_* code (static string, never NULL). */
+const char *moe_error_string(int code);
+
+/* Bytes of device workspace every other entry point needs for this shape
+ * (written to *bytes, a host pointer).  Pure host computation.               */
+int moe_workspace_size(const moe_shape_t *shape, size_t *bytes);
+
+/* Expert capacity C (host pointer *C): ceil(c*k*T/E), or -1 when dropless.  */
+int moe_capacity(const moe_shape_t *shape, int64_t *C);
+
+/* Upper bound R_max on routed rows: T*k dropless, else min(T*k, E*C).        */
+int moe_max_rows(const moe_shape_t *shape, int64_t *rows);
+
+/* Pack canonical SwiGLU gate/up weights for the grouped GEMM.
+ *   w1, w3  [G][Mw][d] bf16 (gate = W1, up = W3; G groups of width Mw)
+ *   w13     [G][2*Mw][d] bf16 output: within each group, row block
+ *           [256 j, 256 j + 128) holds W1 rows [128 j, 128 j + 128) and
+ *           [256 j + 128, 256 j + 256) holds W3 rows [128 j, 128 j + 128),
+ *           so one 256-row tile of w13 yields 128 columns of h.
+ * Mw % 128 == 0, d % 64 == 0.  One-time preparation, not part of the layer.  */
+int moe_pack_w13(int32_t G, int32_t Mw, int32_t d, const uint16_t *w1, const uint16_t *w3,
+                 uint16_t *w13, void *stream);
+
+/* Router ("MoE：条件计算与路由" router and ALF-LB; §7 Eqs.(1)-(2); z-loss
+ * "MOE大模型对比篇" §2.2).
+ *   x           [T][d] bf16 tokens
+ *   w_router    [E][d] bf16 router projection W_r
+ *   logit_offset [E] fp32 or NULL: added to every token's logits (router bias)
+ *   sel_bias    [E] fp32 or NULL: ALF-LB bias b_e, added to the softmax
+ *               probabilities for selection only
+ * Outputs (device):
+ *   ids    [T][k] int32  selected experts, descending key p_e + b_e; equal keys
+ *                        go to the lower expert index
+ *   gates  [T][k] fp32   p_e / sum_{j in S} p_j (unbiased p)
+ *   counts [E]    int32  n_e, pairs routed to e (before any capacity cut)
+ *   f, P   [E]    fp32   n_e / (k T) and (1/T) sum_t p_e(t)
+ *   bal_loss, z_loss [1] fp32  lambda E sum f P  and  (1/T) sum_t lse_t^2
+ * Logits are accumulated in fp32 from bf16 products; softmax in fp32.        */
+int moe_route(const moe_shape_t *shape, const uint16_t *x, const uint16_t *w_router,
+              const float *logit_offset, const float *sel_bias, int32_t *ids, float *gates,
+              int32_t *counts, float *f, float *P, float *bal_loss, float *z_loss, void *ws,
+              size_t ws_bytes, void *stream);
+
+/* Dispatch: capacity cut and permutation into expert-contiguous rows (CSDN
+ * note, moe_infer's histogram + argsort; capacity "MoE：条件计算与路由" §3).
+ *   x    [T][d] bf16;  ids [T][k] int32 (each in [0, E))
+ * Outputs (device):
+ *   offsets   [E+1] int32  offsets[e] = first row of expert e; offsets[E] = R
+ *   slot_row  [T][k] int32 row of pair (t,s) in x_perm, or -1 if dropped
+ *   row_token [R_max] int32 token of each row (entries >= R untouched)
+ *   drop_mask [T][k] uint8 1 where the pair was dropped
+ *   x_perm    [R_max][d] bf16, row r = x[row_token[r]]
+ * Rows of one expert are ordered by (t, s) ascending; a pair is kept iff
+ * fewer than C earlier pairs (token-major) went to its expert.  Bit-exact and
+ * deterministic.  Ids outside [0, E) are undefined behaviour.                */
+int moe_permute(const moe_shape_t *shape, const uint16_t *x, const int32_t *ids,
+                int32_t *offsets, int32_t *slot_row, int32_t *row_token, uint8_t *drop_mask,
+                uint16_t *x_perm, void *ws, size_t ws_bytes, void *stream);
+
+/* Grouped SwiGLU expert FFNs plus the shared experts ("深入理解 MoE" §10.2;
+ * CSDN note, DeepseekV3MoE experts loop and shared_experts).
+ *   x_perm   [R_max][d] bf16 rows, expert e owning [offsets[e], offsets[e+1])
+ *   offsets  [E+1] int32 (device), non-decreasing, offsets[E] <= R_max
+ *   w13      [E][2M][d] bf16, packed by moe_pack_w13 (G = E, Mw = M)
+ *   w2       [E][d][M] bf16
+ *   y_perm   [R_max][d] bf16 output, row r = E_e(x_perm[r])
+ *   x        [T][d] bf16 tokens (read only when n_shared > 0)
+ *   w13_shared [2Ms][d] bf16 packed (G = 1, Mw = Ms), w2_shared [d][Ms] bf16,
+ *   y_shared [T][d] bf16 output Ys(x); all three NULL when n_shared == 0
+ * bf16 tensor-core products accumulated in fp32; h = SiLU(g) * u rounded to
+ * bf16 between the two projections; outputs rounded to bf16.                 */
+int moe_grouped_ffn(const moe_shape_t *shape, const uint16_t *x_perm, const int32_t *offsets,
+                    const uint16_t *w13, const uint16_t *w2, uint16_t *y_perm,
+                    const uint16_t *x, const uint16_t *w13_shared, const uint16_t *w2_shared,
+                    uint16_t *y_shared, void *ws, size_t ws_bytes, void *stream);
+
+/* Combine ("MoE：条件计算与路由" §7 Eq.(3); CSDN note, moe_infer's un-permute
+ * and weighted sum):  y[t] = sum_{s: slot_row[t][s] >= 0} gates[t][s] *
+ * y_perm[slot_row[t][s]] + y_shared[t], accumulated in fp32 in slot order,
+ * stored as bf16.  Dropped pairs add nothing; gates are not renormalised.
+ *   y_perm [R_max][d] bf16; slot_row [T][k] int32; gates [T][k] fp32;
+ *   y_shared [T][d] bf16 or NULL; y [T][d] bf16 output.                        */
+int moe_combine(const moe_shape_t *shape, const uint16_t *y_perm, const int32_t *slot_row,
+                const float *gates, const uint16_t *y_shared, uint16_t *y, void *stream);
+
+/* The whole layer: route -> permute -> grouped FFN (+ shared) -> combine, all
+ * on `stream`, no host synchronisation.  Arguments as in the calls above;
+ * w13_shared / w2_shared are NULL when n_shared == 0.  Outputs: y [T][d] bf16,
+ * ids, gates, counts, drop_mask [T][k] uint8, f, P, bal_loss, z_loss.
+ * Intermediate rows live in the workspace.                                   */
+int moe_layer_forward(const moe_shape_t *shape, const uint16_t *x, const uint16_t *w_router,
+                      const float *logit_offset, const float *sel_bias, const uint16_t *w13,
+                      const uint16_t *w2, const uint16_t *w13_shared, const uint16_t *w2_shared,
+                      uint16_t *y, int32_t *ids, float *gates, int32_t *counts,
+                      uint8_t *drop_mask, float *f, float *P, float *bal_loss, float *z_loss,
+                      void *ws, size_t ws_bytes, void *stream);
+
+/* Same layer with HOST token input and HOST outputs: copies x_host (pinned or
+ * pageable, [T][d] bf16) to x_dev, runs moe_layer_forward, copies y back to
+ * y_host and the two losses to losses_host[0..1] (bal, z), then synchronises
+ * `stream`.  x_dev / y_dev are caller device buffers of [T][d] bf16; the
+ * remaining device outputs are as in moe_layer_forward.                      */
+int moe_layer_forward_host(const moe_shape_t *shape, const uint16_t *x_host, uint16_t *x_dev,
+                           const uint16_t *w_router, const float *logit_offset,
+                           const float *sel_bias, const uint16_t *w13, const uint16_t *w2,
+                           const uint16_t *w13_shared, const uint16_t *w2_shared,
+                           uint16_t *y_dev, uint16_t *y_host, float *losses_host,
+                           int32_t *ids, float *gates, int32_t *counts, uint8_t *drop_mask,
+                           float *f, float *P, float *bal_loss, float *z_loss, void *ws,
+                           size_t ws_bytes, void *stream);
+
+/* Reads (and clears) the device status word kept in the workspace; writes
+ * MOE_OK or MOE_ERR_TIMEOUT to *status (host).  Synchronises `stream`.        */
+int moe_check_status(void *ws, int *status, void *stream);
+
+/* Wait limit, in nanoseconds, for every bounded device wait launched after
+ * this call (default 2e9).  Process-wide.                                    */
+int moe_set_wait_timeout_ns(uint64_t ns);
+
+/* Launches one CTA that waits on a barrier nothing ever signals, bounded by
+ * the current wait limit; it records MOE_ERR_TIMEOUT in the workspace status
+ * word and returns.  Exercises the timeout path without faulting anything.   */
+int moe_debug_timeout_probe(void *ws, size_t ws_bytes, void *stream);
+
+/* Kernel accounting for benchmarks (host-side, process-wide, not thread-safe).
+ * Kernel ids reported by moe_profile_collect: */
+#define MOE_KERNEL_ROUTER 1       /* router logits + softmax + Top-k            */
+#define MOE_KERNEL_FINALIZE 2     /* partial reductions, losses, scan           */
+#define MOE_KERNEL_TILE_HIST 3    /* per-tile expert histogram (moe_permute)    */
+#define MOE_KERNEL_SCATTER 4      /* capacity cut, permutation, row gather      */
+#define MOE_KERNEL_GEMM_SWIGLU 5  /* grouped gate/up projection + SwiGLU        */
+#define MOE_KERNEL_GEMM_DOWN 6    /* grouped down projection                    */
+#define MOE_KERNEL_COMBINE 7      /* gate-weighted un-permute + shared output   */
+#define MOE_KERNEL_OTHER 8        /* packing, probes                            */
+
+/* on != 0: every subsequent kernel launch is bracketed by two CUDA events on
+ * its stream; on == 0 stops recording.  Recording continues until collected. */
+int moe_profile_enable(int on);
+
+/* Waits for the recorded events and returns, in launch order, up to `cap`
+ * (kernel id, duration in ms) pairs (host arrays); *n receives the count.
+ * Clears the record.                                                          */
+int moe_profile_collect(int cap, int *n, int32_t *kernel_ids, float *ms);
+
+/* Number of kernels this library has launched in this process (host *n).   */
+int moe_launch_count(uint64_t *n);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_B300_H */

@@ -30,11 +30,23 @@ def build(src: str = _SRC, out: str = _LIB, extra_flags=()) -> str:
     cmd = ["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c99", *extra_flags,
            src, "-o", out, "-lm"]
     subprocess.run(cmd, check=True)
+    if out == _LIB:
+        with open(_LIB + ".srchash", "w") as fh:
+            fh.write(_src_hash() + "\n")
     return out
 
 
+def _src_hash() -> str:
+    import hashlib
+    with open(_SRC, "rb") as fh:
+        return hashlib.sha256(fh.read()).hexdigest()
+
+
 def _needs_build() -> bool:
-    return (not os.path.exists(_LIB)) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC)
+    if not os.path.exists(_LIB) or not os.path.exists(_LIB + ".srchash"):
+        return True
+    with open(_LIB + ".srchash") as fh:
+        return fh.read().strip() != _src_hash()
 
 
 _P = ctypes.c_void_p
@@ -60,6 +72,7 @@ def load(path: Optional[str] = None):
     lib.oracle_expert_rows.argtypes = [i32, i32, i32, _P, _P, _P, _P, _P, _P]
     lib.oracle_layer_tokens.argtypes = [i32] * 6 + [_P] * 10 + [i32, _P, _P]
     lib.oracle_losses.argtypes = [i32, i32, i32, _P, _P, _P, f64, _P, _P, _P, _P]
+    lib.oracle_combine.argtypes = [i32, i32, i32, _P, _P, _P, _P, _P]
     if path == _LIB:
         _lib = lib
     return lib
@@ -189,6 +202,20 @@ def layer_tokens(x, routing_ids, gates, dropped, w1, w3, w2, ws1=None, ws3=None,
     lib.oracle_layer_tokens(T, d, M, E, k, Ms, _ptr(x), _ptr(ids), _ptr(g), _ptr(dr),
                             _ptr(w1), _ptr(w3), _ptr(w2), _ptr(ws1), _ptr(ws3), _ptr(ws2),
                             len(sel), _ptr(sel), _ptr(y))
+    return y
+
+
+def combine(y_perm, slot_row, gates, y_shared=None, lib=None) -> np.ndarray:
+    """y[t] = sum over kept slots of gates * y_perm[slot_row] (+ y_shared[t])."""
+    lib = lib or load()
+    y_perm = _u16(y_perm)
+    slot_row = np.ascontiguousarray(slot_row, np.int32)
+    T, k = slot_row.shape
+    d = y_perm.shape[1]
+    g = np.ascontiguousarray(gates, np.float64)
+    ys = None if y_shared is None else _u16(y_shared)
+    y = np.empty((T, d), np.float64)
+    lib.oracle_combine(T, d, k, _ptr(y_perm), _ptr(slot_row), _ptr(g), _ptr(ys), _ptr(y))
     return y
 
 

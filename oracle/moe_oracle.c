@@ -314,3 +314,29 @@ void oracle_losses(int T, int E, int k, const int32_t *counts, const double *p,
     *L_bal = lambda * (double)E * sfp;
     *L_z = (T > 0) ? sz / (double)T : 0.0;
 }
+
+/* ------------------------------------------------------------------------- */
+/* Combine alone, from expert-order rows   ([KA] §7 Eq.(3); [CS] moe_infer's  */
+/* un-permute new_x[idxs] = outs, then the fp32 gate-weighted sum over k, and */
+/* DeepseekV3MoE's y + shared_experts(identity)):                             */
+/*   y[t] = sum_{s: slot_row[t][s] >= 0} gates[t][s] * y_perm[slot_row[t][s]] */
+/*          + y_shared[t]                                                     */
+/* y_perm: [R][d] bf16, y_shared: [T][d] bf16 or NULL.                         */
+/* ------------------------------------------------------------------------- */
+void oracle_combine(int T, int d, int k, const uint16_t *y_perm, const int32_t *slot_row,
+                    const double *gates, const uint16_t *y_shared, double *y)
+{
+#pragma omp parallel for schedule(static)
+    for (int t = 0; t < T; ++t) {
+        double *yt = y + (size_t)t * d;
+        for (int o = 0; o < d; ++o) yt[o] = 0.0;
+        for (int s = 0; s < k; ++s) {
+            int r = slot_row[(size_t)t * k + s];
+            if (r < 0) continue;
+            double g = gates[(size_t)t * k + s];
+            for (int o = 0; o < d; ++o) yt[o] += g * bf16_val(y_perm[(size_t)r * d + o]);
+        }
+        if (y_shared)
+            for (int o = 0; o < d; ++o) yt[o] += bf16_val(y_shared[(size_t)t * d + o]);
+    }
+}

@@ -328,6 +328,43 @@ def pin_gap_and_force(lib):
     _close(f.gates[0], [pe[0] / (pe[0] + pe[1]), pe[1] / (pe[0] + pe[1])], 1e-15, "forced")
 
 
-ALL_PINS = [pin_hand_routing, pin_hand_capacity, pin_hand_shared_k0, pin_two_gating_formulas,
+def pin_combine(lib):
+    """The standalone combine against the layer's own composition and a
+    hand-sized case: a dropped slot adds nothing, gates are not renormalised."""
+    yp = bf16_bits(np.array([[1.0, 2.0], [3.0, -4.0], [0.5, 0.25]]))
+    sr = np.array([[0, 1], [2, -1]], np.int32)
+    g = np.array([[0.75, 0.25], [0.5, 0.5]])
+    ys = bf16_bits(np.array([[10.0, 20.0], [30.0, 40.0]]))
+    y = oracle.combine(yp, sr, g, ys, lib=lib)
+    _close(y, [[0.75 * 1 + 0.25 * 3 + 10, 0.75 * 2 - 0.25 * 4 + 20], [0.25 + 30, 0.125 + 40]],
+           1e-15, "combine")
+    # the layer's y equals combine over the oracle's own expert rows
+    rng = np.random.default_rng(13)
+    T, d, E, k, M = 30, 8, 5, 2, 4
+    x, wr, w1, w3, w2, _ = rand_problem(rng, T, d, E, k, M)
+    res = oracle.layer_forward(x, wr, w1, w3, w2, k, capacity_factor=0.6, lib=lib)
+    R = len(res.disp.row_token)
+    exp_rows = np.zeros((R, d))
+    for t in range(T):
+        for s in range(k):
+            r = res.disp.slot_row[t, s]
+            if r >= 0:
+                e = res.routing.ids[t, s]
+                exp_rows[r] = np_swiglu(bf16_val(x[t:t + 1]), bf16_val(w1[e]), bf16_val(w3[e]),
+                                        bf16_val(w2[e]))[0]
+    # combine on exactly-representable rows: compare the two paths on bf16 rows
+    rows_b = bf16_bits(exp_rows)
+    yc = oracle.combine(rows_b, res.disp.slot_row, res.routing.gates, lib=lib)
+    want = np.zeros((T, d))
+    for t in range(T):
+        for s in range(k):
+            r = res.disp.slot_row[t, s]
+            if r >= 0:
+                want[t] += res.routing.gates[t, s] * bf16_val(rows_b[r])
+    _close(yc, want, 1e-12, "combine vs explicit sum")
+    _close(yc, res.y, 2e-2 * np.abs(res.y).max(), "combine vs layer")
+
+
+ALL_PINS = [pin_combine, pin_hand_routing, pin_hand_capacity, pin_hand_shared_k0, pin_two_gating_formulas,
             pin_bruteforce_subsets, pin_dispatch_argsort, pin_capacity_formula, pin_invariants,
             pin_determinism, pin_gap_and_force]

@@ -1,0 +1,177 @@
+"""Shared helpers of the GPU parity tests: run the CUDA layer through the C ABI,
+run the oracle on the same seeded inputs, compare with the stated tolerances.
+
+Tolerances (fixed by the benchmark spec of the layer and restated here):
+  * expert ids, counts, drop masks, offsets, permutation: bit-exact, except
+    tokens whose k-th and (k+1)-th selection keys differ by less than 1e-5
+    ("near ties"), whose choice may differ between fp32 and fp64; for those the
+    oracle is re-run with the GPU's choice forced, after checking that the
+    oracle's own gap really is below the threshold (so both choices are valid);
+  * layer output y: relative Frobenius error <= 1e-2 and
+    max |y - ref| <= 3e-2 * max |ref|;
+  * balance loss, z-loss and P: 1e-4 relative; f exact up to fp32 rounding;
+  * gates (fp32 softmax / renormalisation): 1e-5 absolute.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+from typing import Optional
+
+import numpy as np
+import torch
+
+import oracle
+import synth
+import top_routing_expert_lb_b300 as moe
+
+TIE = 1e-5
+Y_REL_FRO = 1e-2
+Y_MAX_ABS = 3e-2
+LOSS_REL = 1e-4
+GATE_ABS = 1e-5
+
+
+def shape_of(w: synth.Workload) -> moe.Shape:
+    return moe.Shape.of(w.T, w.d, w.M, w.E, w.k, w.n_shared, w.capacity_factor,
+                        w.balance_coef)
+
+
+def np_of(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    t = t.detach().cpu()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16)
+    return t.numpy()
+
+
+def bf16_to_f64(t: torch.Tensor) -> np.ndarray:
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+@dataclass
+class GpuOut:
+    y: torch.Tensor
+    ids: np.ndarray
+    gates: np.ndarray
+    counts: np.ndarray
+    drop: np.ndarray
+    f: np.ndarray
+    P: np.ndarray
+    bal: float
+    z: float
+
+
+def run_layer(inp: synth.Inputs, layer: Optional[moe.MoELayer] = None) -> GpuOut:
+    w = inp.w
+    if layer is None:
+        layer = moe.MoELayer(shape_of(w), inp.wr, inp.w1, inp.w3, inp.w2, inp.ws1, inp.ws3,
+                             inp.ws2, inp.offset, inp.sel_bias, device=inp.x.device)
+    layer.forward(inp.x)
+    torch.cuda.synchronize()
+    assert moe.moe_check_status(layer.ws) == 0
+    return GpuOut(layer.y.clone(), np_of(layer.ids), np_of(layer.gates), np_of(layer.counts),
+                  np_of(layer.drop_mask), np_of(layer.f), np_of(layer.P),
+                  float(layer.losses[0]), float(layer.losses[1]))
+
+
+@dataclass
+class OracleRef:
+    routing: oracle.Routing
+    disp: oracle.Dispatch
+    loss: oracle.Losses
+    exempt: np.ndarray
+    C: int
+
+
+def oracle_routing(inp: synth.Inputs, gpu_ids: np.ndarray) -> OracleRef:
+    """Oracle routing / dispatch / losses for all tokens; near-tie tokens take
+    the GPU's ids after the non-tie tokens were checked bit-exactly."""
+    w = inp.w
+    x, wr = np_of(inp.x), np_of(inp.wr)
+    off = np_of(inp.offset)
+    bias = np_of(inp.sel_bias)
+    logits = oracle.router_logits(x, wr, off)
+    free = oracle.route(logits, w.k, bias)
+    exempt = free.gap < TIE
+    if w.k > 0:
+        bad = np.nonzero(np.any(free.ids != gpu_ids, axis=1) & ~exempt)[0]
+        assert len(bad) == 0, (f"{len(bad)} non-tie tokens routed differently, e.g. token "
+                               f"{bad[0]}: gpu {gpu_ids[bad[0]]} oracle {free.ids[bad[0]]} "
+                               f"gap {free.gap[bad[0]]}")
+        r = oracle.route(logits, w.k, bias, force_ids=gpu_ids, force_mask=exempt)
+    else:
+        r = free
+    C = oracle.capacity(float(np.float32(w.capacity_factor)), w.k, w.T, w.E)
+    disp = oracle.dispatch(r.ids, w.E, C)
+    ls = oracle.losses(disp.counts, r.p, r.lse, w.k, float(np.float32(w.balance_coef)))
+    return OracleRef(r, disp, ls, exempt, C)
+
+
+def oracle_y(inp: synth.Inputs, ref: OracleRef, sel: np.ndarray) -> np.ndarray:
+    """Oracle layer output for the tokens in ``sel``, copying to the host only
+    the expert weights those tokens use."""
+    w = inp.w
+    sel = np.asarray(sel, np.int32)
+    x = np_of(inp.x)
+    ids = ref.routing.ids[sel]
+    used = sorted(set(ids.reshape(-1).tolist())) if w.k > 0 else []
+    remap = {e: i for i, e in enumerate(used)}
+    if used:
+        idx = torch.tensor(used, device=inp.w1.device)
+        w1 = np_of(inp.w1.index_select(0, idx))
+        w3 = np_of(inp.w3.index_select(0, idx))
+        w2 = np_of(inp.w2.index_select(0, idx))
+        ids_c = np.vectorize(remap.get)(ids).astype(np.int32).reshape(ids.shape)
+    else:
+        w1 = w3 = np.zeros((1, w.M, w.d), np.uint16)
+        w2 = np.zeros((1, w.d, w.M), np.uint16)
+        ids_c = np.zeros((len(sel), w.k), np.int32)
+    xs = x[sel]
+    loc = np.arange(len(sel), dtype=np.int32)
+    return oracle.layer_tokens(xs, ids_c, ref.routing.gates[sel], ref.disp.dropped[sel], w1, w3,
+                               w2, np_of(inp.ws1), np_of(inp.ws3), np_of(inp.ws2), loc)
+
+
+def assert_y_close(y_gpu: np.ndarray, y_ref: np.ndarray, what="y"):
+    y_gpu = np.asarray(y_gpu, np.float64)
+    assert y_gpu.shape == y_ref.shape
+    den = np.linalg.norm(y_ref)
+    num = np.linalg.norm(y_gpu - y_ref)
+    mx = np.abs(y_ref).max() if y_ref.size else 0.0
+    if den == 0.0:
+        assert num == 0.0, f"{what}: expected exact zeros, got |y| = {num}"
+        return
+    assert num <= Y_REL_FRO * den, f"{what}: rel Frobenius {num / den:.3e} > {Y_REL_FRO}"
+    err = np.abs(y_gpu - y_ref).max()
+    assert err <= Y_MAX_ABS * mx, f"{what}: max abs {err:.3e} > {Y_MAX_ABS} * {mx:.3e}"
+
+
+def rel_close(a: float, b: float, tol: float, what: str):
+    scale = max(abs(b), 1e-30)
+    assert abs(a - b) <= tol * scale, f"{what}: {a} vs {b} (rel {abs(a - b) / scale:.2e})"
+
+
+def assert_routing_parity(g: GpuOut, ref: OracleRef, w: synth.Workload):
+    if w.k > 0:
+        np.testing.assert_array_equal(g.ids, ref.routing.ids)
+        assert np.abs(g.gates - ref.routing.gates).max() <= GATE_ABS
+    np.testing.assert_array_equal(g.counts, ref.disp.counts)
+    np.testing.assert_array_equal(g.drop.astype(np.uint8), ref.disp.dropped)
+    np.testing.assert_allclose(g.f, ref.loss.f, rtol=1e-6, atol=0)
+    np.testing.assert_allclose(g.P, ref.loss.P, rtol=LOSS_REL, atol=1e-7)
+    rel_close(g.bal, ref.loss.L_bal, LOSS_REL, "balance loss")
+    rel_close(g.z, ref.loss.L_z, LOSS_REL, "z-loss")
+
+
+def check_layer(inp: synth.Inputs, sel: Optional[np.ndarray] = None, layer=None):
+    """Runs the GPU layer and checks it against the oracle.  Returns (gpu, ref)."""
+    g = run_layer(inp, layer)
+    ref = oracle_routing(inp, g.ids)
+    assert_routing_parity(g, ref, inp.w)
+    if sel is None:
+        sel = np.arange(inp.w.T)
+    if len(sel):
+        y_ref = oracle_y(inp, ref, sel)
+        assert_y_close(bf16_to_f64(g.y)[sel], y_ref)
+    return g, ref

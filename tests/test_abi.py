@@ -1,0 +1,132 @@
+"""The C-ABI library builds, loads and exports every declared entry point; host
+argument checks and host-side size logic behave as documented.  No compute
+call is made (CPU only)."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+from top_routing_expert_lb_b300 import _binding as B
+from top_routing_expert_lb_b300 import build as mbuild
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "moe.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    mbuild.ensure_built()
+    return B.lib()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("moe_route", "moe_permute", "moe_grouped_ffn", "moe_combine", "moe_layer_forward",
+              "moe_workspace_size", "moe_pack_w13"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_error_strings(lib):
+    for code in (0, -1, -2, -3, -4, -5):
+        assert B.moe_error_string(code)
+    assert B.moe_error_string(-99) == "unknown error"
+
+
+def shape(**kw):
+    base = dict(T=64, d=64, M=128, E=8, k=2, n_shared=0, capacity_factor=0.0,
+                balance_coef=0.01, flags=0)
+    base.update(kw)
+    return B.Shape.of(**base)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(k=9, E=8), B.MOE_ERR_INVALID_ARG),         # k > E
+    (dict(k=-1), B.MOE_ERR_INVALID_ARG),
+    (dict(T=-1), B.MOE_ERR_INVALID_ARG),
+    (dict(d=100), B.MOE_ERR_UNSUPPORTED),            # d % 64
+    (dict(d=0), B.MOE_ERR_INVALID_ARG),
+    (dict(M=200), B.MOE_ERR_UNSUPPORTED),            # M % 128
+    (dict(E=300, k=2), B.MOE_ERR_UNSUPPORTED),
+    (dict(E=16, k=9), B.MOE_ERR_UNSUPPORTED),        # k > 8
+    (dict(flags=1), B.MOE_ERR_UNSUPPORTED),
+    (dict(n_shared=9), B.MOE_ERR_UNSUPPORTED),
+    (dict(capacity_factor=float("nan")), B.MOE_ERR_INVALID_ARG),
+])
+def test_shape_validation(lib, kw, code):
+    s = shape(**kw)
+    v = ctypes.c_size_t()
+    assert lib.moe_workspace_size(ctypes.byref(s), ctypes.byref(v)) == code
+
+
+def test_workspace_and_pointer_checks(lib):
+    s = shape()
+    need = B.moe_workspace_size(s)
+    assert need > 0
+    buf = (ctypes.c_uint8 * (need + 512))()
+    base = (ctypes.addressof(buf) + 255) // 256 * 256
+    fake = ctypes.c_void_p(base)                      # never dereferenced: checks fail first
+    outs = [fake] * 9
+    # no workspace
+    assert lib.moe_route(ctypes.byref(s), fake, fake, None, None, *outs[:7], None, need,
+                         None) == B.MOE_ERR_INVALID_ARG
+    # workspace too small
+    assert lib.moe_route(ctypes.byref(s), fake, fake, None, None, *outs[:7], fake, need - 1,
+                         None) == B.MOE_ERR_WORKSPACE
+    # misaligned workspace
+    assert lib.moe_route(ctypes.byref(s), fake, fake, None, None, *outs[:7],
+                         ctypes.c_void_p(base + 8), need, None) == B.MOE_ERR_INVALID_ARG
+    # misaligned token pointer
+    assert lib.moe_route(ctypes.byref(s), ctypes.c_void_p(base + 2), fake, None, None,
+                         *outs[:7], fake, need, None) == B.MOE_ERR_INVALID_ARG
+    # missing outputs of the layer
+    assert lib.moe_layer_forward(ctypes.byref(s), fake, fake, None, None, fake, fake, None, None,
+                                 fake, fake, fake, None, fake, fake, fake, fake, fake, fake,
+                                 need, None) == B.MOE_ERR_INVALID_ARG
+    # shared experts requested without their weights
+    s2 = shape(n_shared=1)
+    need2 = B.moe_workspace_size(s2)
+    buf2 = (ctypes.c_uint8 * (need2 + 512))()
+    base2 = ctypes.c_void_p((ctypes.addressof(buf2) + 255) // 256 * 256)
+    assert lib.moe_grouped_ffn(ctypes.byref(s2), base2, base2, base2, base2, base2, base2, None,
+                               None, base2, base2, need2, None) == B.MOE_ERR_INVALID_ARG
+    assert lib.moe_pack_w13(1, 100, 64, fake, fake, fake, None) == B.MOE_ERR_UNSUPPORTED
+    assert lib.moe_set_wait_timeout_ns(0) == B.MOE_ERR_INVALID_ARG
+
+
+def test_capacity_matches_oracle(lib):
+    rng = np.random.default_rng(0)
+    cases = [(1.25, 1, 32768, 128), (0.5, 2, 2, 4), (1.0, 1, 3, 2), (0.0, 2, 10, 4),
+             (2.0, 6, 8192, 160)]
+    for _ in range(200):
+        cases.append((float(np.float32(rng.uniform(0.1, 3.0))), int(rng.integers(1, 9)),
+                      int(rng.integers(1, 70000)), int(rng.integers(8, 257))))
+    for c, k, T, E in cases:
+        k = min(k, E)
+        s = shape(T=T, E=E, k=k, capacity_factor=c)
+        c32 = float(np.float32(c))
+        assert B.moe_capacity(s) == oracle.capacity(c32, k, T, E), (c, k, T, E)
+        C = oracle.capacity(c32, k, T, E)
+        assert B.moe_max_rows(s) == (T * k if C < 0 else min(T * k, E * C))
+
+
+def test_workspace_grows_with_shape(lib):
+    a = B.moe_workspace_size(shape(T=4096, d=4096, M=14336, E=8, k=2))
+    b = B.moe_workspace_size(shape(T=4096, d=4096, M=14336, E=8, k=2, capacity_factor=0.5))
+    assert b < a
+    # intermediate rows: x_perm, h, y_perm for 8192 rows at least
+    assert a >= 8192 * (4096 * 2 * 2 + 14336 * 2)

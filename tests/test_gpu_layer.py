@@ -1,0 +1,139 @@
+"""GPU parity of the whole layer (moe_layer_forward through the C ABI) against
+the oracle, on seeded inputs: small cases that span several 128-token tiles
+with ragged tails, the degenerate cases of the method, and the tiny workload."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+import top_routing_expert_lb_b300 as moe
+from parity import check_layer, run_layer, shape_of, np_of
+from top_routing_expert_lb_b300 import build as mbuild
+
+pytestmark = pytest.mark.gpu
+
+W = synth.Workload
+CASES = {
+    "tiny": synth.WORKLOADS["tiny"],
+    "ragged_shared": W("ragged_shared", T=300, d=256, E=8, k=2, M=256, n_shared=1,
+                       offsets="normal"),
+    "capacity_k4": W("capacity_k4", T=517, d=192, E=16, k=4, M=128, capacity_factor=0.9,
+                     offsets="normal"),
+    "fine_bias_shared": W("fine_bias_shared", T=389, d=128, E=64, k=6, M=128, n_shared=2,
+                          offsets="normal", sel_bias="uniform", bias_range=0.02),
+    "top1_capacity": W("top1_capacity", T=1000, d=64, E=32, k=1, M=128,
+                       capacity_factor=1.25, offsets="normal"),
+    "wide_E160": W("wide_E160", T=260, d=320, E=160, k=6, M=256, sel_bias="uniform",
+                   bias_range=0.005),
+    "E1_k1_dense": W("E1_k1_dense", T=150, d=128, E=1, k=1, M=128),
+    "k_equals_E": W("k_equals_E", T=140, d=64, E=4, k=4, M=128),
+    "k0_shared_only": W("k0_shared_only", T=130, d=128, E=8, k=0, M=128, n_shared=1),
+    "k0_no_experts": W("k0_no_experts", T=70, d=64, E=8, k=0, M=128),
+    "single_token": W("single_token", T=1, d=64, E=8, k=2, M=128, n_shared=1),
+    "E256_k8": W("E256_k8", T=200, d=64, E=256, k=8, M=128, offsets="normal"),
+}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    mbuild.ensure_built()
+    assert torch.cuda.is_available()
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_layer_parity(name):
+    inp = synth.make_inputs(CASES[name], "cuda")
+    g, ref = check_layer(inp)
+    if name == "k0_no_experts":
+        assert torch.count_nonzero(g.y) == 0
+    if CASES[name].capacity_factor > 0:
+        assert ref.disp.dropped.any(), "capacity case should drop pairs"
+
+
+def test_one_expert_takes_every_row():
+    w = W("hot", T=333, d=128, E=8, k=1, M=128, n_shared=0)
+    inp = synth.make_inputs(w, "cuda")
+    off = torch.zeros(8, dtype=torch.float32)
+    off[5] = 30.0
+    inp.offset = off.cuda()
+    g, ref = check_layer(inp)
+    assert g.counts.tolist() == [0, 0, 0, 0, 0, 333, 0, 0]
+
+
+def test_capacity_drops_all_but_first_tokens():
+    # a single hot expert with capacity C = ceil(0.25 * 1 * 260 / 4) = 17:
+    # only its first 17 tokens (token order) are kept, all others output 0
+    w = W("cap_hot", T=260, d=64, E=4, k=1, M=128, capacity_factor=0.25)
+    inp = synth.make_inputs(w, "cuda")
+    off = torch.tensor([0.0, 40.0, 0.0, 0.0], dtype=torch.float32)
+    inp.offset = off.cuda()
+    g, ref = check_layer(inp)
+    assert ref.C == 17
+    assert g.drop[:17].sum() == 0 and g.drop[17:].all()
+    assert torch.count_nonzero(g.y[17:]) == 0
+
+
+def test_empty_batch():
+    w = W("empty", T=0, d=64, E=8, k=2, M=128)
+    s = shape_of(w)
+    dev = "cuda"
+    ws = moe._binding.alloc_workspace(s, dev)
+    wr = torch.zeros((8, 64), dtype=torch.bfloat16, device=dev)
+    counts = torch.full((8,), 7, dtype=torch.int32, device=dev)
+    f = torch.full((8,), 7.0, device=dev)
+    P = torch.full((8,), 7.0, device=dev)
+    lb = torch.full((1,), 7.0, device=dev)
+    lz = torch.full((1,), 7.0, device=dev)
+    moe.moe_layer_forward(s, None, wr, None, None, None, None, None, None, None, None, None,
+                          counts, None, f, P, lb, lz, ws)
+    torch.cuda.synchronize()
+    assert counts.sum().item() == 0 and f.abs().sum().item() == 0 and P.abs().sum().item() == 0
+    assert lb.item() == 0.0 and lz.item() == 0.0
+
+
+def test_deterministic_bitwise():
+    w = CASES["capacity_k4"]
+    inp = synth.make_inputs(w, "cuda")
+    layer = moe.MoELayer(shape_of(w), inp.wr, inp.w1, inp.w3, inp.w2, inp.ws1, inp.ws3,
+                         inp.ws2, inp.offset, inp.sel_bias)
+    a = run_layer(inp, layer)
+    b = run_layer(inp, layer)
+    assert torch.equal(a.y.view(torch.int16), b.y.view(torch.int16))
+    for fld in ("ids", "gates", "counts", "drop", "f", "P"):
+        np.testing.assert_array_equal(getattr(a, fld), getattr(b, fld))
+    assert a.bal == b.bal and a.z == b.z
+
+
+def test_host_io_entry_matches_device_entry():
+    w = CASES["ragged_shared"]
+    inp = synth.make_inputs(w, "cuda")
+    layer = moe.MoELayer(shape_of(w), inp.wr, inp.w1, inp.w3, inp.w2, inp.ws1, inp.ws3,
+                         inp.ws2, inp.offset, inp.sel_bias)
+    dev_out = run_layer(inp, layer)
+    x_host = inp.x.cpu().pin_memory()
+    y_host = torch.empty_like(x_host).pin_memory()
+    losses = torch.empty(2, dtype=torch.float32).pin_memory()
+    x_dev = torch.empty_like(inp.x)
+    y_dev = torch.empty_like(inp.x)
+    moe.moe_layer_forward_host(layer.shape, x_host, x_dev, layer.w_router, layer.logit_offset,
+                               layer.sel_bias, layer.w13, layer.w2, layer.w13_shared,
+                               layer.w2_shared, y_dev, y_host, losses, layer.ids, layer.gates,
+                               layer.counts, layer.drop_mask, layer.f, layer.P,
+                               layer.losses[0:1], layer.losses[1:2], layer.ws)
+    assert torch.equal(y_host.view(torch.int16), dev_out.y.cpu().view(torch.int16))
+    assert losses[0].item() == dev_out.bal and losses[1].item() == dev_out.z
+
+
+def test_bounded_wait_reports_timeout():
+    s = shape_of(CASES["tiny"])
+    ws = moe._binding.alloc_workspace(s)
+    try:
+        moe.moe_set_wait_timeout_ns(1_000_000)          # 1 ms
+        moe.moe_debug_timeout_probe(ws)
+        assert moe.moe_check_status(ws) == moe._binding.MOE_ERR_TIMEOUT
+        assert moe.moe_check_status(ws) == 0             # read clears it
+    finally:
+        moe.moe_set_wait_timeout_ns(2_000_000_000)
+    # the context is still usable afterwards
+    inp = synth.make_inputs(CASES["tiny"], "cuda")
+    check_layer(inp)

@@ -1,0 +1,194 @@
+"""GPU parity of each entry point on its own, with synthetic stage inputs
+(never inputs produced by another GPU stage): moe_route, moe_permute,
+moe_grouped_ffn, moe_combine, moe_pack_w13."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+import top_routing_expert_lb_b300 as moe
+from parity import (GATE_ABS, LOSS_REL, assert_y_close, bf16_to_f64, np_of, oracle_routing,
+                    rel_close, shape_of)
+from top_routing_expert_lb_b300 import build as mbuild
+
+pytestmark = pytest.mark.gpu
+W = synth.Workload
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    mbuild.ensure_built()
+    assert torch.cuda.is_available()
+
+
+def _ws(s):
+    return moe._binding.alloc_workspace(s)
+
+
+# --------------------------------------------------------------------------- route
+@pytest.mark.parametrize("w", [
+    W("r_small", T=257, d=128, E=8, k=2, M=128),
+    W("r_offset", T=1000, d=512, E=64, k=6, M=128, offsets="normal"),
+    W("r_bias", T=700, d=1024, E=160, k=6, M=128, offsets="normal", sel_bias="uniform"),
+    W("r_top1", T=129, d=64, E=128, k=1, M=128, offsets="normal"),
+    W("r_k0", T=200, d=64, E=8, k=0, M=128),
+    W("r_E256", T=300, d=192, E=256, k=8, M=128),
+], ids=lambda w: w.name)
+def test_route(w):
+    inp = synth.make_inputs(w, "cuda", experts=False)
+    s = shape_of(w)
+    dev = "cuda"
+    ids = torch.empty((w.T, w.k), dtype=torch.int32, device=dev)
+    gates = torch.empty((w.T, w.k), dtype=torch.float32, device=dev)
+    counts = torch.empty(w.E, dtype=torch.int32, device=dev)
+    f = torch.empty(w.E, device=dev)
+    P = torch.empty(w.E, device=dev)
+    lb = torch.empty(1, device=dev)
+    lz = torch.empty(1, device=dev)
+    ws = _ws(s)
+    moe.moe_route(s, inp.x, inp.wr, inp.offset, inp.sel_bias, ids, gates, counts, f, P, lb, lz,
+                  ws)
+    torch.cuda.synchronize()
+    assert moe.moe_check_status(ws) == 0
+    ref = oracle_routing(inp, np_of(ids))
+    if w.k:
+        np.testing.assert_array_equal(np_of(ids), ref.routing.ids)
+        assert np.abs(np_of(gates) - ref.routing.gates).max() <= GATE_ABS
+    np.testing.assert_array_equal(np_of(counts), ref.disp.counts)
+    np.testing.assert_allclose(np_of(f), ref.loss.f, rtol=1e-6)
+    np.testing.assert_allclose(np_of(P), ref.loss.P, rtol=LOSS_REL, atol=1e-7)
+    rel_close(lb.item(), ref.loss.L_bal, LOSS_REL, "balance loss")
+    rel_close(lz.item(), ref.loss.L_z, LOSS_REL, "z-loss")
+
+
+# --------------------------------------------------------------------------- permute
+def _synthetic_ids(T, E, k, seed, hot_frac=0.4):
+    rng = np.random.default_rng(seed)
+    ids = np.stack([rng.choice(E, k, replace=False) for _ in range(T)]).astype(np.int32)
+    hot = rng.random(T) < hot_frac                  # skew: many tokens pick expert 1 first
+    for t in np.nonzero(hot)[0]:
+        if 1 not in ids[t]:
+            ids[t, 0] = 1
+    return ids
+
+
+@pytest.mark.parametrize("T,E,k,c,d", [
+    (1, 4, 2, 0.0, 64), (129, 8, 2, 0.0, 128), (300, 16, 3, 0.0, 192),
+    (517, 16, 4, 0.8, 64), (1000, 32, 1, 1.25, 128), (2048, 160, 6, 0.0, 256),
+    (640, 8, 8, 0.5, 64), (130, 256, 8, 1.0, 64),
+])
+def test_permute(T, E, k, c, d):
+    ids_np = _synthetic_ids(T, E, k, seed=T * 7 + E)
+    w = W("p", T=T, d=d, E=E, k=k, M=128, capacity_factor=c)
+    s = shape_of(w)
+    x = synth.normal_bf16(3, synth.TID_X, (T, d), 1.0, "cuda")
+    ids = torch.from_numpy(ids_np).cuda()
+    R_max = moe.moe_max_rows(s)
+    offsets = torch.full((E + 1,), -7, dtype=torch.int32, device="cuda")
+    slot_row = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    row_token = torch.full((max(R_max, 1),), -7, dtype=torch.int32, device="cuda")
+    drop = torch.empty((T, k), dtype=torch.uint8, device="cuda")
+    x_perm = torch.zeros((max(R_max, 1), d), dtype=torch.bfloat16, device="cuda")
+    ws = _ws(s)
+    moe.moe_permute(s, x, ids, offsets, slot_row, row_token, drop, x_perm, ws)
+    torch.cuda.synchronize()
+    C = oracle.capacity(float(np.float32(c)), k, T, E)
+    ref = oracle.dispatch(ids_np, E, C)
+    R = int(ref.offsets[-1])
+    np.testing.assert_array_equal(np_of(offsets), ref.offsets)
+    np.testing.assert_array_equal(np_of(slot_row), ref.slot_row)
+    np.testing.assert_array_equal(np_of(row_token)[:R], ref.row_token)
+    np.testing.assert_array_equal(np_of(drop), ref.dropped)
+    xp = np_of(x_perm)[:R]
+    np.testing.assert_array_equal(xp, np_of(x)[ref.row_token])
+
+
+# --------------------------------------------------------------------------- grouped FFN
+@pytest.mark.parametrize("rows,d,M,n_shared,T", [
+    ([0, 1, 127, 128, 129, 300], 128, 256, 1, 200),    # empty, single, tile edges
+    ([5, 0, 0, 260], 64, 128, 0, 0),                   # d = 64 (second projection N = 64)
+    ([130, 70, 2], 256, 128, 2, 131),                  # d = 256, 2 shared experts
+    ([0, 0, 0], 192, 128, 1, 77),                      # routed rows all empty, shared only
+    ([400], 320, 384, 0, 0),                           # one group, d = 320 (N tile 64)
+])
+def test_grouped_ffn(rows, d, M, n_shared, T):
+    E = len(rows)
+    R = int(sum(rows))
+    Ms = n_shared * M
+    # the shape's T is the shared group's row count; T*k bounds the routed rows
+    Tshape = T if n_shared else max(R, 1)
+    k = max(1, -(-R // Tshape))
+    assert k <= min(E, 8)
+    s_ffn = moe.Shape.of(Tshape, d, M, E, k, n_shared)
+    dev = "cuda"
+    R_max = moe.moe_max_rows(s_ffn)
+    assert R <= R_max
+    x_perm = torch.zeros((max(R_max, 1), d), dtype=torch.bfloat16, device=dev)
+    if R:
+        x_perm[:R] = synth.normal_bf16(5, synth.TID_X, (R, d), 1.0, dev)
+    offsets = torch.tensor(np.concatenate([[0], np.cumsum(rows)]).astype(np.int32), device=dev)
+    w1 = synth.normal_bf16(5, synth.TID_W1, (E, M, d), 0.05, dev)
+    w3 = synth.normal_bf16(5, synth.TID_W3, (E, M, d), 0.05, dev)
+    w2 = synth.normal_bf16(5, synth.TID_W2, (E, d, M), 0.05, dev)
+    w13 = moe.moe_pack_w13(w1, w3)
+    y_perm = torch.zeros((max(R_max, 1), d), dtype=torch.bfloat16, device=dev)
+    x = ws1 = ws3 = ws2 = w13s = y_s = None
+    if n_shared:
+        x = synth.normal_bf16(6, synth.TID_X, (T, d), 1.0, dev)
+        ws1 = synth.normal_bf16(5, synth.TID_WS1, (Ms, d), 0.05, dev)
+        ws3 = synth.normal_bf16(5, synth.TID_WS3, (Ms, d), 0.05, dev)
+        ws2 = synth.normal_bf16(5, synth.TID_WS2, (d, Ms), 0.05, dev)
+        w13s = moe.moe_pack_w13(ws1, ws3)
+        y_s = torch.zeros((T, d), dtype=torch.bfloat16, device=dev)
+    ws = _ws(s_ffn)
+    moe.moe_grouped_ffn(s_ffn, x_perm, offsets, w13, w2, y_perm, x, w13s, ws2, y_s, ws)
+    torch.cuda.synchronize()
+    assert moe.moe_check_status(ws) == 0
+    expert = np.repeat(np.arange(E, dtype=np.int32), rows)
+    if R:
+        ref = oracle.expert_rows(np_of(x_perm)[:R], expert, np_of(w1), np_of(w3), np_of(w2))
+        assert_y_close(bf16_to_f64(y_perm)[:R], ref, "y_perm")
+    if n_shared:
+        ref_s = oracle.expert_rows(np_of(x), np.zeros(T, np.int32), np_of(ws1)[None],
+                                   np_of(ws3)[None], np_of(ws2)[None])
+        assert_y_close(bf16_to_f64(y_s), ref_s, "y_shared")
+
+
+# --------------------------------------------------------------------------- combine
+@pytest.mark.parametrize("T,d,E,k,c,shared", [
+    (1, 64, 4, 2, 0.0, False), (300, 256, 8, 2, 0.0, True), (517, 128, 16, 4, 0.7, True),
+    (999, 64, 32, 1, 1.25, False), (64, 512, 8, 8, 0.0, True),
+])
+def test_combine(T, d, E, k, c, shared):
+    ids_np = _synthetic_ids(T, E, k, seed=T + d)
+    C = oracle.capacity(float(np.float32(c)), k, T, E)
+    disp = oracle.dispatch(ids_np, E, C)
+    R = max(int(disp.offsets[-1]), 1)
+    rng = np.random.default_rng(T)
+    g = rng.random((T, k)).astype(np.float32) + 0.05
+    g /= g.sum(1, keepdims=True)
+    y_perm = synth.normal_bf16(9, synth.TID_X, (R, d), 1.0, "cuda")
+    y_s = synth.normal_bf16(10, synth.TID_X, (T, d), 1.0, "cuda") if shared else None
+    y = torch.empty((T, d), dtype=torch.bfloat16, device="cuda")
+    s = moe.Shape.of(T, d, 128, E, k, 1 if shared else 0, c)
+    moe.moe_combine(s, y_perm, torch.from_numpy(disp.slot_row).cuda(), torch.from_numpy(g).cuda(),
+                    y_s, y)
+    torch.cuda.synchronize()
+    ref = oracle.combine(np_of(y_perm), disp.slot_row, g.astype(np.float64), np_of(y_s))
+    yg = bf16_to_f64(y)
+    # one bf16 rounding of an fp32 sum: |err| <= 2^-8 |ref| + small
+    assert np.all(np.abs(yg - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-5)
+
+
+def test_pack_w13():
+    G, Mw, d = 3, 384, 128
+    w1 = synth.normal_bf16(1, synth.TID_W1, (G, Mw, d), 1.0, "cuda")
+    w3 = synth.normal_bf16(1, synth.TID_W3, (G, Mw, d), 1.0, "cuda")
+    out = np_of(moe.moe_pack_w13(w1, w3))
+    a, b = np_of(w1), np_of(w3)
+    for g in range(G):
+        for j in range(Mw // 128):
+            np.testing.assert_array_equal(out[g, 256 * j:256 * j + 128], a[g, 128 * j:128 * j + 128])
+            np.testing.assert_array_equal(out[g, 256 * j + 128:256 * j + 256],
+                                          b[g, 128 * j:128 * j + 128])

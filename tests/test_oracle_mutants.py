@@ -39,6 +39,8 @@ MUTANTS = {
     "zloss_not_squared": ("sz += lse[t] * lse[t];", "sz += lse[t];"),
     "f_over_T": ("(double)counts[e] / ((double)k * (double)T)", "(double)counts[e] / (double)T"),
     "balance_without_E": ("*L_bal = lambda * (double)E * sfp;", "*L_bal = lambda * sfp;"),
+    "combine_drop_ignored": ("if (r < 0) continue;\n            double g", "if (r < 0) r = 0;\n            double g"),
+    "combine_shared_missing": ("yt[o] += bf16_val(y_shared[(size_t)t * d + o]);", "yt[o] += 0.0;"),
 }
 
 

@@ -1,0 +1,13 @@
+"""B300-native forward pass of one top-k routed Mixture-of-Experts FFN layer.
+
+The compute lives in ``libmoe_b300.so`` (CUDA C++ for sm_103a, C ABI in
+``include/moe.h``); this package is its thin Python binding.  Importing the
+package does not load the library; the first call does, and fails loudly if
+the library has not been built.
+"""
+from ._binding import (  # noqa: F401
+    MoeError, Shape, lib, moe_capacity, moe_check_status, moe_combine, moe_debug_timeout_probe,
+    moe_error_string, moe_grouped_ffn, moe_layer_forward, moe_layer_forward_host, moe_max_rows,
+    moe_pack_w13, moe_permute, moe_route, moe_set_wait_timeout_ns, moe_workspace_size,
+    MoELayer, moe_profile_enable, moe_profile_collect, moe_launch_count, alloc_workspace,
+)

@@ -1,0 +1,564 @@
+// Host side of the C ABI declared in include/moe.h: argument checks,
+// workspace layout, TMA descriptors and the launch sequence of the layer.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <vector>
+
+#include "../../include/moe.h"
+#include "moe_internal.h"
+
+namespace moe {
+
+namespace {
+
+uint64_t g_timeout_ns = 2000000000ull;
+
+// ---------------------------------------------------------------- accounting
+uint64_t g_launches = 0;
+bool g_prof_on = false;
+struct ProfRec {
+  int32_t kernel;
+  cudaEvent_t start, stop;
+};
+std::vector<ProfRec> g_prof;        // recorded pairs, launch order
+std::vector<cudaEvent_t> g_ev_pool;  // reusable events
+size_t g_ev_used = 0;
+
+cudaEvent_t pool_event() {
+  if (g_ev_used == g_ev_pool.size()) {
+    cudaEvent_t e;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    g_ev_pool.push_back(e);
+  }
+  return g_ev_pool[g_ev_used++];
+}
+
+// Runs one launcher; counts it and, when profiling, brackets it with events.
+template <typename F>
+int tracked(int32_t kernel, cudaStream_t st, F&& launch) {
+  cudaEvent_t a = nullptr, b = nullptr;
+  if (g_prof_on) {
+    a = pool_event();
+    b = pool_event();
+    if (a) cudaEventRecord(a, st);
+  }
+  const int rc = launch();
+  if (rc == 0) ++g_launches;
+  if (g_prof_on && a && b) {
+    cudaEventRecord(b, st);
+    g_prof.push_back({kernel, a, b});
+  }
+  return rc;
+}
+
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Workspace regions (byte offsets from the workspace base).
+struct Layout {
+  size_t status, tile_hist, tile_psum, tile_lse2, tile_base, offsets, slot_row, row_token;
+  size_t x_perm, h, y_perm, h_s, y_s, total;
+  int64_t ntiles, rmax, C;
+};
+
+int check_shape(const moe_shape_t* s) {
+  if (s == nullptr) return MOE_ERR_INVALID_ARG;
+  if (s->T < 0 || s->d <= 0 || s->M <= 0 || s->E <= 0 || s->k < 0 || s->n_shared < 0)
+    return MOE_ERR_INVALID_ARG;
+  if (s->k > s->E) return MOE_ERR_INVALID_ARG;
+  if (!std::isfinite(s->capacity_factor) || !std::isfinite(s->balance_coef))
+    return MOE_ERR_INVALID_ARG;
+  if (s->flags != 0) return MOE_ERR_UNSUPPORTED;
+  if (s->E > MOE_MAX_EXPERTS || s->k > MOE_MAX_TOPK) return MOE_ERR_UNSUPPORTED;
+  if (s->T > (1 << 24)) return MOE_ERR_UNSUPPORTED;
+  if (s->d % 64 != 0 || s->d < 64 || s->d > 16384) return MOE_ERR_UNSUPPORTED;
+  if (s->M % 128 != 0 || s->M < 128 || s->M > 32768) return MOE_ERR_UNSUPPORTED;
+  if (s->n_shared > 8) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+int64_t capacity_of(const moe_shape_t* s) {
+  if (!(s->capacity_factor > 0.0f)) return -1;
+  const double c = static_cast<double>(s->capacity_factor);
+  return static_cast<int64_t>(
+      std::ceil(c * static_cast<double>(s->k) * static_cast<double>(s->T) /
+                static_cast<double>(s->E)));
+}
+
+Layout layout_of(const moe_shape_t* s) {
+  Layout L{};
+  const int64_t T = s->T, d = s->d, M = s->M, E = s->E, k = s->k;
+  const int64_t Ms = static_cast<int64_t>(s->n_shared) * M;
+  L.ntiles = (T + kTileTokens - 1) / kTileTokens;
+  L.C = capacity_of(s);
+  L.rmax = T * k;
+  if (L.C >= 0 && E * L.C < L.rmax) L.rmax = E * L.C;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o += align_up(bytes);
+    return at;
+  };
+  L.status = take(kAlign);
+  L.tile_hist = take(L.ntiles * E * 4);
+  L.tile_psum = take(L.ntiles * E * 4);
+  L.tile_lse2 = take(L.ntiles * 4);
+  L.tile_base = take(L.ntiles * E * 4);
+  L.offsets = take((E + 1) * 4);
+  L.slot_row = take(T * k * 4);
+  L.row_token = take(L.rmax * 4);
+  L.x_perm = take(L.rmax * d * 2);
+  L.h = take(L.rmax * M * 2);
+  L.y_perm = take(L.rmax * d * 2);
+  L.h_s = take(T * Ms * 2);
+  L.y_s = take(T * d * 2);
+  L.total = o;
+  return L;
+}
+
+template <typename Tp>
+Tp* at(void* ws, size_t off) {
+  return reinterpret_cast<Tp*>(static_cast<uint8_t*>(ws) + off);
+}
+
+int check_ws(const moe_shape_t* s, void* ws, size_t ws_bytes, Layout* L) {
+  *L = layout_of(s);
+  if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0)
+    return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < L->total) return MOE_ERR_WORKSPACE;
+  return MOE_OK;
+}
+
+int sm_count_cached() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+inline int cuda_rc(int rc) {
+  if (rc == 0) return MOE_OK;
+  if (rc == -2) return MOE_ERR_UNSUPPORTED;
+  return MOE_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------- stages
+int do_route(const moe_shape_t* s, const uint16_t* x, const uint16_t* wr, const float* off,
+             const float* bias, int32_t* ids, float* gates, int32_t* counts, float* f, float* P,
+             float* bal, float* z, void* ws, const Layout& L, int32_t* tile_base,
+             int32_t* offsets, cudaStream_t st) {
+  if (s->T > 0) {
+    CUtensorMap mx, mw;
+    const uint32_t nr = static_cast<uint32_t>((s->E + 15) / 16 * 16);
+    if (!make_tmap_bf16(&mx, x, s->T, s->d, 128)) return MOE_ERR_CUDA;
+    if (!make_tmap_bf16(&mw, wr, s->E, s->d, nr)) return MOE_ERR_CUDA;
+    RouterArgs ra{};
+    ra.T = s->T;
+    ra.d = s->d;
+    ra.E = s->E;
+    ra.k = s->k;
+    ra.logit_offset = off;
+    ra.sel_bias = bias;
+    ra.ids = ids;
+    ra.gates = gates;
+    ra.tile_hist = at<int32_t>(ws, L.tile_hist);
+    ra.tile_psum = at<float>(ws, L.tile_psum);
+    ra.tile_lse2 = at<float>(ws, L.tile_lse2);
+    ra.status = at<int>(ws, L.status);
+    ra.timeout_ns = g_timeout_ns;
+    const int rc = tracked(MOE_KERNEL_ROUTER, st, [&] { return launch_router(mx, mw, ra, st); });
+    if (rc != 0) return cuda_rc(rc);
+  }
+  FinalizeArgs fa{};
+  fa.T = s->T;
+  fa.E = s->E;
+  fa.k = s->k;
+  fa.C = L.C;
+  fa.balance_coef = s->balance_coef;
+  fa.tile_hist = at<int32_t>(ws, L.tile_hist);
+  fa.tile_psum = at<float>(ws, L.tile_psum);
+  fa.tile_lse2 = at<float>(ws, L.tile_lse2);
+  fa.counts = counts;
+  fa.f = f;
+  fa.P = P;
+  fa.bal_loss = bal;
+  fa.z_loss = z;
+  fa.tile_base = tile_base;
+  fa.offsets = offsets;
+  return cuda_rc(tracked(MOE_KERNEL_FINALIZE, st, [&] { return launch_finalize(fa, st); }));
+}
+
+int do_scatter(const moe_shape_t* s, const uint16_t* x, const int32_t* ids, const Layout& L,
+               void* ws, const int32_t* offsets, int32_t* slot_row, int32_t* row_token,
+               uint8_t* drop_mask, uint16_t* x_perm, cudaStream_t st) {
+  ScatterArgs sa{};
+  sa.T = s->T;
+  sa.d = s->d;
+  sa.E = s->E;
+  sa.k = s->k;
+  sa.C = L.C;
+  sa.ids = ids;
+  sa.tile_base = at<int32_t>(ws, L.tile_base);
+  sa.offsets = offsets;
+  sa.x = x;
+  sa.slot_row = slot_row;
+  sa.row_token = row_token;
+  sa.drop_mask = drop_mask;
+  sa.x_perm = x_perm;
+  return cuda_rc(tracked(MOE_KERNEL_SCATTER, st, [&] { return launch_scatter(sa, st); }));
+}
+
+int do_ffn(const moe_shape_t* s, const uint16_t* x_perm, const int32_t* offsets,
+           const uint16_t* w13, const uint16_t* w2, uint16_t* y_perm, const uint16_t* x,
+           const uint16_t* w13s, const uint16_t* w2s, uint16_t* y_s, void* ws, const Layout& L,
+           cudaStream_t st) {
+  const int64_t T = s->T, d = s->d, M = s->M, E = s->E;
+  const int64_t Ms = static_cast<int64_t>(s->n_shared) * M;
+  const bool routed = L.rmax > 0;
+  const bool shared = Ms > 0 && T > 0;
+  if (!routed && !shared) return MOE_OK;
+  uint16_t* h = at<uint16_t>(ws, L.h);
+  uint16_t* h_s = at<uint16_t>(ws, L.h_s);
+  const int bn2 = (d % 256 == 0) ? 256 : (d % 128 == 0 ? 128 : 64);
+  const int nsm = sm_count_cached();
+
+  // projection 1: [x_perm | x] -> h = SiLU(gate) * up
+  CUtensorMap a0, a1, b0, b1;
+  if (routed) {
+    if (!make_tmap_bf16(&a0, x_perm, L.rmax, d, 128)) return MOE_ERR_CUDA;
+    if (!make_tmap_bf16(&b0, w13, E * 2 * M, d, 256)) return MOE_ERR_CUDA;
+  }
+  if (shared) {
+    if (!make_tmap_bf16(&a1, x, T, d, 128)) return MOE_ERR_CUDA;
+    if (!make_tmap_bf16(&b1, w13s, 2 * Ms, d, 256)) return MOE_ERR_CUDA;
+  }
+  if (!routed) { a0 = a1; b0 = b1; }
+  if (!shared) { a1 = a0; b1 = b0; }
+  GroupedGemmArgs g1{};
+  g1.offsets = offsets;
+  g1.n_routed = routed ? static_cast<int32_t>(E) : 0;
+  g1.shared_rows = shared ? static_cast<int32_t>(T) : 0;
+  g1.n_cols_routed = static_cast<int32_t>(2 * M);
+  g1.n_cols_shared = static_cast<int32_t>(2 * Ms);
+  g1.k_routed = static_cast<int32_t>(d);
+  g1.k_shared = static_cast<int32_t>(d);
+  g1.out_routed = h;
+  g1.ld_routed = M;
+  g1.out_shared = h_s;
+  g1.ld_shared = Ms;
+  g1.status = at<int>(ws, L.status);
+  g1.timeout_ns = g_timeout_ns;
+  int rc = tracked(MOE_KERNEL_GEMM_SWIGLU, st,
+                   [&] { return launch_grouped_gemm(a0, a1, b0, b1, g1, true, 256, nsm, st); });
+  if (rc != 0) return cuda_rc(rc);
+
+  // projection 2: [h | h_s] -> [y_perm | y_s]
+  if (routed) {
+    if (!make_tmap_bf16(&a0, h, L.rmax, M, 128)) return MOE_ERR_CUDA;
+    if (!make_tmap_bf16(&b0, w2, E * d, M, static_cast<uint32_t>(bn2))) return MOE_ERR_CUDA;
+  }
+  if (shared) {
+    if (!make_tmap_bf16(&a1, h_s, T, Ms, 128)) return MOE_ERR_CUDA;
+    if (!make_tmap_bf16(&b1, w2s, d, Ms, static_cast<uint32_t>(bn2))) return MOE_ERR_CUDA;
+  }
+  if (!routed) { a0 = a1; b0 = b1; }
+  if (!shared) { a1 = a0; b1 = b0; }
+  GroupedGemmArgs g2 = g1;
+  g2.n_cols_routed = static_cast<int32_t>(d);
+  g2.n_cols_shared = static_cast<int32_t>(d);
+  g2.k_routed = static_cast<int32_t>(M);
+  g2.k_shared = static_cast<int32_t>(Ms > 0 ? Ms : 64);
+  g2.out_routed = y_perm;
+  g2.ld_routed = d;
+  g2.out_shared = y_s;
+  g2.ld_shared = d;
+  rc = tracked(MOE_KERNEL_GEMM_DOWN, st,
+               [&] { return launch_grouped_gemm(a0, a1, b0, b1, g2, false, bn2, nsm, st); });
+  return cuda_rc(rc);
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+const char* moe_error_string(int code) {
+  switch (code) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported shape";
+    case MOE_ERR_CUDA: return "CUDA call failed";
+    case MOE_ERR_TIMEOUT: return "bounded device wait timed out";
+    case MOE_ERR_WORKSPACE: return "workspace too small";
+    default: return "unknown error";
+  }
+}
+
+int moe_workspace_size(const moe_shape_t* shape, size_t* bytes) {
+  const int rc = check_shape(shape);
+  if (rc != MOE_OK) return rc;
+  if (bytes == nullptr) return MOE_ERR_INVALID_ARG;
+  *bytes = layout_of(shape).total;
+  return MOE_OK;
+}
+
+int moe_capacity(const moe_shape_t* shape, int64_t* C) {
+  const int rc = check_shape(shape);
+  if (rc != MOE_OK) return rc;
+  if (C == nullptr) return MOE_ERR_INVALID_ARG;
+  *C = capacity_of(shape);
+  return MOE_OK;
+}
+
+int moe_max_rows(const moe_shape_t* shape, int64_t* rows) {
+  const int rc = check_shape(shape);
+  if (rc != MOE_OK) return rc;
+  if (rows == nullptr) return MOE_ERR_INVALID_ARG;
+  *rows = layout_of(shape).rmax;
+  return MOE_OK;
+}
+
+int moe_pack_w13(int32_t G, int32_t Mw, int32_t d, const uint16_t* w1, const uint16_t* w3,
+                 uint16_t* w13, void* stream) {
+  if (G < 0 || Mw < 0 || d <= 0) return MOE_ERR_INVALID_ARG;
+  if (Mw % 128 != 0 || d % 64 != 0) return MOE_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(G) * Mw == 0) return MOE_OK;
+  if (!w1 || !w3 || !w13 || !aligned16(w1) || !aligned16(w3) || !aligned16(w13))
+    return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return cuda_rc(tracked(MOE_KERNEL_OTHER, st, [&] { return launch_pack_w13(G, Mw, d, w1, w3, w13, st); }));
+}
+
+int moe_route(const moe_shape_t* s, const uint16_t* x, const uint16_t* w_router,
+              const float* logit_offset, const float* sel_bias, int32_t* ids, float* gates,
+              int32_t* counts, float* f, float* P, float* bal_loss, float* z_loss, void* ws,
+              size_t ws_bytes, void* stream) {
+  int rc = check_shape(s);
+  if (rc != MOE_OK) return rc;
+  Layout L;
+  if ((rc = check_ws(s, ws, ws_bytes, &L)) != MOE_OK) return rc;
+  if (!counts || !f || !P || !bal_loss || !z_loss) return MOE_ERR_INVALID_ARG;
+  if (s->T > 0) {
+    if (!x || !w_router || !aligned16(x) || !aligned16(w_router)) return MOE_ERR_INVALID_ARG;
+    if (s->k > 0 && (!ids || !gates)) return MOE_ERR_INVALID_ARG;
+  }
+  return do_route(s, x, w_router, logit_offset, sel_bias, ids, gates, counts, f, P, bal_loss,
+                  z_loss, ws, L, nullptr, nullptr, static_cast<cudaStream_t>(stream));
+}
+
+int moe_permute(const moe_shape_t* s, const uint16_t* x, const int32_t* ids, int32_t* offsets,
+                int32_t* slot_row, int32_t* row_token, uint8_t* drop_mask, uint16_t* x_perm,
+                void* ws, size_t ws_bytes, void* stream) {
+  int rc = check_shape(s);
+  if (rc != MOE_OK) return rc;
+  Layout L;
+  if ((rc = check_ws(s, ws, ws_bytes, &L)) != MOE_OK) return rc;
+  if (!offsets) return MOE_ERR_INVALID_ARG;
+  const bool work = s->T > 0 && s->k > 0;
+  if (work && (!x || !ids || !slot_row || !row_token || !drop_mask || !x_perm ||
+               !aligned16(x) || !aligned16(x_perm)))
+    return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int32_t* tile_hist = at<int32_t>(ws, L.tile_hist);
+  if (work) {
+    if ((rc = cuda_rc(tracked(MOE_KERNEL_TILE_HIST, st, [&] {
+           return launch_tile_hist(ids, s->T, s->k, s->E, tile_hist, st);
+         }))) != MOE_OK)
+      return rc;
+  }
+  FinalizeArgs fa{};
+  fa.T = work ? s->T : 0;
+  fa.E = s->E;
+  fa.k = s->k;
+  fa.C = L.C;
+  fa.tile_hist = tile_hist;
+  fa.tile_base = at<int32_t>(ws, L.tile_base);
+  fa.offsets = offsets;
+  if ((rc = cuda_rc(tracked(MOE_KERNEL_FINALIZE, st, [&] { return launch_finalize(fa, st); }))) !=
+      MOE_OK)
+    return rc;
+  if (!work) return MOE_OK;
+  return do_scatter(s, x, ids, L, ws, offsets, slot_row, row_token, drop_mask, x_perm, st);
+}
+
+int moe_grouped_ffn(const moe_shape_t* s, const uint16_t* x_perm, const int32_t* offsets,
+                    const uint16_t* w13, const uint16_t* w2, uint16_t* y_perm, const uint16_t* x,
+                    const uint16_t* w13_shared, const uint16_t* w2_shared, uint16_t* y_shared,
+                    void* ws, size_t ws_bytes, void* stream) {
+  int rc = check_shape(s);
+  if (rc != MOE_OK) return rc;
+  Layout L;
+  if ((rc = check_ws(s, ws, ws_bytes, &L)) != MOE_OK) return rc;
+  if (L.rmax > 0) {
+    if (!x_perm || !offsets || !w13 || !w2 || !y_perm || !aligned16(x_perm) ||
+        !aligned16(w13) || !aligned16(w2) || !aligned16(y_perm))
+      return MOE_ERR_INVALID_ARG;
+  }
+  if (s->n_shared > 0 && s->T > 0) {
+    if (!x || !w13_shared || !w2_shared || !y_shared || !aligned16(x) ||
+        !aligned16(w13_shared) || !aligned16(w2_shared) || !aligned16(y_shared))
+      return MOE_ERR_INVALID_ARG;
+  }
+  return do_ffn(s, x_perm, offsets, w13, w2, y_perm, x, w13_shared, w2_shared, y_shared, ws, L,
+                static_cast<cudaStream_t>(stream));
+}
+
+int moe_combine(const moe_shape_t* s, const uint16_t* y_perm, const int32_t* slot_row,
+                const float* gates, const uint16_t* y_shared, uint16_t* y, void* stream) {
+  const int rc = check_shape(s);
+  if (rc != MOE_OK) return rc;
+  if (s->T == 0) return MOE_OK;
+  if (!y || !aligned16(y)) return MOE_ERR_INVALID_ARG;
+  if (s->k > 0 && (!y_perm || !slot_row || !gates || !aligned16(y_perm)))
+    return MOE_ERR_INVALID_ARG;
+  if (y_shared && !aligned16(y_shared)) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return cuda_rc(tracked(MOE_KERNEL_COMBINE, st, [&] {
+    return launch_combine(s->T, s->d, s->k, y_perm, slot_row, gates, y_shared, y, st);
+  }));
+}
+
+int moe_layer_forward(const moe_shape_t* s, const uint16_t* x, const uint16_t* w_router,
+                      const float* logit_offset, const float* sel_bias, const uint16_t* w13,
+                      const uint16_t* w2, const uint16_t* w13_shared, const uint16_t* w2_shared,
+                      uint16_t* y, int32_t* ids, float* gates, int32_t* counts,
+                      uint8_t* drop_mask, float* f, float* P, float* bal_loss, float* z_loss,
+                      void* ws, size_t ws_bytes, void* stream) {
+  int rc = check_shape(s);
+  if (rc != MOE_OK) return rc;
+  Layout L;
+  if ((rc = check_ws(s, ws, ws_bytes, &L)) != MOE_OK) return rc;
+  if (!counts || !f || !P || !bal_loss || !z_loss) return MOE_ERR_INVALID_ARG;
+  if (s->T > 0) {
+    if (!x || !w_router || !y || !aligned16(x) || !aligned16(w_router) || !aligned16(y))
+      return MOE_ERR_INVALID_ARG;
+    if (s->k > 0 && (!ids || !gates || !drop_mask || !w13 || !w2 || !aligned16(w13) ||
+                     !aligned16(w2)))
+      return MOE_ERR_INVALID_ARG;
+    if (s->n_shared > 0 && (!w13_shared || !w2_shared || !aligned16(w13_shared) ||
+                            !aligned16(w2_shared)))
+      return MOE_ERR_INVALID_ARG;
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int32_t* offsets = at<int32_t>(ws, L.offsets);
+  rc = do_route(s, x, w_router, logit_offset, sel_bias, ids, gates, counts, f, P, bal_loss,
+                z_loss, ws, L, at<int32_t>(ws, L.tile_base), offsets, st);
+  if (rc != MOE_OK || s->T == 0) return rc;
+  int32_t* slot_row = at<int32_t>(ws, L.slot_row);
+  uint16_t* x_perm = at<uint16_t>(ws, L.x_perm);
+  uint16_t* y_perm = at<uint16_t>(ws, L.y_perm);
+  uint16_t* y_s = s->n_shared > 0 ? at<uint16_t>(ws, L.y_s) : nullptr;
+  if (s->k > 0) {
+    rc = do_scatter(s, x, ids, L, ws, offsets, slot_row, at<int32_t>(ws, L.row_token),
+                    drop_mask, x_perm, st);
+    if (rc != MOE_OK) return rc;
+  }
+  rc = do_ffn(s, x_perm, offsets, w13, w2, y_perm, x, w13_shared, w2_shared, y_s, ws, L, st);
+  if (rc != MOE_OK) return rc;
+  return cuda_rc(tracked(MOE_KERNEL_COMBINE, st, [&] {
+    return launch_combine(s->T, s->d, s->k, y_perm, slot_row, gates, y_s, y, st);
+  }));
+}
+
+int moe_layer_forward_host(const moe_shape_t* s, const uint16_t* x_host, uint16_t* x_dev,
+                           const uint16_t* w_router, const float* logit_offset,
+                           const float* sel_bias, const uint16_t* w13, const uint16_t* w2,
+                           const uint16_t* w13_shared, const uint16_t* w2_shared,
+                           uint16_t* y_dev, uint16_t* y_host, float* losses_host, int32_t* ids,
+                           float* gates, int32_t* counts, uint8_t* drop_mask, float* f,
+                           float* P, float* bal_loss, float* z_loss, void* ws, size_t ws_bytes,
+                           void* stream) {
+  int rc = check_shape(s);
+  if (rc != MOE_OK) return rc;
+  if (s->T > 0 && (!x_host || !x_dev || !y_dev || !y_host)) return MOE_ERR_INVALID_ARG;
+  if (!losses_host) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t bytes = static_cast<size_t>(s->T) * s->d * 2;
+  if (bytes && cudaMemcpyAsync(x_dev, x_host, bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  rc = moe_layer_forward(s, x_dev, w_router, logit_offset, sel_bias, w13, w2, w13_shared,
+                         w2_shared, y_dev, ids, gates, counts, drop_mask, f, P, bal_loss, z_loss,
+                         ws, ws_bytes, stream);
+  if (rc != MOE_OK) return rc;
+  if (bytes && cudaMemcpyAsync(y_host, y_dev, bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (cudaMemcpyAsync(losses_host, bal_loss, 4, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaMemcpyAsync(losses_host + 1, z_loss, 4, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return cudaStreamSynchronize(st) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+int moe_check_status(void* ws, int* status, void* stream) {
+  if (!ws || !status) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int v = 0;
+  if (cudaMemcpyAsync(&v, ws, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (cudaMemsetAsync(ws, 0, sizeof(int), st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+  *status = (v == 0) ? MOE_OK : MOE_ERR_TIMEOUT;
+  return MOE_OK;
+}
+
+int moe_set_wait_timeout_ns(uint64_t ns) {
+  if (ns == 0) return MOE_ERR_INVALID_ARG;
+  g_timeout_ns = ns;
+  return MOE_OK;
+}
+
+int moe_debug_timeout_probe(void* ws, size_t ws_bytes, void* stream) {
+  if (!ws || ws_bytes < sizeof(int) || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0)
+    return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return cuda_rc(tracked(MOE_KERNEL_OTHER, st, [&] {
+    return launch_timeout_probe(static_cast<int*>(ws), g_timeout_ns, st);
+  }));
+}
+
+int moe_profile_enable(int on) {
+  g_prof_on = on != 0;
+  return MOE_OK;
+}
+
+int moe_profile_collect(int cap, int* n, int32_t* kernel_ids, float* ms) {
+  if (!n || cap < 0 || (cap > 0 && (!kernel_ids || !ms))) return MOE_ERR_INVALID_ARG;
+  int out = 0;
+  int rc = MOE_OK;
+  for (const ProfRec& r : g_prof) {
+    if (out >= cap) break;
+    float t = 0.0f;
+    if (cudaEventSynchronize(r.stop) != cudaSuccess ||
+        cudaEventElapsedTime(&t, r.start, r.stop) != cudaSuccess) {
+      rc = MOE_ERR_CUDA;
+      break;
+    }
+    kernel_ids[out] = r.kernel;
+    ms[out] = t;
+    ++out;
+  }
+  *n = out;
+  g_prof.clear();
+  g_ev_used = 0;
+  return rc;
+}
+
+int moe_launch_count(uint64_t* n) {
+  if (!n) return MOE_ERR_INVALID_ARG;
+  *n = g_launches;
+  return MOE_OK;
+}
+
+}  // extern "C"

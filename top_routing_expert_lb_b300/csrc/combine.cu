@@ -1,0 +1,134 @@
+// Combine: gate-weighted un-permute back to token order plus the shared
+// experts' output, and two small utility kernels (weight packing, the bounded
+// wait probe).
+//
+// y[t] = sum_{s kept} g~[t][s] * y_perm[slot_row[t][s]] + y_shared[t]
+// ("MoE：条件计算与路由" §7 Eq.(3); the CSDN note's moe_infer un-permutes with
+// new_x[idxs] = outs, then scales by topk_weight in fp32 and sums over k, and
+// DeepseekV3MoE.forward adds shared_experts(identity)).  Dropped pairs
+// (slot_row = -1) add nothing and the surviving gates are not renormalised
+// (toy MoE demo).  One warp per token; fp32 accumulation in slot order, then
+// the shared row; bf16 store.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "moe_internal.h"
+#include "sm100_primitives.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int kCombineWarps = 8;
+
+__device__ __forceinline__ void acc_bf16x8(float (&acc)[8], const uint4 v, float g) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __bfloat1622float2(h[i]);
+    acc[2 * i] = fmaf(g, f.x, acc[2 * i]);
+    acc[2 * i + 1] = fmaf(g, f.y, acc[2 * i + 1]);
+  }
+}
+
+__device__ __forceinline__ void add_bf16x8(float (&acc)[8], const uint4 v) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __bfloat1622float2(h[i]);
+    acc[2 * i] += f.x;
+    acc[2 * i + 1] += f.y;
+  }
+}
+
+__global__ void __launch_bounds__(kCombineWarps * 32)
+    combine_kernel(int32_t T, int32_t d, int32_t k, const uint16_t* __restrict__ y_perm,
+                   const int32_t* __restrict__ slot_row, const float* __restrict__ gates,
+                   const uint16_t* __restrict__ y_shared, uint16_t* __restrict__ y) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kCombineWarps + warp;
+  if (t >= T) return;
+  int rows[kMaxTopK];
+  float g[kMaxTopK];
+#pragma unroll
+  for (int s = 0; s < kMaxTopK; ++s) {
+    rows[s] = (s < k) ? slot_row[static_cast<int64_t>(t) * k + s] : -1;
+    g[s] = (s < k) ? gates[static_cast<int64_t>(t) * k + s] : 0.0f;
+  }
+  const int nvec = d / 8;
+  const uint4* ys = y_shared ? reinterpret_cast<const uint4*>(y_shared +
+                                                              static_cast<int64_t>(t) * d)
+                             : nullptr;
+  uint4* out = reinterpret_cast<uint4*>(y + static_cast<int64_t>(t) * d);
+  for (int v = lane; v < nvec; v += 32) {
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+#pragma unroll
+    for (int s = 0; s < kMaxTopK; ++s) {
+      if (rows[s] >= 0) {
+        const uint4 val =
+            reinterpret_cast<const uint4*>(y_perm + static_cast<int64_t>(rows[s]) * d)[v];
+        acc_bf16x8(acc, val, g[s]);
+      }
+    }
+    if (ys) add_bf16x8(acc, ys[v]);
+    out[v] = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                        pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+  }
+}
+
+// w13[g][2Mw][d]: 256-row block j = W1 rows [128j, 128j+128) then W3 rows.
+__global__ void pack_w13_kernel(int32_t Mw, int32_t d, const uint16_t* __restrict__ w1,
+                                const uint16_t* __restrict__ w3, uint16_t* __restrict__ w13) {
+  const int64_t r = blockIdx.x;  // output row over G*2Mw
+  const int64_t g = r / (2 * Mw);
+  const int64_t rl = r % (2 * Mw);
+  const int64_t j = rl / 256;
+  const int64_t within = rl % 256;
+  const uint16_t* src = (within < 128 ? w1 : w3) + (g * Mw + j * 128 + (within & 127)) * d;
+  const uint4* s4 = reinterpret_cast<const uint4*>(src);
+  uint4* d4 = reinterpret_cast<uint4*>(w13 + r * d);
+  for (int v = threadIdx.x; v < d / 8; v += blockDim.x) d4[v] = s4[v];
+}
+
+// Waits on a barrier that nothing signals; the bounded wait records a timeout
+// in *status and the kernel returns normally.
+__global__ void timeout_probe_kernel(int* status, uint64_t timeout_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait_bounded(&bar, 0, timeout_ns, status, nullptr);
+  __syncthreads();
+}
+
+}  // namespace
+
+int launch_combine(int32_t T, int32_t d, int32_t k, const uint16_t* y_perm,
+                   const int32_t* slot_row, const float* gates, const uint16_t* y_shared,
+                   uint16_t* y, cudaStream_t stream) {
+  if (T == 0) return 0;
+  const int grid = (T + kCombineWarps - 1) / kCombineWarps;
+  combine_kernel<<<grid, kCombineWarps * 32, 0, stream>>>(T, d, k, y_perm, slot_row, gates,
+                                                           y_shared, y);
+  return cudaGetLastError() == cudaSuccess ? 0 : -3;
+}
+
+int launch_pack_w13(int32_t G, int32_t Mw, int32_t d, const uint16_t* w1, const uint16_t* w3,
+                    uint16_t* w13, cudaStream_t stream) {
+  const int64_t rows = static_cast<int64_t>(G) * 2 * Mw;
+  if (rows == 0) return 0;
+  if (rows > 0x7fffffffLL) return -2;
+  pack_w13_kernel<<<static_cast<unsigned>(rows), 128, 0, stream>>>(Mw, d, w1, w3, w13);
+  return cudaGetLastError() == cudaSuccess ? 0 : -3;
+}
+
+int launch_timeout_probe(int* status, uint64_t timeout_ns, cudaStream_t stream) {
+  timeout_probe_kernel<<<1, 32, 0, stream>>>(status, timeout_ns);
+  return cudaGetLastError() == cudaSuccess ? 0 : -3;
+}
+
+}  // namespace moe

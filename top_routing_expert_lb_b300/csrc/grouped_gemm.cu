@@ -1,0 +1,382 @@
+// Ragged grouped GEMM on tcgen05 tensor cores for the expert FFNs.
+//
+// out_g = A_g * B_g^T for every group g, where the routed groups are the
+// experts (rows [offsets[e], offsets[e+1]) of the permuted activations, one
+// weight slice per expert) and an optional shared group covers every token
+// with the shared-expert weights.  This replaces the per-expert Python loop
+// over contiguous slices of the CSDN note's moe_infer (DeepseekV3MoE excerpt)
+// with one persistent kernel.  With `swiglu`, the first projection's
+// epilogue computes h = SiLU(W1 x) * (W3 x) ("深入理解 MoE" §10.2) from a
+// 256-column tile holding 128 gate and the matching 128 up columns.
+//
+// Design (sm_103a):
+//   * 192 threads: warp 0 = TMA producer, warp 1 = TMEM owner + MMA issuer,
+//     warps 2-5 = epilogue (warp w reads TMEM lanes 32*(w%4) .. +31).
+//   * 128 x BN x 64 tiles per stage, TMA with 128-byte swizzle, kStages-deep
+//     mbarrier ring (full: TMA bytes landed; empty: MMAs reading it retired).
+//   * Accumulators in TMEM, two buffers of BN fp32 columns so the epilogue of
+//     one tile overlaps the main loop of the next.
+//   * Persistent grid (one CTA per SM).  Tiles are numbered group by group,
+//     n-tile major / m-tile minor inside a group, so CTAs running at the same
+//     time share a weight tile through L2; row counts come from device
+//     offsets (no host synchronisation), ragged m-tiles are masked in the
+//     epilogue, and rows past a group's end are computed but never stored.
+//   * Every wait is bounded; on expiry the kernel records a timeout in the
+//     status word, drains its copies and MMAs, frees TMEM and returns.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdio>
+
+#include "moe_internal.h"
+#include "sm100_primitives.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kBK = 64;
+constexpr int kThreads = 192;
+constexpr int kMaxGroups = 257;
+
+struct GemmSmemTail {
+  uint64_t full[8];
+  uint64_t empty[8];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t fin;
+  uint32_t tmem_base;
+  int abort_flag;
+  int prefix[kMaxGroups + 1];
+  int row0[kMaxGroups];
+  int rows[kMaxGroups];
+};
+
+template <int BN, int kStages>
+constexpr size_t gemm_smem_bytes() {
+  return 1024 + static_cast<size_t>(kStages) * (kBM * kBK * 2 + BN * kBK * 2) +
+         sizeof(GemmSmemTail);
+}
+
+struct TileInfo {
+  int g;        // group (0 = shared when present)
+  int shared;   // 1 for the shared group
+  int a_row;    // first A / output row of the tile
+  int rows_left;  // valid rows in this tile (may exceed 128)
+  int b_row;    // first B row of the tile
+  int n;        // n-tile index within the group
+  int nk;       // K blocks
+};
+
+__device__ __forceinline__ TileInfo decode_tile(const GemmSmemTail* st, const GroupedGemmArgs& p,
+                                                int G, int tile, int bn) {
+  int lo = 0, hi = G;  // largest g with prefix[g] <= tile
+  while (hi - lo > 1) {
+    int mid = (lo + hi) >> 1;
+    if (st->prefix[mid] <= tile) lo = mid; else hi = mid;
+  }
+  TileInfo ti;
+  ti.g = lo;
+  const int has_shared = p.shared_rows > 0 ? 1 : 0;
+  ti.shared = (has_shared && lo == 0) ? 1 : 0;
+  const int rows = st->rows[lo];
+  const int mt = (rows + kBM - 1) / kBM;
+  const int local = tile - st->prefix[lo];
+  ti.n = local / mt;
+  const int m = local - ti.n * mt;
+  ti.a_row = st->row0[lo] + m * kBM;
+  ti.rows_left = rows - m * kBM;
+  const int ncols = ti.shared ? p.n_cols_shared : p.n_cols_routed;
+  const int e = lo - has_shared;
+  ti.b_row = (ti.shared ? 0 : e * ncols) + ti.n * bn;
+  ti.nk = (ti.shared ? p.k_shared : p.k_routed) / kBK;
+  return ti;
+}
+
+template <int BN, bool kSwiGLU, int kStages>
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
+                        const __grid_constant__ CUtensorMap tmA1,
+                        const __grid_constant__ CUtensorMap tmB0,
+                        const __grid_constant__ CUtensorMap tmB1, const GroupedGemmArgs p) {
+  static_assert(!kSwiGLU || BN == 256, "SwiGLU tiles pair 128 gate with 128 up columns");
+  constexpr int kABytes = kBM * kBK * 2;
+  constexpr int kBBytes = BN * kBK * 2;
+  constexpr int kStageBytes = kABytes + kBBytes;
+  constexpr uint32_t kTmemCols = 2 * BN;
+  constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, BN);
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+  uint8_t* smem = smem_raw + pad;
+  GemmSmemTail* st = reinterpret_cast<GemmSmemTail*>(smem + kStages * kStageBytes);
+  volatile int* abort_flag = &st->abort_flag;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int has_shared = p.shared_rows > 0 ? 1 : 0;
+  const int G = p.n_routed + has_shared;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&st->full[s], 1);
+      mbar_init(&st->empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&st->tfull[a], 1);
+      mbar_init(&st->tempty[a], 4);
+    }
+    mbar_init(&st->fin, 1);
+    st->abort_flag = 0;
+    int acc = 0;
+    st->prefix[0] = 0;
+    for (int g = 0; g < G; ++g) {
+      const int sh = (has_shared && g == 0);
+      int r0, rows;
+      if (sh) {
+        r0 = 0;
+        rows = p.shared_rows;
+      } else {
+        const int e = g - has_shared;
+        r0 = p.offsets[e];
+        rows = p.offsets[e + 1] - r0;
+        if (rows < 0) rows = 0;
+      }
+      st->row0[g] = r0;
+      st->rows[g] = rows;
+      const int ncols = sh ? p.n_cols_shared : p.n_cols_routed;
+      acc += ((rows + kBM - 1) / kBM) * (ncols / BN);
+      st->prefix[g + 1] = acc;
+    }
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA0);
+    tma_prefetch_desc(&tmA1);
+    tma_prefetch_desc(&tmB0);
+    tma_prefetch_desc(&tmB1);
+  }
+  if (warp == 1) tmem_alloc(&st->tmem_base, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = st->tmem_base;
+  const int total = st->prefix[G];
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t uses[kStages];
+#pragma unroll
+      for (int s = 0; s < kStages; ++s) uses[s] = 0;
+      for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x) {
+        const TileInfo ti = decode_tile(st, p, G, tile, BN);
+        const CUtensorMap* am = ti.shared ? &tmA1 : &tmA0;
+        const CUtensorMap* bm = ti.shared ? &tmB1 : &tmB0;
+        bool ok = true;
+        for (int kb = 0; kb < ti.nk; ++kb) {
+          if (!mbar_wait_bounded(&st->empty[stage], phase ^ 1u, p.timeout_ns, p.status,
+                                 abort_flag)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sa = smem + stage * kStageBytes;
+          mbar_arrive_expect_tx(&st->full[stage], kStageBytes);
+          tma_load_2d(sa, am, &st->full[stage], kb * kBK, ti.a_row);
+          tma_load_2d(sa + kABytes, bm, &st->full[stage], kb * kBK, ti.b_row);
+          uses[stage] += 1;
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+      }
+      // Drain: the last copy issued into each stage must have landed before
+      // the CTA may exit.
+#pragma unroll
+      for (int s = 0; s < kStages; ++s)
+        if (uses[s] > 0)
+          mbar_wait_bounded(&st->full[s], (uses[s] - 1u) & 1u, p.timeout_ns, p.status, nullptr);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int local = 0;
+      for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x, ++local) {
+        const TileInfo ti = decode_tile(st, p, G, tile, BN);
+        const int a = local & 1;
+        const uint32_t q = static_cast<uint32_t>(local >> 1);
+        if (!mbar_wait_bounded(&st->tempty[a], (q & 1u) ^ 1u, p.timeout_ns, p.status,
+                               abort_flag))
+          break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(a * BN);
+        bool ok = true;
+        for (int kb = 0; kb < ti.nk; ++kb) {
+          if (!mbar_wait_bounded(&st->full[stage], phase, p.timeout_ns, p.status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + stage * kStageBytes);
+          const uint32_t sb = sa + kABytes;
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            tc_mma_bf16(d_tmem, smem_desc_sw128(sa + kk * 32), smem_desc_sw128(sb + kk * 32),
+                        kIdesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          tc_commit(&st->empty[stage]);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit(&st->tfull[a]);
+      }
+      // Every MMA issued by this thread must retire before TMEM is freed.
+      tc_commit(&st->fin);
+      mbar_wait_bounded(&st->fin, 0, p.timeout_ns, p.status, nullptr);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
+    const int r_in_tile = quarter * 32 + lane;
+    int local = 0;
+    for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x, ++local) {
+      const TileInfo ti = decode_tile(st, p, G, tile, BN);
+      const int a = local & 1;
+      const uint32_t q = static_cast<uint32_t>(local >> 1);
+      if (!mbar_wait_bounded(&st->tfull[a], q & 1u, p.timeout_ns, p.status, abort_flag)) break;
+      tc_fence_after();
+      const bool valid = r_in_tile < ti.rows_left;
+      const int64_t row = static_cast<int64_t>(ti.a_row) + r_in_tile;
+      const uint32_t taddr =
+          tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(a * BN);
+      __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(ti.shared ? p.out_shared
+                                                                      : p.out_routed);
+      const int64_t ld = ti.shared ? p.ld_shared : p.ld_routed;
+      if constexpr (kSwiGLU) {
+        __nv_bfloat16* dst = out + row * ld + static_cast<int64_t>(ti.n) * 128;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          float g[32], u[32];
+          tmem_ld32(taddr + c * 32, g);
+          tmem_ld32(taddr + 128 + c * 32, u);
+          tmem_ld_wait();
+          uint32_t packed[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            packed[i] = pack_bf16x2(silu_f32(g[2 * i]) * u[2 * i],
+                                    silu_f32(g[2 * i + 1]) * u[2 * i + 1]);
+          if (valid) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              d4[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
+                                 packed[4 * i + 3]);
+          }
+        }
+      } else {
+        __nv_bfloat16* dst = out + row * ld + static_cast<int64_t>(ti.n) * BN;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          float v[32];
+          tmem_ld32(taddr + c * 32, v);
+          tmem_ld_wait();
+          uint32_t packed[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) packed[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+          if (valid) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              d4[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
+                                 packed[4 * i + 3]);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&st->tempty[a]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
+}
+
+template <int BN, bool kSwiGLU, int kStages>
+int launch_impl(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b0,
+                const CUtensorMap& b1, const GroupedGemmArgs& args, int num_sms,
+                cudaStream_t stream) {
+  constexpr size_t smem = gemm_smem_bytes<BN, kStages>();
+  static_assert(smem <= 227 * 1024, "shared memory budget");
+  auto kern = grouped_gemm_kernel<BN, kSwiGLU, kStages>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess)
+      return -3;
+    attr_set = true;
+  }
+  kern<<<num_sms, kThreads, smem, stream>>>(a0, a1, b0, b1, args);
+  return cudaGetLastError() == cudaSuccess ? 0 : -3;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+}  // namespace
+
+bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                    uint32_t box_rows) {
+  auto encode = get_encode_fn();
+  if (encode == nullptr || rows == 0 || cols == 0) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int launch_grouped_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b0,
+                        const CUtensorMap& b1, const GroupedGemmArgs& args, bool swiglu, int bn,
+                        int num_sms, cudaStream_t stream) {
+  if (args.n_routed + (args.shared_rows > 0 ? 1 : 0) > kMaxGroups) return -2;
+  if (swiglu) {
+    if (bn != 256) return -2;
+    return launch_impl<256, true, 4>(a0, a1, b0, b1, args, num_sms, stream);
+  }
+  switch (bn) {
+    case 256: return launch_impl<256, false, 4>(a0, a1, b0, b1, args, num_sms, stream);
+    case 128: return launch_impl<128, false, 6>(a0, a1, b0, b1, args, num_sms, stream);
+    case 64: return launch_impl<64, false, 8>(a0, a1, b0, b1, args, num_sms, stream);
+    default: return -2;
+  }
+}
+
+}  // namespace moe

@@ -1,0 +1,109 @@
+// Internal launcher interfaces shared by the .cu files of libmoe_b300.so.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+namespace moe {
+
+constexpr int kTileTokens = 128;  // tokens per router / permute tile (= MMA M)
+constexpr int kMaxTopK = 8;
+
+// Ragged grouped GEMM  out[g] = A[g] * B[g]^T  over E routed groups (rows from
+// device offsets) and an optional shared group (fixed row count).
+struct GroupedGemmArgs {
+  const int32_t* offsets;  // [E+1] device, routed group row ranges in A0 / out0
+  int32_t n_routed;        // number of routed groups (0 if none)
+  int32_t shared_rows;     // rows of the shared group (0 = no shared group)
+  int32_t n_cols_routed;   // N of every routed group
+  int32_t n_cols_shared;   // N of the shared group
+  int32_t k_routed;        // K of the routed groups (multiple of 64)
+  int32_t k_shared;        // K of the shared group (multiple of 64)
+  void* out_routed;        // bf16 [rows][ld_routed]
+  int64_t ld_routed;
+  void* out_shared;        // bf16 [shared_rows][ld_shared]
+  int64_t ld_shared;
+  int* status;             // device status word
+  uint64_t timeout_ns;
+};
+
+// A0/A1: activations [rows][K] (routed / shared), B0/B1: weights [rows][K].
+// swiglu: epilogue writes h = SiLU(acc[:, :128]) * acc[:, 128:] per 256-wide
+// tile (packed gate/up weights); else writes acc as bf16.
+int launch_grouped_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b0,
+                        const CUtensorMap& b1, const GroupedGemmArgs& args, bool swiglu, int bn,
+                        int num_sms, cudaStream_t stream);
+
+// Encodes a 2-D bf16 tensor map over a row-major [rows][cols] tensor with a
+// 64-column x box_rows box and 128-byte swizzle.  Returns false on failure.
+bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                    uint32_t box_rows);
+
+// Router: logits tile GEMM + softmax / bias / Top-k epilogue (one CTA per
+// 128 tokens).  Writes ids, gates and per-tile partials.
+struct RouterArgs {
+  int32_t T, d, E, k;
+  const float* logit_offset;  // [E] or null
+  const float* sel_bias;      // [E] or null
+  int32_t* ids;               // [T][k]
+  float* gates;               // [T][k]
+  int32_t* tile_hist;         // [ntiles][E]
+  float* tile_psum;           // [ntiles][E]
+  float* tile_lse2;           // [ntiles]
+  int* status;
+  uint64_t timeout_ns;
+};
+int launch_router(const CUtensorMap& x_map, const CUtensorMap& wr_map, const RouterArgs& args,
+                  cudaStream_t stream);
+
+// Per-tile expert histogram of ids (when the router did not produce it).
+int launch_tile_hist(const int32_t* ids, int32_t T, int32_t k, int32_t E, int32_t* tile_hist,
+                     cudaStream_t stream);
+
+// Reduces the per-tile partials: counts, f, P, losses (optional) and the
+// permutation scan (offsets of kept rows, per-tile bases).
+struct FinalizeArgs {
+  int32_t T, E, k;
+  int64_t C;                  // capacity or -1
+  float balance_coef;
+  const int32_t* tile_hist;   // [ntiles][E]
+  const float* tile_psum;     // [ntiles][E] or null (no losses)
+  const float* tile_lse2;     // [ntiles] or null
+  int32_t* counts;            // [E] or null
+  float* f;                   // [E] or null
+  float* P;                   // [E] or null
+  float* bal_loss;            // [1] or null
+  float* z_loss;              // [1] or null
+  int32_t* tile_base;         // [ntiles][E] or null (no scan)
+  int32_t* offsets;           // [E+1] or null
+};
+int launch_finalize(const FinalizeArgs& args, cudaStream_t stream);
+
+// Capacity cut + permutation + row gather, one CTA per 128-token tile.
+struct ScatterArgs {
+  int32_t T, d, E, k;
+  int64_t C;
+  const int32_t* ids;        // [T][k]
+  const int32_t* tile_base;  // [ntiles][E]
+  const int32_t* offsets;    // [E+1]
+  const uint16_t* x;         // [T][d]
+  int32_t* slot_row;         // [T][k]
+  int32_t* row_token;        // [R_max]
+  uint8_t* drop_mask;        // [T][k] or null
+  uint16_t* x_perm;          // [R_max][d]
+};
+int launch_scatter(const ScatterArgs& args, cudaStream_t stream);
+
+int launch_combine(int32_t T, int32_t d, int32_t k, const uint16_t* y_perm,
+                   const int32_t* slot_row, const float* gates, const uint16_t* y_shared,
+                   uint16_t* y, cudaStream_t stream);
+
+int launch_pack_w13(int32_t G, int32_t Mw, int32_t d, const uint16_t* w1, const uint16_t* w3,
+                    uint16_t* w13, cudaStream_t stream);
+
+int launch_timeout_probe(int* status, uint64_t timeout_ns, cudaStream_t stream);
+
+int device_sm_count();
+
+}  // namespace moe
