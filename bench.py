@@ -214,11 +214,15 @@ def run_reference(args, w):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
+    import torch
+
     import synth
     import oracle
     oracle.load()
-    inp = synth.make_inputs(w, "cpu")
+    # inputs are drawn on the GPU when there is one (faster), then copied to the host
+    inp = synth.make_inputs(w, "cuda" if torch.cuda.is_available() else "cpu")
     h = _host_inputs(inp)
+    del inp
     cores = cpu_cores()
     t1 = oracle_tokens(w, h, 0, min(w.T, cores))
     per_tok_round = max(t1, 1e-3)

@@ -75,6 +75,30 @@ def run_layer(inp: synth.Inputs, layer: Optional[moe.MoELayer] = None) -> GpuOut
                   float(layer.losses[0]), float(layer.losses[1]))
 
 
+def routing_force_mask(free: oracle.Routing, gpu_ids: np.ndarray, bias) -> np.ndarray:
+    """Tokens whose GPU selection may be taken over by the oracle.
+
+    The selected set is unique unless the k-th and (k+1)-th keys are within
+    1e-5 (near tie at the cut): such tokens are exempt.  Inside the set, the
+    order of two keys closer than 1e-5 is not unique either; there the GPU's
+    order is accepted after checking that it is descending in the oracle's
+    keys up to 1e-5.  Any other difference fails.  (Slot order inside one
+    token cannot change drops or rows: a token sends at most one pair to an
+    expert.)"""
+    key = free.p + (0.0 if bias is None else np.asarray(bias, np.float64)[None, :])
+    exempt = free.gap < TIE
+    diff = np.any(free.ids != gpu_ids, axis=1)
+    bad = []
+    for t in np.nonzero(diff & ~exempt)[0]:
+        same_set = sorted(free.ids[t].tolist()) == sorted(gpu_ids[t].tolist())
+        kg = key[t, gpu_ids[t]]
+        if not (same_set and np.all(np.diff(kg) <= TIE)):
+            bad.append(t)
+    assert not bad, (f"{len(bad)} non-tie tokens routed differently, e.g. token {bad[0]}: "
+                     f"gpu {gpu_ids[bad[0]]} oracle {free.ids[bad[0]]} gap {free.gap[bad[0]]}")
+    return diff | exempt
+
+
 @dataclass
 class OracleRef:
     routing: oracle.Routing
@@ -95,11 +119,9 @@ def oracle_routing(inp: synth.Inputs, gpu_ids: np.ndarray) -> OracleRef:
     free = oracle.route(logits, w.k, bias)
     exempt = free.gap < TIE
     if w.k > 0:
-        bad = np.nonzero(np.any(free.ids != gpu_ids, axis=1) & ~exempt)[0]
-        assert len(bad) == 0, (f"{len(bad)} non-tie tokens routed differently, e.g. token "
-                               f"{bad[0]}: gpu {gpu_ids[bad[0]]} oracle {free.ids[bad[0]]} "
-                               f"gap {free.gap[bad[0]]}")
-        r = oracle.route(logits, w.k, bias, force_ids=gpu_ids, force_mask=exempt)
+        force = routing_force_mask(free, gpu_ids, bias)
+        r = oracle.route(logits, w.k, bias, force_ids=gpu_ids, force_mask=force)
+        exempt = force
     else:
         r = free
     C = oracle.capacity(float(np.float32(w.capacity_factor)), w.k, w.T, w.E)

@@ -50,6 +50,19 @@ def test_layer_parity(name):
         assert ref.disp.dropped.any(), "capacity case should drop pairs"
 
 
+@pytest.mark.parametrize("name", ["ragged_shared", "capacity_k4", "fine_bias_shared",
+                                  "k0_shared_only", "E1_k1_dense", "wide_E160"])
+def test_layer_parity_paired_tiles(name, monkeypatch):
+    """The same cases with the expert GEMMs forced onto 256-row CTA-pair tiles."""
+    monkeypatch.setenv("MOE_GEMM_TILE", "256")
+    inp = synth.make_inputs(CASES[name], "cuda")
+    g, ref = check_layer(inp)
+    if name == "k0_no_experts":
+        assert torch.count_nonzero(g.y) == 0
+    if CASES[name].capacity_factor > 0:
+        assert ref.disp.dropped.any(), "capacity case should drop pairs"
+
+
 def test_one_expert_takes_every_row():
     w = W("hot", T=333, d=128, E=8, k=1, M=128, n_shared=0)
     inp = synth.make_inputs(w, "cuda")

@@ -105,14 +105,18 @@ def test_permute(T, E, k, c, d):
 
 
 # --------------------------------------------------------------------------- grouped FFN
+@pytest.mark.parametrize("tile", ["128", "256"])
 @pytest.mark.parametrize("rows,d,M,n_shared,T", [
     ([0, 1, 127, 128, 129, 300], 128, 256, 1, 200),    # empty, single, tile edges
     ([5, 0, 0, 260], 64, 128, 0, 0),                   # d = 64 (second projection N = 64)
     ([130, 70, 2], 256, 128, 2, 131),                  # d = 256, 2 shared experts
     ([0, 0, 0], 192, 128, 1, 77),                      # routed rows all empty, shared only
     ([400], 320, 384, 0, 0),                           # one group, d = 320 (N tile 64)
+    ([255, 256, 257, 511, 1], 512, 256, 1, 300),       # 256-row tile edges, d = 512
 ])
-def test_grouped_ffn(rows, d, M, n_shared, T):
+def test_grouped_ffn(rows, d, M, n_shared, T, tile, monkeypatch):
+    # 128: single-CTA 128-row tiles; 256: CTA-pair 256-row tiles
+    monkeypatch.setenv("MOE_GEMM_TILE", tile)
     E = len(rows)
     R = int(sum(rows))
     Ms = n_shared * M

@@ -5,6 +5,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <vector>
 
@@ -61,7 +62,8 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 
 // Workspace regions (byte offsets from the workspace base).
 struct Layout {
-  size_t status, tile_hist, tile_psum, tile_lse2, tile_base, offsets, slot_row, row_token;
+  size_t status, tile_hist, tile_psum, tile_lse2, tile_base, exp_count, exp_psum, offsets;
+  size_t slot_row, row_token;
   size_t x_perm, h, y_perm, h_s, y_s, total;
   int64_t ntiles, rmax, C;
 };
@@ -109,6 +111,8 @@ Layout layout_of(const moe_shape_t* s) {
   L.tile_psum = take(L.ntiles * E * 4);
   L.tile_lse2 = take(L.ntiles * 4);
   L.tile_base = take(L.ntiles * E * 4);
+  L.exp_count = take(E * 4);
+  L.exp_psum = take(E * 8);
   L.offsets = take((E + 1) * 4);
   L.slot_row = take(T * k * 4);
   L.row_token = take(L.rmax * 4);
@@ -177,7 +181,7 @@ int do_route(const moe_shape_t* s, const uint16_t* x, const uint16_t* wr, const 
     ra.tile_lse2 = at<float>(ws, L.tile_lse2);
     ra.status = at<int>(ws, L.status);
     ra.timeout_ns = g_timeout_ns;
-    const int rc = tracked(MOE_KERNEL_ROUTER, st, [&] { return launch_router(mx, mw, ra, st); });
+    const int rc = tracked(MOE_KERNEL_ROUTER, st, [&] { return launch_router(mx, mw, ra, sm_count_cached(), st); });
     if (rc != 0) return cuda_rc(rc);
   }
   FinalizeArgs fa{};
@@ -196,6 +200,9 @@ int do_route(const moe_shape_t* s, const uint16_t* x, const uint16_t* wr, const 
   fa.z_loss = z;
   fa.tile_base = tile_base;
   fa.offsets = offsets;
+  fa.exp_count = at<int32_t>(ws, L.exp_count);
+  fa.exp_psum = at<double>(ws, L.exp_psum);
+  fa.done_counter = at<int>(ws, L.status + 64);
   return cuda_rc(tracked(MOE_KERNEL_FINALIZE, st, [&] { return launch_finalize(fa, st); }));
 }
 
@@ -216,6 +223,7 @@ int do_scatter(const moe_shape_t* s, const uint16_t* x, const int32_t* ids, cons
   sa.row_token = row_token;
   sa.drop_mask = drop_mask;
   sa.x_perm = x_perm;
+  sa.num_sms = sm_count_cached();
   return cuda_rc(tracked(MOE_KERNEL_SCATTER, st, [&] { return launch_scatter(sa, st); }));
 }
 
@@ -232,16 +240,24 @@ int do_ffn(const moe_shape_t* s, const uint16_t* x_perm, const int32_t* offsets,
   uint16_t* h_s = at<uint16_t>(ws, L.h_s);
   const int bn2 = (d % 256 == 0) ? 256 : (d % 128 == 0 ? 128 : 64);
   const int nsm = sm_count_cached();
+  // 128-row tiles on single CTAs by default (measured faster on every
+  // workload so far); 256-row tiles on CTA pairs with MOE_GEMM_TILE=256.
+  bool paired = false;
+  if (const char* env = std::getenv("MOE_GEMM_TILE")) {
+    if (std::strcmp(env, "128") == 0) paired = false;
+    if (std::strcmp(env, "256") == 0) paired = true;
+  }
+  const uint32_t bbox = paired ? 128u : 256u;
 
   // projection 1: [x_perm | x] -> h = SiLU(gate) * up
   CUtensorMap a0, a1, b0, b1;
   if (routed) {
     if (!make_tmap_bf16(&a0, x_perm, L.rmax, d, 128)) return MOE_ERR_CUDA;
-    if (!make_tmap_bf16(&b0, w13, E * 2 * M, d, 256)) return MOE_ERR_CUDA;
+    if (!make_tmap_bf16(&b0, w13, E * 2 * M, d, bbox)) return MOE_ERR_CUDA;
   }
   if (shared) {
     if (!make_tmap_bf16(&a1, x, T, d, 128)) return MOE_ERR_CUDA;
-    if (!make_tmap_bf16(&b1, w13s, 2 * Ms, d, 256)) return MOE_ERR_CUDA;
+    if (!make_tmap_bf16(&b1, w13s, 2 * Ms, d, bbox)) return MOE_ERR_CUDA;
   }
   if (!routed) { a0 = a1; b0 = b1; }
   if (!shared) { a1 = a0; b1 = b0; }
@@ -260,17 +276,19 @@ int do_ffn(const moe_shape_t* s, const uint16_t* x_perm, const int32_t* offsets,
   g1.status = at<int>(ws, L.status);
   g1.timeout_ns = g_timeout_ns;
   int rc = tracked(MOE_KERNEL_GEMM_SWIGLU, st,
-                   [&] { return launch_grouped_gemm(a0, a1, b0, b1, g1, true, 256, nsm, st); });
+                   [&] { return launch_grouped_gemm(a0, a1, b0, b1, g1, true, 256, paired, nsm, st); });
   if (rc != 0) return cuda_rc(rc);
 
   // projection 2: [h | h_s] -> [y_perm | y_s]
+  const bool paired2 = paired && bn2 == 256;
+  const uint32_t bbox2 = paired2 ? 128u : static_cast<uint32_t>(bn2);
   if (routed) {
     if (!make_tmap_bf16(&a0, h, L.rmax, M, 128)) return MOE_ERR_CUDA;
-    if (!make_tmap_bf16(&b0, w2, E * d, M, static_cast<uint32_t>(bn2))) return MOE_ERR_CUDA;
+    if (!make_tmap_bf16(&b0, w2, E * d, M, bbox2)) return MOE_ERR_CUDA;
   }
   if (shared) {
     if (!make_tmap_bf16(&a1, h_s, T, Ms, 128)) return MOE_ERR_CUDA;
-    if (!make_tmap_bf16(&b1, w2s, d, Ms, static_cast<uint32_t>(bn2))) return MOE_ERR_CUDA;
+    if (!make_tmap_bf16(&b1, w2s, d, Ms, bbox2)) return MOE_ERR_CUDA;
   }
   if (!routed) { a0 = a1; b0 = b1; }
   if (!shared) { a1 = a0; b1 = b0; }
@@ -284,7 +302,7 @@ int do_ffn(const moe_shape_t* s, const uint16_t* x_perm, const int32_t* offsets,
   g2.out_shared = y_s;
   g2.ld_shared = d;
   rc = tracked(MOE_KERNEL_GEMM_DOWN, st,
-               [&] { return launch_grouped_gemm(a0, a1, b0, b1, g2, false, bn2, nsm, st); });
+               [&] { return launch_grouped_gemm(a0, a1, b0, b1, g2, false, bn2, paired2, nsm, st); });
   return cuda_rc(rc);
 }
 
@@ -387,6 +405,9 @@ int moe_permute(const moe_shape_t* s, const uint16_t* x, const int32_t* ids, int
   fa.tile_hist = tile_hist;
   fa.tile_base = at<int32_t>(ws, L.tile_base);
   fa.offsets = offsets;
+  fa.exp_count = at<int32_t>(ws, L.exp_count);
+  fa.exp_psum = at<double>(ws, L.exp_psum);
+  fa.done_counter = at<int>(ws, L.status + 64);
   if ((rc = cuda_rc(tracked(MOE_KERNEL_FINALIZE, st, [&] { return launch_finalize(fa, st); }))) !=
       MOE_OK)
     return rc;

@@ -41,40 +41,57 @@ __device__ __forceinline__ void add_bf16x8(float (&acc)[8], const uint4 v) {
   }
 }
 
+template <int K>
 __global__ void __launch_bounds__(kCombineWarps * 32)
-    combine_kernel(int32_t T, int32_t d, int32_t k, const uint16_t* __restrict__ y_perm,
+    combine_kernel(int32_t T, int32_t d, const uint16_t* __restrict__ y_perm,
                    const int32_t* __restrict__ slot_row, const float* __restrict__ gates,
                    const uint16_t* __restrict__ y_shared, uint16_t* __restrict__ y) {
+  // vectors per lane per iteration: about 8 loads of 16 bytes in flight
+  constexpr int U = (K + 1) >= 8 ? 1 : 8 / (K + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * kCombineWarps + warp;
   if (t >= T) return;
-  int rows[kMaxTopK];
-  float g[kMaxTopK];
+  int rows[K > 0 ? K : 1];
+  float g[K > 0 ? K : 1];
 #pragma unroll
-  for (int s = 0; s < kMaxTopK; ++s) {
-    rows[s] = (s < k) ? slot_row[static_cast<int64_t>(t) * k + s] : -1;
-    g[s] = (s < k) ? gates[static_cast<int64_t>(t) * k + s] : 0.0f;
+  for (int s = 0; s < K; ++s) {
+    rows[s] = slot_row[static_cast<int64_t>(t) * K + s];
+    g[s] = gates[static_cast<int64_t>(t) * K + s];
   }
   const int nvec = d / 8;
   const uint4* ys = y_shared ? reinterpret_cast<const uint4*>(y_shared +
                                                               static_cast<int64_t>(t) * d)
                              : nullptr;
   uint4* out = reinterpret_cast<uint4*>(y + static_cast<int64_t>(t) * d);
-  for (int v = lane; v < nvec; v += 32) {
-    float acc[8];
+  for (int v0 = lane; v0 < nvec; v0 += 32 * U) {
+    uint4 val[U][K > 0 ? K : 1];
+    uint4 sv[U];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+    for (int u = 0; u < U; ++u) {
+      const int v = v0 + 32 * u;
+      if (v < nvec) {
 #pragma unroll
-    for (int s = 0; s < kMaxTopK; ++s) {
-      if (rows[s] >= 0) {
-        const uint4 val =
-            reinterpret_cast<const uint4*>(y_perm + static_cast<int64_t>(rows[s]) * d)[v];
-        acc_bf16x8(acc, val, g[s]);
+        for (int s = 0; s < K; ++s)
+          if (rows[s] >= 0)
+            val[u][s] = __ldg(reinterpret_cast<const uint4*>(
+                                  y_perm + static_cast<int64_t>(rows[s]) * d) + v);
+        if (ys) sv[u] = __ldg(ys + v);
       }
     }
-    if (ys) add_bf16x8(acc, ys[v]);
-    out[v] = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
-                        pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int v = v0 + 32 * u;
+      if (v >= nvec) continue;
+      float acc[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+#pragma unroll
+      for (int s = 0; s < K; ++s)
+        if (rows[s] >= 0) acc_bf16x8(acc, val[u][s], g[s]);
+      if (ys) add_bf16x8(acc, sv[u]);
+      out[v] = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                          pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+    }
   }
 }
 
@@ -112,8 +129,19 @@ int launch_combine(int32_t T, int32_t d, int32_t k, const uint16_t* y_perm,
                    uint16_t* y, cudaStream_t stream) {
   if (T == 0) return 0;
   const int grid = (T + kCombineWarps - 1) / kCombineWarps;
-  combine_kernel<<<grid, kCombineWarps * 32, 0, stream>>>(T, d, k, y_perm, slot_row, gates,
-                                                           y_shared, y);
+  const dim3 b(kCombineWarps * 32);
+  switch (k) {
+    case 0: combine_kernel<0><<<grid, b, 0, stream>>>(T, d, y_perm, slot_row, gates, y_shared, y); break;
+    case 1: combine_kernel<1><<<grid, b, 0, stream>>>(T, d, y_perm, slot_row, gates, y_shared, y); break;
+    case 2: combine_kernel<2><<<grid, b, 0, stream>>>(T, d, y_perm, slot_row, gates, y_shared, y); break;
+    case 3: combine_kernel<3><<<grid, b, 0, stream>>>(T, d, y_perm, slot_row, gates, y_shared, y); break;
+    case 4: combine_kernel<4><<<grid, b, 0, stream>>>(T, d, y_perm, slot_row, gates, y_shared, y); break;
+    case 5: combine_kernel<5><<<grid, b, 0, stream>>>(T, d, y_perm, slot_row, gates, y_shared, y); break;
+    case 6: combine_kernel<6><<<grid, b, 0, stream>>>(T, d, y_perm, slot_row, gates, y_shared, y); break;
+    case 7: combine_kernel<7><<<grid, b, 0, stream>>>(T, d, y_perm, slot_row, gates, y_shared, y); break;
+    case 8: combine_kernel<8><<<grid, b, 0, stream>>>(T, d, y_perm, slot_row, gates, y_shared, y); break;
+    default: return -2;
+  }
   return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }
 

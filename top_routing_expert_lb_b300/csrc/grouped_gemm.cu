@@ -70,8 +70,9 @@ struct TileInfo {
   int nk;       // K blocks
 };
 
-__device__ __forceinline__ TileInfo decode_tile(const GemmSmemTail* st, const GroupedGemmArgs& p,
-                                                int G, int tile, int bn) {
+template <typename Tail>
+__device__ __forceinline__ TileInfo decode_tile(const Tail* st, const GroupedGemmArgs& p, int G,
+                                                int tile, int bn, int bm = kBM) {
   int lo = 0, hi = G;  // largest g with prefix[g] <= tile
   while (hi - lo > 1) {
     int mid = (lo + hi) >> 1;
@@ -82,12 +83,12 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmSmemTail* st, const Gr
   const int has_shared = p.shared_rows > 0 ? 1 : 0;
   ti.shared = (has_shared && lo == 0) ? 1 : 0;
   const int rows = st->rows[lo];
-  const int mt = (rows + kBM - 1) / kBM;
+  const int mt = (rows + bm - 1) / bm;
   const int local = tile - st->prefix[lo];
   ti.n = local / mt;
   const int m = local - ti.n * mt;
-  ti.a_row = st->row0[lo] + m * kBM;
-  ti.rows_left = rows - m * kBM;
+  ti.a_row = st->row0[lo] + m * bm;
+  ti.rows_left = rows - m * bm;
   const int ncols = ti.shared ? p.n_cols_shared : p.n_cols_routed;
   const int e = lo - has_shared;
   ti.b_row = (ti.shared ? 0 : e * ncols) + ti.n * bn;
@@ -315,6 +316,306 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
 }
 
+
+// ---------------------------------------------------------------------------
+// Paired (2-SM) variant: a cluster of two CTAs computes 256 x 256 tiles with
+// tcgen05 cta_group::2.  Each CTA stages its 128 rows of A and its 128 rows of
+// B (half of N) per k-block, so one SM moves 32 KB per 64-deep k-block instead
+// of 48 KB and the ring holds 6 stages.  The even CTA issues the MMAs; its
+// full barrier collects the TMA bytes of both CTAs; MMA completion is
+// multicast to the empty / accumulator-full barriers of both CTAs; both CTAs'
+// epilogue warps release an accumulator buffer on the even CTA's barrier.
+// ---------------------------------------------------------------------------
+constexpr int kPairBM = 256;
+constexpr int kPairStages = 6;
+
+struct PairSmemTail {
+  uint64_t full[kPairStages];
+  uint64_t empty[kPairStages];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t fin;
+  uint32_t tmem_base;
+  int abort_flag;
+  int prefix[kMaxGroups + 1];
+  int row0[kMaxGroups];
+  int rows[kMaxGroups];
+};
+
+constexpr size_t pair_smem_bytes() {
+  return 1024 + static_cast<size_t>(kPairStages) * (128 * kBK * 2 + 128 * kBK * 2) +
+         sizeof(PairSmemTail);
+}
+
+template <bool kSwiGLU>
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA0,
+                             const __grid_constant__ CUtensorMap tmA1,
+                             const __grid_constant__ CUtensorMap tmB0,
+                             const __grid_constant__ CUtensorMap tmB1, const GroupedGemmArgs p) {
+  constexpr int BN = 256;                 // N of the pair tile
+  constexpr int kABytes = 128 * kBK * 2;  // this CTA's A rows
+  constexpr int kBBytes = 128 * kBK * 2;  // this CTA's half of B
+  constexpr int kStageBytes = kABytes + kBBytes;
+  constexpr uint32_t kTmemCols = 2 * BN;
+  constexpr uint32_t kIdesc = idesc_bf16_f32(kPairBM, BN);
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+  uint8_t* smem = smem_raw + pad;
+  PairSmemTail* st = reinterpret_cast<PairSmemTail*>(smem + kPairStages * kStageBytes);
+  volatile int* abort_flag = &st->abort_flag;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();  // 0 = even CTA (issues the MMAs)
+  const bool leader = rank == 0;
+  const int pair = blockIdx.x >> 1;
+  const int npairs = gridDim.x >> 1;
+  const int has_shared = p.shared_rows > 0 ? 1 : 0;
+  const int G = p.n_routed + has_shared;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kPairStages; ++s) {
+      mbar_init(&st->full[s], 1);
+      mbar_init(&st->empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&st->tfull[a], 1);
+      mbar_init(&st->tempty[a], 8);  // 4 epilogue warps in each CTA of the pair
+    }
+    mbar_init(&st->fin, 1);
+    st->abort_flag = 0;
+    int acc = 0;
+    st->prefix[0] = 0;
+    for (int g = 0; g < G; ++g) {
+      const int sh = (has_shared && g == 0);
+      int r0, rows;
+      if (sh) {
+        r0 = 0;
+        rows = p.shared_rows;
+      } else {
+        const int e = g - has_shared;
+        r0 = p.offsets[e];
+        rows = p.offsets[e + 1] - r0;
+        if (rows < 0) rows = 0;
+      }
+      st->row0[g] = r0;
+      st->rows[g] = rows;
+      const int ncols = sh ? p.n_cols_shared : p.n_cols_routed;
+      acc += ((rows + kPairBM - 1) / kPairBM) * (ncols / BN);
+      st->prefix[g + 1] = acc;
+    }
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA0);
+    tma_prefetch_desc(&tmA1);
+    tma_prefetch_desc(&tmB0);
+    tma_prefetch_desc(&tmB1);
+  }
+  if (warp == 1) tmem_alloc_pair(&st->tmem_base, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  cluster_arrive_wait();  // both CTAs' barriers initialised before any remote signal
+  tc_fence_after();
+  const uint32_t tmem_base = st->tmem_base;
+  const int total = st->prefix[G];
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t uses[kPairStages];
+#pragma unroll
+      for (int s = 0; s < kPairStages; ++s) uses[s] = 0;
+      for (int tile = pair; tile < total && !*abort_flag; tile += npairs) {
+        const TileInfo ti = decode_tile(st, p, G, tile, BN, kPairBM);
+        const CUtensorMap* am = ti.shared ? &tmA1 : &tmA0;
+        const CUtensorMap* bm = ti.shared ? &tmB1 : &tmB0;
+        const int a_row = ti.a_row + static_cast<int>(rank) * 128;
+        const int b_row = ti.b_row + static_cast<int>(rank) * 128;
+        bool ok = true;
+        for (int kb = 0; kb < ti.nk; ++kb) {
+          if (!mbar_wait_bounded(&st->empty[stage], phase ^ 1u, p.timeout_ns, p.status,
+                                 abort_flag)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sa = smem + stage * kStageBytes;
+          const uint32_t full_leader = mapa_shared(smem_u32(&st->full[stage]), 0);
+          if (leader) mbar_arrive_expect_tx(&st->full[stage], 2 * kStageBytes);
+          tma_load_2d_pair(sa, am, full_leader, kb * kBK, a_row);
+          tma_load_2d_pair(sa + kABytes, bm, full_leader, kb * kBK, b_row);
+          uses[stage] += 1;
+          if (++stage == kPairStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+      }
+      // Drain (even CTA): its full barriers count the bytes of both CTAs, so
+      // this covers every copy of the pair; the odd CTA stays alive through
+      // the final cluster barrier.
+      if (leader) {
+#pragma unroll
+        for (int s = 0; s < kPairStages; ++s)
+          if (uses[s] > 0)
+            mbar_wait_bounded(&st->full[s], (uses[s] - 1u) & 1u, p.timeout_ns, p.status,
+                              nullptr);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (leader && lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int local = 0;
+      for (int tile = pair; tile < total && !*abort_flag; tile += npairs, ++local) {
+        const TileInfo ti = decode_tile(st, p, G, tile, BN, kPairBM);
+        const int a = local & 1;
+        const uint32_t q = static_cast<uint32_t>(local >> 1);
+        if (!mbar_wait_bounded<true>(&st->tempty[a], (q & 1u) ^ 1u, p.timeout_ns, p.status,
+                                     abort_flag))
+          break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(a * BN);
+        bool ok = true;
+        for (int kb = 0; kb < ti.nk; ++kb) {
+          if (!mbar_wait_bounded(&st->full[stage], phase, p.timeout_ns, p.status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + stage * kStageBytes);
+          const uint32_t sb = sa + kABytes;
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            tc_mma_bf16_pair(d_tmem, smem_desc_sw128(sa + kk * 32),
+                             smem_desc_sw128(sb + kk * 32), kIdesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          tc_commit_pair_mc(&st->empty[stage], 0x3);
+          if (++stage == kPairStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit_pair_mc(&st->tfull[a], 0x3);
+      }
+      // every pair MMA must retire before either CTA frees its TMEM
+      tc_commit_pair_mc(&st->fin, 0x1);
+      mbar_wait_bounded(&st->fin, 0, p.timeout_ns, p.status, nullptr);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
+    const int r_in_half = quarter * 32 + lane;
+    const uint32_t tempty_leader0 = mapa_shared(smem_u32(&st->tempty[0]), 0);
+    const uint32_t tempty_leader1 = mapa_shared(smem_u32(&st->tempty[1]), 0);
+    int local = 0;
+    for (int tile = pair; tile < total && !*abort_flag; tile += npairs, ++local) {
+      const TileInfo ti = decode_tile(st, p, G, tile, BN, kPairBM);
+      const int a = local & 1;
+      const uint32_t q = static_cast<uint32_t>(local >> 1);
+      if (!mbar_wait_bounded(&st->tfull[a], q & 1u, p.timeout_ns, p.status, abort_flag)) break;
+      tc_fence_after();
+      const int r_in_tile = static_cast<int>(rank) * 128 + r_in_half;
+      const bool valid = r_in_tile < ti.rows_left;
+      const int64_t row = static_cast<int64_t>(ti.a_row) + r_in_tile;
+      const uint32_t taddr =
+          tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(a * BN);
+      __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(ti.shared ? p.out_shared
+                                                                      : p.out_routed);
+      const int64_t ld = ti.shared ? p.ld_shared : p.ld_routed;
+      if constexpr (kSwiGLU) {
+        __nv_bfloat16* dst = out + row * ld + static_cast<int64_t>(ti.n) * 128;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          float g[32], u[32];
+          tmem_ld32(taddr + c * 32, g);
+          tmem_ld32(taddr + 128 + c * 32, u);
+          tmem_ld_wait();
+          uint32_t packed[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            packed[i] = pack_bf16x2(silu_f32(g[2 * i]) * u[2 * i],
+                                    silu_f32(g[2 * i + 1]) * u[2 * i + 1]);
+          if (valid) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              d4[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
+                                 packed[4 * i + 3]);
+          }
+        }
+      } else {
+        __nv_bfloat16* dst = out + row * ld + static_cast<int64_t>(ti.n) * BN;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          float v[32];
+          tmem_ld32(taddr + c * 32, v);
+          tmem_ld_wait();
+          uint32_t packed[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) packed[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+          if (valid) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              d4[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
+                                 packed[4 * i + 3]);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(a ? tempty_leader1 : tempty_leader0);
+    }
+  }
+
+  // Both CTAs stay until the even CTA's MMAs and the odd CTA's copies are done.
+  tc_fence_before();
+  __syncthreads();
+  cluster_arrive_wait();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc_pair(tmem_base, kTmemCols);
+}
+
+template <bool kSwiGLU>
+int launch_pair_impl(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b0,
+                     const CUtensorMap& b1, const GroupedGemmArgs& args, int num_sms,
+                     cudaStream_t stream) {
+  constexpr size_t smem = pair_smem_bytes();
+  static_assert(smem <= 227 * 1024, "shared memory budget");
+  auto kern = grouped_gemm_pair_kernel<kSwiGLU>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess)
+      return -3;
+    attr_set = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(num_sms & ~1));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attrs[1];
+  attrs[0].id = cudaLaunchAttributeClusterDimension;
+  attrs[0].val.clusterDim.x = 2;
+  attrs[0].val.clusterDim.y = 1;
+  attrs[0].val.clusterDim.z = 1;
+  cfg.attrs = attrs;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, a0, a1, b0, b1, args) != cudaSuccess) return -3;
+  return cudaGetLastError() == cudaSuccess ? 0 : -3;
+}
+
 template <int BN, bool kSwiGLU, int kStages>
 int launch_impl(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b0,
                 const CUtensorMap& b1, const GroupedGemmArgs& args, int num_sms,
@@ -365,8 +666,13 @@ bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t 
 
 int launch_grouped_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b0,
                         const CUtensorMap& b1, const GroupedGemmArgs& args, bool swiglu, int bn,
-                        int num_sms, cudaStream_t stream) {
+                        bool paired, int num_sms, cudaStream_t stream) {
   if (args.n_routed + (args.shared_rows > 0 ? 1 : 0) > kMaxGroups) return -2;
+  if (paired) {
+    if (bn != 256 || num_sms < 2) return -2;
+    return swiglu ? launch_pair_impl<true>(a0, a1, b0, b1, args, num_sms, stream)
+                  : launch_pair_impl<false>(a0, a1, b0, b1, args, num_sms, stream);
+  }
   if (swiglu) {
     if (bn != 256) return -2;
     return launch_impl<256, true, 4>(a0, a1, b0, b1, args, num_sms, stream);

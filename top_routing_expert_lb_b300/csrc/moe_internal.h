@@ -31,9 +31,11 @@ struct GroupedGemmArgs {
 // A0/A1: activations [rows][K] (routed / shared), B0/B1: weights [rows][K].
 // swiglu: epilogue writes h = SiLU(acc[:, :128]) * acc[:, 128:] per 256-wide
 // tile (packed gate/up weights); else writes acc as bf16.
+// paired: 256 x 256 tiles on CTA pairs (tcgen05 cta_group::2; bn must be 256;
+// the B tensor maps then use 128-row boxes); else 128 x bn tiles per CTA.
 int launch_grouped_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b0,
                         const CUtensorMap& b1, const GroupedGemmArgs& args, bool swiglu, int bn,
-                        int num_sms, cudaStream_t stream);
+                        bool paired, int num_sms, cudaStream_t stream);
 
 // Encodes a 2-D bf16 tensor map over a row-major [rows][cols] tensor with a
 // 64-column x box_rows box and 128-byte swizzle.  Returns false on failure.
@@ -53,9 +55,11 @@ struct RouterArgs {
   float* tile_lse2;           // [ntiles]
   int* status;
   uint64_t timeout_ns;
+  int32_t split;              // CTAs of a cluster sharing one tile (set by the launcher)
+  int32_t stages;             // pipeline depth (set by the launcher)
 };
-int launch_router(const CUtensorMap& x_map, const CUtensorMap& wr_map, const RouterArgs& args,
-                  cudaStream_t stream);
+int launch_router(const CUtensorMap& x_map, const CUtensorMap& wr_map, RouterArgs args,
+                  int num_sms, cudaStream_t stream);
 
 // Per-tile expert histogram of ids (when the router did not produce it).
 int launch_tile_hist(const int32_t* ids, int32_t T, int32_t k, int32_t E, int32_t* tile_hist,
@@ -77,6 +81,9 @@ struct FinalizeArgs {
   float* z_loss;              // [1] or null
   int32_t* tile_base;         // [ntiles][E] or null (no scan)
   int32_t* offsets;           // [E+1] or null
+  int32_t* exp_count;         // [E] scratch: per-expert totals
+  double* exp_psum;           // [E] scratch
+  int* done_counter;          // zero between calls; the last CTA resets it
 };
 int launch_finalize(const FinalizeArgs& args, cudaStream_t stream);
 
@@ -92,6 +99,7 @@ struct ScatterArgs {
   int32_t* row_token;        // [R_max]
   uint8_t* drop_mask;        // [T][k] or null
   uint16_t* x_perm;          // [R_max][d]
+  int32_t num_sms;           // sizes the gather split
 };
 int launch_scatter(const ScatterArgs& args, cudaStream_t stream);
 

@@ -44,62 +44,124 @@ __global__ void tile_hist_kernel(const int32_t* __restrict__ ids, int32_t T, int
     tile_hist[static_cast<int64_t>(tile) * E + e] = hist[e];
 }
 
-__global__ void __launch_bounds__(256) finalize_kernel(const FinalizeArgs a) {
-  __shared__ double fp[256];
-  __shared__ int kept[256];
-  const int E = a.E;
-  const int ntiles = (a.T + kTileTokens - 1) / kTileTokens;
-  const int e = threadIdx.x;
-  if (e < E) {
-    int run = 0;
-    double psum = 0.0;
-    for (int tl = 0; tl < ntiles; ++tl) {
-      const int64_t idx = static_cast<int64_t>(tl) * E + e;
-      if (a.tile_base) a.tile_base[idx] = run;
-      run += a.tile_hist[idx];
-      if (a.tile_psum) psum += static_cast<double>(a.tile_psum[idx]);
+constexpr int kFinThreads = 256;
+
+// Exclusive scan of one int per thread over the block (fixed order).
+__device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_tot[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < (kFinThreads / 32) ? warp_tot[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
     }
-    if (a.counts) a.counts[e] = run;
-    const double fe = (a.T > 0 && a.k > 0) ? static_cast<double>(run) /
-                                                 (static_cast<double>(a.k) * a.T)
-                                           : 0.0;
-    const double Pe = (a.T > 0) ? psum / a.T : 0.0;
-    if (a.f) a.f[e] = static_cast<float>(fe);
-    if (a.P) a.P[e] = static_cast<float>(Pe);
-    fp[e] = fe * Pe;
-    kept[e] = (a.C >= 0 && run > a.C) ? static_cast<int>(a.C) : run;
+    if (lane < (kFinThreads / 32)) warp_tot[lane] = w;  // inclusive warp prefix
   }
   __syncthreads();
+  const int before = (warp > 0 ? warp_tot[warp - 1] : 0) + x - v;
+  if (total) *total = warp_tot[kFinThreads / 32 - 1];
+  __syncthreads();
+  return before;
+}
+
+// Sum of one double per thread over the block, fixed tree order; result in
+// thread 0.
+__device__ __forceinline__ double block_sum(double v, double* red) {
+  red[threadIdx.x] = v;
+  __syncthreads();
+  for (int s = kFinThreads / 2; s > 0; s >>= 1) {
+    if (threadIdx.x < s) red[threadIdx.x] += red[threadIdx.x + s];
+    __syncthreads();
+  }
+  const double r = red[0];
+  __syncthreads();
+  return r;
+}
+
+// One CTA per expert: column scan of the tile histogram (tile bases), n_e
+// and sum_t p_e.  The last CTA to finish reduces across experts: offsets of
+// the kept rows, f, P and both losses.  Every sum has a fixed order.
+__global__ void __launch_bounds__(kFinThreads) finalize_kernel(const FinalizeArgs a) {
+  __shared__ int warp_tot[kFinThreads / 32];
+  __shared__ double red[kFinThreads];
+  __shared__ int is_last;
+  const int E = a.E;
+  const int ntiles = (a.T + kTileTokens - 1) / kTileTokens;
+  const int e = blockIdx.x;
+  // ---- phase A: column e
+  int carry = 0;
+  double psum = 0.0;
+  for (int c0 = 0; c0 < ntiles; c0 += kFinThreads) {
+    const int tl = c0 + threadIdx.x;
+    const int64_t idx = static_cast<int64_t>(tl) * E + e;
+    const int h = tl < ntiles ? __ldcg(a.tile_hist + idx) : 0;
+    if (a.tile_psum && tl < ntiles) psum += static_cast<double>(__ldcg(a.tile_psum + idx));
+    int tot = 0;
+    const int ex = block_exclusive_scan(h, warp_tot, &tot);
+    if (a.tile_base && tl < ntiles) a.tile_base[idx] = carry + ex;
+    carry += tot;
+  }
+  const double ps = block_sum(psum, red);
   if (threadIdx.x == 0) {
-    if (a.offsets) {
-      int acc = 0;
-      for (int j = 0; j < E; ++j) {
-        a.offsets[j] = acc;
-        acc += kept[j];
-      }
-      a.offsets[E] = acc;
-    }
-    if (a.bal_loss) {
-      double s = 0.0;
-      for (int j = 0; j < E; ++j) s += fp[j];
-      *a.bal_loss = static_cast<float>(static_cast<double>(a.balance_coef) * E * s);
-    }
-    if (a.z_loss) {
-      double z = 0.0;
-      if (a.tile_lse2)
-        for (int tl = 0; tl < ntiles; ++tl) z += static_cast<double>(a.tile_lse2[tl]);
-      *a.z_loss = (a.T > 0) ? static_cast<float>(z / a.T) : 0.0f;
-    }
+    a.exp_count[e] = carry;
+    a.exp_psum[e] = ps;
+    __threadfence();
+    is_last = (atomicAdd(a.done_counter, 1) == static_cast<int>(gridDim.x) - 1);
+  }
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+  // ---- phase B: across experts (E <= 256 = one per thread)
+  const int j = threadIdx.x;
+  const int n = j < E ? __ldcg(a.exp_count + j) : 0;
+  const double pj = j < E ? __ldcg(a.exp_psum + j) : 0.0;
+  const double fe = (j < E && a.T > 0 && a.k > 0)
+                        ? static_cast<double>(n) / (static_cast<double>(a.k) * a.T) : 0.0;
+  const double Pe = (j < E && a.T > 0) ? pj / a.T : 0.0;
+  if (j < E) {
+    if (a.counts) a.counts[j] = n;
+    if (a.f) a.f[j] = static_cast<float>(fe);
+    if (a.P) a.P[j] = static_cast<float>(Pe);
+  }
+  const int kept = (j < E) ? ((a.C >= 0 && n > a.C) ? static_cast<int>(a.C) : n) : 0;
+  int R = 0;
+  const int off = block_exclusive_scan(kept, warp_tot, &R);
+  if (a.offsets) {
+    if (j < E) a.offsets[j] = off;
+    if (j == 0) a.offsets[E] = R;
+  }
+  const double sfp = block_sum(fe * Pe, red);
+  double z = 0.0;
+  if (a.tile_lse2)
+    for (int tl = j; tl < ntiles; tl += kFinThreads) z += static_cast<double>(__ldcg(a.tile_lse2 + tl));
+  const double zs = block_sum(z, red);
+  if (j == 0) {
+    if (a.bal_loss) *a.bal_loss = static_cast<float>(static_cast<double>(a.balance_coef) * E * sfp);
+    if (a.z_loss) *a.z_loss = (a.T > 0) ? static_cast<float>(zs / a.T) : 0.0f;
+    *a.done_counter = 0;  // ready for the next call on this workspace
   }
 }
 
 constexpr int kScatterThreads = 256;
 constexpr int kScatterWarps = kScatterThreads / 32;
+constexpr int kGatherUnroll = 4;
 
+// grid = (tiles, G): the G CTAs of a tile all compute the tile's destination
+// rows (cheap integer work on <= 1024 pairs); CTA 0 publishes the slot rows,
+// drop mask and row->token map, and each CTA gathers 1/G of the tile's tokens.
 __global__ void __launch_bounds__(kScatterThreads) scatter_kernel(const ScatterArgs a) {
   __shared__ int run[256];                      // pairs of e seen in earlier rounds
   __shared__ int wcnt[kScatterWarps][256];      // pairs of e per warp, this round
-  __shared__ int base[256];                     // tile_base + offsets
+  __shared__ int base[256];                     // tile_base
   __shared__ int rows[kTileTokens * kMaxTopK];  // destination row per pair (-1 dropped)
   const int E = a.E, k = a.k;
   const int tile = blockIdx.x;
@@ -143,28 +205,42 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_kernel(const ScatterA
     }
     __syncthreads();
   }
-  // slot rows, drop mask, row -> token
-  for (int q = threadIdx.x; q < pairs; q += blockDim.x) {
-    const int row = rows[q];
-    const int64_t gq = static_cast<int64_t>(t0) * k + q;
-    a.slot_row[gq] = row;
-    if (a.drop_mask) a.drop_mask[gq] = row < 0 ? 1 : 0;
-    if (row >= 0) a.row_token[row] = t0 + q / k;
+  if (blockIdx.y == 0) {
+    for (int q = threadIdx.x; q < pairs; q += blockDim.x) {
+      const int row = rows[q];
+      const int64_t gq = static_cast<int64_t>(t0) * k + q;
+      a.slot_row[gq] = row;
+      if (a.drop_mask) a.drop_mask[gq] = row < 0 ? 1 : 0;
+      if (row >= 0) a.row_token[row] = t0 + q / k;
+    }
   }
-  // gather: warp per token, the token row is read once
+  // gather this CTA's share of tokens: warp per token, the row is read once
+  const int G = gridDim.y;
+  const int per = (ntok + G - 1) / G;
+  const int tb = blockIdx.y * per;
+  const int te = min(ntok, tb + per);
   const int nvec = a.d / 8;  // 16-byte vectors per row
-  for (int tl = warp; tl < ntok; tl += kScatterWarps) {
+  for (int tl = tb + warp; tl < te; tl += kScatterWarps) {
     const int t = t0 + tl;
     int dst[kMaxTopK];
 #pragma unroll
     for (int s = 0; s < kMaxTopK; ++s) dst[s] = (s < k) ? rows[tl * k + s] : -1;
     const uint4* src = reinterpret_cast<const uint4*>(a.x + static_cast<int64_t>(t) * a.d);
-    for (int v = lane; v < nvec; v += 32) {
-      const uint4 val = src[v];
+    for (int v0 = lane; v0 < nvec; v0 += 32 * kGatherUnroll) {
+      uint4 val[kGatherUnroll];
 #pragma unroll
-      for (int s = 0; s < kMaxTopK; ++s)
-        if (dst[s] >= 0)
-          reinterpret_cast<uint4*>(a.x_perm + static_cast<int64_t>(dst[s]) * a.d)[v] = val;
+      for (int u = 0; u < kGatherUnroll; ++u)
+        if (v0 + 32 * u < nvec) val[u] = __ldg(src + v0 + 32 * u);
+#pragma unroll
+      for (int u = 0; u < kGatherUnroll; ++u) {
+        if (v0 + 32 * u < nvec) {
+#pragma unroll
+          for (int s = 0; s < kMaxTopK; ++s)
+            if (dst[s] >= 0)
+              reinterpret_cast<uint4*>(a.x_perm + static_cast<int64_t>(dst[s]) * a.d)[v0 + 32 * u] =
+                  val[u];
+        }
+      }
     }
   }
 }
@@ -180,14 +256,18 @@ int launch_tile_hist(const int32_t* ids, int32_t T, int32_t k, int32_t E, int32_
 }
 
 int launch_finalize(const FinalizeArgs& args, cudaStream_t stream) {
-  finalize_kernel<<<1, 256, 0, stream>>>(args);
+  if (args.E > kFinThreads) return -2;
+  finalize_kernel<<<args.E, kFinThreads, 0, stream>>>(args);
   return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }
 
 int launch_scatter(const ScatterArgs& args, cudaStream_t stream) {
   const int ntiles = (args.T + kTileTokens - 1) / kTileTokens;
   if (ntiles == 0 || args.k == 0) return 0;
-  scatter_kernel<<<ntiles, kScatterThreads, 0, stream>>>(args);
+  // enough CTAs to keep every SM streaming rows (about 4 per SM)
+  int G = (4 * args.num_sms + ntiles - 1) / ntiles;
+  G = G < 1 ? 1 : (G > 16 ? 16 : G);
+  scatter_kernel<<<dim3(ntiles, G), kScatterThreads, 0, stream>>>(args);
   return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }
 
