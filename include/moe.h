@@ -196,6 +196,29 @@ int moe_set_wait_timeout_ns(uint64_t ns);
  * word and returns.  Exercises the timeout path without faulting anything.   */
 int moe_debug_timeout_probe(void *ws, size_t ws_bytes, void *stream);
 
+/* Router for callers that cannot allocate device memory.  No counterpart in
+ * the pages: it exists for callers that cannot call cudaMalloc or provide a
+ * workspace (code running under a host framework that owns all device memory
+ * through its own pool, plug-ins inside such processes, paths where an
+ * allocation is not allowed).  Same arguments, kernels and outputs as
+ * moe_route, without the workspace: the scratch lives in one static device
+ * array of about 1 MiB inside the library, which every GPU that loads the
+ * library keeps until the process exits.
+ *   Limits: T <= MOE_NOALLOC_MAX_TOKENS (65536) and E <= 256; larger shapes
+ *   return MOE_ERR_UNSUPPORTED before anything is enqueued.
+ *   Allocates nothing (no cudaMalloc/cudaFree or allocating routine).
+ *   All calls share the array, which keeps the last call's contents; each
+ *   call clears the words that must start at zero.  Calls that overlap on
+ *   the GPU (e.g. on unordered streams) race on it: order them.
+ *   The first call on a device looks up the array's device address with that
+ *   device current and caches it; make that first call before any stream
+ *   capture.  Device-side timeouts are recorded in the array, not reported. */
+#define MOE_NOALLOC_MAX_TOKENS 65536
+int moe_route_noalloc(const moe_shape_t *shape, const uint16_t *x, const uint16_t *w_router,
+                      const float *logit_offset, const float *sel_bias, int32_t *ids,
+                      float *gates, int32_t *counts, float *f, float *P, float *bal_loss,
+                      float *z_loss, void *stream);
+
 /* Kernel accounting for benchmarks (host-side, process-wide, not thread-safe).
  * Kernel ids reported by moe_profile_collect: */
 #define MOE_KERNEL_ROUTER 1       /* router logits + softmax + Top-k            */

@@ -73,11 +73,12 @@ def lib():
     L.moe_profile_enable.argtypes = [ctypes.c_int]
     L.moe_profile_collect.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_int), _P, _P]
     L.moe_launch_count.argtypes = [ctypes.POINTER(ctypes.c_uint64)]
+    L.moe_route_noalloc.argtypes = [S] + [_P] * 11 + [_P]
     for name in ("moe_workspace_size", "moe_capacity", "moe_max_rows", "moe_pack_w13",
                  "moe_route", "moe_permute", "moe_grouped_ffn", "moe_combine",
                  "moe_layer_forward", "moe_layer_forward_host", "moe_check_status",
                  "moe_set_wait_timeout_ns", "moe_debug_timeout_probe", "moe_profile_enable",
-                 "moe_profile_collect", "moe_launch_count"):
+                 "moe_profile_collect", "moe_launch_count", "moe_route_noalloc"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -149,6 +150,17 @@ def moe_route(shape, x, w_router, logit_offset, sel_bias, ids, gates, counts, f,
                            _ptr(sel_bias), _ptr(ids), _ptr(gates), _ptr(counts), _ptr(f),
                            _ptr(P), _ptr(bal_loss), _ptr(z_loss), _ptr(ws), ws.numel(),
                            _stream(stream)), "moe_route")
+
+
+def moe_route_noalloc(shape, x, w_router, logit_offset, sel_bias, ids, gates, counts, f, P,
+                      bal_loss, z_loss, stream=None):
+    """moe_route without a workspace, for callers that cannot allocate device
+    memory: the library keeps the scratch in a static device array (T up to
+    65536 tokens).  Calls sharing a device must not overlap on the GPU."""
+    _check(lib().moe_route_noalloc(ctypes.byref(shape), _ptr(x), _ptr(w_router),
+                                   _ptr(logit_offset), _ptr(sel_bias), _ptr(ids), _ptr(gates),
+                                   _ptr(counts), _ptr(f), _ptr(P), _ptr(bal_loss), _ptr(z_loss),
+                                   _stream(stream)), "moe_route_noalloc")
 
 
 def moe_permute(shape, x, ids, offsets, slot_row, row_token, drop_mask, x_perm, ws,

@@ -1,0 +1,146 @@
+// moe_route_noalloc: the router for callers that cannot allocate device memory.
+//
+// Some callers cannot call cudaMalloc or hand over a workspace: code that runs
+// inside a host framework owning every byte of device memory through its own
+// pool, plug-ins loaded into such a process, or code paths where allocating
+// (and the device synchronisation it may imply) is not allowed.  For them this
+// entry point runs the same router and reduction kernels as moe_route, with
+// the scratch those kernels need (per-tile partial sums, per-expert totals,
+// the status word and the reduction's completion counter) placed in one
+// file-scope device array instead of a caller workspace.
+//
+// That array is part of the library image: every GPU that loads the library
+// holds it until the process exits.  All calls share it and it keeps the
+// contents of the last call, so each call clears the words that must start at
+// zero; two calls that overlap on the GPU (different streams, no ordering)
+// race on it.  The first call on a device looks up the array's device address
+// (cudaGetSymbolAddress, with that device current) and caches it; make that
+// first call before any stream capture.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "../../include/moe.h"
+#include "moe_internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int kNoAllocMaxTokens = MOE_NOALLOC_MAX_TOKENS;
+constexpr int kNoAllocMaxTiles = kNoAllocMaxTokens / kTileTokens;
+constexpr int kNoAllocMaxExperts = MOE_MAX_EXPERTS;
+
+// Byte offsets inside the static scratch.
+constexpr size_t kOffStatus = 0;    // int status word
+constexpr size_t kOffCounter = 64;  // int completion counter of the reduction
+constexpr size_t kOffHist = 256;
+constexpr size_t kOffPsum = kOffHist + static_cast<size_t>(kNoAllocMaxTiles) * kNoAllocMaxExperts * 4;
+constexpr size_t kOffLse2 = kOffPsum + static_cast<size_t>(kNoAllocMaxTiles) * kNoAllocMaxExperts * 4;
+constexpr size_t kOffExpCount = kOffLse2 + static_cast<size_t>(kNoAllocMaxTiles) * 4;
+constexpr size_t kOffExpPsum = kOffExpCount + kNoAllocMaxExperts * 4;
+constexpr size_t kScratchBytes = kOffExpPsum + kNoAllocMaxExperts * 8;
+
+static __device__ __align__(256) unsigned char g_route_scratch[kScratchBytes];
+
+constexpr int kMaxDevices = 64;
+unsigned char* g_scratch_dev[kMaxDevices] = {nullptr};  // device address, per device
+int g_sm_count[kMaxDevices] = {0};
+
+// Per-device set-up: the device address of the static array (host code may
+// not use the symbol itself as a device pointer) and the SM count.
+int scratch_for_current_device(unsigned char** ptr, int* num_sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    return MOE_ERR_CUDA;
+  if (g_scratch_dev[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess || p == nullptr)
+      return MOE_ERR_CUDA;
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      return MOE_ERR_CUDA;
+    g_sm_count[dev] = n;
+    g_scratch_dev[dev] = static_cast<unsigned char*>(p);
+  }
+  *ptr = g_scratch_dev[dev];
+  *num_sms = g_sm_count[dev];
+  return MOE_OK;
+}
+
+inline bool aligned16(const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; }
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" int moe_route_noalloc(const moe_shape_t* s, const uint16_t* x,
+                                 const uint16_t* w_router, const float* logit_offset,
+                                 const float* sel_bias, int32_t* ids, float* gates,
+                                 int32_t* counts, float* f, float* P, float* bal_loss,
+                                 float* z_loss, void* stream) {
+  size_t unused = 0;
+  int rc = moe_workspace_size(s, &unused);  // shape checks only
+  if (rc != MOE_OK) return rc;
+  if (s->T > kNoAllocMaxTokens || s->E > kNoAllocMaxExperts) return MOE_ERR_UNSUPPORTED;
+  if (!counts || !f || !P || !bal_loss || !z_loss) return MOE_ERR_INVALID_ARG;
+  if (s->T > 0) {
+    if (!x || !w_router || !aligned16(x) || !aligned16(w_router)) return MOE_ERR_INVALID_ARG;
+    if (s->k > 0 && (!ids || !gates)) return MOE_ERR_INVALID_ARG;
+  }
+  unsigned char* scratch = nullptr;
+  int num_sms = 0;
+  if ((rc = scratch_for_current_device(&scratch, &num_sms)) != MOE_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // status word and completion counter start at zero on every call
+  if (cudaMemsetAsync(scratch, 0, kOffHist, st) != cudaSuccess) return MOE_ERR_CUDA;
+
+  int* status = reinterpret_cast<int*>(scratch + kOffStatus);
+  int32_t* tile_hist = reinterpret_cast<int32_t*>(scratch + kOffHist);
+  float* tile_psum = reinterpret_cast<float*>(scratch + kOffPsum);
+  float* tile_lse2 = reinterpret_cast<float*>(scratch + kOffLse2);
+  if (s->T > 0) {
+    CUtensorMap mx, mw;
+    const uint32_t nr = static_cast<uint32_t>((s->E + 15) / 16 * 16);
+    if (!make_tmap_bf16(&mx, x, s->T, s->d, 128)) return MOE_ERR_CUDA;
+    if (!make_tmap_bf16(&mw, w_router, s->E, s->d, nr)) return MOE_ERR_CUDA;
+    RouterArgs ra{};
+    ra.T = s->T;
+    ra.d = s->d;
+    ra.E = s->E;
+    ra.k = s->k;
+    ra.logit_offset = logit_offset;
+    ra.sel_bias = sel_bias;
+    ra.ids = ids;
+    ra.gates = gates;
+    ra.tile_hist = tile_hist;
+    ra.tile_psum = tile_psum;
+    ra.tile_lse2 = tile_lse2;
+    ra.status = status;
+    ra.timeout_ns = 2000000000ull;
+    rc = launch_router(mx, mw, ra, num_sms, st);
+    if (rc != 0) return rc == -2 ? MOE_ERR_UNSUPPORTED : MOE_ERR_CUDA;
+  }
+  FinalizeArgs fa{};
+  fa.T = s->T;
+  fa.E = s->E;
+  fa.k = s->k;
+  fa.C = -1;
+  fa.balance_coef = s->balance_coef;
+  fa.tile_hist = tile_hist;
+  fa.tile_psum = tile_psum;
+  fa.tile_lse2 = tile_lse2;
+  fa.counts = counts;
+  fa.f = f;
+  fa.P = P;
+  fa.bal_loss = bal_loss;
+  fa.z_loss = z_loss;
+  fa.exp_count = reinterpret_cast<int32_t*>(scratch + kOffExpCount);
+  fa.exp_psum = reinterpret_cast<double*>(scratch + kOffExpPsum);
+  fa.done_counter = reinterpret_cast<int*>(scratch + kOffCounter);
+  rc = launch_finalize(fa, st);
+  if (rc != 0) return rc == -2 ? MOE_ERR_UNSUPPORTED : MOE_ERR_CUDA;
+  return MOE_OK;
+}
