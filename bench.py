@@ -80,6 +80,32 @@ def algorithmic_work(w, R: int):
                                                   "combine": b_combine}
 
 
+def kept_rows_per_expert(layer, w):
+    """Rows each expert computed (after capacity), from the layer's outputs."""
+    import torch
+    if w.k == 0:
+        return [0] * w.E
+    ids = layer.ids.view(-1).long()
+    keep = (layer.drop_mask.view(-1) == 0)
+    return torch.bincount(ids[keep], minlength=w.E).tolist()
+
+
+def attainable_ffn_ms(w, kept, peaks):
+    """Attainable time of the two expert projections: every expert (and the
+    shared group) takes max(its FLOPs at the bf16 peak, its weight bytes at the
+    HBM bandwidth); the sum is the bound when experts run back to back."""
+    peak = peaks["bf16_tflops"] * 1e12
+    bw = peaks["hbm_gbs"] * 1e9
+    wbytes = 3 * w.M * w.d * 2
+    t = 0.0
+    for n in kept:
+        if n > 0:
+            t += max(6.0 * n * w.d * w.M / peak, wbytes / bw)
+    if w.n_shared:
+        t += max(6.0 * w.T * w.d * w.Ms / peak, 3 * w.Ms * w.d * 2 / bw)
+    return 1000.0 * t
+
+
 def workload_desc(w):
     cap = f"capacity c={w.capacity_factor}" if w.capacity_factor > 0 else "dropless"
     sh = f", {w.n_shared} shared" if w.n_shared else ""
@@ -326,6 +352,8 @@ def run_ours(args, w):
     R = int(w.T * w.k - int(layer.drop_mask.sum().item())) if w.k else 0
     flops, bytes_ = algorithmic_work(w, R)
     peaks, peak_src = load_peaks()
+    kept = kept_rows_per_expert(layer, w)
+    attainable_ms = attainable_ffn_ms(w, kept, peaks)
     ffn_ms = kern_ms.get("gemm_swiglu", 0.0) + kern_ms.get("gemm_down", 0.0)
     ffn_tflops = (flops["gemm_swiglu"] + flops["gemm_down"]) / (ffn_ms * 1e-3) / 1e12
     dom = "gemm_swiglu"
@@ -387,6 +415,11 @@ def run_ours(args, w):
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "ffn_tflops": ffn_tflops,
         "ffn_frac_of_bf16_peak": ffn_tflops / peaks["bf16_tflops"],
+        "ffn_attainable_ms": attainable_ms,
+        "ffn_frac_of_attainable": attainable_ms / ffn_ms if ffn_ms > 0 else None,
+        "load": {"max_over_mean": float(max(kept) / (sum(kept) / len(kept))) if sum(kept) else None,
+                 "empty_experts": int(sum(1 for v in kept if v == 0)),
+                 "dropped_pairs": int(w.T * w.k - R)},
         "kernel_ms": kern_ms, "kernel_launches_timed": kern_n,
         "stage_gbs": stage_gbs,
         "stage_frac_of_hbm": {k: v / peaks["hbm_gbs"] for k, v in stage_gbs.items()},
