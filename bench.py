@@ -44,6 +44,9 @@ def parse_args(argv=None):
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=15.0,
                     help="target seconds of oracle work for the CPU baseline sample")
+    ap.add_argument("--stage", choices=["layer", "router"], default="layer",
+                    help="router: time moe_route alone (no expert weights are drawn); "
+                         "for profiling, not the headline number")
     return ap.parse_args(argv)
 
 
@@ -438,12 +441,63 @@ def run_ours(args, w):
     return 0
 
 
+def run_router_stage(args, w):
+    """moe_route alone at the workload's shape: per-call device time and HBM
+    fraction of its algorithmic bytes (one JSON line, not the headline)."""
+    import torch
+
+    import synth
+    import top_routing_expert_lb_b300 as moe
+    from top_routing_expert_lb_b300 import build as mbuild
+
+    mbuild.ensure_built()
+    dev = torch.device("cuda", 0)
+    inp = synth.make_inputs(w, dev, experts=False)
+    s = moe.Shape.of(w.T, w.d, w.M, w.E, w.k, w.n_shared, w.capacity_factor, w.balance_coef)
+    ws = moe.alloc_workspace(s, dev)
+    ids = torch.empty((w.T, w.k), dtype=torch.int32, device=dev)
+    gates = torch.empty((w.T, w.k), dtype=torch.float32, device=dev)
+    counts = torch.empty(w.E, dtype=torch.int32, device=dev)
+    f = torch.empty(w.E, device=dev)
+    P = torch.empty(w.E, device=dev)
+    lb = torch.empty(1, device=dev)
+    lz = torch.empty(1, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def call():
+        moe.moe_route(s, inp.x, inp.wr, inp.offset, inp.sel_bias, ids, gates, counts, f, P, lb,
+                      lz, ws)
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize(dev)
+    moe.moe_profile_enable(True)
+    for _ in range(args.steps):
+        flush.zero_()
+        call()
+    torch.cuda.synchronize(dev)
+    moe.moe_profile_enable(False)
+    per = {}
+    for name, t in moe.moe_profile_collect():
+        per.setdefault(name, []).append(t)
+    kern = {k: statistics.mean(v) for k, v in per.items()}
+    peaks, _ = load_peaks()
+    b = algorithmic_work(w, 0)[1]["router"]
+    print(json.dumps({"stage": "router", "workload": workload_desc(w), "kernel_ms": kern,
+                      "router_gbs": b / (kern["router"] * 1e-3) / 1e9,
+                      "router_frac_of_hbm": b / (kern["router"] * 1e-3) / 1e9 / peaks["hbm_gbs"]}),
+          flush=True)
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     import synth
     w = synth.WORKLOADS[args.workload]
     if args.impl == "reference":
         return run_reference(args, w)
+    if args.stage == "router":
+        return run_router_stage(args, w)
     return run_ours(args, w)
 
 

@@ -11,17 +11,21 @@
 //   g~    = p_S / sum p_S                         (unbiased p)
 // and per-tile partials for the side outputs: expert histogram (n_e), sum of
 // p_e over the tile's tokens (P_e) and sum of lse^2 (z-loss, "MOE大模型对比篇"
-// §2.2).  Reductions over tokens run in a fixed order, so results are
-// bitwise reproducible.
+// §2.2).  Every reduction runs in a fixed order, so results are bitwise
+// reproducible for a given shape.
 //
 // Layout of the work.  The logits tile is 128 x N (N = E rounded up to 16;
-// W_r rows past E are zero-filled by TMA); TMEM lane i holds token i, so one
-// epilogue thread owns one token.  When there are few tiles, S CTAs of a
-// thread-block cluster split the d (K) dimension of one tile: each runs its
-// share of the k-blocks, copies its partial logits TMEM -> shared memory, and
-// the cluster's rank-0 CTA adds the peers' partials over distributed shared
-// memory in rank order (deterministic) before the softmax / Top-k passes,
-// which all read the row from shared memory.
+// W_r rows past E are zero-filled by TMA) in TMEM, lane i = token i.  When
+// there are few tiles, the S CTAs of a thread-block cluster split the d (K)
+// dimension of one tile.  After the main loop every CTA copies its partial
+// logits to shared memory; CTA q of the cluster owns rows [q*128/S,
+// (q+1)*128/S) and receives the peers' partials for them over distributed
+// shared memory (a reduce-scatter), sums them in rank order and runs the
+// softmax / Top-k epilogue for its rows with 8 warps: 2S threads per token,
+// each over a strided subset of the experts, combined by xor butterflies
+// (max, sum) and a merge of per-thread Top-k lists under the total order
+// (key descending, expert index ascending).  Per-CTA column sums, histograms
+// and lse^2 sums go to the cluster's rank-0 CTA, which adds them in rank order.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -34,7 +38,10 @@ namespace {
 
 constexpr int kBK = 64;
 constexpr int kMaxStages = 8;
-constexpr int kThreads = 192;
+constexpr int kEpiWarps = 8;
+constexpr int kEpiThreads = kEpiWarps * 32;
+constexpr int kThreads = 64 + kEpiThreads;  // producer, MMA, 8 epilogue warps
+constexpr int kMaxSplit = 8;
 
 struct RouterSmemTail {
   uint64_t full[kMaxStages];
@@ -46,15 +53,19 @@ struct RouterSmemTail {
   float off[256];
   float bias[256];
   float lse[128];
-  float zw[4];
+  // per-CTA contributions to the tile partials, one slot per cluster rank
+  float slot_colsum[kMaxSplit][256];
+  int slot_hist[kMaxSplit][256];
+  float slot_lse2[kMaxSplit];
 };
 
 struct RouterGeom {
   int N;             // MMA N (E rounded up to 16)
   int stages;        // pipeline depth
   int stage_bytes;   // A tile + B tile
-  int part_floats;   // one [128][E+1] logits tile, rounded up to 4 floats
-  size_t main_bytes;  // stage ring, reused afterwards for S logits tiles
+  int ldl;           // row pitch of a logits row (floats)
+  int rpc;           // rows owned per CTA (128 / S)
+  size_t main_bytes;  // stage ring, reused afterwards for the logits tiles
 };
 
 __host__ __device__ inline RouterGeom router_geom(int E, int stages, int S) {
@@ -62,11 +73,12 @@ __host__ __device__ inline RouterGeom router_geom(int E, int stages, int S) {
   g.N = (E + 15) / 16 * 16;
   g.stages = stages;
   g.stage_bytes = 128 * kBK * 2 + g.N * kBK * 2;
-  g.part_floats = (128 * (E + 1) + 3) / 4 * 4;
+  g.ldl = E + 1;
+  g.rpc = 128 / S;
   const size_t ring = static_cast<size_t>(stages) * g.stage_bytes;
-  // S partial tiles, then [4][E] per-warp column sums
-  const size_t parts = (static_cast<size_t>(S) * g.part_floats + 4 * static_cast<size_t>(E)) * 4;
-  g.main_bytes = ring > parts ? ring : parts;
+  // own partial [128][ldl] + receive slots [S][rpc][ldl] (= another 128 rows)
+  const size_t tiles = static_cast<size_t>(S > 1 ? 256 : 128) * g.ldl * 4;
+  g.main_bytes = ring > tiles ? ring : tiles;
   return g;
 }
 
@@ -76,48 +88,40 @@ __host__ __device__ inline uint32_t router_tmem_cols(int N) {
   return c;
 }
 
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
+__device__ __forceinline__ void st_dsmem_f32(uint32_t remote_addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote_addr), "f"(v) : "memory");
+}
+__device__ __forceinline__ void st_dsmem_s32(uint32_t remote_addr, int v) {
+  asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(remote_addr), "r"(v) : "memory");
 }
 
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+// (key desc, index asc): true when (ka, ia) comes before (kb, ib).
+__device__ __forceinline__ bool before(float ka, int ia, float kb, int ib) {
+  return ka > kb || (ka == kb && ia < ib);
 }
 
-// Address of the same shared-memory location in CTA `rank` of the cluster.
-__device__ __forceinline__ uint32_t map_peer(uint32_t local_addr, uint32_t rank) {
-  uint32_t remote;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));
-  return remote;
-}
-
-__device__ __forceinline__ void st_dsmem_v4(uint32_t remote_addr, uint4 v) {
-  asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(remote_addr), "r"(v.x),
-               "r"(v.y), "r"(v.z), "r"(v.w)
-               : "memory");
-}
-
+template <int K>
 __global__ void __launch_bounds__(kThreads, 1)
     router_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                   const RouterArgs p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* smem = smem_raw + pad;
-  const int E = p.E, k = p.k;
+  const int E = p.E;
   const int S = p.split;
   const RouterGeom geo = router_geom(E, p.stages, S);
   const int a_bytes = 128 * kBK * 2;
   RouterSmemTail* st = reinterpret_cast<RouterSmemTail*>(smem + geo.main_bytes);
   volatile int* abort_flag = &st->abort_flag;
   const uint32_t tmem_cols = router_tmem_cols(geo.N);
-  float* lg = reinterpret_cast<float*>(smem);  // [128][E+1] after the main loop
-  const int ldl = E + 1;
+  const int ldl = geo.ldl;
+  const int rpc = geo.rpc;
+  float* lg = reinterpret_cast<float*>(smem);          // own partial [128][ldl]
+  float* recv = lg + static_cast<size_t>(128) * ldl;   // [S][rpc][ldl], slot q from rank q
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t rank = S > 1 ? cluster_rank() : 0u;
+  const uint32_t rank = S > 1 ? cluster_ctarank() : 0u;
   const int tile = blockIdx.x / S;
   const int nk = p.d / kBK;
   const int kb0 = static_cast<int>(rank) * nk / S;
@@ -189,7 +193,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait_bounded(&st->tfull, 0, p.timeout_ns, p.status, nullptr);
     }
     __syncwarp();
-  } else {
+  } else if (warp < 6) {
     // -------------------------------------------- epilogue, part 1: TMEM -> smem
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
@@ -209,124 +213,181 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
   }
 
-  // Partial logits of every CTA are in its own shared memory and every MMA of
-  // the cluster has retired (so the leader's stage ring is free).  Peers push
-  // their tile into slot `rank` of the leader's ring with vector DSMEM stores;
-  // the second cluster barrier makes them visible to the leader.
+  // Partial logits of every CTA are in its shared memory and every MMA of the
+  // cluster has retired.  Reduce-scatter: rows owned by CTA q go to slot
+  // [this rank] of q's receive area.
   __syncthreads();
+  const int eidx = static_cast<int>(threadIdx.x) - 64;  // epilogue thread index, or < 0
   if (S > 1) {
-    cluster_sync_all();
-    if (rank != 0 && !*abort_flag) {
-      const uint32_t dst = map_peer(smem_u32(lg + static_cast<size_t>(rank) * geo.part_floats), 0);
-      const uint4* src = reinterpret_cast<const uint4*>(lg);
-      for (int i = threadIdx.x; i < geo.part_floats / 4; i += blockDim.x)
-        st_dsmem_v4(dst + 16u * i, src[i]);
+    cluster_arrive_wait();
+    if (eidx >= 0 && !*abort_flag) {
+      const int per = rpc * E;  // values per destination
+      for (int q = 0; q < S; ++q) {
+        if (q == static_cast<int>(rank)) continue;
+        const uint32_t dst =
+            mapa_shared(smem_u32(recv + static_cast<size_t>(rank) * rpc * ldl), q);
+        for (int i = eidx; i < per; i += kEpiThreads) {
+          const int rl = i / E, e = i - rl * E;
+          st_dsmem_f32(dst + 4u * (rl * ldl + e), lg[(q * rpc + rl) * ldl + e]);
+        }
+      }
     }
-    cluster_sync_all();
+    cluster_arrive_wait();
   }
 
-  if (rank == 0 && warp >= 2 && !*abort_flag) {
-    // -------------------------------------------- epilogue, part 2 (leader)
-    const int quarter = warp & 3;
-    const int r = quarter * 32 + lane;
+  const int tpr = kEpiThreads / rpc;  // threads per token row (2S)
+  if (eidx >= 0 && !*abort_flag) {
+    // -------------------------------------------- epilogue, part 2 (owned rows)
+    const int rl = eidx / tpr;        // local row
+    const int sub = eidx - rl * tpr;  // this thread's expert subset: e = sub (mod tpr)
+    const int r = static_cast<int>(rank) * rpc + rl;
     const int t = tile * 128 + r;
     const bool valid = t < p.T;
-    float* row = lg + r * ldl;
-    // full logits: partials summed in rank order, + offset
+    float* row = lg + r * ldl;  // receives the full logits, then exp, then p
     float m = -INFINITY;
-    for (int e = 0; e < E; ++e) {
-      float v = row[e];
-      for (int q = 1; q < S; ++q) v += row[static_cast<size_t>(q) * geo.part_floats + e];
+    for (int e = sub; e < E; e += tpr) {
+      float v = 0.0f;
+      for (int q = 0; q < S; ++q)  // partials in rank order
+        v += (q == static_cast<int>(rank))
+                 ? row[e]
+                 : recv[(static_cast<size_t>(q) * rpc + rl) * ldl + e];
       v += st->off[e];
       row[e] = v;
       m = fmaxf(m, v);
     }
+    for (int o = 1; o < tpr; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
     float s = 0.0f;
-#pragma unroll 4
-    for (int e = 0; e < E; ++e) s += expf(row[e] - m);
-    const float inv_s = 1.0f / s;
-    float top_key[kMaxTopK];
-    float top_p[kMaxTopK];
-    int top_id[kMaxTopK];
-#pragma unroll
-    for (int j = 0; j < kMaxTopK; ++j) {
-      top_key[j] = -INFINITY;
-      top_p[j] = 0.0f;
-      top_id[j] = -1;
+    for (int e = sub; e < E; e += tpr) {
+      const float ex = __expf(row[e] - m);
+      row[e] = ex;
+      s += ex;
     }
-    float thresh = -INFINITY;  // k-th largest key so far
-#pragma unroll 2
-    for (int e = 0; e < E; ++e) {
-      const float pe = expf(row[e] - m) * inv_s;
-      row[e] = valid ? pe : 0.0f;  // the row now holds p (for the P partial)
+    for (int o = 1; o < tpr; o <<= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    const float inv_s = 1.0f / s;
+    float top_key[K > 0 ? K : 1];
+    int top_id[K > 0 ? K : 1];
+#pragma unroll
+    for (int j = 0; j < K; ++j) {
+      top_key[j] = -INFINITY;
+      top_id[j] = 0x7fffffff;
+    }
+    float thresh = -INFINITY;  // K-th largest key of this thread so far
+    for (int e = sub; e < E; e += tpr) {
+      const float pe = row[e] * inv_s;
+      row[e] = valid ? pe : 0.0f;  // the row now holds p (gates, P partial)
       const float key = pe + st->bias[e];
-      // Insertion into the descending list.  Experts arrive in index order,
-      // so a new key goes after every equal key already listed (strict '>');
-      // entries below the insertion point shift down.
-      if (k > 0 && key > thresh) {
-        float ck = key, cp = pe;
+      // experts arrive in index order: strict '>' keeps equal keys in index order
+      if (K > 0 && key > thresh) {
+        float ck = key;
         int ci = e;
         bool placed = false;
 #pragma unroll
-        for (int j = 0; j < kMaxTopK; ++j) {
-          if (j < k && (placed || ck > top_key[j])) {
-            const float tk = top_key[j], tp = top_p[j];
+        for (int j = 0; j < K; ++j) {
+          if (placed || ck > top_key[j]) {
+            const float tk = top_key[j];
             const int ti = top_id[j];
             top_key[j] = ck;
-            top_p[j] = cp;
             top_id[j] = ci;
             ck = tk;
-            cp = tp;
             ci = ti;
             placed = true;
           }
         }
-#pragma unroll
-        for (int j = 0; j < kMaxTopK; ++j)
-          if (j == k - 1) thresh = top_key[j];
+        thresh = top_key[K > 0 ? K - 1 : 0];
       }
     }
-    st->lse[r] = valid ? (m + logf(s)) : 0.0f;
-    if (valid && k > 0) {
-      float denom = 0.0f;
+    __syncwarp();  // the row's p values (written by the whole group) are visible
+    // merge the group's lists: each level inserts the partner's K entries
+    for (int o = 1; o < tpr; o <<= 1) {
+      float pk[K > 0 ? K : 1];
+      int pi[K > 0 ? K : 1];
 #pragma unroll
-      for (int j = 0; j < kMaxTopK; ++j)
-        if (j < k) denom += top_p[j];
-      const float inv_d = 1.0f / denom;
+      for (int j = 0; j < K; ++j) {
+        pk[j] = __shfl_xor_sync(0xffffffffu, top_key[j], o);
+        pi[j] = __shfl_xor_sync(0xffffffffu, top_id[j], o);
+      }
 #pragma unroll
-      for (int j = 0; j < kMaxTopK; ++j) {
-        if (j < k) {
-          p.ids[static_cast<int64_t>(t) * k + j] = top_id[j];
-          p.gates[static_cast<int64_t>(t) * k + j] = top_p[j] * inv_d;
+      for (int i = 0; i < K; ++i) {
+        float ck = pk[i];
+        int ci = pi[i];
+        bool placed = false;
+#pragma unroll
+        for (int j = 0; j < K; ++j) {
+          if (placed || before(ck, ci, top_key[j], top_id[j])) {
+            const float tk = top_key[j];
+            const int ti = top_id[j];
+            top_key[j] = ck;
+            top_id[j] = ci;
+            ck = tk;
+            ci = ti;
+            placed = true;
+          }
+        }
+      }
+    }
+    if (sub == 0) {
+      st->lse[rl] = valid ? (m + logf(s)) : 0.0f;
+      if (valid && K > 0) {
+        float denom = 0.0f;
+#pragma unroll
+        for (int j = 0; j < K; ++j) denom += row[top_id[j]];
+        const float inv_d = 1.0f / denom;
+#pragma unroll
+        for (int j = 0; j < K; ++j) {
+          p.ids[static_cast<int64_t>(t) * K + j] = top_id[j];
+          p.gates[static_cast<int64_t>(t) * K + j] = row[top_id[j]] * inv_d;
           atomicAdd(&st->hist[top_id[j]], 1);
         }
       }
     }
-    // the 128 epilogue threads meet, then reduce the tile partials in a fixed
-    // order: warp w sums rows 32w..32w+31 per expert, then the four warp sums
-    asm volatile("bar.sync 1, 128;" ::: "memory");
-    const int rows_valid = min(128, p.T - tile * 128);
-    float* wsum = lg + static_cast<size_t>(S) * geo.part_floats;  // [4][E] (after the parts)
-    for (int e = lane; e < E; e += 32) {
+    // this CTA's contribution to the tile partials, into slot [rank] of the
+    // cluster's rank-0 CTA (fixed row order inside, rank order across)
+    asm volatile("bar.sync 1, %0;" ::"r"(kEpiThreads) : "memory");
+    const int rows_valid =
+        max(0, min(rpc, p.T - (tile * 128 + static_cast<int>(rank) * rpc)));
+    const bool remote = rank != 0;
+    for (int e = eidx; e < E; e += kEpiThreads) {
       float acc = 0.0f;
-      const int r1 = min(rows_valid, quarter * 32 + 32);
-      for (int rr = quarter * 32; rr < r1; ++rr) acc += lg[rr * ldl + e];
-      wsum[quarter * E + e] = acc;
+      for (int rr = 0; rr < rows_valid; ++rr)
+        acc += lg[(static_cast<int>(rank) * rpc + rr) * ldl + e];
+      if (remote) {
+        st_dsmem_f32(mapa_shared(smem_u32(&st->slot_colsum[rank][e]), 0), acc);
+        st_dsmem_s32(mapa_shared(smem_u32(&st->slot_hist[rank][e]), 0), st->hist[e]);
+      } else {
+        st->slot_colsum[0][e] = acc;
+        st->slot_hist[0][e] = st->hist[e];
+      }
     }
-    float z = st->lse[r] * st->lse[r];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
-    if (lane == 0) st->zw[quarter] = z;
-    asm volatile("bar.sync 1, 128;" ::: "memory");
-    const int et = threadIdx.x - 64;
-    for (int e = et; e < E; e += 128) {
-      p.tile_psum[static_cast<int64_t>(tile) * E + e] =
-          ((wsum[e] + wsum[E + e]) + wsum[2 * E + e]) + wsum[3 * E + e];
-      p.tile_hist[static_cast<int64_t>(tile) * E + e] = st->hist[e];
+    if (eidx == 0) {
+      float z = 0.0f;
+      for (int rr = 0; rr < rows_valid; ++rr) z += st->lse[rr] * st->lse[rr];
+      if (remote)
+        st_dsmem_f32(mapa_shared(smem_u32(&st->slot_lse2[rank]), 0), z);
+      else
+        st->slot_lse2[0] = z;
     }
-    if (et == 0) p.tile_lse2[tile] = ((st->zw[0] + st->zw[1]) + st->zw[2]) + st->zw[3];
   }
-
+  if (S > 1)
+    cluster_arrive_wait();
+  else
+    __syncthreads();
+  if (rank == 0 && eidx >= 0 && !*abort_flag) {
+    for (int e = eidx; e < E; e += kEpiThreads) {
+      float acc = 0.0f;
+      int h = 0;
+      for (int q = 0; q < S; ++q) {
+        acc += st->slot_colsum[q][e];
+        h += st->slot_hist[q][e];
+      }
+      p.tile_psum[static_cast<int64_t>(tile) * E + e] = acc;
+      p.tile_hist[static_cast<int64_t>(tile) * E + e] = h;
+    }
+    if (eidx == 0) {
+      float z = 0.0f;
+      for (int q = 0; q < S; ++q) z += st->slot_lse2[q];
+      p.tile_lse2[tile] = z;
+    }
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -342,11 +403,9 @@ int launch_router(const CUtensorMap& x_map, const CUtensorMap& wr_map, RouterArg
   const int nk = args.d / kBK;
   const size_t tail = sizeof(RouterSmemTail) + 1024;
   // Split K over a cluster while the grid still fits one wave (one CTA per
-  // SM), each CTA keeps >= 2 k-blocks and the S partial tiles fit the ring.
+  // SM) and each CTA keeps >= 2 k-blocks.
   int S = 1;
-  while (S < 8 && ntiles * 2 * S <= num_sms && nk / (2 * S) >= 2 &&
-         router_geom(args.E, 1, 2 * S).main_bytes + tail <= 200 * 1024)
-    S *= 2;
+  while (S < kMaxSplit && ntiles * 2 * S <= num_sms && nk / (2 * S) >= 2) S *= 2;
   const int nk_local = (nk + S - 1) / S;
   const int stage_bytes = router_geom(args.E, 1, S).stage_bytes;
   // With more tiles than SMs, size shared memory for two CTAs per SM.
@@ -360,12 +419,25 @@ int launch_router(const CUtensorMap& x_map, const CUtensorMap& wr_map, RouterArg
   const RouterGeom geo = router_geom(args.E, stages, S);
   const size_t smem = tail + geo.main_bytes;
   if (smem > 227 * 1024) return -2;
-  static bool attr = false;
-  if (!attr) {
-    if (cudaFuncSetAttribute(router_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             227 * 1024) != cudaSuccess)
+  void (*kern)(const CUtensorMap, const CUtensorMap, const RouterArgs) = nullptr;
+  switch (args.k) {
+    case 0: kern = router_kernel<0>; break;
+    case 1: kern = router_kernel<1>; break;
+    case 2: kern = router_kernel<2>; break;
+    case 3: kern = router_kernel<3>; break;
+    case 4: kern = router_kernel<4>; break;
+    case 5: kern = router_kernel<5>; break;
+    case 6: kern = router_kernel<6>; break;
+    case 7: kern = router_kernel<7>; break;
+    case 8: kern = router_kernel<8>; break;
+    default: return -2;
+  }
+  static bool attr[kMaxTopK + 1] = {false};
+  if (!attr[args.k]) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) !=
+        cudaSuccess)
       return -3;
-    attr = true;
+    attr[args.k] = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(ntiles * S);
@@ -379,7 +451,7 @@ int launch_router(const CUtensorMap& x_map, const CUtensorMap& wr_map, RouterArg
   attrs[0].val.clusterDim.z = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, router_kernel, x_map, wr_map, args) != cudaSuccess) return -3;
+  if (cudaLaunchKernelEx(&cfg, kern, x_map, wr_map, args) != cudaSuccess) return -3;
   return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }
 
