@@ -64,7 +64,7 @@ def load(path: Optional[str] = None):
     lib = ctypes.CDLL(path)
     i32, f64 = ctypes.c_int, ctypes.c_double
     lib.oracle_router_logits.argtypes = [i32, i32, i32, _P, _P, _P, _P]
-    lib.oracle_route.argtypes = [i32, i32, i32, _P, _P, _P, _P, _P, _P, _P, _P, _P]
+    lib.oracle_route.argtypes = [i32, i32, i32, i32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]
     lib.oracle_capacity.argtypes = [f64, i32, i32, i32]
     lib.oracle_capacity.restype = ctypes.c_int64
     lib.oracle_dispatch.argtypes = [i32, i32, i32, _P, ctypes.c_int64, _P, _P, _P, _P, _P, _P]
@@ -73,6 +73,7 @@ def load(path: Optional[str] = None):
     lib.oracle_layer_tokens.argtypes = [i32] * 6 + [_P] * 10 + [i32, _P, _P]
     lib.oracle_losses.argtypes = [i32, i32, i32, _P, _P, _P, f64, _P, _P, _P, _P]
     lib.oracle_combine.argtypes = [i32, i32, i32, _P, _P, _P, _P, _P]
+    lib.oracle_importance.argtypes = [i32, i32, i32, _P, _P, _P, _P]
     if path == _LIB:
         _lib = lib
     return lib
@@ -106,16 +107,22 @@ def router_logits(x, wr, offset=None, lib=None) -> np.ndarray:
     return out
 
 
+SIGMOID = 1     # sigmoid scores instead of the softmax
+NO_RENORM = 2   # gates = selected scores, not renormalised
+
+
 @dataclass
 class Routing:
-    p: np.ndarray        # [T,E] softmax probabilities
+    p: np.ndarray        # [T,E] router scores (softmax probabilities, or sigmoids)
     lse: np.ndarray      # [T]   log-sum-exp of the logits
     ids: np.ndarray      # [T,k] selected experts, descending key
-    gates: np.ndarray    # [T,k] renormalised gates
+    gates: np.ndarray    # [T,k] gates (renormalised unless NO_RENORM)
     gap: np.ndarray      # [T]   key_k - key_{k+1}
+    entropy: np.ndarray  # [T]   entropy of the router distribution
 
 
-def route(logits, k, sel_bias=None, force_ids=None, force_mask=None, lib=None) -> Routing:
+def route(logits, k, sel_bias=None, force_ids=None, force_mask=None, flags=0,
+          lib=None) -> Routing:
     lib = lib or load()
     logits = np.ascontiguousarray(logits, np.float64)
     T, E = logits.shape
@@ -124,11 +131,24 @@ def route(logits, k, sel_bias=None, force_ids=None, force_mask=None, lib=None) -
     ids = np.empty((T, k), np.int32)
     gates = np.empty((T, k), np.float64)
     gap = np.empty(T, np.float64)
+    ent = np.empty(T, np.float64)
     fi = None if force_ids is None else np.ascontiguousarray(force_ids, np.int32)
     fm = None if force_mask is None else np.ascontiguousarray(force_mask, np.uint8)
-    lib.oracle_route(T, E, k, _ptr(logits), _ptr(_f32(sel_bias)), _ptr(fi), _ptr(fm),
-                     _ptr(p), _ptr(lse), _ptr(ids), _ptr(gates), _ptr(gap))
-    return Routing(p, lse, ids, gates, gap)
+    lib.oracle_route(T, E, k, int(flags), _ptr(logits), _ptr(_f32(sel_bias)), _ptr(fi),
+                     _ptr(fm), _ptr(p), _ptr(lse), _ptr(ids), _ptr(gates), _ptr(gap), _ptr(ent))
+    return Routing(p, lse, ids, gates, gap, ent)
+
+
+def importance(ids, gates, E: int, lib=None):
+    """(importance [E], CV^2) of the sparse gates, before any capacity cut."""
+    lib = lib or load()
+    ids = np.ascontiguousarray(ids, np.int32)
+    g = np.ascontiguousarray(gates, np.float64)
+    T, k = ids.shape
+    imp = np.empty(E, np.float64)
+    cv2 = ctypes.c_double()
+    lib.oracle_importance(T, E, k, _ptr(ids), _ptr(g), _ptr(imp), ctypes.byref(cv2))
+    return imp, cv2.value
 
 
 def capacity(c: float, k: int, T: int, E: int, lib=None) -> int:
@@ -257,14 +277,14 @@ class LayerResult:
 
 def layer_forward(x, wr, w1, w3, w2, k, offset=None, sel_bias=None, ws1=None, ws3=None,
                   ws2=None, capacity_factor=0.0, lam=0.01, force_ids=None, force_mask=None,
-                  sel=None, lib=None) -> LayerResult:
+                  sel=None, flags=0, lib=None) -> LayerResult:
     """Full oracle forward.  ``sel`` picks the tokens whose output y is computed
     (all by default; routing, dispatch and losses always cover every token)."""
     lib = lib or load()
     T = x.shape[0]
     E = wr.shape[0]
     logits = router_logits(x, wr, offset, lib=lib)
-    r = route(logits, k, sel_bias, force_ids, force_mask, lib=lib)
+    r = route(logits, k, sel_bias, force_ids, force_mask, flags=flags, lib=lib)
     C = capacity(capacity_factor, k, T, E, lib=lib)
     disp = dispatch(r.ids, E, C, lib=lib)
     ls = losses(disp.counts, r.p, r.lse, k, lam, lib=lib)

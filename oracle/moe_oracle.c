@@ -105,9 +105,23 @@ static int keyed_cmp(const void *pa, const void *pb)
 /* lower-precision implementation may legitimately flip); the gates are then   */
 /* computed for that set by the same Eq.(2).                                   */
 /* ------------------------------------------------------------------------- */
-void oracle_route(int T, int E, int k, const double *logits, const float *sel_bias,
+/* Variants (flags):                                                            */
+/*  ORACLE_SIGMOID   scores s_e = 1 / (1 + exp(-l_e)), each expert on its own,  */
+/*                   instead of the softmax (the CSDN note, §9: DeepSeek-V3     */
+/*                   moved the gate from softmax to sigmoid); p below then     */
+/*                   holds s                                                    */
+/*  ORACLE_NO_RENORM gates are the selected scores themselves, not divided by  */
+/*                   their sum ("MoE：条件计算与路由" §7: without the renormal-  */
+/*                   isation the output scale follows the dropped mass)         */
+/* entropy[t] (optional) = -sum_e q_e log q_e of the router distribution q     */
+/* ("MoE：条件计算与路由" §9), q = p for the softmax, q = s / sum s for sigmoid.  */
+#define ORACLE_SIGMOID 1
+#define ORACLE_NO_RENORM 2
+
+void oracle_route(int T, int E, int k, int flags, const double *logits, const float *sel_bias,
                   const int32_t *force_ids, const uint8_t *force_mask,
-                  double *p, double *lse, int32_t *ids, double *gates, double *gap)
+                  double *p, double *lse, int32_t *ids, double *gates, double *gap,
+                  double *entropy)
 {
 #pragma omp parallel
     {
@@ -123,6 +137,17 @@ void oracle_route(int T, int E, int k, const double *logits, const float *sel_bi
             for (int e = 0; e < E; ++e) s += exp(l[e] - m);
             for (int e = 0; e < E; ++e) pt[e] = exp(l[e] - m) / s;
             lse[t] = m + log(s);
+            if (flags & ORACLE_SIGMOID)
+                for (int e = 0; e < E; ++e) pt[e] = 1.0 / (1.0 + exp(-l[e]));
+            if (entropy) {
+                double qs = 0.0, h = 0.0;
+                for (int e = 0; e < E; ++e) qs += pt[e];
+                for (int e = 0; e < E; ++e) {
+                    double q = pt[e] / qs;
+                    if (q > 0.0) h -= q * log(q);
+                }
+                entropy[t] = h;
+            }
 
             for (int e = 0; e < E; ++e) {
                 ord[e].key = pt[e] + (sel_bias ? (double)sel_bias[e] : 0.0);
@@ -139,6 +164,7 @@ void oracle_route(int T, int E, int k, const double *logits, const float *sel_bi
             }
             double denom = 0.0;
             for (int s2 = 0; s2 < k; ++s2) denom += pt[it[s2]];
+            if (flags & ORACLE_NO_RENORM) denom = 1.0;
             for (int s2 = 0; s2 < k; ++s2) gates[(size_t)t * k + s2] = pt[it[s2]] / denom;
         }
         free(ord);
@@ -339,4 +365,28 @@ void oracle_combine(int T, int d, int k, const uint16_t *y_perm, const int32_t *
         if (y_shared)
             for (int o = 0; o < d; ++o) yt[o] += bf16_val(y_shared[(size_t)t * d + o]);
     }
+}
+
+/* ------------------------------------------------------------------------- */
+/* Importance of each expert over the batch and its squared coefficient of    */
+/* variation (the CSDN note, "Balancing Expert Utilization": Importance(X) =  */
+/* sum_x G(x), L_importance = w * CV(Importance)^2).  G(x) is the sparse gate */
+/* vector: the token's gates on its selected experts, zero elsewhere (before  */
+/* any capacity cut).  CV = population standard deviation / mean over the E   */
+/* experts; reported as 0 when the mean is 0.                                */
+/* ------------------------------------------------------------------------- */
+void oracle_importance(int T, int E, int k, const int32_t *ids, const double *gates,
+                       double *importance, double *cv2)
+{
+    for (int e = 0; e < E; ++e) importance[e] = 0.0;
+    for (int t = 0; t < T; ++t)
+        for (int s = 0; s < k; ++s)
+            importance[ids[(size_t)t * k + s]] += gates[(size_t)t * k + s];
+    double mean = 0.0;
+    for (int e = 0; e < E; ++e) mean += importance[e];
+    mean /= (double)E;
+    double var = 0.0;
+    for (int e = 0; e < E; ++e) var += (importance[e] - mean) * (importance[e] - mean);
+    var /= (double)E;
+    *cv2 = (mean != 0.0) ? var / (mean * mean) : 0.0;
 }

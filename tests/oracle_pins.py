@@ -365,6 +365,54 @@ def pin_combine(lib):
     _close(yc, res.y, 2e-2 * np.abs(res.y).max(), "combine vs layer")
 
 
-ALL_PINS = [pin_combine, pin_hand_routing, pin_hand_capacity, pin_hand_shared_k0, pin_two_gating_formulas,
+def pin_routing_variants(lib):
+    """Sigmoid scores and un-renormalised gates on a hand-worked token
+    (CSDN note §9; "MoE：条件计算与路由" §7), with closed-form values."""
+    sig2, sig1 = 0.8807970779778823, 0.7310585786300049
+    logits = np.array([[2.0, 1.0, 0.0, -1.0]])
+    r = oracle.route(logits, 2, flags=oracle.SIGMOID, lib=lib)
+    assert r.ids.tolist() == [[0, 1]]
+    _close(r.p[0], [sig2, sig1, 0.5, 1.0 - sig1], 1e-15, "sigmoid scores")
+    _close(r.gates[0], [sig2 / (sig2 + sig1), sig1 / (sig2 + sig1)], 1e-15, "sigmoid renorm")
+    r = oracle.route(logits, 2, flags=oracle.SIGMOID | oracle.NO_RENORM, lib=lib)
+    _close(r.gates[0], [sig2, sig1], 1e-15, "sigmoid raw gates")
+    r = oracle.route(logits, 2, flags=oracle.NO_RENORM, lib=lib)
+    g = _hand()["expect"]["p"][0]
+    _close(r.gates[0], g[:2], 1e-15, "softmax raw gates")
+    _close(r.lse, oracle.route(logits, 2, lib=lib).lse, 0.0, "lse independent of the scores")
+    # un-renormalised softmax gates with k = E: the same soft mixture (they sum to 1)
+    rng = np.random.default_rng(21)
+    x, wr, w1, w3, w2, _ = rand_problem(rng, 20, 8, 4, 4, 4)
+    a = oracle.layer_forward(x, wr, w1, w3, w2, 4, lib=lib)
+    b = oracle.layer_forward(x, wr, w1, w3, w2, 4, flags=oracle.NO_RENORM, lib=lib)
+    _close(a.y, b.y, 1e-12 * np.abs(a.y).max(), "k=E renorm or not")
+    # sigmoid routing selects the largest logits (sigmoid is increasing)
+    lg = rng.standard_normal((30, 9))
+    rs = oracle.route(lg, 3, flags=oracle.SIGMOID, lib=lib)
+    assert rs.ids.tolist() == np.argsort(-lg, axis=1, kind="stable")[:, :3].tolist()
+
+
+def pin_entropy_and_importance(lib):
+    """Router entropy ("MoE：条件计算与路由" §9) and the importance CV^2 (CSDN
+    note, balancing expert utilization) against closed forms and scipy."""
+    from scipy.stats import entropy as sp_entropy
+    r = oracle.route(np.array([[0.0, np.log(3.0)], [1.0, 1.0]]), 1, lib=lib)
+    _close(r.entropy, [0.5623351446188083, np.log(2.0)], 1e-14, "entropy closed forms")
+    rng = np.random.default_rng(22)
+    lg = rng.standard_normal((25, 12)) * 2
+    r = oracle.route(lg, 3, lib=lib)
+    _close(r.entropy, sp_entropy(r.p, axis=1), 1e-12, "entropy vs scipy")
+    rs = oracle.route(lg, 3, flags=oracle.SIGMOID, lib=lib)
+    q = rs.p / rs.p.sum(1, keepdims=True)
+    _close(rs.entropy, sp_entropy(q, axis=1), 1e-12, "sigmoid entropy vs scipy")
+    imp, cv2 = oracle.importance(np.array([[0, 1], [2, 0]]), np.array([[0.75, 0.25], [0.5, 0.5]]),
+                                 4, lib=lib)
+    _close(imp, [1.25, 0.25, 0.5, 0.0], 1e-15, "importance")
+    _close(cv2, 0.875, 1e-15, "importance CV^2")
+    imp, cv2 = oracle.importance(np.array([[0, 1], [1, 0]]), np.full((2, 2), 0.5), 2, lib=lib)
+    assert cv2 == 0.0
+
+
+ALL_PINS = [pin_routing_variants, pin_entropy_and_importance, pin_combine, pin_hand_routing, pin_hand_capacity, pin_hand_shared_k0, pin_two_gating_formulas,
             pin_bruteforce_subsets, pin_dispatch_argsort, pin_capacity_formula, pin_invariants,
             pin_determinism, pin_gap_and_force]

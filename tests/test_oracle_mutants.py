@@ -39,6 +39,10 @@ MUTANTS = {
     "zloss_not_squared": ("sz += lse[t] * lse[t];", "sz += lse[t];"),
     "f_over_T": ("(double)counts[e] / ((double)k * (double)T)", "(double)counts[e] / (double)T"),
     "balance_without_E": ("*L_bal = lambda * (double)E * sfp;", "*L_bal = lambda * sfp;"),
+    "sigmoid_sign": ("pt[e] = 1.0 / (1.0 + exp(-l[e]));", "pt[e] = 1.0 / (1.0 + exp(l[e]));"),
+    "no_renorm_ignored": ("if (flags & ORACLE_NO_RENORM) denom = 1.0;", "(void)0;"),
+    "entropy_sign": ("if (q > 0.0) h -= q * log(q);", "if (q > 0.0) h += q * log(q);"),
+    "importance_sample_variance": ("    var /= (double)E;", "    var /= (double)(E - 1);"),
     "combine_drop_ignored": ("if (r < 0) continue;\n            double g", "if (r < 0) r = 0;\n            double g"),
     "combine_shared_missing": ("yt[o] += bf16_val(y_shared[(size_t)t * d + o]);", "yt[o] += 0.0;"),
 }
