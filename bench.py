@@ -50,6 +50,24 @@ def parse_args(argv=None):
     return ap.parse_args(argv)
 
 
+def recorded_traffic(workload: str, kernel: str):
+    """DRAM bytes (read + write) per launch of `kernel` from the committed ncu
+    summary, or None when the kernel's sources changed since that capture."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as fh:
+            rec = json.load(fh)[workload]
+        if rec["kernel"] != kernel:
+            return None
+        h = hashlib.sha256()
+        for f in rec["kernel_sources"]:
+            with open(os.path.join(ROOT, f), "rb") as fh:
+                h.update(fh.read())
+        return rec["traffic_bytes"] if h.hexdigest() == rec["sources_sha256"] else None
+    except Exception:
+        return None
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -428,7 +446,8 @@ def run_ours(args, w):
         "stage_frac_of_hbm": {k: v / peaks["hbm_gbs"] for k, v in stage_gbs.items()},
         "roofline": {"bound": "tensor", "kernel": dom, "achieved": ach,
                      "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                     "frac": ach / peaks["bf16_tflops"], "traffic": None,
+                     "frac": ach / peaks["bf16_tflops"],
+                     "traffic": recorded_traffic(w.name, dom),
                      "peak_source": f"bf16_tflops burst, {peak_src}",
                      "frac_of_sustained": ach / peaks["bf16_tflops_sustained"],
                      "algorithmic_flops_per_launch": flops[dom]},

@@ -57,6 +57,17 @@ extern "C" {
 #define MOE_MAX_EXPERTS 256
 #define MOE_MAX_TOPK 8
 
+/* Routing variants, set in moe_shape_t.flags:
+ *   MOE_FLAG_SIGMOID    scores s_e = sigmoid(l_e), each expert on its own,
+ *                       instead of the softmax (CSDN note, §9: DeepSeek-V3
+ *                       moved the gate from softmax to sigmoid); selection on
+ *                       s_e + b_e; P_e is the mean score; the z-loss still
+ *                       uses log sum exp of the logits.
+ *   MOE_FLAG_NO_RENORM  gates are the selected scores themselves, not divided
+ *                       by their sum ("MoE：条件计算与路由" §7).              */
+#define MOE_FLAG_SIGMOID 1u
+#define MOE_FLAG_NO_RENORM 2u
+
 /* Layer shape.
  *   T  tokens;  d  model width;  M  expert intermediate width;
  *   E  routed experts;  k  experts per token;  n_shared  shared experts,
@@ -114,6 +125,32 @@ int moe_route(const moe_shape_t *shape, const uint16_t *x, const uint16_t *w_rou
               const float *logit_offset, const float *sel_bias, int32_t *ids, float *gates,
               int32_t *counts, float *f, float *P, float *bal_loss, float *z_loss, void *ws,
               size_t ws_bytes, void *stream);
+
+/* Router with every output in one struct, including two optional side
+ * outputs (NULL = not computed):
+ *   importance [E]  sum over tokens of each expert's gate (before capacity),
+ *   importance_cv2 [1]  (population std / mean of importance)^2 over experts
+ *                   (CSDN note, balancing expert utilization:
+ *                   L_importance = w * CV(Importance)^2; w is the caller's),
+ *   entropy_mean [1]  mean over tokens of -sum_e q_e log q_e of the router
+ *                   distribution q (softmax; normalised sigmoid scores with
+ *                   MOE_FLAG_SIGMOID) ("MoE：条件计算与路由" §9).
+ * The other fields are those of moe_route (ids/gates may be NULL when k = 0).*/
+typedef struct moe_route_out {
+    int32_t *ids;
+    float *gates;
+    int32_t *counts;
+    float *f;
+    float *P;
+    float *bal_loss;
+    float *z_loss;
+    float *importance;
+    float *importance_cv2;
+    float *entropy_mean;
+} moe_route_out_t;
+int moe_route_ex(const moe_shape_t *shape, const uint16_t *x, const uint16_t *w_router,
+                 const float *logit_offset, const float *sel_bias, const moe_route_out_t *out,
+                 void *ws, size_t ws_bytes, void *stream);
 
 /* Dispatch: capacity cut and permutation into expert-contiguous rows (CSDN
  * note, moe_infer's histogram + argsort; capacity "MoE：条件计算与路由" §3).

@@ -148,6 +148,7 @@ class Workload:
     w_std: float = 0.02
     balance_coef: float = 0.01
     seed: int = 0
+    flags: int = 0                    # routing variant bits (sigmoid scores, no renorm)
 
     @property
     def Ms(self) -> int:

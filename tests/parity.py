@@ -33,7 +33,7 @@ GATE_ABS = 1e-5
 
 def shape_of(w: synth.Workload) -> moe.Shape:
     return moe.Shape.of(w.T, w.d, w.M, w.E, w.k, w.n_shared, w.capacity_factor,
-                        w.balance_coef)
+                        w.balance_coef, w.flags)
 
 
 def np_of(t: Optional[torch.Tensor]):
@@ -116,11 +116,11 @@ def oracle_routing(inp: synth.Inputs, gpu_ids: np.ndarray) -> OracleRef:
     off = np_of(inp.offset)
     bias = np_of(inp.sel_bias)
     logits = oracle.router_logits(x, wr, off)
-    free = oracle.route(logits, w.k, bias)
+    free = oracle.route(logits, w.k, bias, flags=w.flags)
     exempt = free.gap < TIE
     if w.k > 0:
         force = routing_force_mask(free, gpu_ids, bias)
-        r = oracle.route(logits, w.k, bias, force_ids=gpu_ids, force_mask=force)
+        r = oracle.route(logits, w.k, bias, force_ids=gpu_ids, force_mask=force, flags=w.flags)
         exempt = force
     else:
         r = free

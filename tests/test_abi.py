@@ -63,7 +63,7 @@ def shape(**kw):
     (dict(M=200), B.MOE_ERR_UNSUPPORTED),            # M % 128
     (dict(E=300, k=2), B.MOE_ERR_UNSUPPORTED),
     (dict(E=16, k=9), B.MOE_ERR_UNSUPPORTED),        # k > 8
-    (dict(flags=1), B.MOE_ERR_UNSUPPORTED),
+    (dict(flags=4), B.MOE_ERR_UNSUPPORTED),
     (dict(n_shared=9), B.MOE_ERR_UNSUPPORTED),
     (dict(capacity_factor=float("nan")), B.MOE_ERR_INVALID_ARG),
 ])

@@ -29,6 +29,16 @@ class MoeError(RuntimeError):
         super().__init__(f"{where}: {moe_error_string(code)} ({code})")
 
 
+MOE_FLAG_SIGMOID = 1
+MOE_FLAG_NO_RENORM = 2
+
+
+class RouteOut(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("ids", "gates", "counts", "f", "P", "bal_loss",
+                                                "z_loss", "importance", "importance_cv2",
+                                                "entropy_mean")]
+
+
 class Shape(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int32), ("d", ctypes.c_int32), ("M", ctypes.c_int32),
                 ("E", ctypes.c_int32), ("k", ctypes.c_int32), ("n_shared", ctypes.c_int32),
@@ -74,11 +84,13 @@ def lib():
     L.moe_profile_collect.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_int), _P, _P]
     L.moe_launch_count.argtypes = [ctypes.POINTER(ctypes.c_uint64)]
     L.moe_route_noalloc.argtypes = [S] + [_P] * 11 + [_P]
+    L.moe_route_ex.argtypes = [S, _P, _P, _P, _P, ctypes.POINTER(RouteOut), _P, sz, _P]
     for name in ("moe_workspace_size", "moe_capacity", "moe_max_rows", "moe_pack_w13",
                  "moe_route", "moe_permute", "moe_grouped_ffn", "moe_combine",
                  "moe_layer_forward", "moe_layer_forward_host", "moe_check_status",
                  "moe_set_wait_timeout_ns", "moe_debug_timeout_probe", "moe_profile_enable",
-                 "moe_profile_collect", "moe_launch_count", "moe_route_noalloc"):
+                 "moe_profile_collect", "moe_launch_count", "moe_route_noalloc",
+                 "moe_route_ex"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -150,6 +162,18 @@ def moe_route(shape, x, w_router, logit_offset, sel_bias, ids, gates, counts, f,
                            _ptr(sel_bias), _ptr(ids), _ptr(gates), _ptr(counts), _ptr(f),
                            _ptr(P), _ptr(bal_loss), _ptr(z_loss), _ptr(ws), ws.numel(),
                            _stream(stream)), "moe_route")
+
+
+def moe_route_ex(shape, x, w_router, logit_offset, sel_bias, ws, ids=None, gates=None,
+                 counts=None, f=None, P=None, bal_loss=None, z_loss=None, importance=None,
+                 importance_cv2=None, entropy_mean=None, stream=None):
+    """moe_route with the optional side outputs (importance, its CV^2, mean
+    router entropy); every output is a device tensor or None."""
+    out = RouteOut(*[None if t is None else t.data_ptr() for t in (
+        ids, gates, counts, f, P, bal_loss, z_loss, importance, importance_cv2, entropy_mean)])
+    _check(lib().moe_route_ex(ctypes.byref(shape), _ptr(x), _ptr(w_router), _ptr(logit_offset),
+                              _ptr(sel_bias), ctypes.byref(out), _ptr(ws), ws.numel(),
+                              _stream(stream)), "moe_route_ex")
 
 
 def moe_route_noalloc(shape, x, w_router, logit_offset, sel_bias, ids, gates, counts, f, P,

@@ -63,6 +63,7 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 // Workspace regions (byte offsets from the workspace base).
 struct Layout {
   size_t status, tile_hist, tile_psum, tile_lse2, tile_base, exp_count, exp_psum, offsets;
+  size_t tile_imp, tile_ent, exp_imp;
   size_t slot_row, row_token;
   size_t x_perm, h, y_perm, h_s, y_s, total;
   int64_t ntiles, rmax, C;
@@ -75,7 +76,7 @@ int check_shape(const moe_shape_t* s) {
   if (s->k > s->E) return MOE_ERR_INVALID_ARG;
   if (!std::isfinite(s->capacity_factor) || !std::isfinite(s->balance_coef))
     return MOE_ERR_INVALID_ARG;
-  if (s->flags != 0) return MOE_ERR_UNSUPPORTED;
+  if ((s->flags & ~(MOE_FLAG_SIGMOID | MOE_FLAG_NO_RENORM)) != 0) return MOE_ERR_UNSUPPORTED;
   if (s->E > MOE_MAX_EXPERTS || s->k > MOE_MAX_TOPK) return MOE_ERR_UNSUPPORTED;
   if (s->T > (1 << 24)) return MOE_ERR_UNSUPPORTED;
   if (s->d % 64 != 0 || s->d < 64 || s->d > 16384) return MOE_ERR_UNSUPPORTED;
@@ -113,6 +114,9 @@ Layout layout_of(const moe_shape_t* s) {
   L.tile_base = take(L.ntiles * E * 4);
   L.exp_count = take(E * 4);
   L.exp_psum = take(E * 8);
+  L.tile_imp = take(L.ntiles * E * 4);
+  L.tile_ent = take(L.ntiles * 4);
+  L.exp_imp = take(E * 8);
   L.offsets = take((E + 1) * 4);
   L.slot_row = take(T * k * 4);
   L.row_token = take(L.rmax * 4);
@@ -161,7 +165,10 @@ inline int cuda_rc(int rc) {
 int do_route(const moe_shape_t* s, const uint16_t* x, const uint16_t* wr, const float* off,
              const float* bias, int32_t* ids, float* gates, int32_t* counts, float* f, float* P,
              float* bal, float* z, void* ws, const Layout& L, int32_t* tile_base,
-             int32_t* offsets, cudaStream_t st) {
+             int32_t* offsets, cudaStream_t st, float* importance = nullptr,
+             float* importance_cv2 = nullptr, float* entropy_mean = nullptr) {
+  const bool want_imp = (importance != nullptr || importance_cv2 != nullptr) && s->k > 0;
+  const bool want_ent = entropy_mean != nullptr;
   if (s->T > 0) {
     CUtensorMap mx, mw;
     const uint32_t nr = static_cast<uint32_t>((s->E + 15) / 16 * 16);
@@ -181,6 +188,9 @@ int do_route(const moe_shape_t* s, const uint16_t* x, const uint16_t* wr, const 
     ra.tile_lse2 = at<float>(ws, L.tile_lse2);
     ra.status = at<int>(ws, L.status);
     ra.timeout_ns = g_timeout_ns;
+    ra.flags = s->flags;
+    ra.tile_imp = want_imp ? at<float>(ws, L.tile_imp) : nullptr;
+    ra.tile_ent = want_ent ? at<float>(ws, L.tile_ent) : nullptr;
     const int rc = tracked(MOE_KERNEL_ROUTER, st, [&] { return launch_router(mx, mw, ra, sm_count_cached(), st); });
     if (rc != 0) return cuda_rc(rc);
   }
@@ -203,6 +213,21 @@ int do_route(const moe_shape_t* s, const uint16_t* x, const uint16_t* wr, const 
   fa.exp_count = at<int32_t>(ws, L.exp_count);
   fa.exp_psum = at<double>(ws, L.exp_psum);
   fa.done_counter = at<int>(ws, L.status + 64);
+  if (want_imp) {
+    fa.tile_imp = at<float>(ws, L.tile_imp);
+    fa.exp_imp = at<double>(ws, L.exp_imp);
+    fa.importance = importance;
+    fa.importance_cv2 = importance_cv2;
+    if (s->T == 0) {  // no router launch wrote the partials
+      if (importance) cudaMemsetAsync(importance, 0, sizeof(float) * s->E, st);
+      if (importance_cv2) cudaMemsetAsync(importance_cv2, 0, sizeof(float), st);
+      fa.tile_imp = nullptr;
+    }
+  }
+  if (want_ent) {
+    fa.tile_ent = at<float>(ws, L.tile_ent);
+    fa.entropy_mean = entropy_mean;
+  }
   return cuda_rc(tracked(MOE_KERNEL_FINALIZE, st, [&] { return launch_finalize(fa, st); }));
 }
 
@@ -375,6 +400,24 @@ int moe_route(const moe_shape_t* s, const uint16_t* x, const uint16_t* w_router,
   }
   return do_route(s, x, w_router, logit_offset, sel_bias, ids, gates, counts, f, P, bal_loss,
                   z_loss, ws, L, nullptr, nullptr, static_cast<cudaStream_t>(stream));
+}
+
+int moe_route_ex(const moe_shape_t* s, const uint16_t* x, const uint16_t* w_router,
+                 const float* logit_offset, const float* sel_bias, const moe_route_out_t* o,
+                 void* ws, size_t ws_bytes, void* stream) {
+  int rc = check_shape(s);
+  if (rc != MOE_OK) return rc;
+  Layout L;
+  if ((rc = check_ws(s, ws, ws_bytes, &L)) != MOE_OK) return rc;
+  if (!o || !o->counts || !o->f || !o->P || !o->bal_loss || !o->z_loss) return MOE_ERR_INVALID_ARG;
+  if (s->T > 0) {
+    if (!x || !w_router || !aligned16(x) || !aligned16(w_router)) return MOE_ERR_INVALID_ARG;
+    if (s->k > 0 && (!o->ids || !o->gates)) return MOE_ERR_INVALID_ARG;
+  }
+  return do_route(s, x, w_router, logit_offset, sel_bias, o->ids, o->gates, o->counts, o->f,
+                  o->P, o->bal_loss, o->z_loss, ws, L, nullptr, nullptr,
+                  static_cast<cudaStream_t>(stream), o->importance, o->importance_cv2,
+                  o->entropy_mean);
 }
 
 int moe_permute(const moe_shape_t* s, const uint16_t* x, const int32_t* ids, int32_t* offsets,

@@ -9,6 +9,9 @@ namespace moe {
 
 constexpr int kTileTokens = 128;  // tokens per router / permute tile (= MMA M)
 constexpr int kMaxTopK = 8;
+// routing variants (the values of MOE_FLAG_SIGMOID / MOE_FLAG_NO_RENORM)
+constexpr uint32_t kRouteSigmoid = 1u;
+constexpr uint32_t kRouteNoRenorm = 2u;
 
 // Ragged grouped GEMM  out[g] = A[g] * B[g]^T  over E routed groups (rows from
 // device offsets) and an optional shared group (fixed row count).
@@ -57,6 +60,9 @@ struct RouterArgs {
   uint64_t timeout_ns;
   int32_t split;              // CTAs of a cluster sharing one tile (set by the launcher)
   int32_t stages;             // pipeline depth (set by the launcher)
+  uint32_t flags;             // kRouteSigmoid | kRouteNoRenorm
+  float* tile_imp;            // [ntiles][E] importance partials, or null
+  float* tile_ent;            // [ntiles] entropy partials, or null
 };
 int launch_router(const CUtensorMap& x_map, const CUtensorMap& wr_map, RouterArgs args,
                   int num_sms, cudaStream_t stream);
@@ -84,6 +90,12 @@ struct FinalizeArgs {
   int32_t* exp_count;         // [E] scratch: per-expert totals
   double* exp_psum;           // [E] scratch
   int* done_counter;          // zero between calls; the last CTA resets it
+  const float* tile_imp;      // [ntiles][E] or null
+  const float* tile_ent;      // [ntiles] or null
+  double* exp_imp;            // [E] scratch (when tile_imp)
+  float* importance;          // [E] or null
+  float* importance_cv2;      // [1] or null
+  float* entropy_mean;        // [1] or null
 };
 int launch_finalize(const FinalizeArgs& args, cudaStream_t stream);
 

@@ -99,21 +99,24 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const FinalizeArg
   const int e = blockIdx.x;
   // ---- phase A: column e
   int carry = 0;
-  double psum = 0.0;
+  double psum = 0.0, isum = 0.0;
   for (int c0 = 0; c0 < ntiles; c0 += kFinThreads) {
     const int tl = c0 + threadIdx.x;
     const int64_t idx = static_cast<int64_t>(tl) * E + e;
     const int h = tl < ntiles ? __ldcg(a.tile_hist + idx) : 0;
     if (a.tile_psum && tl < ntiles) psum += static_cast<double>(__ldcg(a.tile_psum + idx));
+    if (a.tile_imp && tl < ntiles) isum += static_cast<double>(__ldcg(a.tile_imp + idx));
     int tot = 0;
     const int ex = block_exclusive_scan(h, warp_tot, &tot);
     if (a.tile_base && tl < ntiles) a.tile_base[idx] = carry + ex;
     carry += tot;
   }
   const double ps = block_sum(psum, red);
+  const double is = a.tile_imp ? block_sum(isum, red) : 0.0;
   if (threadIdx.x == 0) {
     a.exp_count[e] = carry;
     a.exp_psum[e] = ps;
+    if (a.tile_imp) a.exp_imp[e] = is;
     __threadfence();
     is_last = (atomicAdd(a.done_counter, 1) == static_cast<int>(gridDim.x) - 1);
   }
@@ -144,6 +147,23 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const FinalizeArg
   if (a.tile_lse2)
     for (int tl = j; tl < ntiles; tl += kFinThreads) z += static_cast<double>(__ldcg(a.tile_lse2 + tl));
   const double zs = block_sum(z, red);
+  if (a.tile_imp) {
+    // importance per expert and its squared coefficient of variation
+    // (population statistics over the E experts)
+    const double imp = j < E ? __ldcg(a.exp_imp + j) : 0.0;
+    if (j < E && a.importance) a.importance[j] = static_cast<float>(imp);
+    const double mean = block_sum(imp, red) / E;
+    const double dev = j < E ? (imp - mean) * (imp - mean) : 0.0;
+    const double var = block_sum(dev, red) / E;
+    if (j == 0 && a.importance_cv2)
+      *a.importance_cv2 = static_cast<float>(mean != 0.0 ? var / (mean * mean) : 0.0);
+  }
+  if (a.tile_ent) {
+    double h = 0.0;
+    for (int tl = j; tl < ntiles; tl += kFinThreads) h += static_cast<double>(__ldcg(a.tile_ent + tl));
+    const double hs = block_sum(h, red);
+    if (j == 0 && a.entropy_mean) *a.entropy_mean = (a.T > 0) ? static_cast<float>(hs / a.T) : 0.0f;
+  }
   if (j == 0) {
     if (a.bal_loss) *a.bal_loss = static_cast<float>(static_cast<double>(a.balance_coef) * E * sfp);
     if (a.z_loss) *a.z_loss = (a.T > 0) ? static_cast<float>(zs / a.T) : 0.0f;

@@ -120,6 +120,7 @@ extern "C" int moe_route_noalloc(const moe_shape_t* s, const uint16_t* x,
     ra.tile_lse2 = tile_lse2;
     ra.status = status;
     ra.timeout_ns = 2000000000ull;
+    ra.flags = s->flags;
     rc = launch_router(mx, mw, ra, num_sms, st);
     if (rc != 0) return rc == -2 ? MOE_ERR_UNSUPPORTED : MOE_ERR_CUDA;
   }

@@ -57,6 +57,9 @@ struct RouterSmemTail {
   float slot_colsum[kMaxSplit][256];
   int slot_hist[kMaxSplit][256];
   float slot_lse2[kMaxSplit];
+  float slot_imp[kMaxSplit][256];
+  float slot_ent[kMaxSplit];
+  float ent[128];
 };
 
 struct RouterGeom {
@@ -243,7 +246,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = static_cast<int>(rank) * rpc + rl;
     const int t = tile * 128 + r;
     const bool valid = t < p.T;
-    float* row = lg + r * ldl;  // receives the full logits, then exp, then p
+    float* row = lg + r * ldl;  // receives the full logits, then exp, then the scores
+    const bool sigmoid = (p.flags & kRouteSigmoid) != 0;
     float m = -INFINITY;
     for (int e = sub; e < E; e += tpr) {
       float v = 0.0f;
@@ -256,13 +260,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       m = fmaxf(m, v);
     }
     for (int o = 1; o < tpr; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    float s = 0.0f;
+    // softmax normaliser (also the z-loss's lse); with sigmoid scores the row
+    // keeps the logits for the next pass
+    float s = 0.0f, hs = 0.0f;  // hs: sum of ex * (l - m), for the entropy
     for (int e = sub; e < E; e += tpr) {
-      const float ex = __expf(row[e] - m);
-      row[e] = ex;
+      const float v = row[e];
+      const float ex = __expf(v - m);
+      if (!sigmoid) row[e] = ex;
       s += ex;
+      hs += ex * (v - m);
     }
-    for (int o = 1; o < tpr; o <<= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    for (int o = 1; o < tpr; o <<= 1) {
+      s += __shfl_xor_sync(0xffffffffu, s, o);
+      hs += __shfl_xor_sync(0xffffffffu, hs, o);
+    }
     const float inv_s = 1.0f / s;
     float top_key[K > 0 ? K : 1];
     int top_id[K > 0 ? K : 1];
@@ -272,9 +283,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       top_id[j] = 0x7fffffff;
     }
     float thresh = -INFINITY;  // K-th largest key of this thread so far
+    float ssum = 0.0f, slog = 0.0f;  // sigmoid: sum s, sum s log s (entropy)
     for (int e = sub; e < E; e += tpr) {
-      const float pe = row[e] * inv_s;
-      row[e] = valid ? pe : 0.0f;  // the row now holds p (gates, P partial)
+      float pe;
+      if (sigmoid) {
+        const float v = row[e];
+        const float en = __expf(-v);
+        pe = 1.0f / (1.0f + en);
+        ssum += pe;
+        if (pe > 0.0f) slog -= pe * log1pf(en);  // s log s = -s log(1 + e^-l)
+      } else {
+        pe = row[e] * inv_s;
+      }
+      row[e] = valid ? pe : 0.0f;  // the row now holds the scores (gates, P partial)
       const float key = pe + st->bias[e];
       // experts arrive in index order: strict '>' keeps equal keys in index order
       if (K > 0 && key > thresh) {
@@ -294,6 +315,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         thresh = top_key[K > 0 ? K - 1 : 0];
+      }
+    }
+    if (sigmoid) {
+      for (int o = 1; o < tpr; o <<= 1) {
+        ssum += __shfl_xor_sync(0xffffffffu, ssum, o);
+        slog += __shfl_xor_sync(0xffffffffu, slog, o);
       }
     }
     __syncwarp();  // the row's p values (written by the whole group) are visible
@@ -325,13 +352,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
+    // entropy of the router distribution: softmax log s - sum ex (l-m) / s;
+    // sigmoid q = s / sum s: log sum s - sum s log s / sum s
+    const float ent = sigmoid ? (logf(ssum) - slog / ssum) : (logf(s) - hs * inv_s);
+    const bool renorm = (p.flags & kRouteNoRenorm) == 0;
     if (sub == 0) {
       st->lse[rl] = valid ? (m + logf(s)) : 0.0f;
+      st->ent[rl] = valid ? ent : 0.0f;
       if (valid && K > 0) {
         float denom = 0.0f;
 #pragma unroll
         for (int j = 0; j < K; ++j) denom += row[top_id[j]];
-        const float inv_d = 1.0f / denom;
+        const float inv_d = renorm ? 1.0f / denom : 1.0f;
 #pragma unroll
         for (int j = 0; j < K; ++j) {
           p.ids[static_cast<int64_t>(t) * K + j] = top_id[j];
@@ -359,12 +391,40 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     if (eidx == 0) {
-      float z = 0.0f;
-      for (int rr = 0; rr < rows_valid; ++rr) z += st->lse[rr] * st->lse[rr];
-      if (remote)
+      float z = 0.0f, h = 0.0f;
+      for (int rr = 0; rr < rows_valid; ++rr) {
+        z += st->lse[rr] * st->lse[rr];
+        h += st->ent[rr];
+      }
+      if (remote) {
         st_dsmem_f32(mapa_shared(smem_u32(&st->slot_lse2[rank]), 0), z);
-      else
+        st_dsmem_f32(mapa_shared(smem_u32(&st->slot_ent[rank]), 0), h);
+      } else {
         st->slot_lse2[0] = z;
+        st->slot_ent[0] = h;
+      }
+    }
+    if (p.tile_imp != nullptr && K > 0) {
+      // importance: each row becomes its sparse gate vector (gates on the
+      // selected experts, 0 elsewhere), then the same fixed-order column sums
+      asm volatile("bar.sync 1, %0;" ::"r"(kEpiThreads) : "memory");
+      for (int e = sub; e < E; e += tpr) row[e] = 0.0f;
+      __syncwarp();
+      if (sub == 0 && valid) {
+#pragma unroll
+        for (int j = 0; j < K; ++j)
+          row[top_id[j]] = p.gates[static_cast<int64_t>(t) * K + j];
+      }
+      asm volatile("bar.sync 1, %0;" ::"r"(kEpiThreads) : "memory");
+      for (int e = eidx; e < E; e += kEpiThreads) {
+        float acc = 0.0f;
+        for (int rr = 0; rr < rows_valid; ++rr)
+          acc += lg[(static_cast<int>(rank) * rpc + rr) * ldl + e];
+        if (remote)
+          st_dsmem_f32(mapa_shared(smem_u32(&st->slot_imp[rank][e]), 0), acc);
+        else
+          st->slot_imp[0][e] = acc;
+      }
     }
   }
   if (S > 1)
@@ -383,9 +443,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       p.tile_hist[static_cast<int64_t>(tile) * E + e] = h;
     }
     if (eidx == 0) {
-      float z = 0.0f;
-      for (int q = 0; q < S; ++q) z += st->slot_lse2[q];
+      float z = 0.0f, h = 0.0f;
+      for (int q = 0; q < S; ++q) {
+        z += st->slot_lse2[q];
+        h += st->slot_ent[q];
+      }
       p.tile_lse2[tile] = z;
+      if (p.tile_ent) p.tile_ent[tile] = h;
+    }
+    if (p.tile_imp != nullptr && K > 0) {
+      for (int e = eidx; e < E; e += kEpiThreads) {
+        float acc = 0.0f;
+        for (int q = 0; q < S; ++q) acc += st->slot_imp[q][e];
+        p.tile_imp[static_cast<int64_t>(tile) * E + e] = acc;
+      }
     }
   }
   tc_fence_before();
