@@ -152,6 +152,15 @@ int moe_route_ex(const moe_shape_t *shape, const uint16_t *x, const uint16_t *w_
                  const float *logit_offset, const float *sel_bias, const moe_route_out_t *out,
                  void *ws, size_t ws_bytes, void *stream);
 
+/* ALF-LB selection-bias update ("MoE：条件计算与路由", ALF-LB section: the bias
+ * of an overloaded expert decreases, of an underloaded one increases, at rate
+ * gamma, outside any backward pass).  The pages give no formula; implemented:
+ *     b_e <- b_e + gamma * sign(k T / E - n_e),   sign(0) = 0,
+ * in place on sel_bias [E] fp32 (device), from counts [E] int32 (device, the
+ * counts output of moe_route for the same shape).  gamma >= 0.             */
+int moe_alf_bias_update(const moe_shape_t *shape, const int32_t *counts, float gamma,
+                        float *sel_bias, void *stream);
+
 /* Dispatch: capacity cut and permutation into expert-contiguous rows (CSDN
  * note, moe_infer's histogram + argsort; capacity "MoE：条件计算与路由" §3).
  *   x    [T][d] bf16;  ids [T][k] int32 (each in [0, E))

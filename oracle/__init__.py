@@ -74,6 +74,7 @@ def load(path: Optional[str] = None):
     lib.oracle_losses.argtypes = [i32, i32, i32, _P, _P, _P, f64, _P, _P, _P, _P]
     lib.oracle_combine.argtypes = [i32, i32, i32, _P, _P, _P, _P, _P]
     lib.oracle_importance.argtypes = [i32, i32, i32, _P, _P, _P, _P]
+    lib.oracle_alf_bias_update.argtypes = [i32, i32, i32, _P, ctypes.c_float, _P, _P]
     if path == _LIB:
         _lib = lib
     return lib
@@ -237,6 +238,17 @@ def combine(y_perm, slot_row, gates, y_shared=None, lib=None) -> np.ndarray:
     y = np.empty((T, d), np.float64)
     lib.oracle_combine(T, d, k, _ptr(y_perm), _ptr(slot_row), _ptr(g), _ptr(ys), _ptr(y))
     return y
+
+
+def alf_bias_update(counts, T: int, k: int, gamma: float, bias, lib=None) -> np.ndarray:
+    """ALF-LB step: b + gamma * sign(kT/E - n_e), fp32."""
+    lib = lib or load()
+    counts = np.ascontiguousarray(counts, np.int32)
+    E = counts.shape[0]
+    b = np.ascontiguousarray(bias, np.float32)
+    out = np.empty(E, np.float32)
+    lib.oracle_alf_bias_update(E, T, k, _ptr(counts), float(gamma), _ptr(b), _ptr(out))
+    return out
 
 
 @dataclass

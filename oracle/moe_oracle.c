@@ -390,3 +390,21 @@ void oracle_importance(int T, int E, int k, const int32_t *ids, const double *ga
     var /= (double)E;
     *cv2 = (mean != 0.0) ? var / (mean * mean) : 0.0;
 }
+
+/* ------------------------------------------------------------------------- */
+/* ALF-LB bias update ("MoE：条件计算与路由", ALF-LB section: the bias of an    */
+/* overloaded expert decreases, that of an underloaded expert increases, at  */
+/* rate gamma, outside the backward graph).  Reading of the unstated rule:   */
+/*   b_e <- b_e + gamma * sign(nbar - n_e),  nbar = k T / E,  sign(0) = 0,   */
+/* with b and gamma in fp32 and the sum rounded once to fp32.                */
+/* ------------------------------------------------------------------------- */
+void oracle_alf_bias_update(int E, int T, int k, const int32_t *counts, float gamma,
+                            const float *bias_in, float *bias_out)
+{
+    const double nbar = (double)k * (double)T / (double)E;
+    for (int e = 0; e < E; ++e) {
+        const double diff = nbar - (double)counts[e];
+        const double sgn = (diff > 0.0) ? 1.0 : ((diff < 0.0) ? -1.0 : 0.0);
+        bias_out[e] = (float)((double)bias_in[e] + (double)gamma * sgn);
+    }
+}

@@ -413,6 +413,27 @@ def pin_entropy_and_importance(lib):
     assert cv2 == 0.0
 
 
-ALL_PINS = [pin_routing_variants, pin_entropy_and_importance, pin_combine, pin_hand_routing, pin_hand_capacity, pin_hand_shared_k0, pin_two_gating_formulas,
+def pin_alf_bias_update(lib):
+    """ALF-LB: overloaded experts' bias goes down, underloaded up, balanced
+    unchanged (hand case); iterating the update on fixed logits with a strong
+    skew reduces the load imbalance (a wrong sign makes it grow)."""
+    b = oracle.alf_bias_update([5, 3, 4, 0], T=8, k=2, gamma=0.25,
+                               bias=np.array([0.0, 0.5, -0.5, 1.0], np.float32), lib=lib)
+    assert b.tolist() == [-0.25, 0.75, -0.5, 1.25]          # nbar = 4
+    rng = np.random.default_rng(31)
+    T, E, k = 512, 16, 2
+    logits = rng.standard_normal((T, E)) + np.linspace(2.0, -2.0, E)[None, :]
+    bias = np.zeros(E, np.float32)
+    first = None
+    for _ in range(300):
+        r = oracle.route(logits, k, bias, lib=lib)
+        n = np.bincount(r.ids.reshape(-1), minlength=E)
+        spread = n.max() / (k * T / E)
+        first = spread if first is None else first
+        bias = oracle.alf_bias_update(n, T, k, 0.002, bias, lib=lib)
+    assert first > 3.0 and spread < 1.5, (first, spread)
+
+
+ALL_PINS = [pin_alf_bias_update, pin_routing_variants, pin_entropy_and_importance, pin_combine, pin_hand_routing, pin_hand_capacity, pin_hand_shared_k0, pin_two_gating_formulas,
             pin_bruteforce_subsets, pin_dispatch_argsort, pin_capacity_formula, pin_invariants,
             pin_determinism, pin_gap_and_force]

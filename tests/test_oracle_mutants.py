@@ -43,6 +43,8 @@ MUTANTS = {
     "no_renorm_ignored": ("if (flags & ORACLE_NO_RENORM) denom = 1.0;", "(void)0;"),
     "entropy_sign": ("if (q > 0.0) h -= q * log(q);", "if (q > 0.0) h += q * log(q);"),
     "importance_sample_variance": ("    var /= (double)E;", "    var /= (double)(E - 1);"),
+    "alf_sign": ("const double diff = nbar - (double)counts[e];",
+                 "const double diff = (double)counts[e] - nbar;"),
     "combine_drop_ignored": ("if (r < 0) continue;\n            double g", "if (r < 0) r = 0;\n            double g"),
     "combine_shared_missing": ("yt[o] += bf16_val(y_shared[(size_t)t * d + o]);", "yt[o] += 0.0;"),
 }

@@ -85,12 +85,13 @@ def lib():
     L.moe_launch_count.argtypes = [ctypes.POINTER(ctypes.c_uint64)]
     L.moe_route_noalloc.argtypes = [S] + [_P] * 11 + [_P]
     L.moe_route_ex.argtypes = [S, _P, _P, _P, _P, ctypes.POINTER(RouteOut), _P, sz, _P]
+    L.moe_alf_bias_update.argtypes = [S, _P, ctypes.c_float, _P, _P]
     for name in ("moe_workspace_size", "moe_capacity", "moe_max_rows", "moe_pack_w13",
                  "moe_route", "moe_permute", "moe_grouped_ffn", "moe_combine",
                  "moe_layer_forward", "moe_layer_forward_host", "moe_check_status",
                  "moe_set_wait_timeout_ns", "moe_debug_timeout_probe", "moe_profile_enable",
                  "moe_profile_collect", "moe_launch_count", "moe_route_noalloc",
-                 "moe_route_ex"):
+                 "moe_route_ex", "moe_alf_bias_update"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -174,6 +175,12 @@ def moe_route_ex(shape, x, w_router, logit_offset, sel_bias, ws, ids=None, gates
     _check(lib().moe_route_ex(ctypes.byref(shape), _ptr(x), _ptr(w_router), _ptr(logit_offset),
                               _ptr(sel_bias), ctypes.byref(out), _ptr(ws), ws.numel(),
                               _stream(stream)), "moe_route_ex")
+
+
+def moe_alf_bias_update(shape, counts, gamma, sel_bias, stream=None):
+    """In place: sel_bias += gamma * sign(k T / E - counts) (device tensors)."""
+    _check(lib().moe_alf_bias_update(ctypes.byref(shape), _ptr(counts), float(gamma),
+                                     _ptr(sel_bias), _stream(stream)), "moe_alf_bias_update")
 
 
 def moe_route_noalloc(shape, x, w_router, logit_offset, sel_bias, ids, gates, counts, f, P,

@@ -565,6 +565,17 @@ int moe_layer_forward_host(const moe_shape_t* s, const uint16_t* x_host, uint16_
   return cudaStreamSynchronize(st) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
+int moe_alf_bias_update(const moe_shape_t* s, const int32_t* counts, float gamma, float* bias,
+                        void* stream) {
+  const int rc = check_shape(s);
+  if (rc != MOE_OK) return rc;
+  if (!counts || !bias || !std::isfinite(gamma) || gamma < 0.0f) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return cuda_rc(tracked(MOE_KERNEL_OTHER, st, [&] {
+    return launch_alf_bias_update(s->E, s->T, s->k, counts, gamma, bias, st);
+  }));
+}
+
 int moe_check_status(void* ws, int* status, void* stream) {
   if (!ws || !status) return MOE_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -109,6 +109,19 @@ __global__ void pack_w13_kernel(int32_t Mw, int32_t d, const uint16_t* __restric
   for (int v = threadIdx.x; v < d / 8; v += blockDim.x) d4[v] = s4[v];
 }
 
+// ALF-LB bias update ("MoE：条件计算与路由", ALF-LB: overloaded experts' bias
+// goes down, underloaded experts' up, rate gamma, outside the backward pass):
+// b_e <- b_e + gamma * sign(k T / E - n_e), sign(0) = 0, one fp32 rounding.
+__global__ void alf_bias_update_kernel(int32_t E, int32_t T, int32_t k,
+                                       const int32_t* __restrict__ counts, float gamma,
+                                       float* __restrict__ bias) {
+  const int e = blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= E) return;
+  const double diff = static_cast<double>(k) * T / E - static_cast<double>(counts[e]);
+  const float step = diff > 0.0 ? gamma : (diff < 0.0 ? -gamma : 0.0f);
+  bias[e] = bias[e] + step;
+}
+
 // Waits on a barrier that nothing signals; the bounded wait records a timeout
 // in *status and the kernel returns normally.
 __global__ void timeout_probe_kernel(int* status, uint64_t timeout_ns) {
@@ -151,6 +164,12 @@ int launch_pack_w13(int32_t G, int32_t Mw, int32_t d, const uint16_t* w1, const 
   if (rows == 0) return 0;
   if (rows > 0x7fffffffLL) return -2;
   pack_w13_kernel<<<static_cast<unsigned>(rows), 128, 0, stream>>>(Mw, d, w1, w3, w13);
+  return cudaGetLastError() == cudaSuccess ? 0 : -3;
+}
+
+int launch_alf_bias_update(int32_t E, int32_t T, int32_t k, const int32_t* counts, float gamma,
+                           float* bias, cudaStream_t stream) {
+  alf_bias_update_kernel<<<(E + 255) / 256, 256, 0, stream>>>(E, T, k, counts, gamma, bias);
   return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }
 

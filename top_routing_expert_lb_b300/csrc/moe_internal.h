@@ -124,6 +124,9 @@ int launch_pack_w13(int32_t G, int32_t Mw, int32_t d, const uint16_t* w1, const 
 
 int launch_timeout_probe(int* status, uint64_t timeout_ns, cudaStream_t stream);
 
+int launch_alf_bias_update(int32_t E, int32_t T, int32_t k, const int32_t* counts, float gamma,
+                           float* bias, cudaStream_t stream);
+
 int device_sm_count();
 
 }  // namespace moe
