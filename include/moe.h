@@ -276,8 +276,10 @@ int moe_route_noalloc(const moe_shape_t *shape, const uint16_t *x, const uint16_
 #define MOE_KERNEL_COMBINE 7      /* gate-weighted un-permute + shared output   */
 #define MOE_KERNEL_OTHER 8        /* packing, probes                            */
 
-/* on != 0: every subsequent kernel launch is bracketed by two CUDA events on
- * its stream; on == 0 stops recording.  Recording continues until collected. */
+/* on == 1: every subsequent kernel launch is bracketed by two CUDA events on
+ * its stream; any other nonzero value is a mask, bit (1 << MOE_KERNEL_*)
+ * selecting the kernels to bracket; on == 0 stops recording.  Recording
+ * continues until collected.                                                 */
 int moe_profile_enable(int on);
 
 /* Waits for the recorded events and returns, in launch order, up to `cap`

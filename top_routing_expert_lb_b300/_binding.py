@@ -257,8 +257,21 @@ KERNEL_NAMES = {1: "router", 2: "finalize", 3: "tile_hist", 4: "scatter", 5: "ge
                 6: "gemm_down", 7: "combine", 8: "other"}
 
 
-def moe_profile_enable(on: bool = True):
-    _check(lib().moe_profile_enable(1 if on else 0), "moe_profile_enable")
+KERNEL_IDS = {v: k for k, v in KERNEL_NAMES.items()}
+
+
+def moe_profile_enable(on=True, kernels=None):
+    """Bracket kernel launches with CUDA events: all of them, or only the
+    named kernels (e.g. ["gemm_swiglu"])."""
+    if not on:
+        mask = 0
+    elif kernels is None:
+        mask = 1
+    else:
+        mask = 0
+        for name in kernels:
+            mask |= 1 << KERNEL_IDS[name]
+    _check(lib().moe_profile_enable(mask), "moe_profile_enable")
 
 
 def moe_profile_collect(cap: int = 1 << 16):

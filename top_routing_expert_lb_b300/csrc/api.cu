@@ -20,7 +20,7 @@ uint64_t g_timeout_ns = 2000000000ull;
 
 // ---------------------------------------------------------------- accounting
 uint64_t g_launches = 0;
-bool g_prof_on = false;
+uint32_t g_prof_mask = 0;  // bit (1 << kernel id) set: that kernel is bracketed
 struct ProfRec {
   int32_t kernel;
   cudaEvent_t start, stop;
@@ -42,14 +42,15 @@ cudaEvent_t pool_event() {
 template <typename F>
 int tracked(int32_t kernel, cudaStream_t st, F&& launch) {
   cudaEvent_t a = nullptr, b = nullptr;
-  if (g_prof_on) {
+  const bool prof = (g_prof_mask >> kernel) & 1u;
+  if (prof) {
     a = pool_event();
     b = pool_event();
     if (a) cudaEventRecord(a, st);
   }
   const int rc = launch();
   if (rc == 0) ++g_launches;
-  if (g_prof_on && a && b) {
+  if (prof && a && b) {
     cudaEventRecord(b, st);
     g_prof.push_back({kernel, a, b});
   }
@@ -604,7 +605,7 @@ int moe_debug_timeout_probe(void* ws, size_t ws_bytes, void* stream) {
 }
 
 int moe_profile_enable(int on) {
-  g_prof_on = on != 0;
+  g_prof_mask = (on == 0) ? 0u : (on == 1 ? 0xFFFFFFFFu : static_cast<uint32_t>(on));
   return MOE_OK;
 }
 
