@@ -75,6 +75,13 @@ def load(path: Optional[str] = None):
     lib.oracle_combine.argtypes = [i32, i32, i32, _P, _P, _P, _P, _P]
     lib.oracle_importance.argtypes = [i32, i32, i32, _P, _P, _P, _P]
     lib.oracle_alf_bias_update.argtypes = [i32, i32, i32, _P, ctypes.c_float, _P, _P]
+    i64 = ctypes.c_int64
+    lib.oracle_dispatch_priority.argtypes = [i32, i32, i32, _P, _P, i64, _P, _P, _P, _P, _P, _P]
+    lib.oracle_ec_capacity.argtypes = [f64, i32, i32, i32]
+    lib.oracle_ec_capacity.restype = i64
+    lib.oracle_expert_choice.argtypes = [i32, i32, i64, _P, _P, _P]
+    lib.oracle_ec_layer_tokens.argtypes = [i32, i32, i32, i32, i64, i32] + [_P] * 9 + [i32, _P, _P]
+    lib.oracle_losses_n.argtypes = [i32, i32, f64, _P, _P, _P, f64, _P, _P, _P, _P]
     if path == _LIB:
         _lib = lib
     return lib
@@ -110,6 +117,7 @@ def router_logits(x, wr, offset=None, lib=None) -> np.ndarray:
 
 SIGMOID = 1     # sigmoid scores instead of the softmax
 NO_RENORM = 2   # gates = selected scores, not renormalised
+PRIORITY = 4    # capacity keeps each expert's highest-score pairs
 
 
 @dataclass
@@ -183,6 +191,48 @@ def dispatch(ids, E: int, C: int, lib=None) -> Dispatch:
     return Dispatch(counts, kept, offsets, slot_row, row_token[:R].copy(), dropped)
 
 
+def dispatch_priority(ids, p, E: int, C: int, lib=None) -> Dispatch:
+    """Dispatch whose capacity cut keeps each expert's C highest-score pairs."""
+    lib = lib or load()
+    ids = np.ascontiguousarray(ids, np.int32)
+    p = np.ascontiguousarray(p, np.float64)
+    T, k = ids.shape
+    assert p.shape == (T, E)
+    counts = np.empty(E, np.int32)
+    kept = np.empty(E, np.int32)
+    offsets = np.empty(E + 1, np.int32)
+    slot_row = np.empty((T, k), np.int32)
+    row_token = np.full(max(T * k, 1), -1, np.int32)
+    dropped = np.empty((T, k), np.uint8)
+    lib.oracle_dispatch_priority(T, E, k, _ptr(ids), _ptr(p), int(C), _ptr(counts), _ptr(kept),
+                                 _ptr(offsets), _ptr(slot_row), _ptr(row_token), _ptr(dropped))
+    R = int(offsets[E])
+    return Dispatch(counts, kept, offsets, slot_row, row_token[:R].copy(), dropped)
+
+
+def ec_capacity(c: float, k: int, T: int, E: int, lib=None) -> int:
+    """Tokens each expert takes under expert-choice routing."""
+    lib = lib or load()
+    return int(lib.oracle_ec_capacity(float(c), k, T, E))
+
+
+@dataclass
+class ExpertChoice:
+    r: int
+    row_token: np.ndarray  # [E*r] token of each row; expert e owns rows e*r .. e*r+r-1
+    row_gate: np.ndarray   # [E*r] gate (the router score) of each row
+
+
+def expert_choice(p, r: int, lib=None) -> ExpertChoice:
+    lib = lib or load()
+    p = np.ascontiguousarray(p, np.float64)
+    T, E = p.shape
+    rt = np.empty(max(E * r, 1), np.int32)
+    rg = np.empty(max(E * r, 1), np.float64)
+    lib.oracle_expert_choice(T, E, int(r), _ptr(p), _ptr(rt), _ptr(rg))
+    return ExpertChoice(int(r), rt[:E * r].copy(), rg[:E * r].copy())
+
+
 def swiglu_row(xrow, w1, w3, w2, lib=None) -> np.ndarray:
     lib = lib or load()
     xrow, w1, w3, w2 = map(_u16, (xrow, w1, w3, w2))
@@ -226,6 +276,25 @@ def layer_tokens(x, routing_ids, gates, dropped, w1, w3, w2, ws1=None, ws3=None,
     return y
 
 
+def ec_layer_tokens(x, ec: ExpertChoice, w1, w3, w2, ws1=None, ws3=None, ws2=None, sel=None,
+                    lib=None) -> np.ndarray:
+    lib = lib or load()
+    x, w1, w3, w2 = map(_u16, (x, w1, w3, w2))
+    T, d = x.shape
+    E, M = w1.shape[0], w1.shape[1]
+    Ms = 0 if ws1 is None else ws1.shape[0]
+    if ws1 is not None:
+        ws1, ws3, ws2 = map(_u16, (ws1, ws3, ws2))
+    sel = np.arange(T, dtype=np.int32) if sel is None else np.ascontiguousarray(sel, np.int32)
+    rt = np.ascontiguousarray(ec.row_token, np.int32)
+    rg = np.ascontiguousarray(ec.row_gate, np.float64)
+    y = np.empty((len(sel), d), np.float64)
+    lib.oracle_ec_layer_tokens(T, d, M, E, ec.r, Ms, _ptr(x), _ptr(rt), _ptr(rg), _ptr(w1),
+                               _ptr(w3), _ptr(w2), _ptr(ws1), _ptr(ws3), _ptr(ws2), len(sel),
+                               _ptr(sel), _ptr(y))
+    return y
+
+
 def combine(y_perm, slot_row, gates, y_shared=None, lib=None) -> np.ndarray:
     """y[t] = sum over kept slots of gates * y_perm[slot_row] (+ y_shared[t])."""
     lib = lib or load()
@@ -259,7 +328,8 @@ class Losses:
     L_z: float
 
 
-def losses(counts, p, lse, k: int, lam: float = 0.01, lib=None) -> Losses:
+def losses(counts, p, lse, k: int, lam: float = 0.01, lib=None, n_pairs=None) -> Losses:
+    """f, P, L_bal, L_z; f_e = n_e / (k T), or n_e / n_pairs when given."""
     lib = lib or load()
     p = np.ascontiguousarray(p, np.float64)
     T, E = p.shape
@@ -269,8 +339,12 @@ def losses(counts, p, lse, k: int, lam: float = 0.01, lib=None) -> Losses:
     P = np.empty(E, np.float64)
     lb = ctypes.c_double()
     lz = ctypes.c_double()
-    lib.oracle_losses(T, E, k, _ptr(counts), _ptr(p), _ptr(lse), float(lam), _ptr(f), _ptr(P),
-                      ctypes.byref(lb), ctypes.byref(lz))
+    if n_pairs is None:
+        lib.oracle_losses(T, E, k, _ptr(counts), _ptr(p), _ptr(lse), float(lam), _ptr(f),
+                          _ptr(P), ctypes.byref(lb), ctypes.byref(lz))
+    else:
+        lib.oracle_losses_n(T, E, float(n_pairs), _ptr(counts), _ptr(p), _ptr(lse), float(lam),
+                            _ptr(f), _ptr(P), ctypes.byref(lb), ctypes.byref(lz))
     return Losses(f, P, lb.value, lz.value)
 
 
@@ -296,9 +370,12 @@ def layer_forward(x, wr, w1, w3, w2, k, offset=None, sel_bias=None, ws1=None, ws
     T = x.shape[0]
     E = wr.shape[0]
     logits = router_logits(x, wr, offset, lib=lib)
-    r = route(logits, k, sel_bias, force_ids, force_mask, flags=flags, lib=lib)
+    r = route(logits, k, sel_bias, force_ids, force_mask, flags=flags & 3, lib=lib)
     C = capacity(capacity_factor, k, T, E, lib=lib)
-    disp = dispatch(r.ids, E, C, lib=lib)
+    if flags & PRIORITY:
+        disp = dispatch_priority(r.ids, r.p, E, C, lib=lib)
+    else:
+        disp = dispatch(r.ids, E, C, lib=lib)
     ls = losses(disp.counts, r.p, r.lse, k, lam, lib=lib)
     if sel is None:
         sel = np.arange(T, dtype=np.int32)
@@ -307,3 +384,32 @@ def layer_forward(x, wr, w1, w3, w2, k, offset=None, sel_bias=None, ws1=None, ws
         y = layer_tokens(x, r.ids, r.gates, disp.dropped, w1, w3, w2, ws1, ws3, ws2, sel,
                          lib=lib)
     return LayerResult(r, disp, C, ls, y, np.asarray(sel, np.int32))
+
+
+@dataclass
+class ECLayerResult:
+    routing: Routing             # p, lse, entropy (ids/gates unused: k = 0 selection)
+    ec: ExpertChoice
+    loss: Losses
+    y: Optional[np.ndarray]
+    sel: np.ndarray
+
+
+def ec_layer_forward(x, wr, w1, w3, w2, k, offset=None, ws1=None, ws3=None, ws2=None,
+                     capacity_factor=0.0, lam=0.01, sel=None, flags=0, lib=None) -> ECLayerResult:
+    """Expert-choice forward: each expert takes its r highest-score tokens."""
+    lib = lib or load()
+    T = x.shape[0]
+    E = wr.shape[0]
+    logits = router_logits(x, wr, offset, lib=lib)
+    r0 = route(logits, 0, None, flags=flags & SIGMOID, lib=lib)
+    r = ec_capacity(capacity_factor, k, T, E, lib=lib)
+    ec = expert_choice(r0.p, r, lib=lib)
+    counts = np.full(E, r, np.int32)
+    ls = losses(counts, r0.p, r0.lse, k, lam, lib=lib, n_pairs=E * r)
+    if sel is None:
+        sel = np.arange(T, dtype=np.int32)
+    y = None
+    if len(sel) > 0:
+        y = ec_layer_tokens(x, ec, w1, w3, w2, ws1, ws3, ws2, sel, lib=lib)
+    return ECLayerResult(r0, ec, ls, y, np.asarray(sel, np.int32))

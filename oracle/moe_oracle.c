@@ -30,6 +30,9 @@
  *         nothing) and the DeepseekV3MoE excerpt (shared experts fused into one
  *         MLP of width n_shared * moe_intermediate_size and added to the routed
  *         output; moe_infer's histogram and argsort permutation).
+ *         §4.2.2 the capacity-bounded router (keep the highest-probability
+ *         tokens of an over-full expert); §9.2 expert-choice MoE (each expert
+ *         picks its own top tokens).
  *   [JN]  "MOE大模型对比篇" (llm.jiangnianmeng.cn): §2.1 balance loss with
  *         P_i = (1/T) sum_x p_i(x); §2.2 router z-loss
  *         L_z = (1/B) sum_i (log sum_j exp(x_j^(i)))^2.
@@ -230,6 +233,111 @@ void oracle_dispatch(int T, int E, int k, const int32_t *ids, int64_t C,
 }
 
 /* ------------------------------------------------------------------------- */
+/* Dispatch with probability-priority capacity ([DU] §4.2.2, the capacity-   */
+/* bounded router: when more pairs reach an expert than its capacity, the    */
+/* ones with the highest routing probability are kept).                      */
+/* Reading: the priority of pair (t,s) is the token's unbiased score of its   */
+/* expert, p[t][ids[t][s]] (softmax probability, or the sigmoid score); one   */
+/* capacity C = ceil(c k T / E) per expert over all its pairs; equal scores   */
+/* are taken in token-major (t, s) order.  Kept rows keep the stable layout   */
+/* of oracle_dispatch: within an expert they are ordered by (t, s).           */
+/* p: [T][E].  Outputs as oracle_dispatch.                                     */
+/* ------------------------------------------------------------------------- */
+typedef struct { double key; int64_t q; } prio_t;
+
+static int prio_cmp(const void *pa, const void *pb)
+{
+    const prio_t *a = (const prio_t *)pa, *b = (const prio_t *)pb;
+    if (a->key > b->key) return -1;
+    if (a->key < b->key) return 1;
+    return (a->q < b->q) ? -1 : (a->q > b->q);
+}
+
+void oracle_dispatch_priority(int T, int E, int k, const int32_t *ids, const double *p,
+                              int64_t C, int32_t *counts, int32_t *kept_counts,
+                              int32_t *offsets, int32_t *slot_row, int32_t *row_token,
+                              uint8_t *dropped)
+{
+    const int64_t n = (int64_t)T * k;
+    prio_t *list = (prio_t *)malloc(sizeof(prio_t) * (size_t)(n > 0 ? n : 1));
+    for (int e = 0; e < E; ++e) { counts[e] = 0; kept_counts[e] = 0; }
+    for (int64_t q = 0; q < n; ++q) dropped[q] = 0;
+    /* the cut, one expert at a time: sort its pairs by (score desc, q asc) */
+    for (int e = 0; e < E; ++e) {
+        int64_t m = 0;
+        for (int64_t q = 0; q < n; ++q) {
+            if (ids[q] != e) continue;
+            list[m].key = p[(q / k) * (int64_t)E + e];
+            list[m].q = q;
+            ++m;
+        }
+        counts[e] = (int32_t)m;
+        if (C >= 0 && m > C) {
+            qsort(list, (size_t)m, sizeof(prio_t), prio_cmp);
+            for (int64_t j = C; j < m; ++j) dropped[list[j].q] = 1;
+        }
+        kept_counts[e] = (int32_t)((C >= 0 && m > C) ? C : m);
+    }
+    /* the permutation: kept pairs of each expert in (t, s) order */
+    offsets[0] = 0;
+    for (int e = 0; e < E; ++e) offsets[e + 1] = kept_counts[e] + offsets[e];
+    int32_t *next = (int32_t *)malloc(sizeof(int32_t) * (size_t)(E > 0 ? E : 1));
+    for (int e = 0; e < E; ++e) next[e] = offsets[e];
+    for (int64_t q = 0; q < n; ++q) {
+        if (dropped[q]) { slot_row[q] = -1; continue; }
+        int r = next[ids[q]]++;
+        slot_row[q] = r;
+        row_token[r] = (int32_t)(q / k);
+    }
+    free(next);
+    free(list);
+}
+
+/* ------------------------------------------------------------------------- */
+/* Expert-choice routing ([DU] §9.2 Expert Choice MoE: every expert picks the */
+/* tokens that matter most to it; "MoE：条件计算与路由", routing table: each    */
+/* expert takes its top-r_e tokens, naturally balanced, a token may be picked */
+/* by several experts or none).                                               */
+/* Readings: the score of token t for expert e is the router score p[t][e]    */
+/* (softmax over experts, or the sigmoid score), which is also the gate; every */
+/* expert takes r tokens, r = min(T, ceil(c k T / E)) with c = 1 when c <= 0,  */
+/* so that at c = 1 the rows computed equal those of token-choice top-k;      */
+/* equal scores go to the lower token index.  Expert e's rows are            */
+/* e*r .. e*r + r - 1, its chosen tokens in ascending order.                 */
+/* p: [T][E]; row_token, row_gate: [E*r].                                     */
+/* ------------------------------------------------------------------------- */
+int64_t oracle_ec_capacity(double c, int k, int T, int E)
+{
+    double cc = (c > 0.0) ? c : 1.0;
+    int64_t r = (int64_t)ceil(cc * (double)k * (double)T / (double)E);
+    return r < T ? r : T;
+}
+
+static int i32_cmp(const void *pa, const void *pb)
+{
+    int32_t a = *(const int32_t *)pa, b = *(const int32_t *)pb;
+    return (a < b) ? -1 : (a > b);
+}
+
+void oracle_expert_choice(int T, int E, int64_t r, const double *p, int32_t *row_token,
+                          double *row_gate)
+{
+    prio_t *list = (prio_t *)malloc(sizeof(prio_t) * (size_t)(T > 0 ? T : 1));
+    for (int e = 0; e < E; ++e) {
+        for (int t = 0; t < T; ++t) {
+            list[t].key = p[(size_t)t * E + e];
+            list[t].q = t;
+        }
+        qsort(list, (size_t)T, sizeof(prio_t), prio_cmp);
+        int32_t *rt = row_token + (size_t)e * r;
+        for (int64_t j = 0; j < r; ++j) rt[j] = (int32_t)list[j].q;
+        qsort(rt, (size_t)r, sizeof(int32_t), i32_cmp);
+        for (int64_t j = 0; j < r; ++j) row_gate[(size_t)e * r + j] = p[(size_t)rt[j] * E + e];
+    }
+    free(list);
+}
+
+/* ------------------------------------------------------------------------- */
 /* One SwiGLU expert on one input row   ([DU] §10.2):                          */
 /*   out[o] = sum_j W2[o][j] * SiLU(sum_i W1[j][i] x_i) * (sum_i W3[j][i] x_i) */
 /* W1, W3: [Mw][d] (nn.Linear(d -> Mw).weight), W2: [d][Mw]                     */
@@ -316,21 +424,62 @@ void oracle_layer_tokens(int T, int d, int M, int E, int k, int Ms,
 }
 
 /* ------------------------------------------------------------------------- */
+/* Expert-choice layer output for the tokens listed in sel[0..n_sel):          */
+/*   y[t] = sum over experts e that picked t (e ascending) of                  */
+/*          row_gate[row] * E_e(x_t)  +  Ys(x_t)                               */
+/* ([KA] §7 Eq.(3) with the selection made by the experts; the shared experts */
+/* as in oracle_layer_tokens).  A token no expert picked gets only Ys.        */
+/* ------------------------------------------------------------------------- */
+void oracle_ec_layer_tokens(int T, int d, int M, int E, int64_t r, int Ms,
+                            const uint16_t *x, const int32_t *row_token, const double *row_gate,
+                            const uint16_t *w1, const uint16_t *w3, const uint16_t *w2,
+                            const uint16_t *ws1, const uint16_t *ws3, const uint16_t *ws2,
+                            int n_sel, const int32_t *sel, double *y_sel)
+{
+    (void)T;
+#pragma omp parallel
+    {
+        double *tmp = (double *)malloc(sizeof(double) * (size_t)d);
+#pragma omp for schedule(dynamic, 1)
+        for (int q = 0; q < n_sel; ++q) {
+            const int32_t t = sel[q];
+            double *yt = y_sel + (size_t)q * d;
+            for (int o = 0; o < d; ++o) yt[o] = 0.0;
+            for (int e = 0; e < E; ++e) {
+                for (int64_t j = 0; j < r; ++j) {
+                    size_t row = (size_t)e * r + j;
+                    if (row_token[row] != t) continue;
+                    oracle_swiglu_row(d, M, x + (size_t)t * d, w1 + (size_t)e * M * d,
+                                      w3 + (size_t)e * M * d, w2 + (size_t)e * d * M, tmp);
+                    for (int o = 0; o < d; ++o) yt[o] += row_gate[row] * tmp[o];
+                }
+            }
+            if (Ms > 0 && ws1) {
+                oracle_swiglu_row(d, Ms, x + (size_t)t * d, ws1, ws3, ws2, tmp);
+                for (int o = 0; o < d; ++o) yt[o] += tmp[o];
+            }
+        }
+        free(tmp);
+    }
+}
+
+/* ------------------------------------------------------------------------- */
 /* Side outputs.                                                                */
-/*   f_e  = n_e / (k T)               (fraction of routed pairs, before any    */
-/*                                     capacity cut; sums to 1)                */
+/*   f_e  = n_e / N                   (fraction of routed pairs, before any    */
+/*                                     capacity cut; sums to 1; N = k T for    */
+/*                                     token choice, E r for expert choice)    */
 /*   P_e  = (1/T) sum_t p_e(t)        ([JN] §2.1, [DU] §4.2.1)                 */
 /*   L_bal = lambda * E * sum_e f_e P_e   ([KA] balance loss)                   */
 /*   L_z  = (1/T) sum_t lse_t^2       ([JN] §2.2)                               */
 /* With T == 0 or k == 0 the undefined ratios are reported as 0.               */
 /* ------------------------------------------------------------------------- */
-void oracle_losses(int T, int E, int k, const int32_t *counts, const double *p,
-                   const double *lse, double lambda, double *f, double *P,
-                   double *L_bal, double *L_z)
+void oracle_losses_n(int T, int E, double N, const int32_t *counts, const double *p,
+                     const double *lse, double lambda, double *f, double *P,
+                     double *L_bal, double *L_z)
 {
     double sfp = 0.0, sz = 0.0;
     for (int e = 0; e < E; ++e) {
-        f[e] = (T > 0 && k > 0) ? (double)counts[e] / ((double)k * (double)T) : 0.0;
+        f[e] = (T > 0 && N > 0.0) ? (double)counts[e] / N : 0.0;
         double acc = 0.0;
         for (int t = 0; t < T; ++t) acc += p[(size_t)t * E + e];
         P[e] = (T > 0) ? acc / (double)T : 0.0;
@@ -339,6 +488,13 @@ void oracle_losses(int T, int E, int k, const int32_t *counts, const double *p,
     for (int t = 0; t < T; ++t) sz += lse[t] * lse[t];
     *L_bal = lambda * (double)E * sfp;
     *L_z = (T > 0) ? sz / (double)T : 0.0;
+}
+
+void oracle_losses(int T, int E, int k, const int32_t *counts, const double *p,
+                   const double *lse, double lambda, double *f, double *P,
+                   double *L_bal, double *L_z)
+{
+    oracle_losses_n(T, E, (double)k * (double)T, counts, p, lse, lambda, f, P, L_bal, L_z);
 }
 
 /* ------------------------------------------------------------------------- */

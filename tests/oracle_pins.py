@@ -16,7 +16,12 @@ mutated build) and raises AssertionError on mismatch.  The pins are:
   sum n_e = kT, uniform logits give L_bal = lambda, L_z from scipy's logsumexp,
   k = 0 gives the shared-only output, c -> inf equals dropless, E = 1 / k = 1
   is the dense SwiGLU FFN, k = E is the dense soft mixture, token permutation
-  equivariance.
+  equivariance;
+* probability-priority capacity: a hand case from closed forms, a numpy
+  lexsort cut, equal scores reduce to the token-order cut;
+* expert-choice routing: a hand case from closed forms (ties, a token no
+  expert picks, a shared expert), numpy lexsort picks with a numpy recompute
+  of y, and r = T equal to the token-choice k = E soft mixture.
 """
 from __future__ import annotations
 
@@ -434,6 +439,136 @@ def pin_alf_bias_update(lib):
     assert first > 3.0 and spread < 1.5, (first, spread)
 
 
-ALL_PINS = [pin_alf_bias_update, pin_routing_variants, pin_entropy_and_importance, pin_combine, pin_hand_routing, pin_hand_capacity, pin_hand_shared_k0, pin_two_gating_formulas,
+# --------------------------------------------------------------------------- #
+# probability-priority capacity and expert-choice routing                      #
+# --------------------------------------------------------------------------- #
+def _sig(z):
+    return 1.0 / (1.0 + np.exp(-z))
+
+
+def pin_priority_capacity(lib):
+    """Capacity that keeps each expert's highest-score pairs (aiattnstudio
+    §4.2.2).  Hand case from closed forms: with W_r = I and x = [1,0,0,0],
+    [3,0,0,0], [2,0,0,0] every token picks expert 0 with p = e^z/(e^z+3); C = 2
+    keeps tokens 1 and 2 (token order would keep 0 and 1); their rows stay in
+    token order.  Random cases against a numpy lexsort cut; equal scores reduce
+    to the token-order dispatch; a capacity above every load is dropless."""
+    w1, w3, w2, I = _hand_weights()
+    x = bf16_bits(np.array([[1, 0, 0, 0], [3, 0, 0, 0], [2, 0, 0, 0]], np.float64))
+    assert oracle.capacity(2.0, 1, 3, 4, lib=lib) == 2
+    res = oracle.layer_forward(x, I, w1, w3, w2, 1, capacity_factor=2.0,
+                               flags=oracle.PRIORITY, lib=lib)
+    e = np.e
+    _close(res.routing.p[:, 0], [e / (e + 3), e ** 3 / (e ** 3 + 3), e ** 2 / (e ** 2 + 3)],
+           1e-14, "hand p")
+    assert res.disp.dropped.reshape(-1).tolist() == [1, 0, 0]
+    assert res.disp.slot_row.reshape(-1).tolist() == [-1, 0, 1]
+    assert res.disp.row_token.tolist() == [1, 2]
+    assert res.disp.counts.tolist() == [3, 0, 0, 0]
+    # y: dropped token 0 gets nothing; E_0(x)_o = SiLU(x_o) x_o = x_o^2 sigmoid(x_o)
+    _close(res.y, [[0, 0, 0, 0], [9 * _sig(3.0), 0, 0, 0], [4 * _sig(2.0), 0, 0, 0]], 1e-12,
+           "hand y")
+    tok = oracle.layer_forward(x, I, w1, w3, w2, 1, capacity_factor=2.0, lib=lib)
+    assert tok.disp.dropped.reshape(-1).tolist() == [0, 0, 1]
+
+    rng = np.random.default_rng(41)
+    for (T, E, k, c) in [(200, 8, 2, 0.5), (129, 4, 1, 1.0), (300, 16, 4, 0.8),
+                         (64, 32, 6, 0.3), (50, 5, 5, 0.7)]:
+        lg = rng.standard_normal((T, E)) * 1.5
+        lg[:, 0] += 1.0                                  # overload expert 0
+        r = oracle.route(lg, k, lib=lib)
+        C = oracle.capacity(c, k, T, E, lib=lib)
+        disp = oracle.dispatch_priority(r.ids, r.p, E, C, lib=lib)
+        flat = r.ids.reshape(-1)
+        score = r.p[np.repeat(np.arange(T), k), flat]
+        q = np.arange(T * k)
+        kept = np.zeros(T * k, bool)
+        for ee in range(E):
+            pos = q[flat == ee]
+            order = pos[np.lexsort((pos, -score[pos]))]  # score desc, then (t, s)
+            kept[order[:C]] = True
+            if len(pos) > C:
+                assert score[order[:C]].min() >= score[order[C:]].max()
+        assert disp.dropped.reshape(-1).tolist() == (~kept).astype(np.uint8).tolist()
+        kp = q[kept]
+        order = kp[np.argsort(flat[kp], kind="stable")]
+        assert disp.row_token.tolist() == (order // k).tolist()
+        sr = np.full(T * k, -1)
+        sr[order] = np.arange(len(order))
+        assert disp.slot_row.reshape(-1).tolist() == sr.tolist()
+        assert disp.counts.tolist() == np.bincount(flat, minlength=E).tolist()
+        assert disp.kept_counts.tolist() == np.minimum(disp.counts, C).tolist()
+        # equal scores: the cut falls back to token order
+        eq = oracle.dispatch_priority(r.ids, np.full((T, E), 0.25), E, C, lib=lib)
+        ref = oracle.dispatch(r.ids, E, C, lib=lib)
+        for f in ("dropped", "slot_row", "row_token", "offsets"):
+            assert getattr(eq, f).tolist() == getattr(ref, f).tolist(), f
+        # no cut when C covers every load
+        big = oracle.dispatch_priority(r.ids, r.p, E, T * k, lib=lib)
+        assert big.slot_row.tolist() == oracle.dispatch(r.ids, E, -1, lib=lib).slot_row.tolist()
+
+
+def pin_expert_choice(lib):
+    """Expert-choice routing (aiattnstudio §9.2; routing table of
+    "MoE：条件计算与路由").  Hand case from closed forms (W_r = I, d = 2,
+    x = [1,0], [0,1], [2,0], [1,0], k = 1, c = 1, so r = ceil(4/2) = 2): expert 0
+    scores sigmoid(1), sigmoid(-1), sigmoid(2), sigmoid(1) and takes tokens 2
+    and 0 (0 beats its duplicate 3 on the index); expert 1 takes 1 and 0; token
+    3 gets nothing.  Random cases against a numpy lexsort; r = T is the dense
+    soft mixture, the same output as token choice with k = E."""
+    assert oracle.ec_capacity(1.0, 1, 4, 2, lib=lib) == 2
+    assert oracle.ec_capacity(0.0, 1, 3, 2, lib=lib) == 2        # c <= 0 reads as c = 1
+    assert oracle.ec_capacity(1.0, 2, 4096, 8, lib=lib) == 1024
+    assert oracle.ec_capacity(5.0, 2, 10, 4, lib=lib) == 10      # at most T
+    assert oracle.ec_capacity(1.25, 1, 32768, 128, lib=lib) == 320
+    I2 = bf16_bits(np.eye(2))
+    w1 = bf16_bits(np.stack([np.eye(2)] * 2))
+    w2 = bf16_bits(np.stack([(e + 1) * np.eye(2) for e in range(2)]))
+    x = bf16_bits(np.array([[1, 0], [0, 1], [2, 0], [1, 0]], np.float64))
+    res = oracle.ec_layer_forward(x, I2, w1, w1, w2, 1, capacity_factor=1.0, lib=lib)
+    s1, s2, sm1 = _sig(1.0), _sig(2.0), _sig(-1.0)
+    assert res.ec.r == 2
+    assert res.ec.row_token.tolist() == [0, 2, 0, 1]
+    _close(res.ec.row_gate, [s1, s2, sm1, s1], 1e-14, "EC gates")
+    # E_e(x)_o = (e+1) x_o^2 sigmoid(x_o)
+    _close(res.y, [[s1 * s1 + sm1 * 2 * s1, 0], [0, s1 * 2 * s1], [s2 * 4 * s2, 0], [0, 0]],
+           1e-12, "EC hand y")
+    # one shared expert of width 2 (W1s = W3s = W2s = I) adds x_o^2 sigmoid(x_o) to
+    # every token, also to token 3, which no expert picked
+    sh = oracle.ec_layer_forward(x, I2, w1, w1, w2, 1, ws1=I2, ws3=I2, ws2=I2,
+                                 capacity_factor=1.0, lib=lib)
+    _close(sh.y - res.y, [[s1, 0], [0, s1], [4 * s2, 0], [s1, 0]], 1e-12, "EC shared expert")
+    _close(res.loss.f, [0.5, 0.5], 1e-15, "EC f")
+    _close(res.loss.L_bal, 0.01, 1e-15, "EC L_bal = lambda")
+
+    rng = np.random.default_rng(43)
+    for (T, d, E, k, M, c) in [(40, 8, 6, 2, 4, 1.0), (33, 8, 4, 1, 4, 0.5),
+                               (25, 16, 8, 3, 8, 2.0)]:
+        xx, wr, w1, w3, w2, _ = rand_problem(rng, T, d, E, k, M)
+        res = oracle.ec_layer_forward(xx, wr, w1, w3, w2, k, capacity_factor=c, lib=lib)
+        xv = bf16_val(xx)
+        lg = xv @ bf16_val(wr).T
+        p = np.exp(lg - lg.max(1, keepdims=True))
+        p /= p.sum(1, keepdims=True)
+        r = min(T, int(np.ceil(c * k * T / E)))
+        assert res.ec.r == r
+        y = np.zeros((T, d))
+        for e in range(E):
+            pick = np.sort(np.lexsort((np.arange(T), -p[:, e]))[:r])
+            assert res.ec.row_token[e * r:(e + 1) * r].tolist() == pick.tolist()
+            _close(res.ec.row_gate[e * r:(e + 1) * r], p[pick, e], 1e-12, "EC gate = p")
+            y[pick] += p[pick, e][:, None] * np_swiglu(xv[pick], bf16_val(w1[e]),
+                                                       bf16_val(w3[e]), bf16_val(w2[e]))
+        _close(res.y, y, 1e-10 * max(1.0, np.abs(y).max()), "EC y vs numpy")
+    # every expert takes every token: the dense soft mixture
+    T, d, E, M = 12, 8, 4, 4
+    xx, wr, w1, w3, w2, _ = rand_problem(rng, T, d, E, E, M)
+    ec = oracle.ec_layer_forward(xx, wr, w1, w3, w2, E, capacity_factor=float(E), lib=lib)
+    assert ec.ec.r == T
+    tc = oracle.layer_forward(xx, wr, w1, w3, w2, E, lib=lib)
+    _close(ec.y, tc.y, 1e-12, "EC with r = T vs token choice k = E")
+
+
+ALL_PINS = [pin_priority_capacity, pin_expert_choice, pin_alf_bias_update, pin_routing_variants, pin_entropy_and_importance, pin_combine, pin_hand_routing, pin_hand_capacity, pin_hand_shared_k0, pin_two_gating_formulas,
             pin_bruteforce_subsets, pin_dispatch_argsort, pin_capacity_formula, pin_invariants,
             pin_determinism, pin_gap_and_force]

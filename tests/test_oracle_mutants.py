@@ -26,7 +26,7 @@ MUTANTS = {
     "gap_wrong_index": ("ord[k - 1].key - ord[k].key", "ord[0].key - ord[k].key"),
     "offset_dropped": ("if (offset) acc += (double)offset[e];", "(void)offset;"),
     "capacity_floor": ("return (int64_t)ceil(", "return (int64_t)floor("),
-    "capacity_without_k": ("c * (double)k * (double)T", "c * (double)T"),
+    "capacity_without_k": ("ceil(c * (double)k * (double)T", "ceil(c * (double)T"),
     "capacity_off_by_one": ("kept_counts[e] < C", "kept_counts[e] <= C"),
     "offsets_from_precap_counts": ("offsets[e + 1] = offsets[e] + kept_counts[e];",
                                    "offsets[e + 1] = offsets[e] + counts[e];"),
@@ -34,10 +34,12 @@ MUTANTS = {
     "gate_up_swapped": ("h[j] = silu(a) * b;", "h[j] = a * silu(b);"),
     "w2_transposed": ("bf16_val(w2[(size_t)o * Mw + j])", "bf16_val(w2[(size_t)j * d + o])"),
     "dropped_pairs_added": ("if (dropped[pq]) continue;", "if (0) continue;"),
-    "shared_not_added": ("for (int o = 0; o < d; ++o) yt[o] += tmp[o];",
-                         "for (int o = 0; o < d; ++o) yt[o] += 0.0 * tmp[o];"),
+    "shared_not_added": ("x + t * d, ws1, ws3, ws2, tmp);\n                for (int o = 0; o < d; ++o) yt[o] += tmp[o];",
+                         "x + t * d, ws1, ws3, ws2, tmp);\n                for (int o = 0; o < d; ++o) yt[o] += 0.0 * tmp[o];"),
+    "priority_offsets_precap": ("offsets[e + 1] = kept_counts[e] + offsets[e];",
+                                "offsets[e + 1] = counts[e] + offsets[e];"),
     "zloss_not_squared": ("sz += lse[t] * lse[t];", "sz += lse[t];"),
-    "f_over_T": ("(double)counts[e] / ((double)k * (double)T)", "(double)counts[e] / (double)T"),
+    "f_over_T": ("oracle_losses_n(T, E, (double)k * (double)T,", "oracle_losses_n(T, E, (double)T,"),
     "balance_without_E": ("*L_bal = lambda * (double)E * sfp;", "*L_bal = lambda * sfp;"),
     "sigmoid_sign": ("pt[e] = 1.0 / (1.0 + exp(-l[e]));", "pt[e] = 1.0 / (1.0 + exp(l[e]));"),
     "no_renorm_ignored": ("if (flags & ORACLE_NO_RENORM) denom = 1.0;", "(void)0;"),
@@ -46,6 +48,21 @@ MUTANTS = {
     "alf_sign": ("const double diff = nbar - (double)counts[e];",
                  "const double diff = (double)counts[e] - nbar;"),
     "combine_drop_ignored": ("if (r < 0) continue;\n            double g", "if (r < 0) r = 0;\n            double g"),
+    "priority_keeps_lowest": ("if (a->key > b->key) return -1;\n    if (a->key < b->key) return 1;\n    return (a->q",
+                              "if (a->key < b->key) return -1;\n    if (a->key > b->key) return 1;\n    return (a->q"),
+    "priority_ties_reversed": ("return (a->q < b->q) ? -1 : (a->q > b->q);",
+                               "return (a->q > b->q) ? -1 : (a->q < b->q);"),
+    "priority_wrong_score": ("list[m].key = p[(q / k) * (int64_t)E + e];",
+                             "list[m].key = p[(q % k) * (int64_t)E + e];"),
+    "priority_cut_off_by_one": ("for (int64_t j = C; j < m; ++j) dropped[list[j].q] = 1;",
+                                "for (int64_t j = C + 1; j < m; ++j) dropped[list[j].q] = 1;"),
+    "ec_rows_unsorted": ("qsort(rt, (size_t)r, sizeof(int32_t), i32_cmp);", "(void)i32_cmp;"),
+    "ec_gate_transposed": ("row_gate[(size_t)e * r + j] = p[(size_t)rt[j] * E + e];",
+                           "row_gate[(size_t)e * r + j] = p[(size_t)e * E + rt[j] % E];"),
+    "ec_capacity_no_cap": ("return r < T ? r : T;", "return r;"),
+    "ec_default_c": ("double cc = (c > 0.0) ? c : 1.0;", "double cc = c;"),
+    "ec_shared_missing": ("oracle_swiglu_row(d, Ms, x + (size_t)t * d, ws1, ws3, ws2, tmp);\n                for (int o = 0; o < d; ++o) yt[o] += tmp[o];",
+                          "oracle_swiglu_row(d, Ms, x + (size_t)t * d, ws1, ws3, ws2, tmp);\n                for (int o = 0; o < d; ++o) yt[o] += 0.0;"),
     "combine_shared_missing": ("yt[o] += bf16_val(y_shared[(size_t)t * d + o]);", "yt[o] += 0.0;"),
 }
 
