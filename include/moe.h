@@ -64,9 +64,33 @@ extern "C" {
  *                       s_e + b_e; P_e is the mean score; the z-loss still
  *                       uses log sum exp of the logits.
  *   MOE_FLAG_NO_RENORM  gates are the selected scores themselves, not divided
- *                       by their sum ("MoE：条件计算与路由" §7).              */
+ *                       by their sum ("MoE：条件计算与路由" §7).
+ *   MOE_FLAG_PRIORITY_CAPACITY
+ *                       with a capacity, an over-full expert keeps the C
+ *                       pairs with the largest unbiased scores (its softmax
+ *                       probability, or sigmoid score, for that token; equal
+ *                       scores in token-major (t, slot) order) instead of the
+ *                       first C in token order ("深入理解 MoE" §4.2.2, the
+ *                       capacity-bounded router).  Kept rows stay in (t, slot)
+ *                       order.  Honoured by moe_layer_forward(_host); the
+ *                       routers ignore it; moe_permute, which receives no
+ *                       scores, returns MOE_ERR_UNSUPPORTED with it.
+ *   MOE_FLAG_EXPERT_CHOICE
+ *                       expert-choice routing ("深入理解 MoE" §9.2): every
+ *                       expert takes the r tokens with the largest scores
+ *                       (equal scores to the lower token), r = min(T,
+ *                       ceil(c k T / E)) with c <= 0 read as 1, so that c = 1
+ *                       computes as many rows as token-choice top-k; the
+ *                       gate of a row is its score.  Only the moe_ec_* entry
+ *                       points accept it, and they require it; the token-
+ *                       choice entry points return MOE_ERR_INVALID_ARG.
+ *                       Combining it with MOE_FLAG_PRIORITY_CAPACITY is
+ *                       MOE_ERR_UNSUPPORTED; MOE_FLAG_NO_RENORM changes
+ *                       nothing (expert-choice gates are never renormalised).*/
 #define MOE_FLAG_SIGMOID 1u
 #define MOE_FLAG_NO_RENORM 2u
+#define MOE_FLAG_PRIORITY_CAPACITY 4u
+#define MOE_FLAG_EXPERT_CHOICE 8u
 
 /* Layer shape.
  *   T  tokens;  d  model width;  M  expert intermediate width;
@@ -75,7 +99,7 @@ extern "C" {
  *   capacity_factor  c; <= 0 means dropless, otherwise C = ceil(c*k*T/E)
  *      evaluated in double precision;
  *   balance_coef  lambda of the balance loss (0.01 is customary);
- *   flags  must be 0 (reserved for routing variants).                          */
+ *   flags  routing variants, a combination of the MOE_FLAG_* bits above.     */
 typedef struct moe_shape {
     int32_t T, d, M, E, k, n_shared;
     float capacity_factor;
@@ -93,7 +117,8 @@ int moe_workspace_size(const moe_shape_t *shape, size_t *bytes);
 /* Expert capacity C (host pointer *C): ceil(c*k*T/E), or -1 when dropless.  */
 int moe_capacity(const moe_shape_t *shape, int64_t *C);
 
-/* Upper bound R_max on routed rows: T*k dropless, else min(T*k, E*C).        */
+/* Upper bound R_max on routed rows: T*k dropless, else min(T*k, E*C); E*r
+ * with MOE_FLAG_EXPERT_CHOICE.                                               */
 int moe_max_rows(const moe_shape_t *shape, int64_t *rows);
 
 /* Pack canonical SwiGLU gate/up weights for the grouped GEMM.
@@ -229,6 +254,42 @@ int moe_layer_forward_host(const moe_shape_t *shape, const uint16_t *x_host, uin
                            float *f, float *P, float *bal_loss, float *z_loss, void *ws,
                            size_t ws_bytes, void *stream);
 
+/* Expert-choice routing (MOE_FLAG_EXPERT_CHOICE must be set in shape->flags).
+ * Tokens each expert takes, r = min(T, ceil(c k T / E)), c <= 0 read as 1
+ * (host pointer *r).                                                          */
+int moe_ec_capacity(const moe_shape_t *shape, int64_t *r);
+
+/* Expert-choice router ("深入理解 MoE" §9.2; the routing table of
+ * "MoE：条件计算与路由").  Scores as in moe_route (softmax over experts, or
+ * sigmoid with MOE_FLAG_SIGMOID; logit_offset added to the logits); expert e
+ * takes the r tokens with the largest scores, equal scores to the lower token.
+ * Outputs (device):
+ *   row_token [E*r] int32  rows e*r .. e*r + r - 1 hold expert e's tokens in
+ *                          ascending order
+ *   row_gate  [E*r] fp32   the score of that (token, expert), the row's gate
+ *   counts    [E]   int32  r
+ *   f [E] = 1/E (n_e / (E r)), P [E] (mean score), bal_loss = lambda E sum f P,
+ *   z_loss as in moe_route.
+ * The cut compares the fp32 scores exactly (a radix select on their bits).  */
+int moe_ec_route(const moe_shape_t *shape, const uint16_t *x, const uint16_t *w_router,
+                 const float *logit_offset, int32_t *row_token, float *row_gate,
+                 int32_t *counts, float *f, float *P, float *bal_loss, float *z_loss,
+                 void *ws, size_t ws_bytes, void *stream);
+
+/* The expert-choice layer: moe_ec_route, row gather, the grouped FFN (+ shared
+ * experts) and the combine
+ *     y[t] = sum over experts e that took t (e ascending) of
+ *            row_gate[row] * E_e(x_t)  +  Ys(x_t),
+ * fp32 accumulation, bf16 store; a token no expert took gets Ys(x_t) (0
+ * without shared experts).  Arguments and outputs as in moe_ec_route and
+ * moe_layer_forward.                                                         */
+int moe_ec_layer_forward(const moe_shape_t *shape, const uint16_t *x, const uint16_t *w_router,
+                         const float *logit_offset, const uint16_t *w13, const uint16_t *w2,
+                         const uint16_t *w13_shared, const uint16_t *w2_shared, uint16_t *y,
+                         int32_t *row_token, float *row_gate, int32_t *counts, float *f,
+                         float *P, float *bal_loss, float *z_loss, void *ws, size_t ws_bytes,
+                         void *stream);
+
 /* Reads (and clears) the device status word kept in the workspace; writes
  * MOE_OK or MOE_ERR_TIMEOUT to *status (host).  Synchronises `stream`.        */
 int moe_check_status(void *ws, int *status, void *stream);
@@ -275,6 +336,8 @@ int moe_route_noalloc(const moe_shape_t *shape, const uint16_t *x, const uint16_
 #define MOE_KERNEL_GEMM_DOWN 6    /* grouped down projection                    */
 #define MOE_KERNEL_COMBINE 7      /* gate-weighted un-permute + shared output   */
 #define MOE_KERNEL_OTHER 8        /* packing, probes                            */
+#define MOE_KERNEL_SELECT 9       /* priority capacity cut / expert-choice cut  */
+#define MOE_KERNEL_GATHER 10      /* row gather after a select                  */
 
 /* on == 1: every subsequent kernel launch is bracketed by two CUDA events on
  * its stream; any other nonzero value is a mask, bit (1 << MOE_KERNEL_*)

@@ -76,10 +76,11 @@ def load(path: Optional[str] = None):
     lib.oracle_importance.argtypes = [i32, i32, i32, _P, _P, _P, _P]
     lib.oracle_alf_bias_update.argtypes = [i32, i32, i32, _P, ctypes.c_float, _P, _P]
     i64 = ctypes.c_int64
-    lib.oracle_dispatch_priority.argtypes = [i32, i32, i32, _P, _P, i64, _P, _P, _P, _P, _P, _P]
+    lib.oracle_dispatch_priority.argtypes = [i32, i32, i32, _P, _P, _P, i64, _P, _P, _P, _P, _P,
+                                             _P]
     lib.oracle_ec_capacity.argtypes = [f64, i32, i32, i32]
     lib.oracle_ec_capacity.restype = i64
-    lib.oracle_expert_choice.argtypes = [i32, i32, i64, _P, _P, _P]
+    lib.oracle_expert_choice.argtypes = [i32, i32, i64, _P, _P, _P, _P]
     lib.oracle_ec_layer_tokens.argtypes = [i32, i32, i32, i32, i64, i32] + [_P] * 9 + [i32, _P, _P]
     lib.oracle_losses_n.argtypes = [i32, i32, f64, _P, _P, _P, f64, _P, _P, _P, _P]
     if path == _LIB:
@@ -191,11 +192,13 @@ def dispatch(ids, E: int, C: int, lib=None) -> Dispatch:
     return Dispatch(counts, kept, offsets, slot_row, row_token[:R].copy(), dropped)
 
 
-def dispatch_priority(ids, p, E: int, C: int, lib=None) -> Dispatch:
-    """Dispatch whose capacity cut keeps each expert's C highest-score pairs."""
+def dispatch_priority(ids, p, E: int, C: int, force=None, lib=None) -> Dispatch:
+    """Dispatch whose capacity cut keeps each expert's C highest-score pairs.
+    ``force`` [T,k] int8: +1 / -1 place a pair above / below every score."""
     lib = lib or load()
     ids = np.ascontiguousarray(ids, np.int32)
     p = np.ascontiguousarray(p, np.float64)
+    fo = None if force is None else np.ascontiguousarray(force, np.int8)
     T, k = ids.shape
     assert p.shape == (T, E)
     counts = np.empty(E, np.int32)
@@ -204,8 +207,9 @@ def dispatch_priority(ids, p, E: int, C: int, lib=None) -> Dispatch:
     slot_row = np.empty((T, k), np.int32)
     row_token = np.full(max(T * k, 1), -1, np.int32)
     dropped = np.empty((T, k), np.uint8)
-    lib.oracle_dispatch_priority(T, E, k, _ptr(ids), _ptr(p), int(C), _ptr(counts), _ptr(kept),
-                                 _ptr(offsets), _ptr(slot_row), _ptr(row_token), _ptr(dropped))
+    lib.oracle_dispatch_priority(T, E, k, _ptr(ids), _ptr(p), _ptr(fo), int(C), _ptr(counts),
+                                 _ptr(kept), _ptr(offsets), _ptr(slot_row), _ptr(row_token),
+                                 _ptr(dropped))
     R = int(offsets[E])
     return Dispatch(counts, kept, offsets, slot_row, row_token[:R].copy(), dropped)
 
@@ -223,13 +227,16 @@ class ExpertChoice:
     row_gate: np.ndarray   # [E*r] gate (the router score) of each row
 
 
-def expert_choice(p, r: int, lib=None) -> ExpertChoice:
+def expert_choice(p, r: int, force=None, lib=None) -> ExpertChoice:
+    """Each expert's r highest-score tokens.  ``force`` [E,T] int8: +1 / -1
+    place (e, t) above / below every score for the pick."""
     lib = lib or load()
     p = np.ascontiguousarray(p, np.float64)
     T, E = p.shape
+    fo = None if force is None else np.ascontiguousarray(force, np.int8)
     rt = np.empty(max(E * r, 1), np.int32)
     rg = np.empty(max(E * r, 1), np.float64)
-    lib.oracle_expert_choice(T, E, int(r), _ptr(p), _ptr(rt), _ptr(rg))
+    lib.oracle_expert_choice(T, E, int(r), _ptr(p), _ptr(fo), _ptr(rt), _ptr(rg))
     return ExpertChoice(int(r), rt[:E * r].copy(), rg[:E * r].copy())
 
 

@@ -22,7 +22,9 @@
  *   [DU]  "深入理解 MoE (混合专家模型)：稀疏激活与高效扩展" (aiattnstudio):
  *         §2.2 the sparse gate Softmax(TopK(W_g x, k)); §4.2.1 the balance loss
  *         with P_i the mean routing probability; §10.2 the SwiGLU expert
- *         E(x) = W2 (SiLU(W1 x) * W3 x).
+ *         E(x) = W2 (SiLU(W1 x) * W3 x); §4.2.2 the capacity-bounded router
+ *         (an over-full expert keeps its highest-probability tokens); §9.2
+ *         expert-choice MoE (each expert picks its own top tokens).
  *   [MO]  "MoE" (t4mako.github.io): training instability, subtracting the
  *         maximum before the softmax exponentials.
  *   [CS]  CSDN note on MoE (adg.csdn.net): the toy MoE demo (capacity keeps the
@@ -30,9 +32,6 @@
  *         nothing) and the DeepseekV3MoE excerpt (shared experts fused into one
  *         MLP of width n_shared * moe_intermediate_size and added to the routed
  *         output; moe_infer's histogram and argsort permutation).
- *         §4.2.2 the capacity-bounded router (keep the highest-probability
- *         tokens of an over-full expert); §9.2 expert-choice MoE (each expert
- *         picks its own top tokens).
  *   [JN]  "MOE大模型对比篇" (llm.jiangnianmeng.cn): §2.1 balance loss with
  *         P_i = (1/T) sum_x p_i(x); §2.2 router z-loss
  *         L_z = (1/B) sum_i (log sum_j exp(x_j^(i)))^2.
@@ -242,6 +241,9 @@ void oracle_dispatch(int T, int E, int k, const int32_t *ids, int64_t C,
 /* are taken in token-major (t, s) order.  Kept rows keep the stable layout   */
 /* of oracle_dispatch: within an expert they are ordered by (t, s).           */
 /* p: [T][E].  Outputs as oracle_dispatch.                                     */
+/* force (optional, [T][k]): +1 / -1 put a pair above / below every score;    */
+/* used only for pairs whose score sits within rounding of an expert's cut,   */
+/* where a lower-precision implementation may legitimately decide otherwise.  */
 /* ------------------------------------------------------------------------- */
 typedef struct { double key; int64_t q; } prio_t;
 
@@ -254,7 +256,8 @@ static int prio_cmp(const void *pa, const void *pb)
 }
 
 void oracle_dispatch_priority(int T, int E, int k, const int32_t *ids, const double *p,
-                              int64_t C, int32_t *counts, int32_t *kept_counts,
+                              const int8_t *force, int64_t C, int32_t *counts,
+                              int32_t *kept_counts,
                               int32_t *offsets, int32_t *slot_row, int32_t *row_token,
                               uint8_t *dropped)
 {
@@ -268,6 +271,7 @@ void oracle_dispatch_priority(int T, int E, int k, const int32_t *ids, const dou
         for (int64_t q = 0; q < n; ++q) {
             if (ids[q] != e) continue;
             list[m].key = p[(q / k) * (int64_t)E + e];
+            if (force && force[q]) list[m].key = (force[q] > 0) ? INFINITY : -INFINITY;
             list[m].q = q;
             ++m;
         }
@@ -304,7 +308,9 @@ void oracle_dispatch_priority(int T, int E, int k, const int32_t *ids, const dou
 /* so that at c = 1 the rows computed equal those of token-choice top-k;      */
 /* equal scores go to the lower token index.  Expert e's rows are            */
 /* e*r .. e*r + r - 1, its chosen tokens in ascending order.                 */
-/* p: [T][E]; row_token, row_gate: [E*r].                                     */
+/* p: [T][E]; row_token, row_gate: [E*r].  force (optional, [E][T]): +1 / -1 */
+/* put (e, t) above / below every score for the pick (never for the gate);    */
+/* used only near an expert's cut, as for oracle_dispatch_priority.           */
 /* ------------------------------------------------------------------------- */
 int64_t oracle_ec_capacity(double c, int k, int T, int E)
 {
@@ -319,13 +325,15 @@ static int i32_cmp(const void *pa, const void *pb)
     return (a < b) ? -1 : (a > b);
 }
 
-void oracle_expert_choice(int T, int E, int64_t r, const double *p, int32_t *row_token,
-                          double *row_gate)
+void oracle_expert_choice(int T, int E, int64_t r, const double *p, const int8_t *force,
+                          int32_t *row_token, double *row_gate)
 {
     prio_t *list = (prio_t *)malloc(sizeof(prio_t) * (size_t)(T > 0 ? T : 1));
     for (int e = 0; e < E; ++e) {
         for (int t = 0; t < T; ++t) {
             list[t].key = p[(size_t)t * E + e];
+            if (force && force[(size_t)e * T + t])
+                list[t].key = (force[(size_t)e * T + t] > 0) ? INFINITY : -INFINITY;
             list[t].q = t;
         }
         qsort(list, (size_t)T, sizeof(prio_t), prio_cmp);

@@ -506,6 +506,19 @@ def pin_priority_capacity(lib):
         # no cut when C covers every load
         big = oracle.dispatch_priority(r.ids, r.p, E, T * k, lib=lib)
         assert big.slot_row.tolist() == oracle.dispatch(r.ids, E, -1, lib=lib).slot_row.tolist()
+        # forcing: zeros change nothing; +1 on expert 0's lowest-score pair keeps
+        # it and drops the lowest of its kept pairs instead
+        f0 = oracle.dispatch_priority(r.ids, r.p, E, C, force=np.zeros((T, k), np.int8), lib=lib)
+        assert f0.slot_row.tolist() == disp.slot_row.tolist()
+        pos = q[flat == 0]
+        if len(pos) > C > 0:
+            order = pos[np.lexsort((pos, -score[pos]))]
+            force = np.zeros(T * k, np.int8)
+            force[order[-1]] = 1
+            fd = oracle.dispatch_priority(r.ids, r.p, E, C, force=force.reshape(T, k), lib=lib)
+            fdr = fd.dropped.reshape(-1)
+            assert fdr[order[-1]] == 0 and fdr[order[C - 1]] == 1
+            assert fd.kept_counts[0] == C
 
 
 def pin_expert_choice(lib):
@@ -560,6 +573,16 @@ def pin_expert_choice(lib):
             y[pick] += p[pick, e][:, None] * np_swiglu(xv[pick], bf16_val(w1[e]),
                                                        bf16_val(w3[e]), bf16_val(w2[e]))
         _close(res.y, y, 1e-10 * max(1.0, np.abs(y).max()), "EC y vs numpy")
+        # forcing expert 0's lowest-score token in swaps it for its r-th pick;
+        # gates stay the scores
+        if 0 < r < T:
+            force = np.zeros((E, T), np.int8)
+            low = int(np.lexsort((np.arange(T), -p[:, 0]))[-1])
+            force[0, low] = 1
+            fe = oracle.expert_choice(res.routing.p, r, force=force, lib=lib)
+            pick = np.sort(np.lexsort((np.arange(T), -p[:, 0]))[:r - 1].tolist() + [low])
+            assert fe.row_token[:r].tolist() == pick.tolist()
+            _close(fe.row_gate[:r], p[pick, 0], 1e-12, "forced EC gate")
     # every expert takes every token: the dense soft mixture
     T, d, E, M = 12, 8, 4, 4
     xx, wr, w1, w3, w2, _ = rand_problem(rng, T, d, E, E, M)

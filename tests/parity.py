@@ -108,24 +108,68 @@ class OracleRef:
     C: int
 
 
-def oracle_routing(inp: synth.Inputs, gpu_ids: np.ndarray) -> OracleRef:
+def cut_force(score: np.ndarray, want: int, gpu_keep: np.ndarray, what: str) -> np.ndarray:
+    """Near-cut protocol of a score-ordered selection (keep the ``want``
+    largest of ``score``).  The kept set is unique except for scores within
+    1e-5 of the cut value (the want-th largest, fp64): there fp32 and fp64 may
+    decide differently.  Checks that the GPU kept exactly ``want`` entries,
+    every entry clearly above the cut and none clearly below; returns the
+    int8 force vector (+1 kept / -1 dropped on the near-cut entries, else 0)
+    that makes the oracle take the GPU's decisions there."""
+    n = len(score)
+    force = np.zeros(n, np.int8)
+    if want >= n:
+        assert gpu_keep.all(), f"{what}: dropped an entry with no cut"
+        return force
+    thr = np.sort(score)[::-1][want - 1] if want > 0 else np.inf
+    assert int(gpu_keep.sum()) == want, f"{what}: kept {int(gpu_keep.sum())}, want {want}"
+    assert gpu_keep[score > thr + TIE].all(), f"{what}: dropped a score above the cut"
+    assert not gpu_keep[score < thr - TIE].any(), f"{what}: kept a score below the cut"
+    band = np.abs(score - thr) <= TIE
+    force[band] = np.where(gpu_keep[band], 1, -1)
+    return force
+
+
+def priority_force(r: oracle.Routing, E: int, C: int, gpu_drop: np.ndarray) -> np.ndarray:
+    """cut_force over each over-full expert's pairs (probability priority)."""
+    T, k = r.ids.shape
+    flat = r.ids.reshape(-1)
+    score = r.p[np.repeat(np.arange(T), k), flat]
+    keep = np.asarray(gpu_drop).reshape(-1) == 0
+    force = np.zeros(T * k, np.int8)
+    for e in range(E):
+        pos = np.nonzero(flat == e)[0]
+        if len(pos) > C:
+            force[pos] = cut_force(score[pos], C, keep[pos], f"expert {e}")
+    return force.reshape(T, k)
+
+
+def oracle_routing(inp: synth.Inputs, gpu_ids: np.ndarray,
+                   gpu_drop: Optional[np.ndarray] = None) -> OracleRef:
     """Oracle routing / dispatch / losses for all tokens; near-tie tokens take
-    the GPU's ids after the non-tie tokens were checked bit-exactly."""
+    the GPU's ids after the non-tie tokens were checked bit-exactly (and, with
+    probability-priority capacity, near-cut pairs the GPU's keep decision)."""
     w = inp.w
     x, wr = np_of(inp.x), np_of(inp.wr)
     off = np_of(inp.offset)
     bias = np_of(inp.sel_bias)
     logits = oracle.router_logits(x, wr, off)
-    free = oracle.route(logits, w.k, bias, flags=w.flags)
+    rflags = w.flags & (oracle.SIGMOID | oracle.NO_RENORM)
+    free = oracle.route(logits, w.k, bias, flags=rflags)
     exempt = free.gap < TIE
     if w.k > 0:
         force = routing_force_mask(free, gpu_ids, bias)
-        r = oracle.route(logits, w.k, bias, force_ids=gpu_ids, force_mask=force, flags=w.flags)
+        r = oracle.route(logits, w.k, bias, force_ids=gpu_ids, force_mask=force, flags=rflags)
         exempt = force
     else:
         r = free
     C = oracle.capacity(float(np.float32(w.capacity_factor)), w.k, w.T, w.E)
-    disp = oracle.dispatch(r.ids, w.E, C)
+    if (w.flags & oracle.PRIORITY) and C >= 0 and w.k > 0:
+        assert gpu_drop is not None
+        pf = priority_force(r, w.E, C, gpu_drop)
+        disp = oracle.dispatch_priority(r.ids, r.p, w.E, C, force=pf)
+    else:
+        disp = oracle.dispatch(r.ids, w.E, C)
     ls = oracle.losses(disp.counts, r.p, r.lse, w.k, float(np.float32(w.balance_coef)))
     return OracleRef(r, disp, ls, exempt, C)
 
@@ -189,11 +233,115 @@ def assert_routing_parity(g: GpuOut, ref: OracleRef, w: synth.Workload):
 def check_layer(inp: synth.Inputs, sel: Optional[np.ndarray] = None, layer=None):
     """Runs the GPU layer and checks it against the oracle.  Returns (gpu, ref)."""
     g = run_layer(inp, layer)
-    ref = oracle_routing(inp, g.ids)
+    ref = oracle_routing(inp, g.ids, g.drop)
     assert_routing_parity(g, ref, inp.w)
     if sel is None:
         sel = np.arange(inp.w.T)
     if len(sel):
         y_ref = oracle_y(inp, ref, sel)
+        assert_y_close(bf16_to_f64(g.y)[sel], y_ref)
+    return g, ref
+
+
+# --------------------------------------------------------------------------- #
+# expert choice                                                                #
+# --------------------------------------------------------------------------- #
+@dataclass
+class EcGpuOut:
+    y: torch.Tensor
+    row_token: np.ndarray
+    row_gate: np.ndarray
+    counts: np.ndarray
+    f: np.ndarray
+    P: np.ndarray
+    bal: float
+    z: float
+    r: int
+
+
+def run_ec_layer(inp: synth.Inputs, layer: Optional[moe.MoELayer] = None) -> EcGpuOut:
+    w = inp.w
+    assert w.flags & moe.MOE_FLAG_EXPERT_CHOICE
+    if layer is None:
+        layer = moe.MoELayer(shape_of(w), inp.wr, inp.w1, inp.w3, inp.w2, inp.ws1, inp.ws3,
+                             inp.ws2, inp.offset, None, device=inp.x.device)
+    layer.forward(inp.x)
+    torch.cuda.synchronize()
+    assert moe.moe_check_status(layer.ws) == 0
+    n = w.E * layer.r
+    return EcGpuOut(layer.y.clone(), np_of(layer.row_token)[:n], np_of(layer.row_gate)[:n],
+                    np_of(layer.counts), np_of(layer.f), np_of(layer.P), float(layer.losses[0]),
+                    float(layer.losses[1]), layer.r)
+
+
+@dataclass
+class EcRef:
+    routing: oracle.Routing
+    ec: oracle.ExpertChoice
+    loss: oracle.Losses
+    forced: int
+
+
+def oracle_ec(inp: synth.Inputs, gpu_row_token: np.ndarray) -> EcRef:
+    """Oracle expert-choice routing; near-cut (expert, token) picks take the
+    GPU's decision after the validity checks of cut_force."""
+    w = inp.w
+    logits = oracle.router_logits(np_of(inp.x), np_of(inp.wr), np_of(inp.offset))
+    r0 = oracle.route(logits, 0, None, flags=w.flags & oracle.SIGMOID)
+    r = oracle.ec_capacity(float(np.float32(w.capacity_factor)), w.k, w.T, w.E)
+    force = np.zeros((w.E, w.T), np.int8)
+    for e in range(w.E):
+        picked = np.zeros(w.T, bool)
+        rows = gpu_row_token[e * r:(e + 1) * r]
+        assert np.all(np.diff(rows) > 0), f"expert {e}: rows not in ascending token order"
+        picked[rows] = True
+        force[e] = cut_force(r0.p[:, e], r, picked, f"expert {e}")
+    ec = oracle.expert_choice(r0.p, r, force=force)
+    ls = oracle.losses(np.full(w.E, r, np.int32), r0.p, r0.lse, w.k,
+                       float(np.float32(w.balance_coef)), n_pairs=w.E * r)
+    return EcRef(r0, ec, ls, int(np.count_nonzero(force)))
+
+
+def oracle_ec_y(inp: synth.Inputs, ref: EcRef, sel: np.ndarray) -> np.ndarray:
+    """Oracle expert-choice output for the tokens in ``sel``, copying to the
+    host only the weights of the experts that picked them."""
+    w = inp.w
+    r = ref.ec.r
+    sel = np.asarray(sel, np.int32)
+    used = [e for e in range(w.E)
+            if r > 0 and np.isin(ref.ec.row_token[e * r:(e + 1) * r], sel).any()]
+    if used:
+        idx = torch.tensor(used, device=inp.w1.device)
+        w1 = np_of(inp.w1.index_select(0, idx))
+        w3 = np_of(inp.w3.index_select(0, idx))
+        w2 = np_of(inp.w2.index_select(0, idx))
+        rows = np.concatenate([np.arange(e * r, (e + 1) * r) for e in used])
+        sub = oracle.ExpertChoice(r, ref.ec.row_token[rows], ref.ec.row_gate[rows])
+    else:
+        w1 = w3 = np.zeros((1, w.M, w.d), np.uint16)
+        w2 = np.zeros((1, w.d, w.M), np.uint16)
+        sub = oracle.ExpertChoice(0, np.zeros(0, np.int32), np.zeros(0))
+    return oracle.ec_layer_tokens(np_of(inp.x), sub, w1, w3, w2, np_of(inp.ws1),
+                                  np_of(inp.ws3), np_of(inp.ws2), sel)
+
+
+def check_ec_layer(inp: synth.Inputs, sel: Optional[np.ndarray] = None, layer=None):
+    """Runs the GPU expert-choice layer and checks it against the oracle."""
+    w = inp.w
+    g = run_ec_layer(inp, layer)
+    ref = oracle_ec(inp, g.row_token)
+    assert g.r == ref.ec.r
+    np.testing.assert_array_equal(g.row_token, ref.ec.row_token)
+    if g.r > 0:
+        assert np.abs(g.row_gate - ref.ec.row_gate).max() <= GATE_ABS
+    np.testing.assert_array_equal(g.counts, np.full(w.E, g.r))
+    np.testing.assert_allclose(g.f, ref.loss.f, rtol=1e-6, atol=0)
+    np.testing.assert_allclose(g.P, ref.loss.P, rtol=LOSS_REL, atol=1e-7)
+    rel_close(g.bal, ref.loss.L_bal, LOSS_REL, "balance loss")
+    rel_close(g.z, ref.loss.L_z, LOSS_REL, "z-loss")
+    if sel is None:
+        sel = np.arange(w.T)
+    if len(sel):
+        y_ref = oracle_ec_y(inp, ref, sel)
         assert_y_close(bf16_to_f64(g.y)[sel], y_ref)
     return g, ref

@@ -63,7 +63,8 @@ def shape(**kw):
     (dict(M=200), B.MOE_ERR_UNSUPPORTED),            # M % 128
     (dict(E=300, k=2), B.MOE_ERR_UNSUPPORTED),
     (dict(E=16, k=9), B.MOE_ERR_UNSUPPORTED),        # k > 8
-    (dict(flags=4), B.MOE_ERR_UNSUPPORTED),
+    (dict(flags=16), B.MOE_ERR_UNSUPPORTED),
+    (dict(flags=B.MOE_FLAG_PRIORITY_CAPACITY | B.MOE_FLAG_EXPERT_CHOICE), B.MOE_ERR_UNSUPPORTED),
     (dict(n_shared=9), B.MOE_ERR_UNSUPPORTED),
     (dict(capacity_factor=float("nan")), B.MOE_ERR_INVALID_ARG),
 ])
@@ -130,3 +131,61 @@ def test_workspace_grows_with_shape(lib):
     assert b < a
     # intermediate rows: x_perm, h, y_perm for 8192 rows at least
     assert a >= 8192 * (4096 * 2 * 2 + 14336 * 2)
+
+
+def test_expert_choice_sizes_match_oracle(lib):
+    rng = np.random.default_rng(3)
+    cases = [(1.0, 2, 4096, 8), (0.0, 1, 3, 2), (5.0, 2, 10, 4), (1.25, 1, 32768, 128),
+             (1.0, 6, 8192, 160), (0.5, 0, 100, 8)]
+    for _ in range(100):
+        cases.append((float(np.float32(rng.uniform(0.1, 4.0))), int(rng.integers(0, 9)),
+                      int(rng.integers(0, 50000)), int(rng.integers(8, 257))))
+    for c, k, T, E in cases:
+        k = min(k, E)
+        s = shape(T=T, E=E, k=k, capacity_factor=c, flags=B.MOE_FLAG_EXPERT_CHOICE)
+        r = oracle.ec_capacity(float(np.float32(c)), k, T, E)
+        assert B.moe_ec_capacity(s) == r, (c, k, T, E)
+        assert B.moe_max_rows(s) == E * r
+    # the expert-choice count needs the flag
+    with pytest.raises(B.MoeError):
+        B.moe_ec_capacity(shape())
+
+
+def test_entry_points_check_the_routing_mode(lib):
+    """Token-choice entry points refuse an expert-choice shape and the other
+    way round; moe_permute cannot run the priority cut (it gets no scores).
+    Every call here is refused by the host checks, so nothing is enqueued (the
+    pointers are host addresses that are never dereferenced)."""
+    ec = shape(flags=B.MOE_FLAG_EXPERT_CHOICE)
+    tc = shape()
+    prio = shape(capacity_factor=1.0, flags=B.MOE_FLAG_PRIORITY_CAPACITY)
+    bufs = []
+
+    def ws_for(s):
+        need = B.moe_workspace_size(s)
+        buf = (ctypes.c_uint8 * (need + 512))()
+        bufs.append(buf)
+        return ctypes.c_void_p((ctypes.addressof(buf) + 255) // 256 * 256), need
+
+    base, need = ws_for(ec)
+    fake = base
+    assert lib.moe_route(ctypes.byref(ec), fake, fake, None, None, *([fake] * 7), base, need,
+                         None) == B.MOE_ERR_INVALID_ARG
+    assert lib.moe_permute(ctypes.byref(ec), fake, fake, fake, fake, fake, fake, fake, base,
+                           need, None) == B.MOE_ERR_INVALID_ARG
+    assert lib.moe_combine(ctypes.byref(ec), fake, fake, fake, None, fake,
+                           None) == B.MOE_ERR_INVALID_ARG
+    assert lib.moe_layer_forward(ctypes.byref(ec), *([fake] * 17), base, need,
+                                 None) == B.MOE_ERR_INVALID_ARG
+    assert lib.moe_route_noalloc(ctypes.byref(ec), *([None] * 12)) == B.MOE_ERR_INVALID_ARG
+    for s in (tc, prio):
+        base, need = ws_for(s)
+        assert lib.moe_ec_route(ctypes.byref(s), base, base, None, base, base, base, base, base,
+                                base, base, base, need, None) == B.MOE_ERR_INVALID_ARG
+        assert lib.moe_ec_layer_forward(ctypes.byref(s), *([base] * 15), base, need,
+                                        None) == B.MOE_ERR_INVALID_ARG
+    base, need = ws_for(prio)
+    assert lib.moe_permute(ctypes.byref(prio), base, base, base, base, base, base, base, base,
+                           need, None) == B.MOE_ERR_UNSUPPORTED
+    # the extra scratch is sized only when a mode needs it
+    assert B.moe_workspace_size(shape(capacity_factor=1.0)) < B.moe_workspace_size(prio)

@@ -11,5 +11,6 @@ from ._binding import (  # noqa: F401
     moe_pack_w13, moe_permute, moe_route, moe_set_wait_timeout_ns, moe_workspace_size,
     MoELayer, moe_profile_enable, moe_profile_collect, moe_launch_count, alloc_workspace,
     moe_route_noalloc, moe_route_ex, MOE_FLAG_SIGMOID, MOE_FLAG_NO_RENORM,
-    moe_alf_bias_update,
+    moe_alf_bias_update, MOE_FLAG_PRIORITY_CAPACITY, MOE_FLAG_EXPERT_CHOICE, moe_ec_capacity,
+    moe_ec_route, moe_ec_layer_forward,
 )

@@ -31,6 +31,8 @@ class MoeError(RuntimeError):
 
 MOE_FLAG_SIGMOID = 1
 MOE_FLAG_NO_RENORM = 2
+MOE_FLAG_PRIORITY_CAPACITY = 4
+MOE_FLAG_EXPERT_CHOICE = 8
 
 
 class RouteOut(ctypes.Structure):
@@ -86,6 +88,9 @@ def lib():
     L.moe_route_noalloc.argtypes = [S] + [_P] * 11 + [_P]
     L.moe_route_ex.argtypes = [S, _P, _P, _P, _P, ctypes.POINTER(RouteOut), _P, sz, _P]
     L.moe_alf_bias_update.argtypes = [S, _P, ctypes.c_float, _P, _P]
+    L.moe_ec_capacity.argtypes = [S, ctypes.POINTER(ctypes.c_int64)]
+    L.moe_ec_route.argtypes = [S] + [_P] * 10 + [_P, sz, _P]
+    L.moe_ec_layer_forward.argtypes = [S] + [_P] * 15 + [_P, sz, _P]
     for name in ("moe_workspace_size", "moe_capacity", "moe_max_rows", "moe_pack_w13",
                  "moe_route", "moe_permute", "moe_grouped_ffn", "moe_combine",
                  "moe_layer_forward", "moe_layer_forward_host", "moe_check_status",
@@ -237,6 +242,29 @@ def moe_layer_forward_host(shape, x_host, x_dev, w_router, logit_offset, sel_bia
         _stream(stream)), "moe_layer_forward_host")
 
 
+def moe_ec_capacity(shape: Shape) -> int:
+    v = ctypes.c_int64()
+    _check(lib().moe_ec_capacity(ctypes.byref(shape), ctypes.byref(v)), "moe_ec_capacity")
+    return v.value
+
+
+def moe_ec_route(shape, x, w_router, logit_offset, row_token, row_gate, counts, f, P, bal_loss,
+                 z_loss, ws, stream=None):
+    _check(lib().moe_ec_route(ctypes.byref(shape), _ptr(x), _ptr(w_router), _ptr(logit_offset),
+                              _ptr(row_token), _ptr(row_gate), _ptr(counts), _ptr(f), _ptr(P),
+                              _ptr(bal_loss), _ptr(z_loss), _ptr(ws), ws.numel(),
+                              _stream(stream)), "moe_ec_route")
+
+
+def moe_ec_layer_forward(shape, x, w_router, logit_offset, w13, w2, w13_shared, w2_shared, y,
+                         row_token, row_gate, counts, f, P, bal_loss, z_loss, ws, stream=None):
+    _check(lib().moe_ec_layer_forward(
+        ctypes.byref(shape), _ptr(x), _ptr(w_router), _ptr(logit_offset), _ptr(w13), _ptr(w2),
+        _ptr(w13_shared), _ptr(w2_shared), _ptr(y), _ptr(row_token), _ptr(row_gate),
+        _ptr(counts), _ptr(f), _ptr(P), _ptr(bal_loss), _ptr(z_loss), _ptr(ws), ws.numel(),
+        _stream(stream)), "moe_ec_layer_forward")
+
+
 def moe_check_status(ws, stream=None) -> int:
     v = ctypes.c_int()
     _check(lib().moe_check_status(_ptr(ws), ctypes.byref(v), _stream(stream)),
@@ -254,7 +282,7 @@ def moe_debug_timeout_probe(ws, stream=None):
 
 
 KERNEL_NAMES = {1: "router", 2: "finalize", 3: "tile_hist", 4: "scatter", 5: "gemm_swiglu",
-                6: "gemm_down", 7: "combine", 8: "other"}
+                6: "gemm_down", 7: "combine", 8: "other", 9: "select", 10: "gather"}
 
 
 KERNEL_IDS = {v: k for k, v in KERNEL_NAMES.items()}
@@ -294,7 +322,8 @@ def moe_launch_count() -> int:
 
 class MoELayer:
     """Owns packed weights, outputs and the workspace of one layer shape and
-    runs ``moe_layer_forward``.  Weights are given in canonical form:
+    runs ``moe_layer_forward`` (``moe_ec_layer_forward`` when the shape has
+    MOE_FLAG_EXPERT_CHOICE).  Weights are given in canonical form:
     w1, w3 [E][M][d], w2 [E][d][M], optional shared ws1, ws3 [Ms][d], ws2 [d][Ms]."""
 
     def __init__(self, shape: Shape, w_router, w1, w3, w2, ws1=None, ws3=None, ws2=None,
@@ -321,8 +350,20 @@ class MoELayer:
         self.f = torch.empty(E, dtype=torch.float32, device=dev)
         self.P = torch.empty(E, dtype=torch.float32, device=dev)
         self.losses = torch.empty(2, dtype=torch.float32, device=dev)
+        self.expert_choice = bool(shape.flags & MOE_FLAG_EXPERT_CHOICE)
+        if self.expert_choice:
+            r = moe_ec_capacity(shape)
+            self.r = r
+            self.row_token = torch.empty(max(E * r, 1), dtype=torch.int32, device=dev)
+            self.row_gate = torch.empty(max(E * r, 1), dtype=torch.float32, device=dev)
 
     def forward(self, x, stream=None):
+        if self.expert_choice:
+            moe_ec_layer_forward(self.shape, x, self.w_router, self.logit_offset, self.w13,
+                                 self.w2, self.w13_shared, self.w2_shared, self.y, self.row_token,
+                                 self.row_gate, self.counts, self.f, self.P, self.losses[0:1],
+                                 self.losses[1:2], self.ws, stream)
+            return self.y
         moe_layer_forward(self.shape, x, self.w_router, self.logit_offset, self.sel_bias,
                           self.w13, self.w2, self.w13_shared, self.w2_shared, self.y, self.ids,
                           self.gates, self.counts, self.drop_mask, self.f, self.P,

@@ -66,8 +66,10 @@ struct Layout {
   size_t status, tile_hist, tile_psum, tile_lse2, tile_base, exp_count, exp_psum, offsets;
   size_t tile_imp, tile_ent, exp_imp;
   size_t slot_row, row_token;
+  size_t pair_score, stage_q, stage_key, all_offsets;  // priority capacity
+  size_t scores_t, sel_t, row_gate;                    // expert choice
   size_t x_perm, h, y_perm, h_s, y_s, total;
-  int64_t ntiles, rmax, C;
+  int64_t ntiles, rmax, C, r;
 };
 
 int check_shape(const moe_shape_t* s) {
@@ -77,7 +79,11 @@ int check_shape(const moe_shape_t* s) {
   if (s->k > s->E) return MOE_ERR_INVALID_ARG;
   if (!std::isfinite(s->capacity_factor) || !std::isfinite(s->balance_coef))
     return MOE_ERR_INVALID_ARG;
-  if ((s->flags & ~(MOE_FLAG_SIGMOID | MOE_FLAG_NO_RENORM)) != 0) return MOE_ERR_UNSUPPORTED;
+  if ((s->flags & ~(MOE_FLAG_SIGMOID | MOE_FLAG_NO_RENORM | MOE_FLAG_PRIORITY_CAPACITY |
+                    MOE_FLAG_EXPERT_CHOICE)) != 0)
+    return MOE_ERR_UNSUPPORTED;
+  if ((s->flags & MOE_FLAG_PRIORITY_CAPACITY) && (s->flags & MOE_FLAG_EXPERT_CHOICE))
+    return MOE_ERR_UNSUPPORTED;
   if (s->E > MOE_MAX_EXPERTS || s->k > MOE_MAX_TOPK) return MOE_ERR_UNSUPPORTED;
   if (s->T > (1 << 24)) return MOE_ERR_UNSUPPORTED;
   if (s->d % 64 != 0 || s->d < 64 || s->d > 16384) return MOE_ERR_UNSUPPORTED;
@@ -94,6 +100,19 @@ int64_t capacity_of(const moe_shape_t* s) {
                 static_cast<double>(s->E)));
 }
 
+inline bool is_ec(const moe_shape_t* s) { return (s->flags & MOE_FLAG_EXPERT_CHOICE) != 0; }
+inline bool is_priority(const moe_shape_t* s) {
+  return (s->flags & MOE_FLAG_PRIORITY_CAPACITY) != 0 && capacity_of(s) >= 0;
+}
+
+// Expert choice: tokens per expert, min(T, ceil(c k T / E)), c <= 0 read as 1.
+int64_t ec_capacity_of(const moe_shape_t* s) {
+  const double c = s->capacity_factor > 0.0f ? static_cast<double>(s->capacity_factor) : 1.0;
+  const int64_t r = static_cast<int64_t>(std::ceil(
+      c * static_cast<double>(s->k) * static_cast<double>(s->T) / static_cast<double>(s->E)));
+  return r < s->T ? r : s->T;
+}
+
 Layout layout_of(const moe_shape_t* s) {
   Layout L{};
   const int64_t T = s->T, d = s->d, M = s->M, E = s->E, k = s->k;
@@ -102,6 +121,13 @@ Layout layout_of(const moe_shape_t* s) {
   L.C = capacity_of(s);
   L.rmax = T * k;
   if (L.C >= 0 && E * L.C < L.rmax) L.rmax = E * L.C;
+  L.r = -1;
+  if (is_ec(s)) {
+    L.C = -1;
+    L.r = ec_capacity_of(s);
+    L.rmax = E * L.r;
+  }
+  const bool prio = is_priority(s) && !is_ec(s);
   size_t o = 0;
   auto take = [&](size_t bytes) {
     const size_t at = o;
@@ -121,6 +147,13 @@ Layout layout_of(const moe_shape_t* s) {
   L.offsets = take((E + 1) * 4);
   L.slot_row = take(T * k * 4);
   L.row_token = take(L.rmax * 4);
+  L.pair_score = take(prio ? T * k * 4 : 0);
+  L.stage_q = take(prio ? T * k * 4 : 0);
+  L.stage_key = take(prio ? T * k * 4 : 0);
+  L.all_offsets = take(prio ? (E + 1) * 4 : 0);
+  L.scores_t = take(is_ec(s) ? E * T * 4 : 0);
+  L.sel_t = take(is_ec(s) ? E * T * 4 : 0);
+  L.row_gate = take(is_ec(s) ? L.rmax * 4 : 0);
   L.x_perm = take(L.rmax * d * 2);
   L.h = take(L.rmax * M * 2);
   L.y_perm = take(L.rmax * d * 2);
@@ -163,11 +196,22 @@ inline int cuda_rc(int rc) {
 }
 
 // ---------------------------------------------------------------- stages
+// Extra router / finalize outputs of the priority-capacity and expert-choice
+// paths.
+struct RouteExtras {
+  float* pair_score = nullptr;      // [T][k] scores of the selected pairs
+  int32_t* all_offsets = nullptr;   // [E+1] scan of the counts before capacity
+  float* scores_t = nullptr;        // [E][T] expert choice: every score
+  int32_t fixed_count = -1;         // expert choice: r
+  double n_pairs = -1.0;            // expert choice: E r
+};
+
 int do_route(const moe_shape_t* s, const uint16_t* x, const uint16_t* wr, const float* off,
              const float* bias, int32_t* ids, float* gates, int32_t* counts, float* f, float* P,
              float* bal, float* z, void* ws, const Layout& L, int32_t* tile_base,
              int32_t* offsets, cudaStream_t st, float* importance = nullptr,
-             float* importance_cv2 = nullptr, float* entropy_mean = nullptr) {
+             float* importance_cv2 = nullptr, float* entropy_mean = nullptr,
+             const RouteExtras& ex = RouteExtras()) {
   const bool want_imp = (importance != nullptr || importance_cv2 != nullptr) && s->k > 0;
   const bool want_ent = entropy_mean != nullptr;
   if (s->T > 0) {
@@ -179,7 +223,7 @@ int do_route(const moe_shape_t* s, const uint16_t* x, const uint16_t* wr, const 
     ra.T = s->T;
     ra.d = s->d;
     ra.E = s->E;
-    ra.k = s->k;
+    ra.k = ex.scores_t ? 0 : s->k;  // expert choice: no per-token Top-k
     ra.logit_offset = off;
     ra.sel_bias = bias;
     ra.ids = ids;
@@ -189,9 +233,11 @@ int do_route(const moe_shape_t* s, const uint16_t* x, const uint16_t* wr, const 
     ra.tile_lse2 = at<float>(ws, L.tile_lse2);
     ra.status = at<int>(ws, L.status);
     ra.timeout_ns = g_timeout_ns;
-    ra.flags = s->flags;
+    ra.flags = s->flags & (kRouteSigmoid | kRouteNoRenorm);
     ra.tile_imp = want_imp ? at<float>(ws, L.tile_imp) : nullptr;
     ra.tile_ent = want_ent ? at<float>(ws, L.tile_ent) : nullptr;
+    ra.pair_score = ex.pair_score;
+    ra.scores_t = ex.scores_t;
     const int rc = tracked(MOE_KERNEL_ROUTER, st, [&] { return launch_router(mx, mw, ra, sm_count_cached(), st); });
     if (rc != 0) return cuda_rc(rc);
   }
@@ -214,6 +260,9 @@ int do_route(const moe_shape_t* s, const uint16_t* x, const uint16_t* wr, const 
   fa.exp_count = at<int32_t>(ws, L.exp_count);
   fa.exp_psum = at<double>(ws, L.exp_psum);
   fa.done_counter = at<int>(ws, L.status + 64);
+  fa.fixed_count = ex.fixed_count;
+  fa.n_pairs = ex.n_pairs;
+  fa.all_offsets = ex.all_offsets;
   if (want_imp) {
     fa.tile_imp = at<float>(ws, L.tile_imp);
     fa.exp_imp = at<double>(ws, L.exp_imp);
@@ -251,6 +300,71 @@ int do_scatter(const moe_shape_t* s, const uint16_t* x, const int32_t* ids, cons
   sa.x_perm = x_perm;
   sa.num_sms = sm_count_cached();
   return cuda_rc(tracked(MOE_KERNEL_SCATTER, st, [&] { return launch_scatter(sa, st); }));
+}
+
+// Priority capacity: stage every pair by expert, cut each expert at its C
+// highest scores, then gather the kept rows.
+int do_priority_dispatch(const moe_shape_t* s, const uint16_t* x, const int32_t* ids,
+                         const Layout& L, void* ws, const int32_t* offsets, int32_t* slot_row,
+                         int32_t* row_token, uint8_t* drop_mask, uint16_t* x_perm,
+                         cudaStream_t st) {
+  ScatterArgs sa{};
+  sa.T = s->T;
+  sa.d = s->d;
+  sa.E = s->E;
+  sa.k = s->k;
+  sa.C = L.C;
+  sa.ids = ids;
+  sa.tile_base = at<int32_t>(ws, L.tile_base);
+  sa.offsets = offsets;
+  sa.x = x;
+  sa.num_sms = sm_count_cached();
+  sa.stage_q = at<int32_t>(ws, L.stage_q);
+  sa.stage_key = at<float>(ws, L.stage_key);
+  sa.pair_score = at<float>(ws, L.pair_score);
+  sa.all_offsets = at<int32_t>(ws, L.all_offsets);
+  int rc = cuda_rc(tracked(MOE_KERNEL_SCATTER, st, [&] { return launch_scatter(sa, st); }));
+  if (rc != MOE_OK) return rc;
+  PrioritySelectArgs pa{};
+  pa.E = s->E;
+  pa.k = s->k;
+  pa.C = L.C;
+  pa.all_offsets = sa.all_offsets;
+  pa.offsets = offsets;
+  pa.stage_q = sa.stage_q;
+  pa.stage_key = sa.stage_key;
+  pa.slot_row = slot_row;
+  pa.drop_mask = drop_mask;
+  pa.row_token = row_token;
+  rc = cuda_rc(tracked(MOE_KERNEL_SELECT, st, [&] { return launch_priority_select(pa, st); }));
+  if (rc != MOE_OK) return rc;
+  return cuda_rc(tracked(MOE_KERNEL_GATHER, st, [&] {
+    return launch_gather_rows(x, row_token, offsets, s->E, s->d, L.rmax, x_perm,
+                              sm_count_cached(), st);
+  }));
+}
+
+// Expert choice: router (every score, expert-major) + finalize with fixed
+// counts, then each expert's top-r cut.
+int do_ec_route(const moe_shape_t* s, const uint16_t* x, const uint16_t* wr, const float* off,
+                int32_t* row_token, float* row_gate, int32_t* counts, float* f, float* P,
+                float* bal, float* z, void* ws, const Layout& L, cudaStream_t st) {
+  RouteExtras ex;
+  ex.scores_t = at<float>(ws, L.scores_t);
+  ex.fixed_count = static_cast<int32_t>(L.r);
+  ex.n_pairs = static_cast<double>(s->E) * static_cast<double>(L.r);
+  int rc = do_route(s, x, wr, off, nullptr, nullptr, nullptr, counts, f, P, bal, z, ws, L,
+                    nullptr, at<int32_t>(ws, L.offsets), st, nullptr, nullptr, nullptr, ex);
+  if (rc != MOE_OK || s->T == 0) return rc;
+  EcSelectArgs ea{};
+  ea.T = s->T;
+  ea.E = s->E;
+  ea.r = static_cast<int32_t>(L.r);
+  ea.scores_t = ex.scores_t;
+  ea.sel_t = at<int32_t>(ws, L.sel_t);
+  ea.row_token = row_token;
+  ea.row_gate = row_gate;
+  return cuda_rc(tracked(MOE_KERNEL_SELECT, st, [&] { return launch_ec_select(ea, st); }));
 }
 
 int do_ffn(const moe_shape_t* s, const uint16_t* x_perm, const int32_t* offsets,
@@ -394,6 +508,7 @@ int moe_route(const moe_shape_t* s, const uint16_t* x, const uint16_t* w_router,
   if (rc != MOE_OK) return rc;
   Layout L;
   if ((rc = check_ws(s, ws, ws_bytes, &L)) != MOE_OK) return rc;
+  if (is_ec(s)) return MOE_ERR_INVALID_ARG;
   if (!counts || !f || !P || !bal_loss || !z_loss) return MOE_ERR_INVALID_ARG;
   if (s->T > 0) {
     if (!x || !w_router || !aligned16(x) || !aligned16(w_router)) return MOE_ERR_INVALID_ARG;
@@ -410,6 +525,7 @@ int moe_route_ex(const moe_shape_t* s, const uint16_t* x, const uint16_t* w_rout
   if (rc != MOE_OK) return rc;
   Layout L;
   if ((rc = check_ws(s, ws, ws_bytes, &L)) != MOE_OK) return rc;
+  if (is_ec(s)) return MOE_ERR_INVALID_ARG;
   if (!o || !o->counts || !o->f || !o->P || !o->bal_loss || !o->z_loss) return MOE_ERR_INVALID_ARG;
   if (s->T > 0) {
     if (!x || !w_router || !aligned16(x) || !aligned16(w_router)) return MOE_ERR_INVALID_ARG;
@@ -428,6 +544,8 @@ int moe_permute(const moe_shape_t* s, const uint16_t* x, const int32_t* ids, int
   if (rc != MOE_OK) return rc;
   Layout L;
   if ((rc = check_ws(s, ws, ws_bytes, &L)) != MOE_OK) return rc;
+  if (is_ec(s)) return MOE_ERR_INVALID_ARG;
+  if (is_priority(s)) return MOE_ERR_UNSUPPORTED;  // needs the router's pair scores
   if (!offsets) return MOE_ERR_INVALID_ARG;
   const bool work = s->T > 0 && s->k > 0;
   if (work && (!x || !ids || !slot_row || !row_token || !drop_mask || !x_perm ||
@@ -485,6 +603,7 @@ int moe_combine(const moe_shape_t* s, const uint16_t* y_perm, const int32_t* slo
                 const float* gates, const uint16_t* y_shared, uint16_t* y, void* stream) {
   const int rc = check_shape(s);
   if (rc != MOE_OK) return rc;
+  if (is_ec(s)) return MOE_ERR_INVALID_ARG;
   if (s->T == 0) return MOE_OK;
   if (!y || !aligned16(y)) return MOE_ERR_INVALID_ARG;
   if (s->k > 0 && (!y_perm || !slot_row || !gates || !aligned16(y_perm)))
@@ -506,6 +625,7 @@ int moe_layer_forward(const moe_shape_t* s, const uint16_t* x, const uint16_t* w
   if (rc != MOE_OK) return rc;
   Layout L;
   if ((rc = check_ws(s, ws, ws_bytes, &L)) != MOE_OK) return rc;
+  if (is_ec(s)) return MOE_ERR_INVALID_ARG;
   if (!counts || !f || !P || !bal_loss || !z_loss) return MOE_ERR_INVALID_ARG;
   if (s->T > 0) {
     if (!x || !w_router || !y || !aligned16(x) || !aligned16(w_router) || !aligned16(y))
@@ -519,16 +639,27 @@ int moe_layer_forward(const moe_shape_t* s, const uint16_t* x, const uint16_t* w
   }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int32_t* offsets = at<int32_t>(ws, L.offsets);
+  const bool prio = is_priority(s);
+  RouteExtras ex;
+  if (prio) {
+    ex.pair_score = at<float>(ws, L.pair_score);
+    ex.all_offsets = at<int32_t>(ws, L.all_offsets);
+  }
   rc = do_route(s, x, w_router, logit_offset, sel_bias, ids, gates, counts, f, P, bal_loss,
-                z_loss, ws, L, at<int32_t>(ws, L.tile_base), offsets, st);
+                z_loss, ws, L, at<int32_t>(ws, L.tile_base), offsets, st, nullptr, nullptr,
+                nullptr, ex);
   if (rc != MOE_OK || s->T == 0) return rc;
   int32_t* slot_row = at<int32_t>(ws, L.slot_row);
   uint16_t* x_perm = at<uint16_t>(ws, L.x_perm);
   uint16_t* y_perm = at<uint16_t>(ws, L.y_perm);
   uint16_t* y_s = s->n_shared > 0 ? at<uint16_t>(ws, L.y_s) : nullptr;
   if (s->k > 0) {
-    rc = do_scatter(s, x, ids, L, ws, offsets, slot_row, at<int32_t>(ws, L.row_token),
-                    drop_mask, x_perm, st);
+    if (prio)
+      rc = do_priority_dispatch(s, x, ids, L, ws, offsets, slot_row,
+                                at<int32_t>(ws, L.row_token), drop_mask, x_perm, st);
+    else
+      rc = do_scatter(s, x, ids, L, ws, offsets, slot_row, at<int32_t>(ws, L.row_token),
+                      drop_mask, x_perm, st);
     if (rc != MOE_OK) return rc;
   }
   rc = do_ffn(s, x_perm, offsets, w13, w2, y_perm, x, w13_shared, w2_shared, y_s, ws, L, st);
@@ -574,6 +705,77 @@ int moe_alf_bias_update(const moe_shape_t* s, const int32_t* counts, float gamma
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   return cuda_rc(tracked(MOE_KERNEL_OTHER, st, [&] {
     return launch_alf_bias_update(s->E, s->T, s->k, counts, gamma, bias, st);
+  }));
+}
+
+int moe_ec_capacity(const moe_shape_t* s, int64_t* r) {
+  const int rc = check_shape(s);
+  if (rc != MOE_OK) return rc;
+  if (!is_ec(s) || r == nullptr) return MOE_ERR_INVALID_ARG;
+  *r = ec_capacity_of(s);
+  return MOE_OK;
+}
+
+int moe_ec_route(const moe_shape_t* s, const uint16_t* x, const uint16_t* w_router,
+                 const float* logit_offset, int32_t* row_token, float* row_gate, int32_t* counts,
+                 float* f, float* P, float* bal_loss, float* z_loss, void* ws, size_t ws_bytes,
+                 void* stream) {
+  int rc = check_shape(s);
+  if (rc != MOE_OK) return rc;
+  if (!is_ec(s)) return MOE_ERR_INVALID_ARG;
+  Layout L;
+  if ((rc = check_ws(s, ws, ws_bytes, &L)) != MOE_OK) return rc;
+  if (!counts || !f || !P || !bal_loss || !z_loss) return MOE_ERR_INVALID_ARG;
+  if (s->T > 0) {
+    if (!x || !w_router || !aligned16(x) || !aligned16(w_router)) return MOE_ERR_INVALID_ARG;
+    if (L.rmax > 0 && (!row_token || !row_gate)) return MOE_ERR_INVALID_ARG;
+  }
+  return do_ec_route(s, x, w_router, logit_offset, row_token, row_gate, counts, f, P, bal_loss,
+                     z_loss, ws, L, static_cast<cudaStream_t>(stream));
+}
+
+int moe_ec_layer_forward(const moe_shape_t* s, const uint16_t* x, const uint16_t* w_router,
+                         const float* logit_offset, const uint16_t* w13, const uint16_t* w2,
+                         const uint16_t* w13_shared, const uint16_t* w2_shared, uint16_t* y,
+                         int32_t* row_token, float* row_gate, int32_t* counts, float* f,
+                         float* P, float* bal_loss, float* z_loss, void* ws, size_t ws_bytes,
+                         void* stream) {
+  int rc = check_shape(s);
+  if (rc != MOE_OK) return rc;
+  if (!is_ec(s)) return MOE_ERR_INVALID_ARG;
+  Layout L;
+  if ((rc = check_ws(s, ws, ws_bytes, &L)) != MOE_OK) return rc;
+  if (!counts || !f || !P || !bal_loss || !z_loss) return MOE_ERR_INVALID_ARG;
+  if (s->T > 0) {
+    if (!x || !w_router || !y || !aligned16(x) || !aligned16(w_router) || !aligned16(y))
+      return MOE_ERR_INVALID_ARG;
+    if (L.rmax > 0 && (!row_token || !row_gate || !w13 || !w2 || !aligned16(w13) ||
+                       !aligned16(w2)))
+      return MOE_ERR_INVALID_ARG;
+    if (s->n_shared > 0 && (!w13_shared || !w2_shared || !aligned16(w13_shared) ||
+                            !aligned16(w2_shared)))
+      return MOE_ERR_INVALID_ARG;
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  rc = do_ec_route(s, x, w_router, logit_offset, row_token, row_gate, counts, f, P, bal_loss,
+                   z_loss, ws, L, st);
+  if (rc != MOE_OK || s->T == 0) return rc;
+  const int32_t* offsets = at<int32_t>(ws, L.offsets);
+  uint16_t* x_perm = at<uint16_t>(ws, L.x_perm);
+  uint16_t* y_perm = at<uint16_t>(ws, L.y_perm);
+  uint16_t* y_s = s->n_shared > 0 ? at<uint16_t>(ws, L.y_s) : nullptr;
+  if (L.rmax > 0) {
+    rc = cuda_rc(tracked(MOE_KERNEL_GATHER, st, [&] {
+      return launch_gather_rows(x, row_token, offsets, s->E, s->d, L.rmax, x_perm,
+                                sm_count_cached(), st);
+    }));
+    if (rc != MOE_OK) return rc;
+  }
+  rc = do_ffn(s, x_perm, offsets, w13, w2, y_perm, x, w13_shared, w2_shared, y_s, ws, L, st);
+  if (rc != MOE_OK) return rc;
+  return cuda_rc(tracked(MOE_KERNEL_COMBINE, st, [&] {
+    return launch_ec_combine(s->T, s->d, s->E, at<int32_t>(ws, L.sel_t), row_gate, y_perm, y_s,
+                             y, st);
   }));
 }
 

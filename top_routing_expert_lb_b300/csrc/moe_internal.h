@@ -12,6 +12,8 @@ constexpr int kMaxTopK = 8;
 // routing variants (the values of MOE_FLAG_SIGMOID / MOE_FLAG_NO_RENORM)
 constexpr uint32_t kRouteSigmoid = 1u;
 constexpr uint32_t kRouteNoRenorm = 2u;
+constexpr uint32_t kRoutePriority = 4u;      // capacity keeps the highest scores
+constexpr uint32_t kRouteExpertChoice = 8u;  // experts pick tokens
 
 // Ragged grouped GEMM  out[g] = A[g] * B[g]^T  over E routed groups (rows from
 // device offsets) and an optional shared group (fixed row count).
@@ -63,6 +65,8 @@ struct RouterArgs {
   uint32_t flags;             // kRouteSigmoid | kRouteNoRenorm
   float* tile_imp;            // [ntiles][E] importance partials, or null
   float* tile_ent;            // [ntiles] entropy partials, or null
+  float* pair_score = nullptr;  // [T][k] unbiased score of each selected pair, or null
+  float* scores_t = nullptr;    // [E][T] every score, expert-major, or null
 };
 int launch_router(const CUtensorMap& x_map, const CUtensorMap& wr_map, RouterArgs args,
                   int num_sms, cudaStream_t stream);
@@ -96,6 +100,9 @@ struct FinalizeArgs {
   float* importance;          // [E] or null
   float* importance_cv2;      // [1] or null
   float* entropy_mean;        // [1] or null
+  int32_t fixed_count = -1;   // >= 0: every expert's count (expert choice); -1: from tile_hist
+  double n_pairs = -1.0;      // denominator of f; < 0: k T (E r for expert choice)
+  int32_t* all_offsets = nullptr;  // [E+1] scan of the counts before capacity, or null
 };
 int launch_finalize(const FinalizeArgs& args, cudaStream_t stream);
 
@@ -112,8 +119,48 @@ struct ScatterArgs {
   uint8_t* drop_mask;        // [T][k] or null
   uint16_t* x_perm;          // [R_max][d]
   int32_t num_sms;           // sizes the gather split
+  // staging mode (priority capacity): when stage_q is set, the pair at rank r
+  // of expert e goes to stage_q/stage_key[all_offsets[e] + r] instead (its
+  // flat index and pair_score); nothing else is written
+  int32_t* stage_q = nullptr;          // [T*k] or null
+  float* stage_key = nullptr;          // [T*k]
+  const float* pair_score = nullptr;   // [T][k]
+  const int32_t* all_offsets = nullptr;  // [E+1]
 };
 int launch_scatter(const ScatterArgs& args, cudaStream_t stream);
+
+// Priority capacity cut over the staged pairs: one CTA per expert.
+struct PrioritySelectArgs {
+  int32_t E, k;
+  int64_t C;
+  const int32_t* all_offsets;  // [E+1] staging segments
+  const int32_t* offsets;      // [E+1] kept-row offsets
+  const int32_t* stage_q;      // [T*k]
+  const float* stage_key;      // [T*k]
+  int32_t* slot_row;           // [T][k]
+  uint8_t* drop_mask;          // [T][k] or null
+  int32_t* row_token;          // [R]
+};
+int launch_priority_select(const PrioritySelectArgs& args, cudaStream_t stream);
+
+// Expert choice: expert e takes the r largest scores of scores_t[e][0..T).
+struct EcSelectArgs {
+  int32_t T, E, r;
+  const float* scores_t;  // [E][T]
+  int32_t* sel_t;         // [E][T] row of (e, t), or -1
+  int32_t* row_token;     // [E*r]
+  float* row_gate;        // [E*r]
+};
+int launch_ec_select(const EcSelectArgs& args, cudaStream_t stream);
+
+// x_perm[row] = x[row_token[row]] for row < offsets[E] (read on the device).
+int launch_gather_rows(const uint16_t* x, const int32_t* row_token, const int32_t* offsets,
+                       int32_t E, int32_t d, int64_t max_rows, uint16_t* x_perm, int num_sms,
+                       cudaStream_t stream);
+
+int launch_ec_combine(int32_t T, int32_t d, int32_t E, const int32_t* sel_t,
+                      const float* row_gate, const uint16_t* y_perm, const uint16_t* y_shared,
+                      uint16_t* y, cudaStream_t stream);
 
 int launch_combine(int32_t T, int32_t d, int32_t k, const uint16_t* y_perm,
                    const int32_t* slot_row, const float* gates, const uint16_t* y_shared,

@@ -14,7 +14,9 @@
 //      token-major order is tile_base + rank inside the tile (warp match +
 //      per-warp counts); the pair is kept iff rank < C and lands on row
 //      offsets[e] + rank.  Each token row is read once and written to each of
-//      its kept rows.
+//      its kept rows.  With probability-priority capacity the same ranks
+//      instead place every pair (and its score) in a per-expert staging list,
+//      which the priority cut (select.cu) turns into rows.
 // Every step is deterministic and bit-reproducible.
 //
 // finalize_kernel also reduces the side outputs in a fixed order:
@@ -103,7 +105,7 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const FinalizeArg
   for (int c0 = 0; c0 < ntiles; c0 += kFinThreads) {
     const int tl = c0 + threadIdx.x;
     const int64_t idx = static_cast<int64_t>(tl) * E + e;
-    const int h = tl < ntiles ? __ldcg(a.tile_hist + idx) : 0;
+    const int h = (tl < ntiles && a.fixed_count < 0) ? __ldcg(a.tile_hist + idx) : 0;
     if (a.tile_psum && tl < ntiles) psum += static_cast<double>(__ldcg(a.tile_psum + idx));
     if (a.tile_imp && tl < ntiles) isum += static_cast<double>(__ldcg(a.tile_imp + idx));
     int tot = 0;
@@ -113,6 +115,7 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const FinalizeArg
   }
   const double ps = block_sum(psum, red);
   const double is = a.tile_imp ? block_sum(isum, red) : 0.0;
+  if (a.fixed_count >= 0) carry = a.fixed_count;
   if (threadIdx.x == 0) {
     a.exp_count[e] = carry;
     a.exp_psum[e] = ps;
@@ -127,8 +130,9 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const FinalizeArg
   const int j = threadIdx.x;
   const int n = j < E ? __ldcg(a.exp_count + j) : 0;
   const double pj = j < E ? __ldcg(a.exp_psum + j) : 0.0;
-  const double fe = (j < E && a.T > 0 && a.k > 0)
-                        ? static_cast<double>(n) / (static_cast<double>(a.k) * a.T) : 0.0;
+  const double n_pairs =
+      a.n_pairs >= 0.0 ? a.n_pairs : static_cast<double>(a.k) * static_cast<double>(a.T);
+  const double fe = (j < E && a.T > 0 && n_pairs > 0.0) ? static_cast<double>(n) / n_pairs : 0.0;
   const double Pe = (j < E && a.T > 0) ? pj / a.T : 0.0;
   if (j < E) {
     if (a.counts) a.counts[j] = n;
@@ -141,6 +145,12 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const FinalizeArg
   if (a.offsets) {
     if (j < E) a.offsets[j] = off;
     if (j == 0) a.offsets[E] = R;
+  }
+  if (a.all_offsets) {
+    int n_all = 0;
+    const int off_all = block_exclusive_scan(j < E ? n : 0, warp_tot, &n_all);
+    if (j < E) a.all_offsets[j] = off_all;
+    if (j == 0) a.all_offsets[E] = n_all;
   }
   const double sfp = block_sum(fe * Pe, red);
   double z = 0.0;
@@ -198,6 +208,7 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_kernel(const ScatterA
   __syncthreads();
   const int32_t* tid = a.ids + static_cast<int64_t>(t0) * k;
   const unsigned lt_mask = (1u << lane) - 1u;
+  const bool staging = a.stage_q != nullptr;
   for (int q0 = 0; q0 < pairs; q0 += kScatterThreads) {
     const int q = q0 + threadIdx.x;
     const bool active = q < pairs;
@@ -210,8 +221,12 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_kernel(const ScatterA
       int r = run[e] + rank_w;
       for (int w = 0; w < warp; ++w) r += wcnt[w][e];
       const int64_t rank = static_cast<int64_t>(base[e]) + r;  // rank within expert
-      const bool kept = (a.C < 0) || (rank < a.C);
-      rows[q] = kept ? static_cast<int>(a.offsets[e] + rank) : -1;
+      if (staging) {
+        rows[q] = static_cast<int>(a.all_offsets[e] + rank);
+      } else {
+        const bool kept = (a.C < 0) || (rank < a.C);
+        rows[q] = kept ? static_cast<int>(a.offsets[e] + rank) : -1;
+      }
     }
     __syncthreads();
     for (int ee = threadIdx.x; ee < E; ee += blockDim.x) {
@@ -224,6 +239,14 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_kernel(const ScatterA
       run[ee] += s;
     }
     __syncthreads();
+  }
+  if (staging) {
+    for (int q = threadIdx.x; q < pairs; q += blockDim.x) {
+      const int64_t gq = static_cast<int64_t>(t0) * k + q;
+      a.stage_q[rows[q]] = static_cast<int32_t>(gq);
+      a.stage_key[rows[q]] = __ldg(a.pair_score + gq);
+    }
+    return;
   }
   if (blockIdx.y == 0) {
     for (int q = threadIdx.x; q < pairs; q += blockDim.x) {
@@ -287,6 +310,7 @@ int launch_scatter(const ScatterArgs& args, cudaStream_t stream) {
   // enough CTAs to keep every SM streaming rows (about 4 per SM)
   int G = (4 * args.num_sms + ntiles - 1) / ntiles;
   G = G < 1 ? 1 : (G > 16 ? 16 : G);
+  if (args.stage_q) G = 1;  // staging writes indices only
   scatter_kernel<<<dim3(ntiles, G), kScatterThreads, 0, stream>>>(args);
   return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }

@@ -84,6 +84,7 @@ extern "C" int moe_route_noalloc(const moe_shape_t* s, const uint16_t* x,
   size_t unused = 0;
   int rc = moe_workspace_size(s, &unused);  // shape checks only
   if (rc != MOE_OK) return rc;
+  if (s->flags & MOE_FLAG_EXPERT_CHOICE) return MOE_ERR_INVALID_ARG;
   if (s->T > kNoAllocMaxTokens || s->E > kNoAllocMaxExperts) return MOE_ERR_UNSUPPORTED;
   if (!counts || !f || !P || !bal_loss || !z_loss) return MOE_ERR_INVALID_ARG;
   if (s->T > 0) {

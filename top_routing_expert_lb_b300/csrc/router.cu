@@ -26,6 +26,9 @@
 // (max, sum) and a merge of per-thread Top-k lists under the total order
 // (key descending, expert index ascending).  Per-CTA column sums, histograms
 // and lse^2 sums go to the cluster's rank-0 CTA, which adds them in rank order.
+// Optional outputs: the unbiased score of every selected pair (priority
+// capacity) and the whole score matrix, expert-major (expert-choice routing,
+// launched with k = 0).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -368,6 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < K; ++j) {
           p.ids[static_cast<int64_t>(t) * K + j] = top_id[j];
           p.gates[static_cast<int64_t>(t) * K + j] = row[top_id[j]] * inv_d;
+          if (p.pair_score) p.pair_score[static_cast<int64_t>(t) * K + j] = row[top_id[j]];
           atomicAdd(&st->hist[top_id[j]], 1);
         }
       }
@@ -378,6 +382,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int rows_valid =
         max(0, min(rpc, p.T - (tile * 128 + static_cast<int>(rank) * rpc)));
     const bool remote = rank != 0;
+    if (p.scores_t != nullptr) {
+      // every score, expert-major: consecutive threads write consecutive tokens
+      const int t0 = tile * 128 + static_cast<int>(rank) * rpc;
+      for (int i = eidx; i < rows_valid * E; i += kEpiThreads) {
+        const int e = i / rows_valid, rr = i - e * rows_valid;
+        p.scores_t[static_cast<int64_t>(e) * p.T + t0 + rr] =
+            lg[(static_cast<int>(rank) * rpc + rr) * ldl + e];
+      }
+    }
     for (int e = eidx; e < E; e += kEpiThreads) {
       float acc = 0.0f;
       for (int rr = 0; rr < rows_valid; ++rr)
