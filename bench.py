@@ -44,6 +44,11 @@ def parse_args(argv=None):
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=15.0,
                     help="target seconds of oracle work for the CPU baseline sample")
+    ap.add_argument("--routing", choices=["token", "priority", "expert-choice"],
+                    default="token",
+                    help="token: token-choice top-k (the headline); priority: capacity "
+                         "keeps each expert's highest scores; expert-choice: every expert "
+                         "takes its top-r tokens (secondary lines: no e2e or CPU leg)")
     ap.add_argument("--stage", choices=["layer", "router"], default="layer",
                     help="router: time moe_route alone (no expert weights are drawn); "
                          "for profiling, not the headline number")
@@ -81,6 +86,9 @@ def load_peaks():
 # --------------------------------------------------------------------------- #
 # algorithmic work                                                             #
 # --------------------------------------------------------------------------- #
+ROUTING_FLAGS = {"token": 0, "priority": 4, "expert-choice": 8}  # MOE_FLAG_* bits
+
+
 def algorithmic_work(w, R: int):
     """FLOPs of the two grouped projections and bytes of the memory stages.
 
@@ -97,13 +105,32 @@ def algorithmic_work(w, R: int):
     b_router = T * d * 2 + E * d * 2 + T * k * 8
     b_scatter = T * d * 2 + R * d * 2 + T * k * 5 + R * 4
     b_combine = R * d * 2 + (T * d * 2 if Ms else 0) + T * d * 2 + T * k * 8
-    return {"gemm_swiglu": f1, "gemm_down": f2}, {"router": b_router, "scatter": b_scatter,
-                                                  "combine": b_combine}
+    bytes_ = {"router": b_router, "scatter": b_scatter, "combine": b_combine}
+    if w.flags & 8:
+        # expert choice: the router also writes every score (E T 4); the cut
+        # reads them and writes the (expert, token) row map (E T 4) and R rows
+        # of token + gate (R 8); the gather reads and writes R rows; the
+        # combine reads the row map instead of slot rows
+        bytes_["router"] = T * d * 2 + E * d * 2 + E * T * 4
+        bytes_["select"] = E * T * 4 + E * T * 4 + R * 8
+        bytes_["gather"] = 2 * R * d * 2 + R * 4
+        bytes_["combine"] = R * d * 2 + (T * d * 2 if Ms else 0) + T * d * 2 + E * T * 4 + R * 4
+        del bytes_["scatter"]
+    elif w.flags & 4 and w.capacity_factor > 0:
+        # priority capacity: the scatter only stages (pair, score) per expert;
+        # the cut reads them and writes slot rows / drop mask / row tokens;
+        # the gather moves the kept rows
+        bytes_["scatter"] = T * k * 4 + T * k * 16
+        bytes_["select"] = T * k * 8 + T * k * 5 + R * 4
+        bytes_["gather"] = 2 * R * d * 2 + R * 4
+    return {"gemm_swiglu": f1, "gemm_down": f2}, bytes_
 
 
 def kept_rows_per_expert(layer, w):
     """Rows each expert computed (after capacity), from the layer's outputs."""
     import torch
+    if getattr(layer, "expert_choice", False):
+        return [layer.r] * w.E
     if w.k == 0:
         return [0] * w.E
     ids = layer.ids.view(-1).long()
@@ -130,8 +157,9 @@ def attainable_ffn_ms(w, kept, peaks):
 def workload_desc(w):
     cap = f"capacity c={w.capacity_factor}" if w.capacity_factor > 0 else "dropless"
     sh = f", {w.n_shared} shared" if w.n_shared else ""
+    rt = {4: ", probability-priority capacity", 8: ", expert-choice routing"}.get(w.flags & 12, "")
     return (f"{w.name}: T={w.T} d={w.d} E={w.E} k={w.k} M={w.M}{sh}, {cap}, "
-            f"offsets={w.offsets}, sel_bias={w.sel_bias}")
+            f"offsets={w.offsets}, sel_bias={w.sel_bias}{rt}")
 
 
 # --------------------------------------------------------------------------- #
@@ -324,7 +352,7 @@ def run_ours(args, w):
 
     inp = synth.make_inputs(w, dev)
     shape = moe.Shape.of(w.T, w.d, w.M, w.E, w.k, w.n_shared, w.capacity_factor,
-                         w.balance_coef)
+                         w.balance_coef, w.flags)
     layer = moe.MoELayer(shape, inp.wr, inp.w1, inp.w3, inp.w2, inp.ws1, inp.ws3, inp.ws2,
                          inp.offset, inp.sel_bias, device=dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -381,7 +409,10 @@ def run_ours(args, w):
     kern_ms = {k: statistics.mean(v) for k, v in per_kernel.items()}
     kern_n = {k: len(v) for k, v in per_kernel.items()}
 
-    R = int(w.T * w.k - int(layer.drop_mask.sum().item())) if w.k else 0
+    if layer.expert_choice:
+        R = w.E * layer.r
+    else:
+        R = int(w.T * w.k - int(layer.drop_mask.sum().item())) if w.k else 0
     flops, bytes_ = algorithmic_work(w, R)
     peaks, peak_src = load_peaks()
     kept = kept_rows_per_expert(layer, w)
@@ -395,7 +426,7 @@ def run_ours(args, w):
 
     # end to end: host tokens in, host output and losses out, through the C ABI
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and args.routing == "token":
         x_host = inp.x.cpu().pin_memory()
         y_host = torch.empty_like(x_host).pin_memory()
         losses_host = torch.empty(2, dtype=torch.float32).pin_memory()
@@ -431,7 +462,7 @@ def run_ours(args, w):
                "path": "moe_layer_forward_host (pinned host x in, y and losses out)"}
 
     cpu = None
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and not args.no_cpu_baseline and args.routing == "token":
         cpu = cpu_baseline(w, inp, args.cpu_budget_s)
 
     if rank != 0:
@@ -450,9 +481,10 @@ def run_ours(args, w):
         "ffn_frac_of_bf16_peak": ffn_tflops / peaks["bf16_tflops"],
         "ffn_attainable_ms": attainable_ms,
         "ffn_frac_of_attainable": attainable_ms / ffn_ms if ffn_ms > 0 else None,
+        "routing": args.routing,
         "load": {"max_over_mean": float(max(kept) / (sum(kept) / len(kept))) if sum(kept) else None,
                  "empty_experts": int(sum(1 for v in kept if v == 0)),
-                 "dropped_pairs": int(w.T * w.k - R)},
+                 "dropped_pairs": int(w.T * w.k - R) if not layer.expert_choice else None},
         "kernel_ms": kern_ms, "kernel_launches_stage_pass": kern_n,
         "stage_gbs": stage_gbs,
         "stage_frac_of_hbm": {k: v / peaks["hbm_gbs"] for k, v in stage_gbs.items()},
@@ -526,7 +558,15 @@ def main(argv=None):
     args = parse_args(argv)
     import synth
     w = synth.WORKLOADS[args.workload]
+    if args.routing != "token":
+        w = w.replace(flags=w.flags | ROUTING_FLAGS[args.routing])
+        if args.routing == "expert-choice":
+            w = w.replace(sel_bias="none")      # a selection bias has no role there
     if args.impl == "reference":
+        if args.routing != "token":
+            print(json.dumps({"impl": "reference", "unavailable": "the CPU leg times the "
+                              "token-choice layer only"}), flush=True)
+            return 0
         return run_reference(args, w)
     if args.stage == "router":
         return run_router_stage(args, w)

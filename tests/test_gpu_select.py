@@ -8,6 +8,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import synth
 from parity import (assert_routing_parity, assert_y_close, bf16_to_f64, check_ec_layer,
                     check_layer, oracle_routing, oracle_y, run_layer)
@@ -66,7 +67,11 @@ def test_priority_capacity_exact_ties(k, distinct):
     w = W("p_ties", T=640, d=128, E=8, k=k, M=128, offsets="normal", capacity_factor=0.5,
           flags=PRIO)
     inp = with_duplicate_rows(synth.make_inputs(w, "cuda"), distinct)
-    check_layer(inp)
+    g, ref = check_layer(inp)
+    # exact ties at the cut are broken identically on both sides (token order)
+    free = oracle.dispatch_priority(ref.routing.ids, ref.routing.p, w.E, ref.C)
+    np.testing.assert_array_equal(g.drop.astype(np.uint8), free.dropped)
+    assert free.dropped.any()
 
 
 def test_priority_capacity_full_switch():
@@ -108,7 +113,8 @@ def test_expert_choice_exact_ties(distinct):
     w = W("ec_ties", T=640, d=128, E=8, k=2, M=128, offsets="normal", flags=EC)
     inp = with_duplicate_rows(synth.make_inputs(w, "cuda"), distinct)
     g, ref = check_ec_layer(inp)
-    assert ref.forced == 0     # exact ties are decided identically on both sides
+    assert ref.forced > 0      # the cuts do fall inside groups of equal scores
+    assert ref.flipped == 0    # and both sides break those ties identically
 
 
 def test_expert_choice_empty_batch():
@@ -134,8 +140,8 @@ def test_expert_choice_full_size(name):
     sel = np.array(sorted(set(rng.choice(w.T, size=12, replace=False).tolist())
                           | {0, w.T - 1}), dtype=np.int32)
     g, ref = check_ec_layer(inp, sel)
-    print(f"{name} expert choice: r = {g.r}, near-cut picks forced {ref.forced}, tokens "
-          f"picked by none {int((np.bincount(g.row_token, minlength=w.T) == 0).sum())}")
+    print(f"{name} expert choice: r = {g.r}, near-cut picks {ref.forced} (flipped "
+          f"{ref.flipped}), tokens picked by none {int((np.bincount(g.row_token, minlength=w.T) == 0).sum())}")
 
 
 def test_deterministic_bitwise_select():

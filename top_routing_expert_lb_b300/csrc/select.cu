@@ -311,27 +311,25 @@ __global__ void __launch_bounds__(kEcCombineWarps * 32)
   const uint4* ys =
       y_shared ? reinterpret_cast<const uint4*>(y_shared + static_cast<int64_t>(t) * d) : nullptr;
   uint4* out = reinterpret_cast<uint4*>(y + static_cast<int64_t>(t) * d);
+  constexpr int kInFlight = 8;  // row loads issued before the first FMA
   for (int v = lane; v < nvec; v += 32) {
     float acc[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-    int j = 0;
-    for (; j + 4 <= n; j += 4) {
-      uint4 val[4];
+    uint4 sv = make_uint4(0u, 0u, 0u, 0u);
+    if (ys) sv = __ldg(ys + v);
+    for (int j0 = 0; j0 < n; j0 += kInFlight) {
+      uint4 val[kInFlight];
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
-        val[u] = __ldg(reinterpret_cast<const uint4*>(
-                           y_perm + static_cast<int64_t>(lrow[warp][j + u]) * d) + v);
+      for (int u = 0; u < kInFlight; ++u)
+        if (j0 + u < n)
+          val[u] = __ldg(reinterpret_cast<const uint4*>(
+                             y_perm + static_cast<int64_t>(lrow[warp][j0 + u]) * d) + v);
 #pragma unroll
-      for (int u = 0; u < 4; ++u) fma_bf16x8(acc, val[u], lgate[warp][j + u]);
+      for (int u = 0; u < kInFlight; ++u)  // experts in ascending order
+        if (j0 + u < n) fma_bf16x8(acc, val[u], lgate[warp][j0 + u]);
     }
-    for (; j < n; ++j)
-      fma_bf16x8(acc,
-                 __ldg(reinterpret_cast<const uint4*>(
-                           y_perm + static_cast<int64_t>(lrow[warp][j]) * d) + v),
-                 lgate[warp][j]);
     if (ys) {
-      const uint4 sv = __ldg(ys + v);
       const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&sv);
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
