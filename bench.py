@@ -170,16 +170,74 @@ CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.a
                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
 
+class NvmlPoller:
+    """SM clock and power every ~5 ms through NVML (read-only queries) on a
+    host thread, so that a timed region of a few hundred ms still gets tens of
+    samples; mark() brackets the region of interest."""
+
+    def __init__(self, device_index: int, period_s: float = 0.005):
+        import threading
+        self.samples = []  # (host time, sm MHz, power W)
+        self.window = None
+        self.period = period_s
+        self.stop = threading.Event()
+        self.thread = None
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self.nv = pynvml
+            self.h = pynvml.nvmlDeviceGetHandleByIndex(device_index)
+        except Exception:
+            self.nv = None
+
+    def _run(self):
+        nv, h = self.nv, self.h
+        while not self.stop.is_set():
+            try:
+                sm = nv.nvmlDeviceGetClockInfo(h, nv.NVML_CLOCK_SM)
+                pw = nv.nvmlDeviceGetPowerUsage(h) / 1000.0
+                self.samples.append((time.perf_counter(), float(sm), pw))
+            except Exception:
+                pass
+            time.sleep(self.period)
+
+    def start(self):
+        import threading
+        if self.nv is not None:
+            self.thread = threading.Thread(target=self._run, daemon=True)
+            self.thread.start()
+
+    def finish(self):
+        self.stop.set()
+        if self.thread is not None:
+            self.thread.join(timeout=2)
+
+    def in_window(self):
+        if not self.window:
+            return []
+        a, b = self.window
+        return [s for s in self.samples if a <= s[0] <= b]
+
+
 class ClockSampler:
     def __init__(self, device_index: int, enabled: bool = True):
         self.proc = None
         self.enabled = enabled
         self.idx = device_index
         self.path = None
+        self.poll = NvmlPoller(device_index) if enabled else None
+
+    def mark_start(self):
+        self.t0 = time.perf_counter()
+
+    def mark_end(self):
+        if self.poll is not None:
+            self.poll.window = (getattr(self, "t0", 0.0), time.perf_counter())
 
     def __enter__(self):
         if not self.enabled:
             return self
+        self.poll.start()
         out_dir = os.path.join(ROOT, "gpurun_out")
         os.makedirs(out_dir, exist_ok=True)
         self.path = os.path.join(out_dir, f"clocks_rank{self.idx}.csv")
@@ -195,6 +253,8 @@ class ClockSampler:
         return self
 
     def __exit__(self, *exc):
+        if self.poll is not None:
+            self.poll.finish()
         if self.proc is not None:
             time.sleep(0.15)
             self.proc.terminate()
@@ -228,10 +288,27 @@ class ClockSampler:
         reasons = sorted({names[i] for r in rows for i in range(4)
                           if r[5 + i].lower().startswith("active")})
         busy = [s for s in sm if s is not None]
-        return {"sm_mhz": statistics.median(busy) if busy else None,
+        win = self.window_summary()
+        region = win.get("sm_mhz_region_median")
+        return {"sm_mhz": region if region is not None else
+                (statistics.median(busy) if busy else None),
+                "sm_mhz_smi_median": statistics.median(busy) if busy else None,
                 "sm_max_mhz": max(mx) if mx else None,
                 "power_w_max": max(pw) if pw else None,
-                "samples": len(rows), "reasons": reasons}
+                "samples": len(rows), "reasons": reasons, **win}
+
+    def window_summary(self):
+        """Median SM clock and power over NVML samples taken inside the timed
+        region only (the nvidia-smi median above also counts idle samples)."""
+        if self.poll is None:
+            return {}
+        win = self.poll.in_window()
+        if not win:
+            return {"nvml_samples_in_region": 0}
+        return {"nvml_samples_in_region": len(win),
+                "sm_mhz_region_median": statistics.median(s[1] for s in win),
+                "sm_mhz_region_min": min(s[1] for s in win),
+                "power_w_region_median": statistics.median(s[2] for s in win)}
 
 
 # --------------------------------------------------------------------------- #
@@ -373,12 +450,14 @@ def run_ours(args, w):
     # inside the headline loop only the dominant kernel is bracketed by events
     moe.moe_profile_enable(True, kernels=["gemm_swiglu"])
     with ClockSampler(local, enabled=not args.no_clocks) as clk:
+        clk.mark_start()
         for i in range(args.steps):
             flush.zero_()                                  # evict L2 between steps
             starts[i].record(stream)
             layer.forward(inp.x)
             ends[i].record(stream)
         torch.cuda.synchronize(dev)
+        clk.mark_end()
     moe.moe_profile_enable(False)
     prof = moe.moe_profile_collect()
     launches = moe.moe_launch_count() - launches0
@@ -495,7 +574,10 @@ def run_ours(args, w):
                      "peak_source": f"bf16_tflops burst, {peak_src}",
                      "frac_of_sustained": ach / peaks["bf16_tflops_sustained"],
                      "algorithmic_flops_per_launch": flops[dom],
-                     "launch_ms": dom_ms, "launches_timed": len(dom_times)},
+                     "launch_ms": dom_ms, "launches_timed": len(dom_times),
+                     "launch_ms_first_last": [statistics.mean(dom_times[:5]),
+                                              statistics.mean(dom_times[-5:])]
+                     if len(dom_times) >= 5 else None},
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": launches,

@@ -113,6 +113,9 @@ def test_permute(T, E, k, c, d):
     ([0, 0, 0], 192, 128, 1, 77),                      # routed rows all empty, shared only
     ([400], 320, 384, 0, 0),                           # one group, d = 320 (N tile 64)
     ([255, 256, 257, 511, 1], 512, 256, 1, 300),       # 256-row tile edges, d = 512
+    # tails of 1..112 rows run transposed (weights as the MMA's M); 113..127 do not
+    ([16, 17, 111, 112, 113, 240, 33, 128], 256, 256, 1, 200),  # second projection N = 256
+    ([48, 200, 97, 1], 384, 128, 0, 0),                # second projection N = 128
 ])
 def test_grouped_ffn(rows, d, M, n_shared, T, tile, monkeypatch):
     # 128: single-CTA 128-row tiles; 256: CTA-pair 256-row tiles

@@ -70,6 +70,21 @@ struct TileInfo {
   int nk;       // K blocks
 };
 
+// Tail tiles.  The last m-tile of a group often holds few rows; a 128-row
+// MMA would spend most of its work on rows that are never stored.  When the
+// tile has r <= 112 valid rows it is computed transposed instead: D^T = B A^T
+// with the weight rows as the MMA's M (128 per half of the B tile) and the
+// r token rows, rounded up to 16, as its N.  The staged shared-memory tiles
+// are the same (both are K-major, 128-byte swizzled); only the descriptors
+// swap roles, and the epilogue reads TMEM lane = output column, TMEM column =
+// token row.  Returns that N, or 0 for a normal tile.
+template <int BN>
+__device__ __forceinline__ int swapped_n(int rows_left) {
+  if (BN < 128 || rows_left >= kBM) return 0;
+  const int n = (rows_left + 15) & ~15;
+  return n <= 112 ? n : 0;
+}
+
 template <typename Tail>
 __device__ __forceinline__ TileInfo decode_tile(const Tail* st, const GroupedGemmArgs& p, int G,
                                                 int tile, int bn, int bm = kBM) {
@@ -219,6 +234,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(a * BN);
+        const int nsw = swapped_n<BN>(ti.rows_left);
+        const uint32_t idesc_sw = idesc_bf16_f32(kBM, static_cast<uint32_t>(nsw > 0 ? nsw : 16));
         bool ok = true;
         for (int kb = 0; kb < ti.nk; ++kb) {
           if (!mbar_wait_bounded(&st->full[stage], phase, p.timeout_ns, p.status, abort_flag)) {
@@ -228,10 +245,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + stage * kStageBytes);
           const uint32_t sb = sa + kABytes;
+          if (nsw == 0) {
 #pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk) {
-            tc_mma_bf16(d_tmem, smem_desc_sw128(sa + kk * 32), smem_desc_sw128(sb + kk * 32),
-                        kIdesc, (kb | kk) != 0 ? 1u : 0u);
+            for (int kk = 0; kk < kBK / 16; ++kk) {
+              tc_mma_bf16(d_tmem, smem_desc_sw128(sa + kk * 32), smem_desc_sw128(sb + kk * 32),
+                          kIdesc, (kb | kk) != 0 ? 1u : 0u);
+            }
+          } else {
+            // transposed tail: half h of the B tile (weight rows 128h ..) as M,
+            // the first nsw rows of the A tile as N; result columns
+            // [h * nsw, (h + 1) * nsw) of the accumulator buffer
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk) {
+#pragma unroll
+              for (int h = 0; h < BN / 128; ++h)
+                tc_mma_bf16(d_tmem + static_cast<uint32_t>(h * nsw),
+                            smem_desc_sw128(sb + h * (128 * kBK * 2) + kk * 32),
+                            smem_desc_sw128(sa + kk * 32), idesc_sw, (kb | kk) != 0 ? 1u : 0u);
+            }
           }
           tc_commit(&st->empty[stage]);
           if (++stage == kStages) {
@@ -264,7 +295,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(ti.shared ? p.out_shared
                                                                       : p.out_routed);
       const int64_t ld = ti.shared ? p.ld_shared : p.ld_routed;
-      if constexpr (kSwiGLU) {
+      const int nsw = swapped_n<BN>(ti.rows_left);
+      if (nsw > 0) {
+        // transposed tail: this thread's TMEM lane is output column r_in_tile
+        // of each 128-wide half; TMEM column j of a half is token row j
+        __nv_bfloat16* base = out + static_cast<int64_t>(ti.a_row) * ld;
+        if constexpr (kSwiGLU) {
+          __nv_bfloat16* dst = base + static_cast<int64_t>(ti.n) * 128 + r_in_tile;
+#pragma unroll 1
+          for (int c = 0; c < nsw; c += 32) {
+            float g[32], u[32];
+            tmem_ld32(taddr + c, g);
+            tmem_ld32(taddr + nsw + c, u);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (c + j < ti.rows_left)
+                dst[static_cast<int64_t>(c + j) * ld] = __float2bfloat16_rn(silu_f32(g[j]) * u[j]);
+          }
+        } else {
+#pragma unroll 1
+          for (int h = 0; h < BN / 128; ++h) {
+            __nv_bfloat16* dst = base + static_cast<int64_t>(ti.n) * BN + h * 128 + r_in_tile;
+#pragma unroll 1
+            for (int c = 0; c < nsw; c += 32) {
+              float v[32];
+              tmem_ld32(taddr + h * nsw + c, v);
+              tmem_ld_wait();
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (c + j < ti.rows_left)
+                  dst[static_cast<int64_t>(c + j) * ld] = __float2bfloat16_rn(v[j]);
+            }
+          }
+        }
+      } else if constexpr (kSwiGLU) {
         __nv_bfloat16* dst = out + row * ld + static_cast<int64_t>(ti.n) * 128;
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
