@@ -63,6 +63,27 @@ def test_layer_parity_paired_tiles(name, monkeypatch):
         assert ref.disp.dropped.any(), "capacity case should drop pairs"
 
 
+@pytest.mark.parametrize("name", ["ragged_shared", "capacity_k4", "fine_bias_shared",
+                                  "top1_capacity", "wide_E160", "single_token"])
+def test_layer_parity_fused_gather(name, monkeypatch):
+    """The same cases with GEMM-1 gathering the token rows itself (TMA 4-row
+    gathers by row_token) instead of reading the scatter's x_perm."""
+    monkeypatch.setenv("MOE_FUSED_GATHER", "1")
+    check_layer(synth.make_inputs(CASES[name], "cuda"))
+
+
+def test_fused_and_materialised_rows_agree_bitwise(monkeypatch):
+    """Gathering the rows inside GEMM-1 stages the same bytes as the scatter's
+    copy, so the two paths give bit-identical outputs."""
+    w = CASES["fine_bias_shared"]
+    inp = synth.make_inputs(w, "cuda")
+    outs = []
+    for flag in ("1", "0"):
+        monkeypatch.setenv("MOE_FUSED_GATHER", flag)
+        outs.append(run_layer(inp).y)
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+
+
 def test_one_expert_takes_every_row():
     w = W("hot", T=333, d=128, E=8, k=1, M=128, n_shared=0)
     inp = synth.make_inputs(w, "cuda")

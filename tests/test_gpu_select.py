@@ -144,6 +144,18 @@ def test_expert_choice_full_size(name):
           f"{ref.flipped}), tokens picked by none {int((np.bincount(g.row_token, minlength=w.T) == 0).sum())}")
 
 
+@pytest.mark.parametrize("w", [PRIO_CASES[0], PRIO_CASES[2], EC_CASES[1], EC_CASES[2]],
+                         ids=lambda w: w.name)
+def test_select_paths_with_fused_gather(w, monkeypatch):
+    """Priority capacity and expert choice with GEMM-1 gathering token rows by
+    row_token instead of the gather kernel's x_perm."""
+    monkeypatch.setenv("MOE_FUSED_GATHER", "1")
+    if w.flags & EC:
+        check_ec_layer(synth.make_inputs(w, "cuda"))
+    else:
+        check_layer(synth.make_inputs(w, "cuda"))
+
+
 def test_deterministic_bitwise_select():
     for w in (PRIO_CASES[0], EC_CASES[0]):
         inp = synth.make_inputs(w, "cuda")

@@ -337,7 +337,7 @@ int do_priority_dispatch(const moe_shape_t* s, const uint16_t* x, const int32_t*
   pa.drop_mask = drop_mask;
   pa.row_token = row_token;
   rc = cuda_rc(tracked(MOE_KERNEL_SELECT, st, [&] { return launch_priority_select(pa, st); }));
-  if (rc != MOE_OK) return rc;
+  if (rc != MOE_OK || x_perm == nullptr) return rc;  // no x_perm: GEMM-1 gathers the rows
   return cuda_rc(tracked(MOE_KERNEL_GATHER, st, [&] {
     return launch_gather_rows(x, row_token, offsets, s->E, s->d, L.rmax, x_perm,
                               sm_count_cached(), st);
@@ -367,10 +367,31 @@ int do_ec_route(const moe_shape_t* s, const uint16_t* x, const uint16_t* wr, con
   return cuda_rc(tracked(MOE_KERNEL_SELECT, st, [&] { return launch_ec_select(ea, st); }));
 }
 
+// 128-row tiles on single CTAs by default (measured faster on every workload
+// so far); 256-row tiles on CTA pairs with MOE_GEMM_TILE=256.
+bool gemm_paired() {
+  const char* env = std::getenv("MOE_GEMM_TILE");
+  return env != nullptr && std::strcmp(env, "256") == 0;
+}
+
+// With MOE_FUSED_GATHER=1 the layer feeds GEMM-1 straight from the token
+// rows (TMA 4-row gathers by row_token, no x_perm); by default the scatter
+// materialises x_perm and GEMM-1 reads it with one box load per k-block.  The
+// gather issues 32 TMA instructions per k-block instead of one and measured
+// about 3.5x slower in GEMM-1, so it stays opt-in.  The paired GEMM always
+// reads x_perm.
+bool fused_gather() {
+  const char* env = std::getenv("MOE_FUSED_GATHER");
+  if (env == nullptr || std::strcmp(env, "1") != 0) return false;
+  return !gemm_paired();
+}
+
+// x_perm: routed rows, or null with gather_rows (token row of every routed
+// row, read from x by the GEMM's producer).
 int do_ffn(const moe_shape_t* s, const uint16_t* x_perm, const int32_t* offsets,
            const uint16_t* w13, const uint16_t* w2, uint16_t* y_perm, const uint16_t* x,
            const uint16_t* w13s, const uint16_t* w2s, uint16_t* y_s, void* ws, const Layout& L,
-           cudaStream_t st) {
+           cudaStream_t st, const int32_t* gather_rows = nullptr) {
   const int64_t T = s->T, d = s->d, M = s->M, E = s->E;
   const int64_t Ms = static_cast<int64_t>(s->n_shared) * M;
   const bool routed = L.rmax > 0;
@@ -380,19 +401,18 @@ int do_ffn(const moe_shape_t* s, const uint16_t* x_perm, const int32_t* offsets,
   uint16_t* h_s = at<uint16_t>(ws, L.h_s);
   const int bn2 = (d % 256 == 0) ? 256 : (d % 128 == 0 ? 128 : 64);
   const int nsm = sm_count_cached();
-  // 128-row tiles on single CTAs by default (measured faster on every
-  // workload so far); 256-row tiles on CTA pairs with MOE_GEMM_TILE=256.
-  bool paired = false;
-  if (const char* env = std::getenv("MOE_GEMM_TILE")) {
-    if (std::strcmp(env, "128") == 0) paired = false;
-    if (std::strcmp(env, "256") == 0) paired = true;
-  }
+  const bool paired = gemm_paired();
+  if (paired && gather_rows != nullptr) return MOE_ERR_INVALID_ARG;  // needs x_perm
   const uint32_t bbox = paired ? 128u : 256u;
 
   // projection 1: [x_perm | x] -> h = SiLU(gate) * up
   CUtensorMap a0, a1, b0, b1;
   if (routed) {
-    if (!make_tmap_bf16(&a0, x_perm, L.rmax, d, 128)) return MOE_ERR_CUDA;
+    if (gather_rows != nullptr) {
+      if (!make_tmap_bf16(&a0, x, T, d, 1)) return MOE_ERR_CUDA;  // one-row box: gather
+    } else if (!make_tmap_bf16(&a0, x_perm, L.rmax, d, 128)) {
+      return MOE_ERR_CUDA;
+    }
     if (!make_tmap_bf16(&b0, w13, E * 2 * M, d, bbox)) return MOE_ERR_CUDA;
   }
   if (shared) {
@@ -415,6 +435,7 @@ int do_ffn(const moe_shape_t* s, const uint16_t* x_perm, const int32_t* offsets,
   g1.ld_shared = Ms;
   g1.status = at<int>(ws, L.status);
   g1.timeout_ns = g_timeout_ns;
+  g1.gather_rows = routed ? gather_rows : nullptr;
   int rc = tracked(MOE_KERNEL_GEMM_SWIGLU, st,
                    [&] { return launch_grouped_gemm(a0, a1, b0, b1, g1, true, 256, paired, nsm, st); });
   if (rc != 0) return cuda_rc(rc);
@@ -433,6 +454,7 @@ int do_ffn(const moe_shape_t* s, const uint16_t* x_perm, const int32_t* offsets,
   if (!routed) { a0 = a1; b0 = b1; }
   if (!shared) { a1 = a0; b1 = b0; }
   GroupedGemmArgs g2 = g1;
+  g2.gather_rows = nullptr;
   g2.n_cols_routed = static_cast<int32_t>(d);
   g2.n_cols_shared = static_cast<int32_t>(d);
   g2.k_routed = static_cast<int32_t>(M);
@@ -653,16 +675,19 @@ int moe_layer_forward(const moe_shape_t* s, const uint16_t* x, const uint16_t* w
   uint16_t* x_perm = at<uint16_t>(ws, L.x_perm);
   uint16_t* y_perm = at<uint16_t>(ws, L.y_perm);
   uint16_t* y_s = s->n_shared > 0 ? at<uint16_t>(ws, L.y_s) : nullptr;
+  const bool fused = fused_gather();
+  int32_t* row_token = at<int32_t>(ws, L.row_token);
   if (s->k > 0) {
+    uint16_t* xp = fused ? nullptr : x_perm;
     if (prio)
-      rc = do_priority_dispatch(s, x, ids, L, ws, offsets, slot_row,
-                                at<int32_t>(ws, L.row_token), drop_mask, x_perm, st);
+      rc = do_priority_dispatch(s, x, ids, L, ws, offsets, slot_row, row_token, drop_mask, xp,
+                                st);
     else
-      rc = do_scatter(s, x, ids, L, ws, offsets, slot_row, at<int32_t>(ws, L.row_token),
-                      drop_mask, x_perm, st);
+      rc = do_scatter(s, x, ids, L, ws, offsets, slot_row, row_token, drop_mask, xp, st);
     if (rc != MOE_OK) return rc;
   }
-  rc = do_ffn(s, x_perm, offsets, w13, w2, y_perm, x, w13_shared, w2_shared, y_s, ws, L, st);
+  rc = do_ffn(s, fused ? nullptr : x_perm, offsets, w13, w2, y_perm, x, w13_shared, w2_shared,
+              y_s, ws, L, st, fused ? row_token : nullptr);
   if (rc != MOE_OK) return rc;
   return cuda_rc(tracked(MOE_KERNEL_COMBINE, st, [&] {
     return launch_combine(s->T, s->d, s->k, y_perm, slot_row, gates, y_s, y, st);
@@ -764,14 +789,16 @@ int moe_ec_layer_forward(const moe_shape_t* s, const uint16_t* x, const uint16_t
   uint16_t* x_perm = at<uint16_t>(ws, L.x_perm);
   uint16_t* y_perm = at<uint16_t>(ws, L.y_perm);
   uint16_t* y_s = s->n_shared > 0 ? at<uint16_t>(ws, L.y_s) : nullptr;
-  if (L.rmax > 0) {
+  const bool fused = fused_gather();
+  if (L.rmax > 0 && !fused) {
     rc = cuda_rc(tracked(MOE_KERNEL_GATHER, st, [&] {
       return launch_gather_rows(x, row_token, offsets, s->E, s->d, L.rmax, x_perm,
                                 sm_count_cached(), st);
     }));
     if (rc != MOE_OK) return rc;
   }
-  rc = do_ffn(s, x_perm, offsets, w13, w2, y_perm, x, w13_shared, w2_shared, y_s, ws, L, st);
+  rc = do_ffn(s, fused ? nullptr : x_perm, offsets, w13, w2, y_perm, x, w13_shared, w2_shared,
+              y_s, ws, L, st, fused ? row_token : nullptr);
   if (rc != MOE_OK) return rc;
   return cuda_rc(tracked(MOE_KERNEL_COMBINE, st, [&] {
     return launch_ec_combine(s->T, s->d, s->E, at<int32_t>(ws, L.sel_t), row_gate, y_perm, y_s,

@@ -183,42 +183,70 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      uint32_t uses[kStages];
+    // The whole warp runs the loop (control flow is uniform: lane 0 waits and
+    // broadcasts); lane 0 issues the box loads.  With gathered A rows every
+    // lane issues one 4-row gather per k-block: lane l loads tile rows
+    // 4l .. 4l+3, whose token rows it looked up once per tile.
+    const bool gather = p.gather_rows != nullptr;
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t uses[kStages];
 #pragma unroll
-      for (int s = 0; s < kStages; ++s) uses[s] = 0;
-      for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x) {
-        const TileInfo ti = decode_tile(st, p, G, tile, BN);
-        const CUtensorMap* am = ti.shared ? &tmA1 : &tmA0;
-        const CUtensorMap* bm = ti.shared ? &tmB1 : &tmB0;
-        bool ok = true;
-        for (int kb = 0; kb < ti.nk; ++kb) {
-          if (!mbar_wait_bounded(&st->empty[stage], phase ^ 1u, p.timeout_ns, p.status,
-                                 abort_flag)) {
-            ok = false;
-            break;
-          }
-          uint8_t* sa = smem + stage * kStageBytes;
-          mbar_arrive_expect_tx(&st->full[stage], kStageBytes);
-          tma_load_2d(sa, am, &st->full[stage], kb * kBK, ti.a_row);
-          tma_load_2d(sa + kABytes, bm, &st->full[stage], kb * kBK, ti.b_row);
-          uses[stage] += 1;
-          if (++stage == kStages) {
-            stage = 0;
-            phase ^= 1u;
-          }
+    for (int s = 0; s < kStages; ++s) uses[s] = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      int stop = (lane == 0) ? *abort_flag : 0;
+      if (__shfl_sync(0xffffffffu, stop, 0)) break;
+      const TileInfo ti = decode_tile(st, p, G, tile, BN);
+      const CUtensorMap* am = ti.shared ? &tmA1 : &tmA0;
+      const CUtensorMap* bm = ti.shared ? &tmB1 : &tmB0;
+      const bool gathered = gather && !ti.shared;
+      int rr[4] = {0, 0, 0, 0};
+      if (gathered) {
+        // rows past the tile's valid rows repeat its last valid row (their
+        // results are never stored)
+        const int nvalid = ti.rows_left < kBM ? ti.rows_left : kBM;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int i = 4 * lane + j;
+          rr[j] = __ldg(p.gather_rows + ti.a_row + (i < nvalid ? i : nvalid - 1));
         }
-        if (!ok) break;
       }
-      // Drain: the last copy issued into each stage must have landed before
-      // the CTA may exit.
+      bool ok = true;
+      for (int kb = 0; kb < ti.nk; ++kb) {
+        int waited = 1;
+        if (lane == 0) {
+          waited = mbar_wait_bounded(&st->empty[stage], phase ^ 1u, p.timeout_ns, p.status,
+                                     abort_flag) ? 1 : 0;
+          if (waited) mbar_arrive_expect_tx(&st->full[stage], kStageBytes);
+        }
+        if (!__shfl_sync(0xffffffffu, waited, 0)) {
+          ok = false;
+          break;
+        }
+        uint8_t* sa = smem + stage * kStageBytes;
+        if (gathered)
+          tma_gather4(sa + lane * 4 * (kBK * 2), am, &st->full[stage], kb * kBK, rr[0], rr[1],
+                      rr[2], rr[3]);
+        else if (lane == 0)
+          tma_load_2d(sa, am, &st->full[stage], kb * kBK, ti.a_row);
+        if (lane == 0) tma_load_2d(sa + kABytes, bm, &st->full[stage], kb * kBK, ti.b_row);
+        uses[stage] += 1;
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+    }
+    // Drain: the last copy issued into each stage must have landed before
+    // the CTA may exit.
+    if (lane == 0) {
 #pragma unroll
       for (int s = 0; s < kStages; ++s)
         if (uses[s] > 0)
           mbar_wait_bounded(&st->full[s], (uses[s] - 1u) & 1u, p.timeout_ns, p.status, nullptr);
     }
+    __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {

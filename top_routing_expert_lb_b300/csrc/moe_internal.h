@@ -31,6 +31,10 @@ struct GroupedGemmArgs {
   int64_t ld_shared;
   int* status;             // device status word
   uint64_t timeout_ns;
+  // When set (single-CTA kernel only), routed A rows are gathered: row r of
+  // the routed activations is row gather_rows[r] of the tensor behind A0,
+  // whose map then has a 64 x 1 box.
+  const int32_t* gather_rows = nullptr;
 };
 
 // A0/A1: activations [rows][K] (routed / shared), B0/B1: weights [rows][K].

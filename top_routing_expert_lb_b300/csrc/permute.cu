@@ -257,6 +257,7 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_kernel(const ScatterA
       if (row >= 0) a.row_token[row] = t0 + q / k;
     }
   }
+  if (a.x_perm == nullptr) return;  // rows only: the GEMM gathers the token rows itself
   // gather this CTA's share of tokens: warp per token, the row is read once
   const int G = gridDim.y;
   const int per = (ntok + G - 1) / G;
@@ -310,7 +311,7 @@ int launch_scatter(const ScatterArgs& args, cudaStream_t stream) {
   // enough CTAs to keep every SM streaming rows (about 4 per SM)
   int G = (4 * args.num_sms + ntiles - 1) / ntiles;
   G = G < 1 ? 1 : (G > 16 ? 16 : G);
-  if (args.stage_q) G = 1;  // staging writes indices only
+  if (args.stage_q || args.x_perm == nullptr) G = 1;  // indices only, no row copies
   scatter_kernel<<<dim3(ntiles, G), kScatterThreads, 0, stream>>>(args);
   return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }

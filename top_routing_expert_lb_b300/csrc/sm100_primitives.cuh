@@ -115,6 +115,22 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, uint64_
       : "memory");
 }
 
+// Row gather: rows r0..r3 of a 2-D tensor map whose box is 64 columns x 1 row,
+// columns [c0, c0 + 64), written to four consecutive 128-byte rows at dst.
+// With 128-byte swizzling the placement follows the shared-memory address, so
+// 32 such loads at dst, dst + 512, ... lay out the same tile as one 128-row
+// box load.
+__device__ __forceinline__ void tma_gather4(void* dst, const void* tmap, uint64_t* bar,
+                                            int32_t c0, int32_t r0, int32_t r1, int32_t r2,
+                                            int32_t r3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(smem_u32(bar)), "r"(c0), "r"(r0), "r"(r1),
+      "r"(r2), "r"(r3)
+      : "memory");
+}
+
 // Same, with an L2 cache-policy hint (createpolicy result).
 __device__ __forceinline__ void tma_load_2d_hint(void* dst, const void* tmap, uint64_t* bar,
                                                  int32_t c0, int32_t c1, uint64_t policy) {
