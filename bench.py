@@ -405,6 +405,28 @@ def run_reference(args, w):
 
 
 # --------------------------------------------------------------------------- #
+# replicas across ranks                                                        #
+# --------------------------------------------------------------------------- #
+def max_over_ranks(value: float, device) -> float:
+    """The slowest rank's time: every rank runs its own replica of the
+    workload (there is no data-path exchange), so the job's step time is the
+    maximum over ranks.  A no-op without an initialised process group."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(world: int, tokens_per_rank: int, ms: float) -> float:
+    """Whole-job throughput: every rank processes its own batch of tokens in
+    the (max-over-ranks) step time."""
+    return world * tokens_per_rank / (ms * 1e-3)
+
+
+# --------------------------------------------------------------------------- #
 # our arm                                                                      #
 # --------------------------------------------------------------------------- #
 def run_ours(args, w):
@@ -466,11 +488,7 @@ def run_ours(args, w):
     if moe.moe_check_status(layer.ws) != 0:
         raise RuntimeError("device wait timed out during the timed steps")
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    ms = statistics.mean(step_ms)
-    if world > 1:
-        t = torch.tensor([ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(statistics.mean(step_ms), dev)
 
     dom_times = [t for name, t in prof if name == "gemm_swiglu"]
 
@@ -530,12 +548,8 @@ def run_ours(args, w):
             e2e_step()
             b.record(stream)
         torch.cuda.synchronize(dev)
-        e2e_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
-        if world > 1:
-            t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
-        e2e = {"value": world * w.T / (e2e_ms * 1e-3), "unit": "tokens/s",
+        e2e_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in ev), dev)
+        e2e = {"value": job_tokens_per_s(world, w.T, e2e_ms), "unit": "tokens/s",
                "ms_per_step": e2e_ms, "h2d_bytes_per_step": w.T * w.d * 2,
                "d2h_bytes_per_step": w.T * w.d * 2 + 8,
                "path": "moe_layer_forward_host (pinned host x in, y and losses out)"}
@@ -547,7 +561,7 @@ def run_ours(args, w):
     if rank != 0:
         return 0
     line = {
-        "metric": METRIC, "value": world * w.T / (ms * 1e-3), "unit": "tokens/s",
+        "metric": METRIC, "value": job_tokens_per_s(world, w.T, ms), "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic: seeded N(0,1) tokens, random-init N(0,0.02) weights",
