@@ -182,23 +182,33 @@ class NvmlPoller:
         self.period = period_s
         self.stop = threading.Event()
         self.thread = None
+        self.err = None
+        self.nv = None
         try:
-            import pynvml
-            pynvml.nvmlInit()
-            self.nv = pynvml
-            self.h = pynvml.nvmlDeviceGetHandleByIndex(device_index)
-        except Exception:
-            self.nv = None
+            # the driver's NVML library through ctypes (read-only queries)
+            import ctypes
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                raise RuntimeError("nvmlInit_v2 failed")
+            h = ctypes.c_void_p()
+            if lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(device_index),
+                                                 ctypes.byref(h)) != 0:
+                raise RuntimeError("nvmlDeviceGetHandleByIndex_v2 failed")
+            self.nv, self.h = lib, h
+        except Exception as e:  # reported in the summary
+            self.err = f"{type(e).__name__}: {e}"
 
     def _run(self):
+        import ctypes
         nv, h = self.nv, self.h
+        clk, mw = ctypes.c_uint(), ctypes.c_uint()
+        NVML_CLOCK_SM = 1
         while not self.stop.is_set():
-            try:
-                sm = nv.nvmlDeviceGetClockInfo(h, nv.NVML_CLOCK_SM)
-                pw = nv.nvmlDeviceGetPowerUsage(h) / 1000.0
-                self.samples.append((time.perf_counter(), float(sm), pw))
-            except Exception:
-                pass
+            if (nv.nvmlDeviceGetClockInfo(h, NVML_CLOCK_SM, ctypes.byref(clk)) == 0 and
+                    nv.nvmlDeviceGetPowerUsage(h, ctypes.byref(mw)) == 0):
+                self.samples.append((time.perf_counter(), float(clk.value), mw.value / 1000.0))
+            else:
+                self.err = "NVML query failed"
             time.sleep(self.period)
 
     def start(self):
@@ -304,7 +314,8 @@ class ClockSampler:
             return {}
         win = self.poll.in_window()
         if not win:
-            return {"nvml_samples_in_region": 0}
+            return {"nvml_samples_in_region": 0, "nvml_samples": len(self.poll.samples),
+                    "nvml_error": self.poll.err}
         return {"nvml_samples_in_region": len(win),
                 "sm_mhz_region_median": statistics.median(s[1] for s in win),
                 "sm_mhz_region_min": min(s[1] for s in win),
