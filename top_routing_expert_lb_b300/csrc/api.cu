@@ -444,7 +444,7 @@ int do_ffn(const moe_shape_t* s, const uint16_t* x_perm, const int32_t* offsets,
   const bool paired2 = paired && bn2 == 256;
   // 256-column tiles of the single-CTA kernel load B as two 128-row boxes (so
   // that its last round can run 128-column halves)
-  const uint32_t bbox2 = (paired2 || bn2 == 256) ? 128u : static_cast<uint32_t>(bn2);
+  const uint32_t bbox2 = paired2 ? 128u : static_cast<uint32_t>(bn2);
   if (routed) {
     if (!make_tmap_bf16(&a0, h, L.rmax, M, 128)) return MOE_ERR_CUDA;
     if (!make_tmap_bf16(&b0, w2, E * d, M, bbox2)) return MOE_ERR_CUDA;
@@ -457,8 +457,6 @@ int do_ffn(const moe_shape_t* s, const uint16_t* x_perm, const int32_t* offsets,
   if (!shared) { a1 = a0; b1 = b0; }
   GroupedGemmArgs g2 = g1;
   g2.gather_rows = nullptr;
-  if (const char* env = std::getenv("MOE_GEMM_SPLIT_LAST"))  // 0: whole tiles in the last round
-    g2.split_last = std::strcmp(env, "0") != 0;
   g2.n_cols_routed = static_cast<int32_t>(d);
   g2.n_cols_shared = static_cast<int32_t>(d);
   g2.k_routed = static_cast<int32_t>(M);

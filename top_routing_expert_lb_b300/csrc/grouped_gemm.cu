@@ -49,8 +49,6 @@ struct GemmSmemTail {
   uint64_t fin;
   uint32_t tmem_base;
   int abort_flag;
-  int split_from;  // tiles from here on are halves of the last round's tiles
-  int total;       // tile count after the split
   int prefix[kMaxGroups + 1];
   int row0[kMaxGroups];
   int rows[kMaxGroups];
@@ -70,8 +68,6 @@ struct TileInfo {
   int b_row;    // first B row of the tile
   int n;        // n-tile index within the group
   int nk;       // K blocks
-  int bn_eff;   // columns of this tile (BN, or BN / 2 for a split tile)
-  int col_off;  // first column of this tile inside n-tile n
 };
 
 // Tail tiles.  The last m-tile of a group often holds few rows; a 128-row
@@ -112,26 +108,6 @@ __device__ __forceinline__ TileInfo decode_tile(const Tail* st, const GroupedGem
   const int e = lo - has_shared;
   ti.b_row = (ti.shared ? 0 : e * ncols) + ti.n * bn;
   ti.nk = (ti.shared ? p.k_shared : p.k_routed) / kBK;
-  ti.bn_eff = bn;
-  ti.col_off = 0;
-  return ti;
-}
-
-// Last-round split (single-CTA kernel, second projection with BN = 256).
-// Tiles of one projection all take about the same time, so when the tile
-// count is not a multiple of the grid the last round leaves most SMs idle
-// for a whole tile; with K = M = 14336 that is ~0.1 ms.  When the last round
-// holds at most half a grid of tiles, each of its tiles is computed as two
-// 128-column halves on two CTAs, which halves the length of that round.
-template <int BN>
-__device__ __forceinline__ TileInfo decode_split_tile(const GemmSmemTail* st,
-                                                      const GroupedGemmArgs& p, int G, int tile) {
-  if (tile < st->split_from) return decode_tile(st, p, G, tile, BN);
-  const int h = tile - st->split_from;
-  TileInfo ti = decode_tile(st, p, G, st->split_from + (h >> 1), BN);
-  ti.bn_eff = BN / 2;
-  ti.col_off = (h & 1) * (BN / 2);
-  ti.b_row += ti.col_off;
   return ti;
 }
 
@@ -146,10 +122,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kBBytes = BN * kBK * 2;
   constexpr int kStageBytes = kABytes + kBBytes;
   constexpr uint32_t kTmemCols = 2 * BN;
-  // the down projection's BN = 256 tiles may be split in the last round;
-  // its B tensor map then has a 128-row box (two loads per full tile)
-  constexpr bool kSplitLast = !kSwiGLU && BN == 256;
-  constexpr int kBBox = kSplitLast ? BN / 2 : BN;
+  constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, BN);
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
@@ -193,16 +166,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       acc += ((rows + kBM - 1) / kBM) * (ncols / BN);
       st->prefix[g + 1] = acc;
     }
-    int split_from = acc, total = acc;
-    if (kSplitLast && p.split_last) {
-      const int last = acc % static_cast<int>(gridDim.x);
-      if (last > 0 && 2 * last <= static_cast<int>(gridDim.x)) {
-        split_from = acc - last;
-        total = acc + last;
-      }
-    }
-    st->split_from = split_from;
-    st->total = total;
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
@@ -216,79 +179,118 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = st->tmem_base;
-  const int total = st->total;
+  const int total = st->prefix[G];
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    // The whole warp runs the loop (control flow is uniform: lane 0 waits and
-    // broadcasts); lane 0 issues the box loads.  With gathered A rows every
-    // lane issues one 4-row gather per k-block: lane l loads tile rows
-    // 4l .. 4l+3, whose token rows it looked up once per tile.
-    const bool gather = p.gather_rows != nullptr;
-    int stage = 0;
-    uint32_t phase = 0;
-    uint32_t uses[kStages];
+    if (p.gather_rows == nullptr) {
+      // box loads: lane 0 alone runs the ring
+      if (lane == 0) {
+        int stage = 0;
+        uint32_t phase = 0;
+        uint32_t uses[kStages];
 #pragma unroll
-    for (int s = 0; s < kStages; ++s) uses[s] = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-      int stop = (lane == 0) ? *abort_flag : 0;
-      if (__shfl_sync(0xffffffffu, stop, 0)) break;
-      const TileInfo ti = decode_split_tile<BN>(st, p, G, tile);
-      const CUtensorMap* am = ti.shared ? &tmA1 : &tmA0;
-      const CUtensorMap* bm = ti.shared ? &tmB1 : &tmB0;
-      const bool gathered = gather && !ti.shared;
-      const uint32_t stage_bytes = static_cast<uint32_t>(kABytes + ti.bn_eff * kBK * 2);
-      int rr[4] = {0, 0, 0, 0};
-      if (gathered) {
-        // rows past the tile's valid rows repeat its last valid row (their
-        // results are never stored)
-        const int nvalid = ti.rows_left < kBM ? ti.rows_left : kBM;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int i = 4 * lane + j;
-          rr[j] = __ldg(p.gather_rows + ti.a_row + (i < nvalid ? i : nvalid - 1));
+        for (int s = 0; s < kStages; ++s) uses[s] = 0;
+        for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x) {
+          const TileInfo ti = decode_tile(st, p, G, tile, BN);
+          const CUtensorMap* am = ti.shared ? &tmA1 : &tmA0;
+          const CUtensorMap* bm = ti.shared ? &tmB1 : &tmB0;
+          bool ok = true;
+          for (int kb = 0; kb < ti.nk; ++kb) {
+            if (!mbar_wait_bounded(&st->empty[stage], phase ^ 1u, p.timeout_ns, p.status,
+                                   abort_flag)) {
+              ok = false;
+              break;
+            }
+            uint8_t* sa = smem + stage * kStageBytes;
+            mbar_arrive_expect_tx(&st->full[stage], kStageBytes);
+            tma_load_2d(sa, am, &st->full[stage], kb * kBK, ti.a_row);
+            tma_load_2d(sa + kABytes, bm, &st->full[stage], kb * kBK, ti.b_row);
+            uses[stage] += 1;
+            if (++stage == kStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+          if (!ok) break;
         }
+        // Drain: the last copy issued into each stage must have landed before
+        // the CTA may exit.
+#pragma unroll
+        for (int s = 0; s < kStages; ++s)
+          if (uses[s] > 0)
+            mbar_wait_bounded(&st->full[s], (uses[s] - 1u) & 1u, p.timeout_ns, p.status,
+                              nullptr);
       }
-      bool ok = true;
-      for (int kb = 0; kb < ti.nk; ++kb) {
-        int waited = 1;
-        if (lane == 0) {
-          waited = mbar_wait_bounded(&st->empty[stage], phase ^ 1u, p.timeout_ns, p.status,
-                                     abort_flag) ? 1 : 0;
-          if (waited) mbar_arrive_expect_tx(&st->full[stage], stage_bytes);
-        }
-        if (!__shfl_sync(0xffffffffu, waited, 0)) {
-          ok = false;
-          break;
-        }
-        uint8_t* sa = smem + stage * kStageBytes;
-        if (gathered)
-          tma_gather4(sa + lane * 4 * (kBK * 2), am, &st->full[stage], kb * kBK, rr[0], rr[1],
-                      rr[2], rr[3]);
-        else if (lane == 0)
-          tma_load_2d(sa, am, &st->full[stage], kb * kBK, ti.a_row);
-        if (lane == 0) {
-          for (int b0 = 0; b0 < ti.bn_eff; b0 += kBBox)
-            tma_load_2d(sa + kABytes + b0 * (kBK * 2), bm, &st->full[stage], kb * kBK,
-                        ti.b_row + b0);
-        }
-        uses[stage] += 1;
-        if (++stage == kStages) {
-          stage = 0;
-          phase ^= 1u;
-        }
-      }
-      if (!ok) break;
-    }
-    // Drain: the last copy issued into each stage must have landed before
-    // the CTA may exit.
-    if (lane == 0) {
+      __syncwarp();
+    } else {
+      // Gathered A rows: the whole warp runs the loop (control flow is uniform:
+      // lane 0 waits and broadcasts) and every lane issues one 4-row gather per
+      // k-block: lane l loads tile rows 4l .. 4l+3, whose token rows it looked
+      // up once per tile.  Lane 0 issues the box loads (B, and A of the
+      // shared group).
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t uses[kStages];
 #pragma unroll
-      for (int s = 0; s < kStages; ++s)
-        if (uses[s] > 0)
-          mbar_wait_bounded(&st->full[s], (uses[s] - 1u) & 1u, p.timeout_ns, p.status, nullptr);
+      for (int s = 0; s < kStages; ++s) uses[s] = 0;
+      for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+        int stop = (lane == 0) ? *abort_flag : 0;
+        if (__shfl_sync(0xffffffffu, stop, 0)) break;
+        const TileInfo ti = decode_tile(st, p, G, tile, BN);
+        const CUtensorMap* am = ti.shared ? &tmA1 : &tmA0;
+        const CUtensorMap* bm = ti.shared ? &tmB1 : &tmB0;
+        const bool gathered = !ti.shared;
+        int rr[4] = {0, 0, 0, 0};
+        if (gathered) {
+          // rows past the tile's valid rows repeat its last valid row (their
+          // results are never stored)
+          const int nvalid = ti.rows_left < kBM ? ti.rows_left : kBM;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int i = 4 * lane + j;
+            rr[j] = __ldg(p.gather_rows + ti.a_row + (i < nvalid ? i : nvalid - 1));
+          }
+        }
+        bool ok = true;
+        for (int kb = 0; kb < ti.nk; ++kb) {
+          int waited = 1;
+          if (lane == 0) {
+            waited = mbar_wait_bounded(&st->empty[stage], phase ^ 1u, p.timeout_ns, p.status,
+                                       abort_flag) ? 1 : 0;
+            if (waited) mbar_arrive_expect_tx(&st->full[stage], kStageBytes);
+          }
+          if (!__shfl_sync(0xffffffffu, waited, 0)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sa = smem + stage * kStageBytes;
+          if (gathered)
+            tma_gather4(sa + lane * 4 * (kBK * 2), am, &st->full[stage], kb * kBK, rr[0], rr[1],
+                        rr[2], rr[3]);
+          else if (lane == 0)
+            tma_load_2d(sa, am, &st->full[stage], kb * kBK, ti.a_row);
+          if (lane == 0) {
+            tma_load_2d(sa + kABytes, bm, &st->full[stage], kb * kBK, ti.b_row);
+          }
+          uses[stage] += 1;
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+      }
+      // Drain: the last copy issued into each stage must have landed before
+      // the CTA may exit.
+      if (lane == 0) {
+#pragma unroll
+        for (int s = 0; s < kStages; ++s)
+          if (uses[s] > 0)
+            mbar_wait_bounded(&st->full[s], (uses[s] - 1u) & 1u, p.timeout_ns, p.status, nullptr);
+      }
+      __syncwarp();
     }
-    __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
@@ -296,8 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       int local = 0;
       for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x, ++local) {
-        const TileInfo ti = decode_split_tile<BN>(st, p, G, tile);
-        const uint32_t idesc_n = idesc_bf16_f32(kBM, static_cast<uint32_t>(ti.bn_eff));
+        const TileInfo ti = decode_tile(st, p, G, tile, BN);
         const int a = local & 1;
         const uint32_t q = static_cast<uint32_t>(local >> 1);
         if (!mbar_wait_bounded(&st->tempty[a], (q & 1u) ^ 1u, p.timeout_ns, p.status,
@@ -320,7 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int kk = 0; kk < kBK / 16; ++kk) {
               tc_mma_bf16(d_tmem, smem_desc_sw128(sa + kk * 32), smem_desc_sw128(sb + kk * 32),
-                          idesc_n, (kb | kk) != 0 ? 1u : 0u);
+                          kIdesc, (kb | kk) != 0 ? 1u : 0u);
             }
           } else {
             // transposed tail: half h of the B tile (weight rows 128h ..) as M,
@@ -328,7 +329,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // [h * nsw, (h + 1) * nsw) of the accumulator buffer
 #pragma unroll
             for (int kk = 0; kk < kBK / 16; ++kk) {
-              for (int h = 0; h < ti.bn_eff / 128; ++h)
+#pragma unroll
+              for (int h = 0; h < BN / 128; ++h)
                 tc_mma_bf16(d_tmem + static_cast<uint32_t>(h * nsw),
                             smem_desc_sw128(sb + h * (128 * kBK * 2) + kk * 32),
                             smem_desc_sw128(sa + kk * 32), idesc_sw, (kb | kk) != 0 ? 1u : 0u);
@@ -353,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r_in_tile = quarter * 32 + lane;
     int local = 0;
     for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x, ++local) {
-      const TileInfo ti = decode_split_tile<BN>(st, p, G, tile);
+      const TileInfo ti = decode_tile(st, p, G, tile, BN);
       const int a = local & 1;
       const uint32_t q = static_cast<uint32_t>(local >> 1);
       if (!mbar_wait_bounded(&st->tfull[a], q & 1u, p.timeout_ns, p.status, abort_flag)) break;
@@ -385,9 +387,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         } else {
 #pragma unroll 1
-          for (int h = 0; h < ti.bn_eff / 128; ++h) {
-            __nv_bfloat16* dst =
-                base + static_cast<int64_t>(ti.n) * BN + ti.col_off + h * 128 + r_in_tile;
+          for (int h = 0; h < BN / 128; ++h) {
+            __nv_bfloat16* dst = base + static_cast<int64_t>(ti.n) * BN + h * 128 + r_in_tile;
 #pragma unroll 1
             for (int c = 0; c < nsw; c += 32) {
               float v[32];
@@ -422,9 +423,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else {
-        __nv_bfloat16* dst = out + row * ld + static_cast<int64_t>(ti.n) * BN + ti.col_off;
+        __nv_bfloat16* dst = out + row * ld + static_cast<int64_t>(ti.n) * BN;
 #pragma unroll 1
-        for (int c = 0; c < ti.bn_eff / 32; ++c) {
+        for (int c = 0; c < BN / 32; ++c) {
           float v[32];
           tmem_ld32(taddr + c * 32, v);
           tmem_ld_wait();

@@ -35,9 +35,6 @@ struct GroupedGemmArgs {
   // the routed activations is row gather_rows[r] of the tensor behind A0,
   // whose map then has a 64 x 1 box.
   const int32_t* gather_rows = nullptr;
-  // Second projection, BN = 256: split the last round's tiles into 128-column
-  // halves when it holds at most half a grid (see the kernel).
-  bool split_last = true;
 };
 
 // A0/A1: activations [rows][K] (routed / shared), B0/B1: weights [rows][K].
