@@ -72,6 +72,26 @@ def test_layer_parity_fused_gather(name, monkeypatch):
     check_layer(synth.make_inputs(CASES[name], "cuda"))
 
 
+@pytest.mark.parametrize("name", ["ragged_shared", "capacity_k4", "fine_bias_shared",
+                                  "wide_E160", "single_token", "E1_k1_dense"])
+def test_layer_parity_multicast(name, monkeypatch):
+    """The same cases with the 256-column GEMM tiles on clusters of two CTAs
+    that share each B tile by TMA multicast."""
+    monkeypatch.setenv("MOE_GEMM_MC", "1")
+    check_layer(synth.make_inputs(CASES[name], "cuda"))
+
+
+def test_multicast_and_single_cta_agree_bitwise(monkeypatch):
+    """Sharing the B tiles changes only who loads them: outputs are bitwise equal."""
+    w = CASES["fine_bias_shared"]
+    inp = synth.make_inputs(w, "cuda")
+    outs = []
+    for flag in ("1", "0"):
+        monkeypatch.setenv("MOE_GEMM_MC", flag)
+        outs.append(run_layer(inp).y)
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+
+
 def test_fused_and_materialised_rows_agree_bitwise(monkeypatch):
     """Gathering the rows inside GEMM-1 stages the same bytes as the scatter's
     copy, so the two paths give bit-identical outputs."""

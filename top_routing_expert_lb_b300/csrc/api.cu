@@ -403,7 +403,14 @@ int do_ffn(const moe_shape_t* s, const uint16_t* x_perm, const int32_t* offsets,
   const int nsm = sm_count_cached();
   const bool paired = gemm_paired();
   if (paired && gather_rows != nullptr) return MOE_ERR_INVALID_ARG;  // needs x_perm
-  const uint32_t bbox = paired ? 128u : 256u;
+  // MOE_GEMM_MC=1: clusters of two CTAs sharing each B tile through TMA
+  // multicast (half the B bytes from L2 per tile; measured slower than
+  // independent CTAs on every workload, so off by default); not with the
+  // paired tiles or gathered rows
+  bool mc = false;
+  if (const char* env = std::getenv("MOE_GEMM_MC")) mc = !paired && std::strcmp(env, "1") == 0;
+  const bool mc1 = mc && gather_rows == nullptr;
+  const uint32_t bbox = (paired || mc1) ? 128u : 256u;
 
   // projection 1: [x_perm | x] -> h = SiLU(gate) * up
   CUtensorMap a0, a1, b0, b1;
@@ -437,14 +444,18 @@ int do_ffn(const moe_shape_t* s, const uint16_t* x_perm, const int32_t* offsets,
   g1.timeout_ns = g_timeout_ns;
   g1.gather_rows = routed ? gather_rows : nullptr;
   int rc = tracked(MOE_KERNEL_GEMM_SWIGLU, st,
-                   [&] { return launch_grouped_gemm(a0, a1, b0, b1, g1, true, 256, paired, nsm, st); });
+                   [&] {
+                     return launch_grouped_gemm(a0, a1, b0, b1, g1, true, 256, paired, nsm, st,
+                                                mc1);
+                   });
   if (rc != 0) return cuda_rc(rc);
 
   // projection 2: [h | h_s] -> [y_perm | y_s]
   const bool paired2 = paired && bn2 == 256;
   // 256-column tiles of the single-CTA kernel load B as two 128-row boxes (so
   // that its last round can run 128-column halves)
-  const uint32_t bbox2 = paired2 ? 128u : static_cast<uint32_t>(bn2);
+  const bool mc2 = mc && bn2 == 256;
+  const uint32_t bbox2 = (paired2 || mc2) ? 128u : static_cast<uint32_t>(bn2);
   if (routed) {
     if (!make_tmap_bf16(&a0, h, L.rmax, M, 128)) return MOE_ERR_CUDA;
     if (!make_tmap_bf16(&b0, w2, E * d, M, bbox2)) return MOE_ERR_CUDA;
@@ -466,7 +477,10 @@ int do_ffn(const moe_shape_t* s, const uint16_t* x_perm, const int32_t* offsets,
   g2.out_shared = y_s;
   g2.ld_shared = d;
   rc = tracked(MOE_KERNEL_GEMM_DOWN, st,
-               [&] { return launch_grouped_gemm(a0, a1, b0, b1, g2, false, bn2, paired2, nsm, st); });
+               [&] {
+                 return launch_grouped_gemm(a0, a1, b0, b1, g2, false, bn2, paired2, nsm, st,
+                                            mc2);
+               });
   return cuda_rc(rc);
 }
 

@@ -42,9 +42,12 @@ struct GroupedGemmArgs {
 // tile (packed gate/up weights); else writes acc as bf16.
 // paired: 256 x 256 tiles on CTA pairs (tcgen05 cta_group::2; bn must be 256;
 // the B tensor maps then use 128-row boxes); else 128 x bn tiles per CTA.
+// multicast: single-CTA 128 x 256 tiles on clusters of two CTAs that share
+// each B tile (each loads one 128-row half, multicast to both; the B maps
+// then use 128-row boxes); not with paired or gathered rows.
 int launch_grouped_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b0,
                         const CUtensorMap& b1, const GroupedGemmArgs& args, bool swiglu, int bn,
-                        bool paired, int num_sms, cudaStream_t stream);
+                        bool paired, int num_sms, cudaStream_t stream, bool multicast = false);
 
 // Encodes a 2-D bf16 tensor map over a row-major [rows][cols] tensor with a
 // 64-column x box_rows box and 128-byte swizzle.  Returns false on failure.
