@@ -451,10 +451,21 @@ int do_ffn(const moe_shape_t* s, const uint16_t* x_perm, const int32_t* offsets,
   if (rc != 0) return cuda_rc(rc);
 
   // projection 2: [h | h_s] -> [y_perm | y_s]
-  const bool paired2 = paired && bn2 == 256;
+  // The down projection (K = M, long tiles) runs on 256 x 256 CTA-pair tiles
+  // when experts average at least 512 rows: the pair halves the operand bytes
+  // per FLOP and the 256-row padding stays small (measured 3 % faster steps on
+  // Mixtral in the power-limited loop); with fewer rows per expert the padding
+  // costs more than the pair saves.  MOE_GEMM2_TILE=128|256 overrides.
+  const int64_t rows_per_expert =
+      L.r >= 0 ? L.r : (E > 0 ? (static_cast<int64_t>(T) * s->k) / E : 0);
+  bool paired2 = bn2 == 256 && (paired || rows_per_expert >= 512);
+  if (const char* env = std::getenv("MOE_GEMM2_TILE")) {
+    if (std::strcmp(env, "128") == 0) paired2 = false;
+    if (std::strcmp(env, "256") == 0) paired2 = bn2 == 256;
+  }
   // 256-column tiles of the single-CTA kernel load B as two 128-row boxes (so
   // that its last round can run 128-column halves)
-  const bool mc2 = mc && bn2 == 256;
+  const bool mc2 = mc && bn2 == 256 && !paired2;
   const uint32_t bbox2 = (paired2 || mc2) ? 128u : static_cast<uint32_t>(bn2);
   if (routed) {
     if (!make_tmap_bf16(&a0, h, L.rmax, M, 128)) return MOE_ERR_CUDA;
