@@ -81,6 +81,15 @@ def test_layer_parity_multicast(name, monkeypatch):
     check_layer(synth.make_inputs(CASES[name], "cuda"))
 
 
+@pytest.mark.parametrize("name", ["ragged_shared", "capacity_k4", "fine_bias_shared",
+                                  "top1_capacity", "E1_k1_dense", "k_equals_E"])
+def test_layer_parity_split_gate_up(name, monkeypatch):
+    """The same cases with the gate/up projection split into CTA-pair tiles for
+    whole 256-row blocks and single-CTA tiles for the rest."""
+    monkeypatch.setenv("MOE_GEMM1_SPLIT", "1")
+    check_layer(synth.make_inputs(CASES[name], "cuda"))
+
+
 def test_multicast_and_single_cta_agree_bitwise(monkeypatch):
     """Sharing the B tiles changes only who loads them: outputs are bitwise equal."""
     w = CASES["fine_bias_shared"]

@@ -411,6 +411,16 @@ int do_ffn(const moe_shape_t* s, const uint16_t* x_perm, const int32_t* offsets,
   if (const char* env = std::getenv("MOE_GEMM_MC")) mc = !paired && std::strcmp(env, "1") == 0;
   const bool mc1 = mc && gather_rows == nullptr;
   const uint32_t bbox = (paired || mc1) ? 128u : 256u;
+  // MOE_GEMM1_SPLIT=1: the first projection runs each group's whole 256-row
+  // blocks on CTA-pair tiles and only the remaining rows (< 256 per group) on
+  // single-CTA tiles (two launches, both counted as the gate/up kernel).
+  // Measured 9 % slower than single-CTA tiles throughout on Mixtral, so off
+  // by default.
+  const int64_t rows_per_expert =
+      L.r >= 0 ? L.r : (E > 0 ? (static_cast<int64_t>(T) * s->k) / E : 0);
+  bool split1 = false;
+  if (const char* env = std::getenv("MOE_GEMM1_SPLIT")) split1 = std::strcmp(env, "1") == 0;
+  split1 = split1 && !paired && !mc1 && gather_rows == nullptr && nsm >= 2;
 
   // projection 1: [x_perm | x] -> h = SiLU(gate) * up
   CUtensorMap a0, a1, b0, b1;
@@ -428,6 +438,13 @@ int do_ffn(const moe_shape_t* s, const uint16_t* x_perm, const int32_t* offsets,
   }
   if (!routed) { a0 = a1; b0 = b1; }
   if (!shared) { a1 = a0; b1 = b0; }
+  CUtensorMap bp0 = b0, bp1 = b1;  // 128-row boxes for the pair launch
+  if (split1) {
+    if (routed && !make_tmap_bf16(&bp0, w13, E * 2 * M, d, 128)) return MOE_ERR_CUDA;
+    if (shared && !make_tmap_bf16(&bp1, w13s, 2 * Ms, d, 128)) return MOE_ERR_CUDA;
+    if (!routed) bp0 = bp1;
+    if (!shared) bp1 = bp0;
+  }
   GroupedGemmArgs g1{};
   g1.offsets = offsets;
   g1.n_routed = routed ? static_cast<int32_t>(E) : 0;
@@ -443,12 +460,23 @@ int do_ffn(const moe_shape_t* s, const uint16_t* x_perm, const int32_t* offsets,
   g1.status = at<int>(ws, L.status);
   g1.timeout_ns = g_timeout_ns;
   g1.gather_rows = routed ? gather_rows : nullptr;
-  int rc = tracked(MOE_KERNEL_GEMM_SWIGLU, st,
-                   [&] {
-                     return launch_grouped_gemm(a0, a1, b0, b1, g1, true, 256, paired, nsm, st,
-                                                mc1);
-                   });
+  int rc = 0;
+  if (split1) {
+    GroupedGemmArgs g1p = g1;
+    g1p.row_split = 1;
+    rc = tracked(MOE_KERNEL_GEMM_SWIGLU, st, [&] {
+      return launch_grouped_gemm(a0, a1, bp0, bp1, g1p, true, 256, true, nsm, st);
+    });
+    if (rc != 0) return cuda_rc(rc);
+    g1.row_split = 2;
+  }
+  rc = tracked(MOE_KERNEL_GEMM_SWIGLU, st,
+               [&] {
+                 return launch_grouped_gemm(a0, a1, b0, b1, g1, true, 256, paired, nsm, st,
+                                            mc1);
+               });
   if (rc != 0) return cuda_rc(rc);
+  g1.row_split = 0;
 
   // projection 2: [h | h_s] -> [y_perm | y_s]
   // The down projection (K = M, long tiles) runs on 256 x 256 CTA-pair tiles
@@ -456,15 +484,12 @@ int do_ffn(const moe_shape_t* s, const uint16_t* x_perm, const int32_t* offsets,
   // per FLOP and the 256-row padding stays small (measured 3 % faster steps on
   // Mixtral in the power-limited loop); with fewer rows per expert the padding
   // costs more than the pair saves.  MOE_GEMM2_TILE=128|256 overrides.
-  const int64_t rows_per_expert =
-      L.r >= 0 ? L.r : (E > 0 ? (static_cast<int64_t>(T) * s->k) / E : 0);
   bool paired2 = bn2 == 256 && (paired || rows_per_expert >= 512);
   if (const char* env = std::getenv("MOE_GEMM2_TILE")) {
     if (std::strcmp(env, "128") == 0) paired2 = false;
     if (std::strcmp(env, "256") == 0) paired2 = bn2 == 256;
   }
-  // 256-column tiles of the single-CTA kernel load B as two 128-row boxes (so
-  // that its last round can run 128-column halves)
+  // the pair and multicast forms load B in 128-row halves
   const bool mc2 = mc && bn2 == 256 && !paired2;
   const uint32_t bbox2 = (paired2 || mc2) ? 128u : static_cast<uint32_t>(bn2);
   if (routed) {

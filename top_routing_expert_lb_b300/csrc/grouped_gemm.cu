@@ -200,6 +200,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         rows = p.offsets[e + 1] - r0;
         if (rows < 0) rows = 0;
       }
+      if (p.row_split != 0) {  // whole 256-row blocks, or the rows after them
+        const int whole = rows & ~255;
+        if (p.row_split == 1) {
+          rows = whole;
+        } else {
+          r0 += whole;
+          rows -= whole;
+        }
+      }
       st->row0[g] = r0;
       st->rows[g] = rows;
       const int ncols = sh ? p.n_cols_shared : p.n_cols_routed;
@@ -607,6 +616,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         r0 = p.offsets[e];
         rows = p.offsets[e + 1] - r0;
         if (rows < 0) rows = 0;
+      }
+      if (p.row_split != 0) {  // whole 256-row blocks, or the rows after them
+        const int whole = rows & ~255;
+        if (p.row_split == 1) {
+          rows = whole;
+        } else {
+          r0 += whole;
+          rows -= whole;
+        }
       }
       st->row0[g] = r0;
       st->rows[g] = rows;

@@ -35,6 +35,10 @@ struct GroupedGemmArgs {
   // the routed activations is row gather_rows[r] of the tensor behind A0,
   // whose map then has a 64 x 1 box.
   const int32_t* gather_rows = nullptr;
+  // 0: every row of each group; 1: only its whole 256-row blocks; 2: only the
+  // rows after them (fewer than 256).  One projection can thus run its long
+  // blocks on CTA pairs and the remainders on single CTAs.
+  int32_t row_split = 0;
 };
 
 // A0/A1: activations [rows][K] (routed / shared), B0/B1: weights [rows][K].
