@@ -42,6 +42,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--clocks-dir", default=None,
+                    help="keep the nvidia-smi clock samples as CSV in this directory")
     ap.add_argument("--cpu-budget-s", type=float, default=15.0,
                     help="target seconds of oracle work for the CPU baseline sample")
     ap.add_argument("--routing", choices=["token", "priority", "expert-choice"],
@@ -230,11 +232,16 @@ class NvmlPoller:
 
 
 class ClockSampler:
-    def __init__(self, device_index: int, enabled: bool = True):
+    """nvidia-smi clock / throttle-reason samples (CSV, every 100 ms) plus the
+    NVML poller.  The CSV goes to `csv_dir` when given, else to a temporary
+    file removed after the summary."""
+
+    def __init__(self, device_index: int, enabled: bool = True, csv_dir=None):
         self.proc = None
         self.enabled = enabled
         self.idx = device_index
         self.path = None
+        self.csv_dir = csv_dir
         self.poll = NvmlPoller(device_index) if enabled else None
 
     def mark_start(self):
@@ -248,9 +255,13 @@ class ClockSampler:
         if not self.enabled:
             return self
         self.poll.start()
-        out_dir = os.path.join(ROOT, "gpurun_out")
-        os.makedirs(out_dir, exist_ok=True)
-        self.path = os.path.join(out_dir, f"clocks_rank{self.idx}.csv")
+        if self.csv_dir:
+            os.makedirs(self.csv_dir, exist_ok=True)
+            self.path = os.path.join(self.csv_dir, f"clocks_rank{self.idx}.csv")
+        else:
+            import tempfile
+            fd, self.path = tempfile.mkstemp(prefix="moe_clocks_", suffix=".csv")
+            os.close(fd)
         try:
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
@@ -283,6 +294,8 @@ class ClockSampler:
                 parts = [p.strip() for p in line.split(",")]
                 if len(parts) >= 9:
                     rows.append(parts)
+        if not self.csv_dir:
+            os.remove(self.path)
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
 
@@ -482,7 +495,7 @@ def run_ours(args, w):
     launches0 = moe.moe_launch_count()
     # inside the headline loop only the dominant kernel is bracketed by events
     moe.moe_profile_enable(True, kernels=["gemm_swiglu"])
-    with ClockSampler(local, enabled=not args.no_clocks) as clk:
+    with ClockSampler(local, enabled=not args.no_clocks, csv_dir=args.clocks_dir) as clk:
         clk.mark_start()
         for i in range(args.steps):
             flush.zero_()                                  # evict L2 between steps
