@@ -4,7 +4,8 @@ against the bf16 tensor roofline; memory stages against the HBM roofline).
 
 One step = one whole layer forward (router, permute, grouped SwiGLU FFN with
 shared experts, combine, losses) over one batch of seeded synthetic tokens,
-through the C ABI (moe_layer_forward).  Default workload: the Mixtral-shaped
+through the C ABI (moe_layer_forward), each timed step replaying a CUDA graph
+of that call (--no-graph: direct calls).  Default workload: the Mixtral-shaped
 layer (T=4096, d=4096, E=8, k=2, M=14336, dropless).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
@@ -51,6 +52,8 @@ def parse_args(argv=None):
                     help="token: token-choice top-k (the headline); priority: capacity "
                          "keeps each expert's highest scores; expert-choice: every expert "
                          "takes its top-r tokens (secondary lines: no e2e or CPU leg)")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="launch every timed step directly instead of replaying CUDA graphs")
     ap.add_argument("--stage", choices=["layer", "router"], default="layer",
                     help="router: time moe_route alone (no expert weights are drawn); "
                          "for profiling, not the headline number")
@@ -492,21 +495,46 @@ def run_ours(args, w):
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
-    launches0 = moe.moe_launch_count()
-    # inside the headline loop only the dominant kernel is bracketed by events
+    # Inside the headline loop only the dominant kernel is bracketed by events.
+    # By default each timed step replays its own CUDA graph of one layer
+    # forward (captured here, events included), which drops the host-side
+    # launch work from the step; --no-graph launches every step directly.
+    graphs = None
+    per_forward = 0
     moe.moe_profile_enable(True, kernels=["gemm_swiglu"])
+    if not args.no_graph:
+        graphs = []
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        c0 = moe.moe_launch_count()
+        with torch.cuda.stream(side):
+            for _ in range(args.steps):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=side):
+                    layer.forward(inp.x)
+                graphs.append(g)
+        per_forward = (moe.moe_launch_count() - c0) // max(1, args.steps)
+        stream.wait_stream(side)
+        torch.cuda.synchronize(dev)
+    launches0 = moe.moe_launch_count()
     with ClockSampler(local, enabled=not args.no_clocks, csv_dir=args.clocks_dir) as clk:
         clk.mark_start()
         for i in range(args.steps):
             flush.zero_()                                  # evict L2 between steps
             starts[i].record(stream)
-            layer.forward(inp.x)
+            if graphs is None:
+                layer.forward(inp.x)
+            else:
+                graphs[i].replay()
             ends[i].record(stream)
         torch.cuda.synchronize(dev)
         clk.mark_end()
     moe.moe_profile_enable(False)
     prof = moe.moe_profile_collect()
     launches = moe.moe_launch_count() - launches0
+    if graphs is not None:
+        # each replay runs the kernels captured once (counted at capture)
+        launches = per_forward * args.steps
     if world > 1:
         dist.barrier()
     if moe.moe_check_status(layer.ws) != 0:
@@ -597,7 +625,8 @@ def run_ours(args, w):
                    "M": w.M, "n_shared": w.n_shared, "capacity_factor": w.capacity_factor,
                    "rows_computed": R,
                    "l2": f"flushed: {FLUSH_BYTES >> 20} MiB written before every timed step",
-                   "parallelism": "replicas" if world > 1 else "single GPU"},
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "cuda_graph": graphs is not None},
         "ffn_tflops": ffn_tflops,
         "ffn_frac_of_bf16_peak": ffn_tflops / peaks["bf16_tflops"],
         "ffn_attainable_ms": attainable_ms,

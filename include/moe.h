@@ -342,7 +342,9 @@ int moe_route_noalloc(const moe_shape_t *shape, const uint16_t *x, const uint16_
 /* on == 1: every subsequent kernel launch is bracketed by two CUDA events on
  * its stream; any other nonzero value is a mask, bit (1 << MOE_KERNEL_*)
  * selecting the kernels to bracket; on == 0 stops recording.  Recording
- * continues until collected.                                                 */
+ * continues until collected.  Inside a stream capture the events become
+ * external event nodes of the graph: each replay records them again, and a
+ * collect after the replay returns that replay's durations.                 */
 int moe_profile_enable(int on);
 
 /* Waits for the recorded events and returns, in launch order, up to `cap`

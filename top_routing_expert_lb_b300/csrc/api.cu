@@ -38,6 +38,16 @@ cudaEvent_t pool_event() {
   return g_ev_pool[g_ev_used++];
 }
 
+// Records `e` on `st`; inside a stream capture as an external event node, so
+// that every replay of the graph records it again.
+void record_event(cudaEvent_t e, cudaStream_t st) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusActive)
+    cudaEventRecordWithFlags(e, st, cudaEventRecordExternal);
+  else
+    cudaEventRecord(e, st);
+}
+
 // Runs one launcher; counts it and, when profiling, brackets it with events.
 template <typename F>
 int tracked(int32_t kernel, cudaStream_t st, F&& launch) {
@@ -46,12 +56,12 @@ int tracked(int32_t kernel, cudaStream_t st, F&& launch) {
   if (prof) {
     a = pool_event();
     b = pool_event();
-    if (a) cudaEventRecord(a, st);
+    if (a) record_event(a, st);
   }
   const int rc = launch();
   if (rc == 0) ++g_launches;
   if (prof && a && b) {
-    cudaEventRecord(b, st);
+    record_event(b, st);
     g_prof.push_back({kernel, a, b});
   }
   return rc;
