@@ -79,10 +79,10 @@ struct TileInfo {
 // swap roles, and the epilogue reads TMEM lane = output column, TMEM column =
 // token row.  Returns that N, or 0 for a normal tile.
 template <int BN>
-__device__ __forceinline__ int swapped_n(int rows_left) {
+__device__ __forceinline__ int swapped_n(int rows_left, int max_n) {
   if (BN < 128 || rows_left >= kBM) return 0;
   const int n = (rows_left + 15) & ~15;
-  return n <= 112 ? n : 0;
+  return n <= max_n ? n : 0;
 }
 
 template <typename Tail>
@@ -378,7 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(a * BN);
-        const int nsw = swapped_n<BN>(ti.rows_left);
+        const int nsw = swapped_n<BN>(ti.rows_left, p.tail_max_n);
         const uint32_t idesc_sw = idesc_bf16_f32(kBM, static_cast<uint32_t>(nsw > 0 ? nsw : 16));
         bool ok = true;
         for (int kb = 0; kb < ti.nk; ++kb) {
@@ -446,7 +446,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(ti.shared ? p.out_shared
                                                                       : p.out_routed);
       const int64_t ld = ti.shared ? p.ld_shared : p.ld_routed;
-      const int nsw = swapped_n<BN>(ti.rows_left);
+      const int nsw = swapped_n<BN>(ti.rows_left, p.tail_max_n);
       if (nsw > 0) {
         // transposed tail: this thread's TMEM lane is output column r_in_tile
         // of each 128-wide half; TMEM column j of a half is token row j

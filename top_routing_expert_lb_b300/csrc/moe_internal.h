@@ -39,6 +39,9 @@ struct GroupedGemmArgs {
   // rows after them (fewer than 256).  One projection can thus run its long
   // blocks on CTA pairs and the remainders on single CTAs.
   int32_t row_split = 0;
+  // A group's last m-tile with r valid rows runs transposed when r rounded up
+  // to 16 is at most tail_max_n (0: never).
+  int32_t tail_max_n = 112;
 };
 
 // A0/A1: activations [rows][K] (routed / shared), B0/B1: weights [rows][K].
