@@ -326,6 +326,24 @@ int moe_route_noalloc(const moe_shape_t *shape, const uint16_t *x, const uint16_
                       float *gates, int32_t *counts, float *f, float *P, float *bal_loss,
                       float *z_loss, void *stream);
 
+/* Expert-GEMM variants, read from the environment at every grouped-FFN
+ * launch (the defaults are the measured fastest; every variant gives
+ * parity-tested results, most bit-identical to the default):
+ *   MOE_GEMM_TILE=256        both projections on 256 x 256 CTA-pair tiles
+ *   MOE_GEMM2_TILE=128|256   the down projection on single-CTA 128 x BN or
+ *                            CTA-pair 256 x 256 tiles (default: pairs when
+ *                            d % 256 == 0 and experts average >= 512 rows)
+ *   MOE_GEMM_MC=1            clusters of two single CTAs sharing each B tile
+ *                            through TMA multicast
+ *   MOE_GEMM1_SPLIT=1        gate/up projection: whole 256-row blocks on CTA
+ *                            pairs, the remaining rows on single CTAs
+ *   MOE_GEMM_TAIL_MAX_N=n    a group's last m-tile with r rows runs transposed
+ *                            (weights as the MMA's M) when r rounded up to 16
+ *                            is <= n (default 112; 0 never)
+ *   MOE_FUSED_GATHER=1       moe_layer_forward: the gate/up projection gathers
+ *                            token rows itself (TMA 4-row gathers), no x_perm
+ * All are tuning switches, not part of the layer's definition.               */
+
 /* Kernel accounting for benchmarks (host-side, process-wide, not thread-safe).
  * Kernel ids reported by moe_profile_collect: */
 #define MOE_KERNEL_ROUTER 1       /* router logits + softmax + Top-k            */
