@@ -342,6 +342,10 @@ int moe_route_noalloc(const moe_shape_t *shape, const uint16_t *x, const uint16_
  *                            is <= n (default 112; 0 never)
  *   MOE_FUSED_GATHER=1       moe_layer_forward: the gate/up projection gathers
  *                            token rows itself (TMA 4-row gathers), no x_perm
+ *   MOE_GATE_IN_EPILOGUE=1   moe_layer_forward / moe_ec_layer_forward: the down
+ *                            projection's epilogue scales each routed row by
+ *                            its gate (fp32, before rounding) and the combine
+ *                            only adds rows, in the same fixed order
  * All are tuning switches, not part of the layer's definition.               */
 
 /* Kernel accounting for benchmarks (host-side, process-wide, not thread-safe).

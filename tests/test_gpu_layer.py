@@ -90,6 +90,18 @@ def test_layer_parity_split_gate_up(name, monkeypatch):
     check_layer(synth.make_inputs(CASES[name], "cuda"))
 
 
+@pytest.mark.parametrize("name,tile2", [("ragged_shared", "128"), ("ragged_shared", "256"),
+                                        ("capacity_k4", "128"), ("fine_bias_shared", "128"),
+                                        ("wide_E160", "128"), ("k_equals_E", "128"),
+                                        ("single_token", "128"), ("top1_capacity", "128")])
+def test_layer_parity_gate_in_epilogue(name, tile2, monkeypatch):
+    """The same cases with each routed row scaled by its gate in the down
+    projection's epilogue and a combine that only adds rows."""
+    monkeypatch.setenv("MOE_GATE_IN_EPILOGUE", "1")
+    monkeypatch.setenv("MOE_GEMM2_TILE", tile2)
+    check_layer(synth.make_inputs(CASES[name], "cuda"))
+
+
 def test_multicast_and_single_cta_agree_bitwise(monkeypatch):
     """Sharing the B tiles changes only who loads them: outputs are bitwise equal."""
     w = CASES["fine_bias_shared"]

@@ -156,6 +156,18 @@ def test_select_paths_with_fused_gather(w, monkeypatch):
         check_layer(synth.make_inputs(w, "cuda"))
 
 
+@pytest.mark.parametrize("w", [PRIO_CASES[0], PRIO_CASES[2], EC_CASES[0], EC_CASES[2]],
+                         ids=lambda w: w.name)
+def test_select_paths_gate_in_epilogue(w, monkeypatch):
+    """Priority capacity and expert choice with the gates applied in the down
+    projection's epilogue."""
+    monkeypatch.setenv("MOE_GATE_IN_EPILOGUE", "1")
+    if w.flags & EC:
+        check_ec_layer(synth.make_inputs(w, "cuda"))
+    else:
+        check_layer(synth.make_inputs(w, "cuda"))
+
+
 def test_deterministic_bitwise_select():
     for w in (PRIO_CASES[0], EC_CASES[0]):
         inp = synth.make_inputs(w, "cuda")

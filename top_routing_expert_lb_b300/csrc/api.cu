@@ -163,7 +163,7 @@ Layout layout_of(const moe_shape_t* s) {
   L.all_offsets = take(prio ? (E + 1) * 4 : 0);
   L.scores_t = take(is_ec(s) ? E * T * 4 : 0);
   L.sel_t = take(is_ec(s) ? E * T * 4 : 0);
-  L.row_gate = take(is_ec(s) ? L.rmax * 4 : 0);
+  L.row_gate = take(L.rmax * 4);
   L.x_perm = take(L.rmax * d * 2);
   L.h = take(L.rmax * M * 2);
   L.y_perm = take(L.rmax * d * 2);
@@ -293,7 +293,8 @@ int do_route(const moe_shape_t* s, const uint16_t* x, const uint16_t* wr, const 
 
 int do_scatter(const moe_shape_t* s, const uint16_t* x, const int32_t* ids, const Layout& L,
                void* ws, const int32_t* offsets, int32_t* slot_row, int32_t* row_token,
-               uint8_t* drop_mask, uint16_t* x_perm, cudaStream_t st) {
+               uint8_t* drop_mask, uint16_t* x_perm, cudaStream_t st,
+               const float* gates = nullptr, float* row_gate = nullptr) {
   ScatterArgs sa{};
   sa.T = s->T;
   sa.d = s->d;
@@ -309,6 +310,8 @@ int do_scatter(const moe_shape_t* s, const uint16_t* x, const int32_t* ids, cons
   sa.drop_mask = drop_mask;
   sa.x_perm = x_perm;
   sa.num_sms = sm_count_cached();
+  sa.gates = gates;
+  sa.row_gate = row_gate;
   return cuda_rc(tracked(MOE_KERNEL_SCATTER, st, [&] { return launch_scatter(sa, st); }));
 }
 
@@ -317,7 +320,8 @@ int do_scatter(const moe_shape_t* s, const uint16_t* x, const int32_t* ids, cons
 int do_priority_dispatch(const moe_shape_t* s, const uint16_t* x, const int32_t* ids,
                          const Layout& L, void* ws, const int32_t* offsets, int32_t* slot_row,
                          int32_t* row_token, uint8_t* drop_mask, uint16_t* x_perm,
-                         cudaStream_t st) {
+                         cudaStream_t st, const float* gates = nullptr,
+                         float* row_gate = nullptr) {
   ScatterArgs sa{};
   sa.T = s->T;
   sa.d = s->d;
@@ -346,6 +350,8 @@ int do_priority_dispatch(const moe_shape_t* s, const uint16_t* x, const int32_t*
   pa.slot_row = slot_row;
   pa.drop_mask = drop_mask;
   pa.row_token = row_token;
+  pa.gates = gates;
+  pa.row_gate = row_gate;
   rc = cuda_rc(tracked(MOE_KERNEL_SELECT, st, [&] { return launch_priority_select(pa, st); }));
   if (rc != MOE_OK || x_perm == nullptr) return rc;  // no x_perm: GEMM-1 gathers the rows
   return cuda_rc(tracked(MOE_KERNEL_GATHER, st, [&] {
@@ -390,6 +396,15 @@ bool gemm_paired() {
 // gather issues 32 TMA instructions per k-block instead of one and measured
 // about 3.5x slower in GEMM-1, so it stays opt-in.  The paired GEMM always
 // reads x_perm.
+// MOE_GATE_IN_EPILOGUE=1: the down projection's epilogue multiplies each
+// routed row by its gate (fp32, before rounding) and the combine only adds the
+// rows in slot order (or expert order).  Same bytes, one multiply moved; off
+// by default.
+bool gate_in_epilogue() {
+  const char* env = std::getenv("MOE_GATE_IN_EPILOGUE");
+  return env != nullptr && std::strcmp(env, "1") == 0;
+}
+
 bool fused_gather() {
   const char* env = std::getenv("MOE_FUSED_GATHER");
   if (env == nullptr || std::strcmp(env, "1") != 0) return false;
@@ -401,7 +416,8 @@ bool fused_gather() {
 int do_ffn(const moe_shape_t* s, const uint16_t* x_perm, const int32_t* offsets,
            const uint16_t* w13, const uint16_t* w2, uint16_t* y_perm, const uint16_t* x,
            const uint16_t* w13s, const uint16_t* w2s, uint16_t* y_s, void* ws, const Layout& L,
-           cudaStream_t st, const int32_t* gather_rows = nullptr) {
+           cudaStream_t st, const int32_t* gather_rows = nullptr,
+           const float* row_scale = nullptr) {
   const int64_t T = s->T, d = s->d, M = s->M, E = s->E;
   const int64_t Ms = static_cast<int64_t>(s->n_shared) * M;
   const bool routed = L.rmax > 0;
@@ -515,6 +531,7 @@ int do_ffn(const moe_shape_t* s, const uint16_t* x_perm, const int32_t* offsets,
   if (!shared) { a1 = a0; b1 = b0; }
   GroupedGemmArgs g2 = g1;
   g2.gather_rows = nullptr;
+  g2.row_scale = routed ? row_scale : nullptr;
   g2.n_cols_routed = static_cast<int32_t>(d);
   g2.n_cols_shared = static_cast<int32_t>(d);
   g2.k_routed = static_cast<int32_t>(M);
@@ -739,21 +756,25 @@ int moe_layer_forward(const moe_shape_t* s, const uint16_t* x, const uint16_t* w
   uint16_t* y_perm = at<uint16_t>(ws, L.y_perm);
   uint16_t* y_s = s->n_shared > 0 ? at<uint16_t>(ws, L.y_s) : nullptr;
   const bool fused = fused_gather();
+  const bool gate_epi = gate_in_epilogue() && s->k > 0;
   int32_t* row_token = at<int32_t>(ws, L.row_token);
+  float* row_gate = gate_epi ? at<float>(ws, L.row_gate) : nullptr;
   if (s->k > 0) {
     uint16_t* xp = fused ? nullptr : x_perm;
     if (prio)
       rc = do_priority_dispatch(s, x, ids, L, ws, offsets, slot_row, row_token, drop_mask, xp,
-                                st);
+                                st, gates, row_gate);
     else
-      rc = do_scatter(s, x, ids, L, ws, offsets, slot_row, row_token, drop_mask, xp, st);
+      rc = do_scatter(s, x, ids, L, ws, offsets, slot_row, row_token, drop_mask, xp, st, gates,
+                      row_gate);
     if (rc != MOE_OK) return rc;
   }
   rc = do_ffn(s, fused ? nullptr : x_perm, offsets, w13, w2, y_perm, x, w13_shared, w2_shared,
-              y_s, ws, L, st, fused ? row_token : nullptr);
+              y_s, ws, L, st, fused ? row_token : nullptr, row_gate);
   if (rc != MOE_OK) return rc;
+  const float* combine_gates = gate_epi ? nullptr : gates;
   return cuda_rc(tracked(MOE_KERNEL_COMBINE, st, [&] {
-    return launch_combine(s->T, s->d, s->k, y_perm, slot_row, gates, y_s, y, st);
+    return launch_combine(s->T, s->d, s->k, y_perm, slot_row, combine_gates, y_s, y, st);
   }));
 }
 
@@ -860,12 +881,14 @@ int moe_ec_layer_forward(const moe_shape_t* s, const uint16_t* x, const uint16_t
     }));
     if (rc != MOE_OK) return rc;
   }
+  const bool gate_epi = gate_in_epilogue() && L.rmax > 0;
   rc = do_ffn(s, fused ? nullptr : x_perm, offsets, w13, w2, y_perm, x, w13_shared, w2_shared,
-              y_s, ws, L, st, fused ? row_token : nullptr);
+              y_s, ws, L, st, fused ? row_token : nullptr, gate_epi ? row_gate : nullptr);
   if (rc != MOE_OK) return rc;
+  const float* combine_gates = gate_epi ? nullptr : row_gate;
   return cuda_rc(tracked(MOE_KERNEL_COMBINE, st, [&] {
-    return launch_ec_combine(s->T, s->d, s->E, at<int32_t>(ws, L.sel_t), row_gate, y_perm, y_s,
-                             y, st);
+    return launch_ec_combine(s->T, s->d, s->E, at<int32_t>(ws, L.sel_t), combine_gates, y_perm,
+                             y_s, y, st);
   }));
 }
 

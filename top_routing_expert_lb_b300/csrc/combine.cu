@@ -56,7 +56,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
 #pragma unroll
   for (int s = 0; s < K; ++s) {
     rows[s] = slot_row[static_cast<int64_t>(t) * K + s];
-    g[s] = gates[static_cast<int64_t>(t) * K + s];
+    g[s] = gates ? gates[static_cast<int64_t>(t) * K + s] : 1.0f;  // null: rows pre-scaled
   }
   const int nvec = d / 8;
   const uint4* ys = y_shared ? reinterpret_cast<const uint4*>(y_shared +

@@ -146,7 +146,9 @@ __device__ __forceinline__ TileInfo decode_mc_tile(const Tail* st, const Grouped
   return ti;
 }
 
-template <int BN, bool kSwiGLU, int kStages, bool kMC = false>
+// kRowScale (plain projections only): every routed output row r is multiplied
+// by p.row_scale[r] in fp32 before rounding (the combine's gate, applied here).
+template <int BN, bool kSwiGLU, int kStages, bool kMC = false, bool kRowScale = false>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
                         const __grid_constant__ CUtensorMap tmA1,
@@ -159,6 +161,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint32_t kTmemCols = 2 * BN;
   constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, BN);
   static_assert(!kMC || BN == 256, "multicast halves a 256-row B tile");
+  static_assert(!(kRowScale && kSwiGLU), "row scaling applies to the plain projection");
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
@@ -475,8 +478,12 @@ __global__ void __launch_bounds__(kThreads, 1)
               tmem_ld_wait();
 #pragma unroll
               for (int j = 0; j < 32; ++j)
-                if (c + j < ti.rows_left)
-                  dst[static_cast<int64_t>(c + j) * ld] = __float2bfloat16_rn(v[j]);
+                if (c + j < ti.rows_left) {
+                  float o = v[j];
+                  if constexpr (kRowScale)
+                    if (!ti.shared) o *= __ldg(p.row_scale + ti.a_row + c + j);
+                  dst[static_cast<int64_t>(c + j) * ld] = __float2bfloat16_rn(o);
+                }
             }
           }
         }
@@ -503,11 +510,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       } else {
         __nv_bfloat16* dst = out + row * ld + static_cast<int64_t>(ti.n) * BN;
+        float sc = 1.0f;
+        if constexpr (kRowScale) sc = (valid && !ti.shared) ? __ldg(p.row_scale + row) : 1.0f;
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
           float v[32];
           tmem_ld32(taddr + c * 32, v);
           tmem_ld_wait();
+          if constexpr (kRowScale) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] *= sc;
+          }
           uint32_t packed[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) packed[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
@@ -564,7 +577,7 @@ constexpr size_t pair_smem_bytes() {
          sizeof(PairSmemTail);
 }
 
-template <bool kSwiGLU>
+template <bool kSwiGLU, bool kRowScale = false>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA0,
                              const __grid_constant__ CUtensorMap tmA1,
@@ -781,11 +794,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       } else {
         __nv_bfloat16* dst = out + row * ld + static_cast<int64_t>(ti.n) * BN;
+        float sc = 1.0f;
+        if constexpr (kRowScale) sc = (valid && !ti.shared) ? __ldg(p.row_scale + row) : 1.0f;
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
           float v[32];
           tmem_ld32(taddr + c * 32, v);
           tmem_ld_wait();
+          if constexpr (kRowScale) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] *= sc;
+          }
           uint32_t packed[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) packed[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
@@ -812,13 +831,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc_pair(tmem_base, kTmemCols);
 }
 
-template <bool kSwiGLU>
+template <bool kSwiGLU, bool kRowScale = false>
 int launch_pair_impl(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b0,
                      const CUtensorMap& b1, const GroupedGemmArgs& args, int num_sms,
                      cudaStream_t stream) {
   constexpr size_t smem = pair_smem_bytes();
   static_assert(smem <= 227 * 1024, "shared memory budget");
-  auto kern = grouped_gemm_pair_kernel<kSwiGLU>;
+  auto kern = grouped_gemm_pair_kernel<kSwiGLU, kRowScale>;
   static bool attr_set = false;
   if (!attr_set) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -842,13 +861,13 @@ int launch_pair_impl(const CUtensorMap& a0, const CUtensorMap& a1, const CUtenso
   return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }
 
-template <int BN, bool kSwiGLU, int kStages>
+template <int BN, bool kSwiGLU, int kStages, bool kRowScale = false>
 int launch_impl(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b0,
                 const CUtensorMap& b1, const GroupedGemmArgs& args, int num_sms,
                 cudaStream_t stream) {
   constexpr size_t smem = gemm_smem_bytes<BN, kStages>();
   static_assert(smem <= 227 * 1024, "shared memory budget");
-  auto kern = grouped_gemm_kernel<BN, kSwiGLU, kStages>;
+  auto kern = grouped_gemm_kernel<BN, kSwiGLU, kStages, false, kRowScale>;
   static bool attr_set = false;
   if (!attr_set) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -930,6 +949,8 @@ int launch_grouped_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUte
                         const CUtensorMap& b1, const GroupedGemmArgs& args, bool swiglu, int bn,
                         bool paired, int num_sms, cudaStream_t stream, bool multicast) {
   if (args.n_routed + (args.shared_rows > 0 ? 1 : 0) > kMaxGroups) return -2;
+  const bool scale = args.row_scale != nullptr;
+  if (scale && (swiglu || multicast)) return -2;
   if (multicast) {
     if (paired || bn != 256 || args.gather_rows != nullptr || num_sms < 2) return -2;
     return swiglu ? launch_mc_impl<256, true, 4>(a0, a1, b0, b1, args, num_sms, stream)
@@ -937,12 +958,21 @@ int launch_grouped_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUte
   }
   if (paired) {
     if (bn != 256 || num_sms < 2) return -2;
+    if (scale) return launch_pair_impl<false, true>(a0, a1, b0, b1, args, num_sms, stream);
     return swiglu ? launch_pair_impl<true>(a0, a1, b0, b1, args, num_sms, stream)
                   : launch_pair_impl<false>(a0, a1, b0, b1, args, num_sms, stream);
   }
   if (swiglu) {
     if (bn != 256) return -2;
     return launch_impl<256, true, 4>(a0, a1, b0, b1, args, num_sms, stream);
+  }
+  if (scale) {
+    switch (bn) {
+      case 256: return launch_impl<256, false, 4, true>(a0, a1, b0, b1, args, num_sms, stream);
+      case 128: return launch_impl<128, false, 6, true>(a0, a1, b0, b1, args, num_sms, stream);
+      case 64: return launch_impl<64, false, 8, true>(a0, a1, b0, b1, args, num_sms, stream);
+      default: return -2;
+    }
   }
   switch (bn) {
     case 256: return launch_impl<256, false, 4>(a0, a1, b0, b1, args, num_sms, stream);

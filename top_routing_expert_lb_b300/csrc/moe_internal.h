@@ -42,6 +42,9 @@ struct GroupedGemmArgs {
   // A group's last m-tile with r valid rows runs transposed when r rounded up
   // to 16 is at most tail_max_n (0: never).
   int32_t tail_max_n = 112;
+  // Plain projection only: routed output row r is scaled by row_scale[r]
+  // (fp32, before rounding); the shared group is never scaled.
+  const float* row_scale = nullptr;
 };
 
 // A0/A1: activations [rows][K] (routed / shared), B0/B1: weights [rows][K].
@@ -133,6 +136,9 @@ struct ScatterArgs {
   uint8_t* drop_mask;        // [T][k] or null
   uint16_t* x_perm;          // [R_max][d]
   int32_t num_sms;           // sizes the gather split
+  // when set, the gate of each kept pair is written to its row (row_gate[row])
+  const float* gates = nullptr;  // [T][k]
+  float* row_gate = nullptr;     // [R_max]
   // staging mode (priority capacity): when stage_q is set, the pair at rank r
   // of expert e goes to stage_q/stage_key[all_offsets[e] + r] instead (its
   // flat index and pair_score); nothing else is written
@@ -154,6 +160,8 @@ struct PrioritySelectArgs {
   int32_t* slot_row;           // [T][k]
   uint8_t* drop_mask;          // [T][k] or null
   int32_t* row_token;          // [R]
+  const float* gates = nullptr;  // [T][k]; with row_gate, each kept row gets its gate
+  float* row_gate = nullptr;     // [R] or null
 };
 int launch_priority_select(const PrioritySelectArgs& args, cudaStream_t stream);
 

@@ -254,7 +254,10 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_kernel(const ScatterA
       const int64_t gq = static_cast<int64_t>(t0) * k + q;
       a.slot_row[gq] = row;
       if (a.drop_mask) a.drop_mask[gq] = row < 0 ? 1 : 0;
-      if (row >= 0) a.row_token[row] = t0 + q / k;
+      if (row >= 0) {
+        a.row_token[row] = t0 + q / k;
+        if (a.row_gate) a.row_gate[row] = a.gates[gq];
+      }
     }
   }
   if (a.x_perm == nullptr) return;  // rows only: the GEMM gathers the token rows itself

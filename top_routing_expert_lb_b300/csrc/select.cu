@@ -186,6 +186,7 @@ __global__ void __launch_bounds__(kSelThreads) priority_select_kernel(const Prio
         a.slot_row[q] = row;
         if (a.drop_mask) a.drop_mask[q] = 0;
         a.row_token[row] = q / k;
+        if (a.row_gate) a.row_gate[row] = a.gates[q];
       } else {
         a.slot_row[q] = -1;
         if (a.drop_mask) a.drop_mask[q] = 1;
@@ -302,7 +303,7 @@ __global__ void __launch_bounds__(kEcCombineWarps * 32)
     if (row >= 0) {
       const int pos = n + __popc(m & ((1u << lane) - 1u));
       lrow[warp][pos] = row;
-      lgate[warp][pos] = __ldg(row_gate + row);
+      lgate[warp][pos] = row_gate ? __ldg(row_gate + row) : 1.0f;  // null: applied upstream
     }
     n += __popc(m);
   }
