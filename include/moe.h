@@ -254,6 +254,37 @@ int moe_layer_forward_host(const moe_shape_t *shape, const uint16_t *x_host, uin
                            float *f, float *P, float *bal_loss, float *z_loss, void *ws,
                            size_t ws_bytes, void *stream);
 
+/* A stream of n_batches token batches from HOST memory through the layer, with
+ * the copies overlapped with the compute (double-buffered device slots):
+ *   h2d_stream  copies batch i's tokens into x slot i%2 (after the layer of
+ *               batch i-2 has read that slot);
+ *   stream      runs moe_layer_forward on slot i%2 (after its copy-in, and
+ *               after batch i-2's output has left y slot i%2);
+ *   d2h_stream  copies y and the two losses of batch i out.
+ * Batch i+1 is copied in and batch i-1 copied out while batch i computes, so
+ * with pinned host buffers the copies hide behind the layer.  Returns after
+ * all three streams have drained (synchronous for the host).
+ * Arguments (all sizes from shape; T tokens per batch):
+ *   x_host      [n_batches][T][d] bf16 host (pinned for overlap; pageable works
+ *               but copies then block)
+ *   y_host      [n_batches][T][d] bf16 host, written
+ *   losses_host [n_batches][2] fp32 host, (bal, z) per batch, written
+ *   x_dev, y_dev [2][T][d] bf16 device slots, 16-byte aligned
+ *   loss_dev    [2][2] fp32 device slots
+ *   ids, gates, counts, drop_mask, f, P: device outputs as in
+ *               moe_layer_forward; they hold the last batch's values.
+ * The three streams may be the same stream (no overlap).  Errors: as
+ * moe_layer_forward; n_batches < 0 or a null host buffer -> MOE_ERR_INVALID_ARG.
+ * A failing step stops the loop; what was enqueued is drained before return. */
+int moe_layer_forward_host_batches(
+    const moe_shape_t *shape, int32_t n_batches, const uint16_t *x_host, uint16_t *y_host,
+    float *losses_host, uint16_t *x_dev, uint16_t *y_dev, float *loss_dev,
+    const uint16_t *w_router, const float *logit_offset, const float *sel_bias,
+    const uint16_t *w13, const uint16_t *w2, const uint16_t *w13_shared,
+    const uint16_t *w2_shared, int32_t *ids, float *gates, int32_t *counts,
+    uint8_t *drop_mask, float *f, float *P, void *ws, size_t ws_bytes, void *stream,
+    void *h2d_stream, void *d2h_stream);
+
 /* Expert-choice routing (MOE_FLAG_EXPERT_CHOICE must be set in shape->flags).
  * Tokens each expert takes, r = min(T, ceil(c k T / E)), c <= 0 read as 1
  * (host pointer *r).                                                          */

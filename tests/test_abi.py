@@ -105,6 +105,21 @@ def test_workspace_and_pointer_checks(lib):
     base2 = ctypes.c_void_p((ctypes.addressof(buf2) + 255) // 256 * 256)
     assert lib.moe_grouped_ffn(ctypes.byref(s2), base2, base2, base2, base2, base2, base2, None,
                                None, base2, base2, need2, None) == B.MOE_ERR_INVALID_ARG
+    # the batched host stream: argument checks come before anything is enqueued
+    fwd_b = lib.moe_layer_forward_host_batches
+    tail = [fake] * 13 + [fake, need, None, None, None]   # weights .. P, ws, ws_bytes, streams
+    assert fwd_b(ctypes.byref(s), -1, fake, fake, fake, fake, fake, fake,
+                 *tail) == B.MOE_ERR_INVALID_ARG            # negative batch count
+    assert fwd_b(ctypes.byref(s), 2, fake, fake, None, fake, fake, fake,
+                 *tail) == B.MOE_ERR_INVALID_ARG            # no host losses buffer
+    assert fwd_b(ctypes.byref(s), 2, None, fake, fake, fake, fake, fake,
+                 *tail) == B.MOE_ERR_INVALID_ARG            # no host tokens
+    assert fwd_b(ctypes.byref(s), 2, fake, fake, fake, fake, fake, fake,
+                 *tail[:13], fake, need - 1, None, None, None) == B.MOE_ERR_WORKSPACE
+    assert fwd_b(ctypes.byref(s), 0, fake, fake, fake, fake, fake, fake, *tail) == B.MOE_OK
+    ec = shape(flags=B.MOE_FLAG_EXPERT_CHOICE)
+    assert fwd_b(ctypes.byref(ec), 1, fake, fake, fake, fake, fake, fake,
+                 *tail) == B.MOE_ERR_INVALID_ARG
     assert lib.moe_pack_w13(1, 100, 64, fake, fake, fake, None) == B.MOE_ERR_UNSUPPORTED
     assert lib.moe_set_wait_timeout_ns(0) == B.MOE_ERR_INVALID_ARG
 

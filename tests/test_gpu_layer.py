@@ -199,6 +199,43 @@ def test_host_io_entry_matches_device_entry():
     assert losses[0].item() == dev_out.bal and losses[1].item() == dev_out.z
 
 
+@pytest.mark.parametrize("n_batches,same_stream", [(5, False), (1, False), (3, True)])
+def test_host_batches_stream_matches_per_batch_calls(n_batches, same_stream):
+    """The double-buffered host stream (copy-in, layer and copy-out on three
+    streams) gives, batch for batch, the bits of separate layer calls."""
+    w = CASES["ragged_shared"]
+    inp = synth.make_inputs(w, "cuda")
+    layer = moe.MoELayer(shape_of(w), inp.wr, inp.w1, inp.w3, inp.w2, inp.ws1, inp.ws3,
+                         inp.ws2, inp.offset, inp.sel_bias)
+    xs = [synth.make_inputs(w.replace(seed=w.seed + 100 + i), "cuda").x for i in range(n_batches)]
+    expect = []
+    for x in xs:
+        layer.forward(x)
+        torch.cuda.synchronize()
+        expect.append((layer.y.cpu().clone(), layer.losses.cpu().clone()))
+    x_host = torch.stack([x.cpu() for x in xs]).pin_memory()
+    y_host = torch.zeros_like(x_host).pin_memory()
+    losses = torch.zeros(n_batches, 2, dtype=torch.float32).pin_memory()
+    x_dev = torch.empty((2,) + tuple(inp.x.shape), dtype=inp.x.dtype, device="cuda")
+    y_dev = torch.empty_like(x_dev)
+    loss_dev = torch.empty(2, 2, dtype=torch.float32, device="cuda")
+    main = torch.cuda.current_stream()
+    h2d = main if same_stream else torch.cuda.Stream()
+    d2h = main if same_stream else torch.cuda.Stream()
+    moe.moe_layer_forward_host_batches(
+        layer.shape, x_host, y_host, losses, x_dev, y_dev, loss_dev, layer.w_router,
+        layer.logit_offset, layer.sel_bias, layer.w13, layer.w2, layer.w13_shared,
+        layer.w2_shared, layer.ids, layer.gates, layer.counts, layer.drop_mask, layer.f,
+        layer.P, layer.ws, main, h2d, d2h)
+    for i, (y, l) in enumerate(expect):
+        assert torch.equal(y_host[i].view(torch.int16), y.view(torch.int16)), i
+        assert torch.equal(losses[i], l), i
+    # the device outputs hold the last batch's routing
+    ref_last = run_layer(synth.make_inputs(w.replace(seed=w.seed + 100 + n_batches - 1), "cuda"),
+                         layer)
+    assert torch.equal(y_host[-1].view(torch.int16), ref_last.y.cpu().view(torch.int16))
+
+
 def test_bounded_wait_reports_timeout():
     s = shape_of(CASES["tiny"])
     ws = moe._binding.alloc_workspace(s)

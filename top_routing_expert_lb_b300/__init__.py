@@ -7,7 +7,8 @@ the library has not been built.
 """
 from ._binding import (  # noqa: F401
     MoeError, Shape, lib, moe_capacity, moe_check_status, moe_combine, moe_debug_timeout_probe,
-    moe_error_string, moe_grouped_ffn, moe_layer_forward, moe_layer_forward_host, moe_max_rows,
+    moe_error_string, moe_grouped_ffn, moe_layer_forward, moe_layer_forward_host,
+    moe_layer_forward_host_batches, moe_max_rows,
     moe_pack_w13, moe_permute, moe_route, moe_set_wait_timeout_ns, moe_workspace_size,
     MoELayer, moe_profile_enable, moe_profile_collect, moe_launch_count, alloc_workspace,
     moe_route_noalloc, moe_route_ex, MOE_FLAG_SIGMOID, MOE_FLAG_NO_RENORM,

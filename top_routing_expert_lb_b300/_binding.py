@@ -79,6 +79,7 @@ def lib():
     L.moe_combine.argtypes = [S] + [_P] * 5 + [_P]
     L.moe_layer_forward.argtypes = [S] + [_P] * 17 + [_P, sz, _P]
     L.moe_layer_forward_host.argtypes = [S] + [_P] * 20 + [_P, sz, _P]
+    L.moe_layer_forward_host_batches.argtypes = [S, ctypes.c_int32] + [_P] * 20 + [sz] + [_P] * 3
     L.moe_check_status.argtypes = [_P, ctypes.POINTER(ctypes.c_int), _P]
     L.moe_set_wait_timeout_ns.argtypes = [u64]
     L.moe_debug_timeout_probe.argtypes = [_P, sz, _P]
@@ -93,7 +94,7 @@ def lib():
     L.moe_ec_layer_forward.argtypes = [S] + [_P] * 15 + [_P, sz, _P]
     for name in ("moe_workspace_size", "moe_capacity", "moe_max_rows", "moe_pack_w13",
                  "moe_route", "moe_permute", "moe_grouped_ffn", "moe_combine",
-                 "moe_layer_forward", "moe_layer_forward_host", "moe_check_status",
+                 "moe_layer_forward", "moe_layer_forward_host", "moe_layer_forward_host_batches", "moe_check_status",
                  "moe_set_wait_timeout_ns", "moe_debug_timeout_probe", "moe_profile_enable",
                  "moe_profile_collect", "moe_launch_count", "moe_route_noalloc",
                  "moe_route_ex", "moe_alf_bias_update"):
@@ -240,6 +241,24 @@ def moe_layer_forward_host(shape, x_host, x_dev, w_router, logit_offset, sel_bia
         ctypes.c_void_p(losses_host.data_ptr()), _ptr(ids), _ptr(gates), _ptr(counts),
         _ptr(drop_mask), _ptr(f), _ptr(P), _ptr(bal_loss), _ptr(z_loss), _ptr(ws), ws.numel(),
         _stream(stream)), "moe_layer_forward_host")
+
+
+def moe_layer_forward_host_batches(shape, x_host, y_host, losses_host, x_dev, y_dev, loss_dev,
+                                   w_router, logit_offset, sel_bias, w13, w2, w13_shared,
+                                   w2_shared, ids, gates, counts, drop_mask, f, P, ws, stream=None,
+                                   h2d_stream=None, d2h_stream=None):
+    """x_host / y_host: [n][T][d] bf16 host tensors (pinned for overlap);
+    losses_host [n][2] fp32 host; x_dev / y_dev [2][T][d], loss_dev [2][2]."""
+    n = x_host.shape[0] if x_host.dim() == 3 else 0
+    if y_host.shape != x_host.shape or losses_host.numel() < 2 * n:
+        raise ValueError("moe_layer_forward_host_batches: host buffer shapes")
+    _check(lib().moe_layer_forward_host_batches(
+        ctypes.byref(shape), n, ctypes.c_void_p(x_host.data_ptr()),
+        ctypes.c_void_p(y_host.data_ptr()), ctypes.c_void_p(losses_host.data_ptr()), _ptr(x_dev),
+        _ptr(y_dev), _ptr(loss_dev), _ptr(w_router), _ptr(logit_offset), _ptr(sel_bias),
+        _ptr(w13), _ptr(w2), _ptr(w13_shared), _ptr(w2_shared), _ptr(ids), _ptr(gates),
+        _ptr(counts), _ptr(drop_mask), _ptr(f), _ptr(P), _ptr(ws), ws.numel(), _stream(stream),
+        _stream(h2d_stream), _stream(d2h_stream)), "moe_layer_forward_host_batches")
 
 
 def moe_ec_capacity(shape: Shape) -> int:

@@ -806,6 +806,81 @@ int moe_layer_forward_host(const moe_shape_t* s, const uint16_t* x_host, uint16_
   return cudaStreamSynchronize(st) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
+int moe_layer_forward_host_batches(
+    const moe_shape_t* s, int32_t n_batches, const uint16_t* x_host, uint16_t* y_host,
+    float* losses_host, uint16_t* x_dev, uint16_t* y_dev, float* loss_dev,
+    const uint16_t* w_router, const float* logit_offset, const float* sel_bias,
+    const uint16_t* w13, const uint16_t* w2, const uint16_t* w13_shared, const uint16_t* w2_shared,
+    int32_t* ids, float* gates, int32_t* counts, uint8_t* drop_mask, float* f, float* P,
+    void* ws, size_t ws_bytes, void* stream, void* h2d_stream, void* d2h_stream) {
+  int rc = check_shape(s);
+  if (rc != MOE_OK) return rc;
+  if (n_batches < 0 || !losses_host || !loss_dev) return MOE_ERR_INVALID_ARG;
+  if (s->T > 0 && (!x_host || !x_dev || !y_dev || !y_host)) return MOE_ERR_INVALID_ARG;
+  if (is_ec(s)) return MOE_ERR_INVALID_ARG;
+  Layout L;  // the workspace is checked before anything is enqueued
+  if ((rc = check_ws(s, ws, ws_bytes, &L)) != MOE_OK) return rc;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  cudaStream_t hs = static_cast<cudaStream_t>(h2d_stream);
+  cudaStream_t ds = static_cast<cudaStream_t>(d2h_stream);
+  if (n_batches == 0) return MOE_OK;
+  const size_t elems = static_cast<size_t>(s->T) * s->d;
+  const size_t bytes = elems * 2;
+  // per slot: x copied in, layer done, y and losses copied out
+  cudaEvent_t in_done[2] = {}, fwd_done[2] = {}, out_done[2] = {};
+  bool ev_ok = true;
+  for (int a = 0; a < 2; ++a)
+    ev_ok = ev_ok &&
+            cudaEventCreateWithFlags(&in_done[a], cudaEventDisableTiming) == cudaSuccess &&
+            cudaEventCreateWithFlags(&fwd_done[a], cudaEventDisableTiming) == cudaSuccess &&
+            cudaEventCreateWithFlags(&out_done[a], cudaEventDisableTiming) == cudaSuccess;
+  auto ok = [](cudaError_t e) { return e == cudaSuccess; };
+  rc = ev_ok ? MOE_OK : MOE_ERR_CUDA;
+  for (int32_t i = 0; i < n_batches && rc == MOE_OK; ++i) {
+    const int a = i & 1;
+    uint16_t* xd = x_dev + a * elems;
+    uint16_t* yd = y_dev + a * elems;
+    float* ld = loss_dev + 2 * a;
+    // copy in batch i once the layer of batch i-2 has read this x slot
+    if (i >= 2 && !ok(cudaStreamWaitEvent(hs, fwd_done[a], 0))) { rc = MOE_ERR_CUDA; break; }
+    if (bytes && !ok(cudaMemcpyAsync(xd, x_host + i * elems, bytes, cudaMemcpyHostToDevice, hs))) {
+      rc = MOE_ERR_CUDA;
+      break;
+    }
+    if (!ok(cudaEventRecord(in_done[a], hs)) || !ok(cudaStreamWaitEvent(cs, in_done[a], 0))) {
+      rc = MOE_ERR_CUDA;
+      break;
+    }
+    // the layer may overwrite this y slot once batch i-2 has been copied out
+    if (i >= 2 && !ok(cudaStreamWaitEvent(cs, out_done[a], 0))) { rc = MOE_ERR_CUDA; break; }
+    rc = moe_layer_forward(s, xd, w_router, logit_offset, sel_bias, w13, w2, w13_shared,
+                           w2_shared, yd, ids, gates, counts, drop_mask, f, P, ld, ld + 1, ws,
+                           ws_bytes, stream);
+    if (rc != MOE_OK) break;
+    if (!ok(cudaEventRecord(fwd_done[a], cs)) || !ok(cudaStreamWaitEvent(ds, fwd_done[a], 0))) {
+      rc = MOE_ERR_CUDA;
+      break;
+    }
+    if ((bytes && !ok(cudaMemcpyAsync(y_host + i * elems, yd, bytes, cudaMemcpyDeviceToHost, ds))) ||
+        !ok(cudaMemcpyAsync(losses_host + 2 * static_cast<size_t>(i), ld, 8,
+                            cudaMemcpyDeviceToHost, ds)) ||
+        !ok(cudaEventRecord(out_done[a], ds))) {
+      rc = MOE_ERR_CUDA;
+      break;
+    }
+  }
+  // wait for everything enqueued so far, whether or not a step failed
+  const bool synced = ok(cudaStreamSynchronize(hs)) & ok(cudaStreamSynchronize(cs)) &
+                      ok(cudaStreamSynchronize(ds));
+  for (int a = 0; a < 2; ++a) {
+    if (in_done[a]) cudaEventDestroy(in_done[a]);
+    if (fwd_done[a]) cudaEventDestroy(fwd_done[a]);
+    if (out_done[a]) cudaEventDestroy(out_done[a]);
+  }
+  if (rc == MOE_OK && !synced) rc = MOE_ERR_CUDA;
+  return rc;
+}
+
 int moe_alf_bias_update(const moe_shape_t* s, const int32_t* counts, float gamma, float* bias,
                         void* stream) {
   const int rc = check_shape(s);
