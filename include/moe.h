@@ -371,6 +371,10 @@ int moe_route_noalloc(const moe_shape_t *shape, const uint16_t *x, const uint16_
  *   MOE_GEMM_TAIL_MAX_N=n    a group's last m-tile with r rows runs transposed
  *                            (weights as the MMA's M) when r rounded up to 16
  *                            is <= n (default 112; 0 never)
+ *   MOE_GEMM_NBLOCK=b        tile order inside a group with more rows than
+ *                            MOE_GEMM_BLOCK_MIN_ROWS (default 2048): blocks of
+ *                            b n-tiles, m-tile major inside a block (default 8;
+ *                            0 or 1: n-tile major, m-tile minor throughout)
  *   MOE_FUSED_GATHER=1       moe_layer_forward: the gate/up projection gathers
  *                            token rows itself (TMA 4-row gathers), no x_perm
  *   MOE_GATE_IN_EPILOGUE=1   moe_layer_forward / moe_ec_layer_forward: the down

@@ -487,6 +487,8 @@ int do_ffn(const moe_shape_t* s, const uint16_t* x_perm, const int32_t* offsets,
   g1.timeout_ns = g_timeout_ns;
   g1.gather_rows = routed ? gather_rows : nullptr;
   if (const char* env = std::getenv("MOE_GEMM_TAIL_MAX_N")) g1.tail_max_n = std::atoi(env);
+  if (const char* env = std::getenv("MOE_GEMM_NBLOCK")) g1.n_block = std::atoi(env);
+  if (const char* env = std::getenv("MOE_GEMM_BLOCK_MIN_ROWS")) g1.block_min_rows = std::atoi(env);
   int rc = 0;
   if (split1) {
     GroupedGemmArgs g1p = g1;

@@ -18,7 +18,9 @@
 //     one tile overlaps the main loop of the next.
 //   * Persistent grid (one CTA per SM).  Tiles are numbered group by group,
 //     n-tile major / m-tile minor inside a group, so CTAs running at the same
-//     time share a weight tile through L2; row counts come from device
+//     time share a weight tile through L2 (groups with many rows go in blocks
+//     of a few n-tiles, m-tile major inside a block, so a wave also shares
+//     its A rows instead of sweeping the whole group); row counts come from device
 //     offsets (no host synchronisation), ragged m-tiles are masked in the
 //     epilogue, and rows past a group's end are computed but never stored.
 //   * Every wait is bounded; on expiry the kernel records a timeout in the
@@ -100,11 +102,26 @@ __device__ __forceinline__ TileInfo decode_tile(const Tail* st, const GroupedGem
   const int rows = st->rows[lo];
   const int mt = (rows + bm - 1) / bm;
   const int local = tile - st->prefix[lo];
-  ti.n = local / mt;
-  const int m = local - ti.n * mt;
+  const int ncols = ti.shared ? p.n_cols_shared : p.n_cols_routed;
+  const int nt = ncols / bn;
+  int m;
+  if (p.n_block > 1 && rows > p.block_min_rows && nt > 1) {
+    // long group: blocks of n_block n-tiles, m-tile major inside a block, so
+    // the CTAs of one wave share a few A rows and a few weight tiles instead of
+    // sweeping every A row of the group once per n-tile
+    const int nb = p.n_block;
+    const int b = local / (mt * nb);
+    const int n0 = b * nb;
+    const int w = min(nb, nt - n0);
+    const int j = local - b * (mt * nb);
+    m = j / w;
+    ti.n = n0 + (j - m * w);
+  } else {
+    ti.n = local / mt;
+    m = local - ti.n * mt;
+  }
   ti.a_row = st->row0[lo] + m * bm;
   ti.rows_left = rows - m * bm;
-  const int ncols = ti.shared ? p.n_cols_shared : p.n_cols_routed;
   const int e = lo - has_shared;
   ti.b_row = (ti.shared ? 0 : e * ncols) + ti.n * bn;
   ti.nk = (ti.shared ? p.k_shared : p.k_routed) / kBK;

@@ -45,6 +45,11 @@ struct GroupedGemmArgs {
   // Plain projection only: routed output row r is scaled by row_scale[r]
   // (fp32, before rounding); the shared group is never scaled.
   const float* row_scale = nullptr;
+  // Tile order inside a group with more than block_min_rows rows: blocks of
+  // n_block n-tiles, m-tile major inside a block (n_block <= 1: n-tile major
+  // throughout).  Not with multicast.
+  int32_t n_block = 8;
+  int32_t block_min_rows = 2048;
 };
 
 // A0/A1: activations [rows][K] (routed / shared), B0/B1: weights [rows][K].
