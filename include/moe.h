@@ -111,7 +111,10 @@ typedef struct moe_shape {
 const char *moe_error_string(int code);
 
 /* Bytes of device workspace every other entry point needs for this shape
- * (written to *bytes, a host pointer).  Pure host computation.               */
+ * (written to *bytes, a host pointer).  Pure host computation.  Zero the
+ * workspace once before its first use (e.g. cudaMemset): it holds a status
+ * word and counters that must start at zero; every call leaves them at zero
+ * again, so later calls need no clearing.                                    */
 int moe_workspace_size(const moe_shape_t *shape, size_t *bytes);
 
 /* Expert capacity C (host pointer *C): ceil(c*k*T/E), or -1 when dropless.  */
@@ -360,7 +363,14 @@ int moe_route_noalloc(const moe_shape_t *shape, const uint16_t *x, const uint16_
 /* Expert-GEMM variants, read from the environment at every grouped-FFN
  * launch (the defaults are the measured fastest; every variant gives
  * parity-tested results, most bit-identical to the default):
- *   MOE_GEMM_TILE=256        both projections on 256 x 256 CTA-pair tiles
+ *   MOE_GEMM_TILE=128|256    the gate/up projection on single-CTA 128 x 256 or
+ *                            CTA-pair 256 x 256 tiles (256 also puts the down
+ *                            projection on pairs; default: pairs when E <= 16,
+ *                            experts average >= 512 rows and rows are not
+ *                            gathered)
+ *   MOE_GEMM_DYNAMIC=0|1     CTA-pair launches take tiles in a static
+ *                            round-robin order (0) or from a tile counter in
+ *                            the workspace (1; default when K >= 4096)
  *   MOE_GEMM2_TILE=128|256   the down projection on single-CTA 128 x BN or
  *                            CTA-pair 256 x 256 tiles (default: pairs when
  *                            d % 256 == 0 and experts average >= 512 rows)

@@ -383,11 +383,15 @@ int do_ec_route(const moe_shape_t* s, const uint16_t* x, const uint16_t* wr, con
   return cuda_rc(tracked(MOE_KERNEL_SELECT, st, [&] { return launch_ec_select(ea, st); }));
 }
 
-// 128-row tiles on single CTAs by default (measured faster on every workload
-// so far); 256-row tiles on CTA pairs with MOE_GEMM_TILE=256.
-bool gemm_paired() {
+// Gate/up projection tile: MOE_GEMM_TILE=256 forces 256-row tiles on CTA
+// pairs, =128 single-CTA 128-row tiles; unset, the layer picks by the
+// average rows per expert (see do_ffn).  Returns 1, 0 or -1 (unset).
+int gemm_tile_env() {
   const char* env = std::getenv("MOE_GEMM_TILE");
-  return env != nullptr && std::strcmp(env, "256") == 0;
+  if (env == nullptr) return -1;
+  if (std::strcmp(env, "256") == 0) return 1;
+  if (std::strcmp(env, "128") == 0) return 0;
+  return -1;
 }
 
 // With MOE_FUSED_GATHER=1 the layer feeds GEMM-1 straight from the token
@@ -408,7 +412,7 @@ bool gate_in_epilogue() {
 bool fused_gather() {
   const char* env = std::getenv("MOE_FUSED_GATHER");
   if (env == nullptr || std::strcmp(env, "1") != 0) return false;
-  return !gemm_paired();
+  return gemm_tile_env() != 1;
 }
 
 // x_perm: routed rows, or null with gather_rows (token row of every routed
@@ -427,8 +431,21 @@ int do_ffn(const moe_shape_t* s, const uint16_t* x_perm, const int32_t* offsets,
   uint16_t* h_s = at<uint16_t>(ws, L.h_s);
   const int bn2 = (d % 256 == 0) ? 256 : (d % 128 == 0 ? 128 : 64);
   const int nsm = sm_count_cached();
-  const bool paired = gemm_paired();
-  if (paired && gather_rows != nullptr) return MOE_ERR_INVALID_ARG;  // needs x_perm
+  const int64_t rows_per_expert =
+      L.r >= 0 ? L.r : (E > 0 ? (static_cast<int64_t>(T) * s->k) / E : 0);
+  // The gate/up projection runs on 256 x 256 CTA-pair tiles for a few large
+  // experts (at most 16, averaging at least 512 rows): the pair halves the
+  // weight bytes each SM stages per FLOP, and with the dynamic tile order its
+  // DRAM traffic is the algorithmic one; it measured 1.7 % faster steps than
+  // single-CTA tiles on Mixtral although each expert's last tile is padded to
+  // 256 rows.  With many experts of skewed sizes (DeepSeekMoE-16B) that
+  // padding cost 13 % in this projection, so single-CTA tiles (transposed
+  // tails) stay the default there.  Gathered rows need the single-CTA kernel.
+  const int tile_env = gemm_tile_env();
+  if (tile_env == 1 && gather_rows != nullptr) return MOE_ERR_INVALID_ARG;  // needs x_perm
+  const bool paired =
+      gather_rows == nullptr &&
+      (tile_env == 1 || (tile_env < 0 && rows_per_expert >= 512 && E <= 16));
   // MOE_GEMM_MC=1: clusters of two CTAs sharing each B tile through TMA
   // multicast (half the B bytes from L2 per tile; measured slower than
   // independent CTAs on every workload, so off by default); not with the
@@ -442,8 +459,6 @@ int do_ffn(const moe_shape_t* s, const uint16_t* x_perm, const int32_t* offsets,
   // single-CTA tiles (two launches, both counted as the gate/up kernel).
   // Measured 9 % slower than single-CTA tiles throughout on Mixtral, so off
   // by default.
-  const int64_t rows_per_expert =
-      L.r >= 0 ? L.r : (E > 0 ? (static_cast<int64_t>(T) * s->k) / E : 0);
   bool split1 = false;
   if (const char* env = std::getenv("MOE_GEMM1_SPLIT")) split1 = std::strcmp(env, "1") == 0;
   split1 = split1 && !paired && !mc1 && gather_rows == nullptr && nsm >= 2;
@@ -488,6 +503,21 @@ int do_ffn(const moe_shape_t* s, const uint16_t* x_perm, const int32_t* offsets,
   g1.gather_rows = routed ? gather_rows : nullptr;
   if (const char* env = std::getenv("MOE_GEMM_TAIL_MAX_N")) g1.tail_max_n = std::atoi(env);
   if (const char* env = std::getenv("MOE_GEMM_NBLOCK")) g1.n_block = std::atoi(env);
+  // CTA-pair launches with long tiles (K >= 4096) take their tiles from a
+  // counter in the workspace: the dynamic order keeps the pairs that share a
+  // weight tile in step (Mixtral: DRAM bytes of the gate/up projection down
+  // from 2.7 GB to the algorithmic 1.95 GB).  With short tiles on skewed
+  // shapes (DeepSeekMoE-16B, K = 1408) the static round-robin order measured
+  // 3 % faster.  MOE_GEMM_DYNAMIC=0|1 forces either order.
+  int dyn_env = -1;
+  if (const char* env = std::getenv("MOE_GEMM_DYNAMIC")) dyn_env = std::atoi(env) != 0 ? 1 : 0;
+  int* tile_counter = at<int>(ws, L.status + 128);
+  auto dynamic_for = [&](int64_t K) {
+    return (dyn_env == 1 || (dyn_env < 0 && K >= 4096)) ? tile_counter : nullptr;
+  };
+  g1.tile_counter = dynamic_for(d);
+  if (const char* env = std::getenv("MOE_GEMM_L2A")) g1.l2_hint_a = std::atoi(env);
+  if (const char* env = std::getenv("MOE_GEMM_L2B")) g1.l2_hint_b = std::atoi(env);
   if (const char* env = std::getenv("MOE_GEMM_BLOCK_MIN_ROWS")) g1.block_min_rows = std::atoi(env);
   int rc = 0;
   if (split1) {
@@ -532,6 +562,7 @@ int do_ffn(const moe_shape_t* s, const uint16_t* x_perm, const int32_t* offsets,
   if (!routed) { a0 = a1; b0 = b1; }
   if (!shared) { a1 = a0; b1 = b0; }
   GroupedGemmArgs g2 = g1;
+  g2.tile_counter = dynamic_for(M);
   g2.gather_rows = nullptr;
   g2.row_scale = routed ? row_scale : nullptr;
   g2.n_cols_routed = static_cast<int32_t>(d);

@@ -575,6 +575,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ---------------------------------------------------------------------------
 constexpr int kPairBM = 256;
 constexpr int kPairStages = 6;
+constexpr int kTileQ = 4;  // tile queue depth (dynamic schedule)
+// consumers of a queue slot, counted on the even CTA's q_empty: its MMA warp
+// and 4 epilogue warps, the odd CTA's producer and 4 epilogue warps
+constexpr int kTileQConsumers = 10;
 
 struct PairSmemTail {
   uint64_t full[kPairStages];
@@ -582,6 +586,9 @@ struct PairSmemTail {
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t fin;
+  uint64_t q_full[kTileQ];
+  uint64_t q_empty[kTileQ];
+  int qtile[kTileQ];
   uint32_t tmem_base;
   int abort_flag;
   int prefix[kMaxGroups + 1];
@@ -592,6 +599,25 @@ struct PairSmemTail {
 constexpr size_t pair_smem_bytes() {
   return 1024 + static_cast<size_t>(kPairStages) * (128 * kBK * 2 + 128 * kBK * 2) +
          sizeof(PairSmemTail);
+}
+
+// Dynamic schedule of the pair kernel.  The even CTA's producer takes the
+// next tile number from a global counter when it is ready to load it and
+// publishes it in slot q of both CTAs' tile queues; every other role reads the
+// same sequence from its own queue.  Pairs thus take tiles in the order they
+// free up, so the pairs sharing a weight tile start it together however far
+// their speeds drift apart.  Consumer side: returns the tile (>= total ends
+// the loop) or -1 when the wait ran out.
+__device__ __forceinline__ int pair_next_tile(PairSmemTail* st, int q_pos,
+                                              const GroupedGemmArgs& p,
+                                              volatile int* abort_flag) {
+  const int q = q_pos % kTileQ;
+  const uint32_t ph = static_cast<uint32_t>(q_pos / kTileQ) & 1u;
+  if (!mbar_wait_bounded<true>(&st->q_full[q], ph, p.timeout_ns, p.status, abort_flag))
+    return -1;
+  const int t = *reinterpret_cast<volatile int*>(&st->qtile[q]);
+  mbar_arrive_cluster(mapa_shared(smem_u32(&st->q_empty[q]), 0));
+  return t;
 }
 
 template <bool kSwiGLU, bool kRowScale = false>
@@ -632,6 +658,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&st->tempty[a], 8);  // 4 epilogue warps in each CTA of the pair
     }
     mbar_init(&st->fin, 1);
+    for (int q = 0; q < kTileQ; ++q) {
+      mbar_init(&st->q_full[q], 1);
+      mbar_init(&st->q_empty[q], kTileQConsumers);
+    }
     st->abort_flag = 0;
     int acc = 0;
     st->prefix[0] = 0;
@@ -681,12 +711,47 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
+      const uint64_t pol_a = l2_policy(p.l2_hint_a);
+      const uint64_t pol_b = l2_policy(p.l2_hint_b);
       int stage = 0;
       uint32_t phase = 0;
       uint32_t uses[kPairStages];
 #pragma unroll
       for (int s = 0; s < kPairStages; ++s) uses[s] = 0;
-      for (int tile = pair; tile < total && !*abort_flag; tile += npairs) {
+      const bool dyn = p.tile_counter != nullptr;
+      // Even CTA, dynamic schedule: publishes tile number `t` in queue
+      // position `pos` of both CTAs once every reader has freed that slot.
+      auto publish = [&](int pos, int t) -> bool {
+        const int q = pos % kTileQ;
+        const uint32_t ph = static_cast<uint32_t>(pos / kTileQ) & 1u;
+        if (!mbar_wait_bounded<true>(&st->q_empty[q], ph ^ 1u, p.timeout_ns, p.status,
+                                     abort_flag))
+          return false;
+        st->qtile[q] = t;
+        st_shared_cluster_u32(mapa_shared(smem_u32(&st->qtile[q]), 1), static_cast<uint32_t>(t));
+        mbar_arrive_cluster(mapa_shared(smem_u32(&st->q_full[q]), 0));
+        mbar_arrive_cluster(mapa_shared(smem_u32(&st->q_full[q]), 1));
+        return true;
+      };
+      int cur = 0;  // even CTA, dynamic: the tile published at q_pos
+      if (dyn && leader) {
+        cur = atomicAdd(p.tile_counter, 1);
+        if (!publish(0, cur)) cur = total;
+      }
+      for (int tile = pair, q_pos = 0; !*abort_flag; tile += npairs, ++q_pos) {
+        if (dyn) {
+          if (leader) {
+            tile = cur;
+          } else if ((tile = pair_next_tile(st, q_pos, p, abort_flag)) < 0) {
+            break;
+          }
+        }
+        if (tile >= total) break;
+        // the next tile number is taken now and published during this tile's
+        // first k-blocks, so neither CTA waits for it at the tile boundary
+        int next = 0;
+        if (dyn && leader) next = atomicAdd(p.tile_counter, 1);
+        bool published = !(dyn && leader);
         const TileInfo ti = decode_tile(st, p, G, tile, BN, kPairBM);
         const CUtensorMap* am = ti.shared ? &tmA1 : &tmA0;
         const CUtensorMap* bm = ti.shared ? &tmB1 : &tmB0;
@@ -702,14 +767,30 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* sa = smem + stage * kStageBytes;
           const uint32_t full_leader = mapa_shared(smem_u32(&st->full[stage]), 0);
           if (leader) mbar_arrive_expect_tx(&st->full[stage], 2 * kStageBytes);
-          tma_load_2d_pair(sa, am, full_leader, kb * kBK, a_row);
-          tma_load_2d_pair(sa + kABytes, bm, full_leader, kb * kBK, b_row);
+          if (p.l2_hint_a != 0)
+            tma_load_2d_pair_hint(sa, am, full_leader, kb * kBK, a_row, pol_a);
+          else
+            tma_load_2d_pair(sa, am, full_leader, kb * kBK, a_row);
+          if (p.l2_hint_b != 0)
+            tma_load_2d_pair_hint(sa + kABytes, bm, full_leader, kb * kBK, b_row, pol_b);
+          else
+            tma_load_2d_pair(sa + kABytes, bm, full_leader, kb * kBK, b_row);
           uses[stage] += 1;
           if (++stage == kPairStages) {
             stage = 0;
             phase ^= 1u;
           }
+          if (!published && (kb == 1 || kb == ti.nk - 1)) {
+            if (!publish(q_pos + 1, next)) {
+              ok = false;
+              break;
+            }
+            published = true;
+          }
         }
+        if (ok && !published) ok = publish(q_pos + 1, next);
+        if (!ok) break;
+        cur = next;
         if (!ok) break;
       }
       // Drain (even CTA): its full barriers count the bytes of both CTAs, so
@@ -730,7 +811,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       int local = 0;
-      for (int tile = pair; tile < total && !*abort_flag; tile += npairs, ++local) {
+      const bool dyn = p.tile_counter != nullptr;
+      for (int tile = pair; !*abort_flag; tile += npairs, ++local) {
+        if (dyn && (tile = pair_next_tile(st, local, p, abort_flag)) < 0) break;
+        if (tile >= total) break;
         const TileInfo ti = decode_tile(st, p, G, tile, BN, kPairBM);
         const int a = local & 1;
         const uint32_t q = static_cast<uint32_t>(local >> 1);
@@ -774,7 +858,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tempty_leader0 = mapa_shared(smem_u32(&st->tempty[0]), 0);
     const uint32_t tempty_leader1 = mapa_shared(smem_u32(&st->tempty[1]), 0);
     int local = 0;
-    for (int tile = pair; tile < total && !*abort_flag; tile += npairs, ++local) {
+    const bool dyn = p.tile_counter != nullptr;
+    for (int tile = pair; !*abort_flag; tile += npairs, ++local) {
+      if (dyn) {
+        int t = 0;
+        if (lane == 0) t = pair_next_tile(st, local, p, abort_flag);
+        tile = __shfl_sync(0xffffffffu, t, 0);
+        if (tile < 0) break;
+      }
+      if (tile >= total) break;
       const TileInfo ti = decode_tile(st, p, G, tile, BN, kPairBM);
       const int a = local & 1;
       const uint32_t q = static_cast<uint32_t>(local >> 1);
@@ -846,6 +938,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   cluster_arrive_wait();
   tc_fence_after();
   if (warp == 1) tmem_dealloc_pair(tmem_base, kTmemCols);
+  // The last CTA out puts the tile counter back to zero for the next launch
+  // (every CTA has taken its last tile before it counts itself out).
+  if (p.tile_counter != nullptr && threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(p.tile_counter + 1, 1) == static_cast<int>(gridDim.x) - 1) {
+      atomicExch(p.tile_counter, 0);
+      atomicExch(p.tile_counter + 1, 0);
+    }
+  }
 }
 
 template <bool kSwiGLU, bool kRowScale = false>
