@@ -516,8 +516,6 @@ int do_ffn(const moe_shape_t* s, const uint16_t* x_perm, const int32_t* offsets,
     return (dyn_env == 1 || (dyn_env < 0 && K >= 4096)) ? tile_counter : nullptr;
   };
   g1.tile_counter = dynamic_for(d);
-  if (const char* env = std::getenv("MOE_GEMM_L2A")) g1.l2_hint_a = std::atoi(env);
-  if (const char* env = std::getenv("MOE_GEMM_L2B")) g1.l2_hint_b = std::atoi(env);
   if (const char* env = std::getenv("MOE_GEMM_BLOCK_MIN_ROWS")) g1.block_min_rows = std::atoi(env);
   int rc = 0;
   if (split1) {

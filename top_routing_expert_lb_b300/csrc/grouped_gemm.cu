@@ -711,8 +711,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      const uint64_t pol_a = l2_policy(p.l2_hint_a);
-      const uint64_t pol_b = l2_policy(p.l2_hint_b);
       int stage = 0;
       uint32_t phase = 0;
       uint32_t uses[kPairStages];
@@ -767,14 +765,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* sa = smem + stage * kStageBytes;
           const uint32_t full_leader = mapa_shared(smem_u32(&st->full[stage]), 0);
           if (leader) mbar_arrive_expect_tx(&st->full[stage], 2 * kStageBytes);
-          if (p.l2_hint_a != 0)
-            tma_load_2d_pair_hint(sa, am, full_leader, kb * kBK, a_row, pol_a);
-          else
-            tma_load_2d_pair(sa, am, full_leader, kb * kBK, a_row);
-          if (p.l2_hint_b != 0)
-            tma_load_2d_pair_hint(sa + kABytes, bm, full_leader, kb * kBK, b_row, pol_b);
-          else
-            tma_load_2d_pair(sa + kABytes, bm, full_leader, kb * kBK, b_row);
+          tma_load_2d_pair(sa, am, full_leader, kb * kBK, a_row);
+          tma_load_2d_pair(sa + kABytes, bm, full_leader, kb * kBK, b_row);
           uses[stage] += 1;
           if (++stage == kPairStages) {
             stage = 0;

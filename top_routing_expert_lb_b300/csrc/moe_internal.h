@@ -50,10 +50,6 @@ struct GroupedGemmArgs {
   // throughout).  Not with multicast.
   int32_t n_block = 8;
   int32_t block_min_rows = 2048;
-  // Pair kernel: L2 eviction priority of the A / B tile loads (0 normal,
-  // 1 evict first, 2 evict last).
-  int32_t l2_hint_a = 0;
-  int32_t l2_hint_b = 0;
   // Pair kernel: when set, tiles are taken dynamically from this counter
   // ([0] next tile, [1] CTAs done; both zero before the launch, and left zero
   // by it); null: static round-robin schedule.

@@ -334,31 +334,6 @@ __device__ __forceinline__ void tma_load_2d_pair(void* dst, const void* tmap, ui
       : "memory");
 }
 
-// The same load with an L2 eviction-priority policy (from l2_policy).
-__device__ __forceinline__ void tma_load_2d_pair_hint(void* dst, const void* tmap,
-                                                      uint32_t bar_cluster, int32_t c0, int32_t c1,
-                                                      uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar_cluster), "r"(c0), "r"(c1), "l"(policy)
-      : "memory");
-}
-
-// L2 policy for cache-hinted loads: 1 = evict first, 2 = evict last (all of
-// the accessed lines), anything else = evict normal.
-__device__ __forceinline__ uint64_t l2_policy(int kind) {
-  uint64_t pol;
-  if (kind == 1) {
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
-  } else if (kind == 2) {
-    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
-  } else {
-    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
-  }
-  return pol;
-}
-
 // One warp of each CTA of the pair allocates `ncols` TMEM columns together.// One warp of each CTA of the pair allocates `ncols` TMEM columns together.
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
