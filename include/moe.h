@@ -371,6 +371,9 @@ int moe_route_noalloc(const moe_shape_t *shape, const uint16_t *x, const uint16_
  *   MOE_GEMM_DYNAMIC=0|1     CTA-pair launches take tiles in a static
  *                            round-robin order (0) or from a tile counter in
  *                            the workspace (1; default when K >= 4096)
+ *   MOE_GEMM_HALF=0          CTA-pair launches pad a group's last tile of at
+ *                            most 128 rows to a 256-row tile instead of running
+ *                            it as one M = 128 pair MMA (64 rows per CTA)
  *   MOE_GEMM2_TILE=128|256   the down projection on single-CTA 128 x BN or
  *                            CTA-pair 256 x 256 tiles (default: pairs when
  *                            d % 256 == 0 and experts average >= 512 rows)

@@ -105,8 +105,8 @@ def test_permute(T, E, k, c, d):
 
 
 # --------------------------------------------------------------------------- grouped FFN
-@pytest.mark.parametrize("tile", ["128", "256", "256-static", "128-mc", "128-split", "128-block",
-                                  "256-block"])
+@pytest.mark.parametrize("tile", ["128", "256", "256-static", "256-nohalf", "128-mc", "128-split",
+                                  "128-block", "256-block"])
 @pytest.mark.parametrize("rows,d,M,n_shared,T", [
     ([0, 1, 127, 128, 129, 300], 128, 256, 1, 200),    # empty, single, tile edges
     ([5, 0, 0, 260], 64, 128, 0, 0),                   # d = 64 (second projection N = 64)
@@ -124,9 +124,12 @@ def test_grouped_ffn(rows, d, M, n_shared, T, tile, monkeypatch):
     # 128-split: the gate/up projection's whole 256-row blocks on CTA pairs,
     # the remaining rows on single CTAs; *-block: every group of more than 100
     # rows in blocks of two n-tiles, m-tile major inside a block; CTA pairs take
-    # their tiles from the workspace counter except with 256-static
+    # their tiles from the workspace counter except with 256-static; a group's
+    # last pair tile of at most 128 rows runs as an M = 128 pair MMA except
+    # with 256-nohalf
     monkeypatch.setenv("MOE_GEMM_TILE", tile.split("-")[0])
     monkeypatch.setenv("MOE_GEMM_DYNAMIC", "0" if tile.endswith("static") else "1")
+    monkeypatch.setenv("MOE_GEMM_HALF", "0" if tile.endswith("nohalf") else "1")
     monkeypatch.setenv("MOE_GEMM_NBLOCK", "2" if tile.endswith("block") else "0")
     monkeypatch.setenv("MOE_GEMM_BLOCK_MIN_ROWS", "100")
     monkeypatch.setenv("MOE_GEMM_MC", "1" if tile.endswith("mc") else "0")

@@ -479,6 +479,15 @@ int do_ffn(const moe_shape_t* s, const uint16_t* x_perm, const int32_t* offsets,
   }
   if (!routed) { a0 = a1; b0 = b1; }
   if (!shared) { a1 = a0; b1 = b0; }
+  // pair launches of this projection: the B tensors again with 64-row boxes
+  // (a group's last tile of at most 128 rows loads 64 gate + 64 up rows per CTA)
+  CUtensorMap bh0 = b0, bh1 = b1;
+  if (paired || split1) {
+    if (routed && !make_tmap_bf16(&bh0, w13, E * 2 * M, d, 64)) return MOE_ERR_CUDA;
+    if (shared && !make_tmap_bf16(&bh1, w13s, 2 * Ms, d, 64)) return MOE_ERR_CUDA;
+    if (!routed) bh0 = bh1;
+    if (!shared) bh1 = bh0;
+  }
   CUtensorMap bp0 = b0, bp1 = b1;  // 128-row boxes for the pair launch
   if (split1) {
     if (routed && !make_tmap_bf16(&bp0, w13, E * 2 * M, d, 128)) return MOE_ERR_CUDA;
@@ -516,13 +525,15 @@ int do_ffn(const moe_shape_t* s, const uint16_t* x_perm, const int32_t* offsets,
     return (dyn_env == 1 || (dyn_env < 0 && K >= 4096)) ? tile_counter : nullptr;
   };
   g1.tile_counter = dynamic_for(d);
+  if (const char* env = std::getenv("MOE_GEMM_HALF")) g1.half_tiles = std::atoi(env) != 0 ? 1 : 0;
   if (const char* env = std::getenv("MOE_GEMM_BLOCK_MIN_ROWS")) g1.block_min_rows = std::atoi(env);
   int rc = 0;
   if (split1) {
     GroupedGemmArgs g1p = g1;
     g1p.row_split = 1;
     rc = tracked(MOE_KERNEL_GEMM_SWIGLU, st, [&] {
-      return launch_grouped_gemm(a0, a1, bp0, bp1, g1p, true, 256, true, nsm, st);
+      return launch_grouped_gemm(a0, a1, bp0, bp1, g1p, true, 256, true, nsm, st, false, &bh0,
+                                 &bh1);
     });
     if (rc != 0) return cuda_rc(rc);
     g1.row_split = 2;
@@ -530,7 +541,7 @@ int do_ffn(const moe_shape_t* s, const uint16_t* x_perm, const int32_t* offsets,
   rc = tracked(MOE_KERNEL_GEMM_SWIGLU, st,
                [&] {
                  return launch_grouped_gemm(a0, a1, b0, b1, g1, true, 256, paired, nsm, st,
-                                            mc1);
+                                            mc1, &bh0, &bh1);
                });
   if (rc != 0) return cuda_rc(rc);
   g1.row_split = 0;

@@ -625,10 +625,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA0,
                              const __grid_constant__ CUtensorMap tmA1,
                              const __grid_constant__ CUtensorMap tmB0,
-                             const __grid_constant__ CUtensorMap tmB1, const GroupedGemmArgs p) {
+                             const __grid_constant__ CUtensorMap tmB1,
+                             const __grid_constant__ CUtensorMap tmB0h,
+                             const __grid_constant__ CUtensorMap tmB1h, const GroupedGemmArgs p) {
   constexpr int BN = 256;                 // N of the pair tile
   constexpr int kABytes = 128 * kBK * 2;  // this CTA's A rows
   constexpr int kBBytes = 128 * kBK * 2;  // this CTA's half of B
+  // Half tiles: a group's last tile with at most 128 rows runs as one M = 128
+  // pair MMA (64 A rows per CTA).  Its accumulator puts row i of CTA r
+  // (tile row 64 r + i) in TMEM lanes i and 64 + i: lanes 0-63 hold the
+  // tile's columns 0-127, lanes 64-127 columns 128-255, 128 TMEM columns in
+  // all.  With SwiGLU each CTA then loads 64 gate rows and the matching 64 up
+  // rows of B (tmB0h / tmB1h: 64-row boxes), so that every lane holds the
+  // gate and the up values of the same output columns.
+  constexpr uint32_t kIdescHalf = idesc_bf16_f32(128, BN);
   constexpr int kStageBytes = kABytes + kBBytes;
   constexpr uint32_t kTmemCols = 2 * BN;
   constexpr uint32_t kIdesc = idesc_bf16_f32(kPairBM, BN);
@@ -753,8 +763,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const TileInfo ti = decode_tile(st, p, G, tile, BN, kPairBM);
         const CUtensorMap* am = ti.shared ? &tmA1 : &tmA0;
         const CUtensorMap* bm = ti.shared ? &tmB1 : &tmB0;
-        const int a_row = ti.a_row + static_cast<int>(rank) * 128;
+        const CUtensorMap* bmh = ti.shared ? &tmB1h : &tmB0h;
+        const bool half = (p.half_tiles && ti.rows_left <= 128);
+        const int a_row = ti.a_row + static_cast<int>(rank) * (half ? 64 : 128);
         const int b_row = ti.b_row + static_cast<int>(rank) * 128;
+        // half SwiGLU tile: this CTA's 64 gate rows, then the matching 64 up rows
+        const int g_row = ti.b_row + static_cast<int>(rank) * 64;
         bool ok = true;
         for (int kb = 0; kb < ti.nk; ++kb) {
           if (!mbar_wait_bounded(&st->empty[stage], phase ^ 1u, p.timeout_ns, p.status,
@@ -766,7 +780,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t full_leader = mapa_shared(smem_u32(&st->full[stage]), 0);
           if (leader) mbar_arrive_expect_tx(&st->full[stage], 2 * kStageBytes);
           tma_load_2d_pair(sa, am, full_leader, kb * kBK, a_row);
-          tma_load_2d_pair(sa + kABytes, bm, full_leader, kb * kBK, b_row);
+          if (kSwiGLU && half) {
+            tma_load_2d_pair(sa + kABytes, bmh, full_leader, kb * kBK, g_row);
+            tma_load_2d_pair(sa + kABytes + kBBytes / 2, bmh, full_leader, kb * kBK,
+                             g_row + 128);
+          } else {
+            tma_load_2d_pair(sa + kABytes, bm, full_leader, kb * kBK, b_row);
+          }
           uses[stage] += 1;
           if (++stage == kPairStages) {
             stage = 0;
@@ -815,6 +835,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(a * BN);
+        const uint32_t idesc = (p.half_tiles && ti.rows_left <= 128) ? kIdescHalf : kIdesc;
         bool ok = true;
         for (int kb = 0; kb < ti.nk; ++kb) {
           if (!mbar_wait_bounded(&st->full[stage], phase, p.timeout_ns, p.status, abort_flag)) {
@@ -827,7 +848,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
             tc_mma_bf16_pair(d_tmem, smem_desc_sw128(sa + kk * 32),
-                             smem_desc_sw128(sb + kk * 32), kIdesc, (kb | kk) != 0 ? 1u : 0u);
+                             smem_desc_sw128(sb + kk * 32), idesc, (kb | kk) != 0 ? 1u : 0u);
           }
           tc_commit_pair_mc(&st->empty[stage], 0x3);
           if (++stage == kPairStages) {
@@ -864,7 +885,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t q = static_cast<uint32_t>(local >> 1);
       if (!mbar_wait_bounded(&st->tfull[a], q & 1u, p.timeout_ns, p.status, abort_flag)) break;
       tc_fence_after();
-      const int r_in_tile = static_cast<int>(rank) * 128 + r_in_half;
+      // full tile: TMEM lane = this CTA's tile row; half tile: lanes i and
+      // 64 + i hold row i, columns [0, 128) and [128, 256) of the tile
+      const bool half = (p.half_tiles && ti.rows_left <= 128);
+      const int r_in_tile = static_cast<int>(rank) * (half ? 64 : 128) +
+                            (half ? (r_in_half & 63) : r_in_half);
+      const int col_half = half ? (r_in_half >> 6) : 0;
       const bool valid = r_in_tile < ti.rows_left;
       const int64_t row = static_cast<int64_t>(ti.a_row) + r_in_tile;
       const uint32_t taddr =
@@ -873,12 +899,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                                       : p.out_routed);
       const int64_t ld = ti.shared ? p.ld_shared : p.ld_routed;
       if constexpr (kSwiGLU) {
-        __nv_bfloat16* dst = out + row * ld + static_cast<int64_t>(ti.n) * 128;
+        // full: gate in TMEM columns [0, 128), up in [128, 256); half: this
+        // lane's 64 output columns, gate in [0, 64), up in [64, 128)
+        __nv_bfloat16* dst =
+            out + row * ld + static_cast<int64_t>(ti.n) * 128 + static_cast<int64_t>(col_half) * 64;
+        const int nc = half ? 2 : 4;
+        const uint32_t up = half ? 64u : 128u;
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < nc; ++c) {
           float g[32], u[32];
           tmem_ld32(taddr + c * 32, g);
-          tmem_ld32(taddr + 128 + c * 32, u);
+          tmem_ld32(taddr + up + c * 32, u);
           tmem_ld_wait();
           uint32_t packed[16];
 #pragma unroll
@@ -894,11 +925,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else {
-        __nv_bfloat16* dst = out + row * ld + static_cast<int64_t>(ti.n) * BN;
+        __nv_bfloat16* dst = out + row * ld + static_cast<int64_t>(ti.n) * BN +
+                             static_cast<int64_t>(col_half) * 128;
         float sc = 1.0f;
         if constexpr (kRowScale) sc = (valid && !ti.shared) ? __ldg(p.row_scale + row) : 1.0f;
+        const int nc = half ? 4 : BN / 32;
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
+        for (int c = 0; c < nc; ++c) {
           float v[32];
           tmem_ld32(taddr + c * 32, v);
           tmem_ld_wait();
@@ -943,8 +976,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <bool kSwiGLU, bool kRowScale = false>
 int launch_pair_impl(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b0,
-                     const CUtensorMap& b1, const GroupedGemmArgs& args, int num_sms,
-                     cudaStream_t stream) {
+                     const CUtensorMap& b1, const CUtensorMap& b0h, const CUtensorMap& b1h,
+                     const GroupedGemmArgs& args, int num_sms, cudaStream_t stream) {
   constexpr size_t smem = pair_smem_bytes();
   static_assert(smem <= 227 * 1024, "shared memory budget");
   auto kern = grouped_gemm_pair_kernel<kSwiGLU, kRowScale>;
@@ -967,7 +1000,7 @@ int launch_pair_impl(const CUtensorMap& a0, const CUtensorMap& a1, const CUtenso
   attrs[0].val.clusterDim.z = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, kern, a0, a1, b0, b1, args) != cudaSuccess) return -3;
+  if (cudaLaunchKernelEx(&cfg, kern, a0, a1, b0, b1, b0h, b1h, args) != cudaSuccess) return -3;
   return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }
 
@@ -1057,7 +1090,8 @@ bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t 
 
 int launch_grouped_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b0,
                         const CUtensorMap& b1, const GroupedGemmArgs& args, bool swiglu, int bn,
-                        bool paired, int num_sms, cudaStream_t stream, bool multicast) {
+                        bool paired, int num_sms, cudaStream_t stream, bool multicast,
+                        const CUtensorMap* b0h, const CUtensorMap* b1h) {
   if (args.n_routed + (args.shared_rows > 0 ? 1 : 0) > kMaxGroups) return -2;
   const bool scale = args.row_scale != nullptr;
   if (scale && (swiglu || multicast)) return -2;
@@ -1068,9 +1102,10 @@ int launch_grouped_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUte
   }
   if (paired) {
     if (bn != 256 || num_sms < 2) return -2;
-    if (scale) return launch_pair_impl<false, true>(a0, a1, b0, b1, args, num_sms, stream);
-    return swiglu ? launch_pair_impl<true>(a0, a1, b0, b1, args, num_sms, stream)
-                  : launch_pair_impl<false>(a0, a1, b0, b1, args, num_sms, stream);
+    if (scale) return launch_pair_impl<false, true>(a0, a1, b0, b1, b0, b1, args, num_sms, stream);
+    if (!swiglu) return launch_pair_impl<false>(a0, a1, b0, b1, b0, b1, args, num_sms, stream);
+    if (b0h == nullptr || b1h == nullptr) return -2;  // half tiles need 64-row B boxes
+    return launch_pair_impl<true>(a0, a1, b0, b1, *b0h, *b1h, args, num_sms, stream);
   }
   if (swiglu) {
     if (bn != 256) return -2;

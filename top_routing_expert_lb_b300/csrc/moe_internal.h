@@ -54,6 +54,9 @@ struct GroupedGemmArgs {
   // ([0] next tile, [1] CTAs done; both zero before the launch, and left zero
   // by it); null: static round-robin schedule.
   int* tile_counter = nullptr;
+  // Pair kernel: a group's last tile with at most 128 rows runs as one M = 128
+  // pair MMA (half the padding) instead of a 256-row tile.
+  int32_t half_tiles = 1;
 };
 
 // A0/A1: activations [rows][K] (routed / shared), B0/B1: weights [rows][K].
@@ -64,9 +67,12 @@ struct GroupedGemmArgs {
 // multicast: single-CTA 128 x 256 tiles on clusters of two CTAs that share
 // each B tile (each loads one 128-row half, multicast to both; the B maps
 // then use 128-row boxes); not with paired or gathered rows.
+// b0h / b1h (paired SwiGLU only): the same B tensors with 64-row boxes, for
+// the half-height tiles that end a group with at most 128 rows.
 int launch_grouped_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b0,
                         const CUtensorMap& b1, const GroupedGemmArgs& args, bool swiglu, int bn,
-                        bool paired, int num_sms, cudaStream_t stream, bool multicast = false);
+                        bool paired, int num_sms, cudaStream_t stream, bool multicast = false,
+                        const CUtensorMap* b0h = nullptr, const CUtensorMap* b1h = nullptr);
 
 // Encodes a 2-D bf16 tensor map over a row-major [rows][cols] tensor with a
 // 64-column x box_rows box and 128-byte swizzle.  Returns false on failure.
