@@ -176,6 +176,42 @@ def test_grouped_ffn(rows, d, M, n_shared, T, tile, monkeypatch):
         assert_y_close(bf16_to_f64(y_s), ref_s, "y_shared")
 
 
+def test_grouped_ffn_dynamic_order_repeats(monkeypatch):
+    """CTA-pair launches that take tiles from the workspace counter leave it at
+    zero: back-to-back calls on one workspace (and a run of a different shape
+    on it in between) give the same bits, and the oracle's values."""
+    monkeypatch.setenv("MOE_GEMM_TILE", "256")
+    monkeypatch.setenv("MOE_GEMM_DYNAMIC", "1")
+    dev = "cuda"
+    rows = [300, 0, 513, 77, 256, 129]
+    E, d, M = len(rows), 256, 256
+    R = sum(rows)
+    s_ffn = moe.Shape.of(R, d, M, E, 1, 0)
+    x_perm = synth.normal_bf16(7, synth.TID_X, (R, d), 1.0, dev)
+    offsets = torch.tensor(np.concatenate([[0], np.cumsum(rows)]).astype(np.int32), device=dev)
+    w1 = synth.normal_bf16(7, synth.TID_W1, (E, M, d), 0.05, dev)
+    w3 = synth.normal_bf16(7, synth.TID_W3, (E, M, d), 0.05, dev)
+    w2 = synth.normal_bf16(7, synth.TID_W2, (E, d, M), 0.05, dev)
+    w13 = moe.moe_pack_w13(w1, w3)
+    ws = _ws(s_ffn)
+    outs = []
+    for i in range(3):
+        y = torch.zeros((R, d), dtype=torch.bfloat16, device=dev)
+        moe.moe_grouped_ffn(s_ffn, x_perm, offsets, w13, w2, y, None, None, None, None, ws)
+        if i == 1:   # another grouping on the same workspace in between
+            off2 = torch.tensor([0, R // 2, R, R, R, R, R], dtype=torch.int32, device=dev)
+            y2 = torch.zeros_like(y)
+            moe.moe_grouped_ffn(s_ffn, x_perm, off2, w13, w2, y2, None, None, None, None, ws)
+        torch.cuda.synchronize()
+        assert moe.moe_check_status(ws) == 0
+        outs.append(y)
+    for y in outs[1:]:
+        assert torch.equal(y.view(torch.int16), outs[0].view(torch.int16))
+    expert = np.repeat(np.arange(E, dtype=np.int32), rows)
+    ref = oracle.expert_rows(np_of(x_perm), expert, np_of(w1), np_of(w3), np_of(w2))
+    assert_y_close(bf16_to_f64(outs[-1]), ref, "y_perm after repeated dynamic launches")
+
+
 # --------------------------------------------------------------------------- combine
 @pytest.mark.parametrize("T,d,E,k,c,shared", [
     (1, 64, 4, 2, 0.0, False), (300, 256, 8, 2, 0.0, True), (517, 128, 16, 4, 0.7, True),
