@@ -57,13 +57,30 @@ struct RouterSmemTail {
   float bias[256];
   float lse[128];
   // per-CTA contributions to the tile partials, one slot per cluster rank
-  float slot_colsum[kMaxSplit][256];
-  int slot_hist[kMaxSplit][256];
+  // (the per-expert slots follow the struct: router_slots, S x 256 each)
   float slot_lse2[kMaxSplit];
-  float slot_imp[kMaxSplit][256];
   float slot_ent[kMaxSplit];
   float ent[128];
 };
+
+// Per-expert tile-partial slots after the tail struct, sized by the cluster
+// split S (a split of 1 needs one slot, which leaves room for another ring
+// stage when two CTAs share an SM): column sums, histograms, importance.
+struct RouterSlots {
+  float* colsum;  // [S][256]
+  int* hist;      // [S][256]
+  float* imp;     // [S][256]
+};
+__host__ __device__ inline size_t router_slot_bytes(int S) {
+  return static_cast<size_t>(S) * 256 * 3 * 4;
+}
+__device__ inline RouterSlots router_slots(RouterSmemTail* st, int S) {
+  RouterSlots r;
+  r.colsum = reinterpret_cast<float*>(st + 1);
+  r.hist = reinterpret_cast<int*>(r.colsum + S * 256);
+  r.imp = reinterpret_cast<float*>(r.hist + S * 256);
+  return r;
+}
 
 struct RouterGeom {
   int N;             // MMA N (E rounded up to 16)
@@ -118,6 +135,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const RouterGeom geo = router_geom(E, p.stages, S);
   const int a_bytes = 128 * kBK * 2;
   RouterSmemTail* st = reinterpret_cast<RouterSmemTail*>(smem + geo.main_bytes);
+  const RouterSlots slots = router_slots(st, S);
   volatile int* abort_flag = &st->abort_flag;
   const uint32_t tmem_cols = router_tmem_cols(geo.N);
   const int ldl = geo.ldl;
@@ -396,11 +414,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int rr = 0; rr < rows_valid; ++rr)
         acc += lg[(static_cast<int>(rank) * rpc + rr) * ldl + e];
       if (remote) {
-        st_dsmem_f32(mapa_shared(smem_u32(&st->slot_colsum[rank][e]), 0), acc);
-        st_dsmem_s32(mapa_shared(smem_u32(&st->slot_hist[rank][e]), 0), st->hist[e]);
+        st_dsmem_f32(mapa_shared(smem_u32(&slots.colsum[rank * 256 + e]), 0), acc);
+        st_dsmem_s32(mapa_shared(smem_u32(&slots.hist[rank * 256 + e]), 0), st->hist[e]);
       } else {
-        st->slot_colsum[0][e] = acc;
-        st->slot_hist[0][e] = st->hist[e];
+        slots.colsum[e] = acc;
+        slots.hist[e] = st->hist[e];
       }
     }
     if (eidx == 0) {
@@ -434,9 +452,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int rr = 0; rr < rows_valid; ++rr)
           acc += lg[(static_cast<int>(rank) * rpc + rr) * ldl + e];
         if (remote)
-          st_dsmem_f32(mapa_shared(smem_u32(&st->slot_imp[rank][e]), 0), acc);
+          st_dsmem_f32(mapa_shared(smem_u32(&slots.imp[rank * 256 + e]), 0), acc);
         else
-          st->slot_imp[0][e] = acc;
+          slots.imp[e] = acc;
       }
     }
   }
@@ -449,8 +467,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       float acc = 0.0f;
       int h = 0;
       for (int q = 0; q < S; ++q) {
-        acc += st->slot_colsum[q][e];
-        h += st->slot_hist[q][e];
+        acc += slots.colsum[q * 256 + e];
+        h += slots.hist[q * 256 + e];
       }
       p.tile_psum[static_cast<int64_t>(tile) * E + e] = acc;
       p.tile_hist[static_cast<int64_t>(tile) * E + e] = h;
@@ -467,7 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (p.tile_imp != nullptr && K > 0) {
       for (int e = eidx; e < E; e += kEpiThreads) {
         float acc = 0.0f;
-        for (int q = 0; q < S; ++q) acc += st->slot_imp[q][e];
+        for (int q = 0; q < S; ++q) acc += slots.imp[q * 256 + e];
         p.tile_imp[static_cast<int64_t>(tile) * E + e] = acc;
       }
     }
@@ -485,11 +503,11 @@ int launch_router(const CUtensorMap& x_map, const CUtensorMap& wr_map, RouterArg
   const int ntiles = (args.T + 127) / 128;
   if (ntiles == 0) return 0;
   const int nk = args.d / kBK;
-  const size_t tail = sizeof(RouterSmemTail) + 1024;
   // Split K over a cluster while the grid still fits one wave (one CTA per
   // SM) and each CTA keeps >= 2 k-blocks.
   int S = 1;
   while (S < kMaxSplit && ntiles * 2 * S <= num_sms && nk / (2 * S) >= 2) S *= 2;
+  const size_t tail = sizeof(RouterSmemTail) + router_slot_bytes(S) + 1024;
   const int nk_local = (nk + S - 1) / S;
   const int stage_bytes = router_geom(args.E, 1, S).stage_bytes;
   // With more tiles than SMs, size shared memory for two CTAs per SM.
