@@ -50,11 +50,14 @@ def test_layer_parity(name):
         assert ref.disp.dropped.any(), "capacity case should drop pairs"
 
 
+@pytest.mark.parametrize("dynamic", ["0", "1"])
 @pytest.mark.parametrize("name", ["ragged_shared", "capacity_k4", "fine_bias_shared",
                                   "k0_shared_only", "E1_k1_dense", "wide_E160"])
-def test_layer_parity_paired_tiles(name, monkeypatch):
-    """The same cases with the expert GEMMs forced onto 256-row CTA-pair tiles."""
+def test_layer_parity_paired_tiles(name, dynamic, monkeypatch):
+    """The same cases with the expert GEMMs forced onto 256-row CTA-pair tiles,
+    in the static and in the dynamic (tile counter) order."""
     monkeypatch.setenv("MOE_GEMM_TILE", "256")
+    monkeypatch.setenv("MOE_GEMM_DYNAMIC", dynamic)
     inp = synth.make_inputs(CASES[name], "cuda")
     g, ref = check_layer(inp)
     if name == "k0_no_experts":
