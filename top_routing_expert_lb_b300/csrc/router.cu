@@ -96,7 +96,9 @@ __host__ __device__ inline RouterGeom router_geom(int E, int stages, int S) {
   g.N = (E + 15) / 16 * 16;
   g.stages = stages;
   g.stage_bytes = 128 * kBK * 2 + g.N * kBK * 2;
-  g.ldl = E + 1;
+  // Row pitch = 2S (mod 32) floats: the 2S threads that share a row in the
+  // epilogue read consecutive experts, so one warp's 32 lanes hit 32 banks.
+  g.ldl = E + (((2 * S - E) % 32) + 32) % 32;
   g.rpc = 128 / S;
   const size_t ring = static_cast<size_t>(stages) * g.stage_bytes;
   // own partial [128][ldl] + receive slots [S][rpc][ldl] (= another 128 rows)
@@ -269,14 +271,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool valid = t < p.T;
     float* row = lg + r * ldl;  // receives the full logits, then exp, then the scores
     const bool sigmoid = (p.flags & kRouteSigmoid) != 0;
+    // The three passes over the row below handle four experts per step:
+    // their loads and arithmetic overlap, while every sum and the Top-k
+    // insertion still take the experts in ascending order (same results as
+    // one expert at a time).
     float m = -INFINITY;
-    for (int e = sub; e < E; e += tpr) {
+    auto full_logit = [&](int e) {
       float v = 0.0f;
       for (int q = 0; q < S; ++q)  // partials in rank order
         v += (q == static_cast<int>(rank))
                  ? row[e]
                  : recv[(static_cast<size_t>(q) * rpc + rl) * ldl + e];
-      v += st->off[e];
+      return v + st->off[e];
+    };
+    int e = sub;
+    for (; e + 3 * tpr < E; e += 4 * tpr) {
+      float v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) v[u] = full_logit(e + u * tpr);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        row[e + u * tpr] = v[u];
+        m = fmaxf(m, v[u]);
+      }
+    }
+    for (; e < E; e += tpr) {
+      const float v = full_logit(e);
       row[e] = v;
       m = fmaxf(m, v);
     }
@@ -284,7 +304,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     // softmax normaliser (also the z-loss's lse); with sigmoid scores the row
     // keeps the logits for the next pass
     float s = 0.0f, hs = 0.0f;  // hs: sum of ex * (l - m), for the entropy
-    for (int e = sub; e < E; e += tpr) {
+    for (e = sub; e + 3 * tpr < E; e += 4 * tpr) {
+      float v[4], ex[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        v[u] = row[e + u * tpr];
+        ex[u] = __expf(v[u] - m);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (!sigmoid) row[e + u * tpr] = ex[u];
+        s += ex[u];
+        hs += ex[u] * (v[u] - m);
+      }
+    }
+    for (; e < E; e += tpr) {
       const float v = row[e];
       const float ex = __expf(v - m);
       if (!sigmoid) row[e] = ex;
@@ -305,16 +339,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     float thresh = -INFINITY;  // K-th largest key of this thread so far
     float ssum = 0.0f, slog = 0.0f;  // sigmoid: sum s, sum s log s (entropy)
-    for (int e = sub; e < E; e += tpr) {
-      float pe;
+    // score of expert e (and its sigmoid entropy term), independent per expert
+    auto score = [&](int e, float* term) {
       if (sigmoid) {
-        const float v = row[e];
-        const float en = __expf(-v);
-        pe = 1.0f / (1.0f + en);
+        const float en = __expf(-row[e]);
+        const float pe = 1.0f / (1.0f + en);
+        *term = pe > 0.0f ? pe * log1pf(en) : 0.0f;  // s log s = -s log(1 + e^-l)
+        return pe;
+      }
+      *term = 0.0f;
+      return row[e] * inv_s;
+    };
+    // in ascending expert order: the sums, the row's score and the Top-k list
+    auto commit = [&](int e, float pe, float term) {
+      if (sigmoid) {
         ssum += pe;
-        if (pe > 0.0f) slog -= pe * log1pf(en);  // s log s = -s log(1 + e^-l)
-      } else {
-        pe = row[e] * inv_s;
+        if (pe > 0.0f) slog -= term;
       }
       row[e] = valid ? pe : 0.0f;  // the row now holds the scores (gates, P partial)
       const float key = pe + st->bias[e];
@@ -337,6 +377,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         thresh = top_key[K > 0 ? K - 1 : 0];
       }
+    };
+    for (e = sub; e + 3 * tpr < E; e += 4 * tpr) {
+      float pe[4], term[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) pe[u] = score(e + u * tpr, &term[u]);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) commit(e + u * tpr, pe[u], term[u]);
+    }
+    for (; e < E; e += tpr) {
+      float term;
+      const float pe = score(e, &term);
+      commit(e, pe, term);
     }
     if (sigmoid) {
       for (int o = 1; o < tpr; o <<= 1) {
