@@ -41,6 +41,18 @@ def test_every_declared_symbol_is_exported(lib):
         assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
 
 
+def test_every_tuning_switch_is_documented():
+    """Each environment switch the library reads is described in the header."""
+    csrc = os.path.join(os.path.dirname(HEADER), "..", "top_routing_expert_lb_b300", "csrc")
+    names = set()
+    for fn in os.listdir(csrc):
+        if fn.endswith((".cu", ".cuh", ".h")):
+            names |= set(re.findall(r'getenv\("([A-Z0-9_]+)"\)', open(os.path.join(csrc, fn)).read()))
+    assert names, "no switches found"
+    header = open(HEADER).read()
+    assert not [n for n in sorted(names) if n not in header]
+
+
 def test_error_strings(lib):
     for code in (0, -1, -2, -3, -4, -5):
         assert B.moe_error_string(code)
