@@ -276,7 +276,9 @@ int moe_layer_forward_host(const moe_shape_t *shape, const uint16_t *x_host, uin
  *   loss_dev    [2][2] fp32 device slots
  *   ids, gates, counts, drop_mask, f, P: device outputs as in
  *               moe_layer_forward; they hold the last batch's values.
- * The three streams may be the same stream (no overlap).  Errors: as
+ * The three streams may be the same stream (no overlap).  The call creates
+ * six CUDA events (no device memory) and destroys them before returning.
+ * Errors: as
  * moe_layer_forward; n_batches < 0 or a null host buffer -> MOE_ERR_INVALID_ARG.
  * A failing step stops the loop; what was enqueued is drained before return. */
 int moe_layer_forward_host_batches(
