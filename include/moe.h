@@ -92,6 +92,57 @@ extern "C" {
 #define MOE_FLAG_PRIORITY_CAPACITY 4u
 #define MOE_FLAG_EXPERT_CHOICE 8u
 
+/* How the expert GEMMs and the layer are scheduled: tuning choices, not part
+ * of the layer's definition.  Every field at zero selects the measured-
+ * fastest default; every choice gives parity-tested results (most of them
+ * bit-identical to the default).  Invalid values -> MOE_ERR_INVALID_ARG.
+ *   gemm1_tile      gate/up projection tiles.  0: CTA-pair 256 x 256 tiles
+ *                   when E <= 16, experts average >= 512 rows and rows are not
+ *                   gathered, else single-CTA 128 x 256 tiles; 128: single-CTA
+ *                   tiles; 256: CTA-pair tiles (then the down projection too,
+ *                   unless gemm2_tile is 128)
+ *   gemm2_tile      down projection tiles.  0: CTA pairs when d % 256 == 0 and
+ *                   experts average >= 512 rows (or gemm1_tile is 256), else
+ *                   single-CTA 128 x BN (BN = 256, 128 or 64 by d); 128:
+ *                   single-CTA tiles; 256: CTA pairs (needs d % 256 == 0)
+ *   tile_order      CTA-pair launches.  0: tiles from a counter in the
+ *                   workspace when K >= 4096, else round-robin; 1: round-robin
+ *                   throughout; 2: counter throughout
+ *   tail_max_n      a group's last m-tile with r valid rows runs transposed
+ *                   (weights as the MMA's M) when r rounded up to 16 is at most
+ *                   this.  0: 112; < 0: never; 16..112 in steps of 16
+ *   n_block         tile order inside a group with more than block_min_rows
+ *                   rows: blocks of n_block n-tiles, m-tile major inside a
+ *                   block.  0: 8; 1: n-tile major, m-tile minor throughout
+ *   block_min_rows  0: 2048
+ *   options         MOE_TUNE_* bits:
+ *     MOE_TUNE_NO_HALF_TILES    CTA-pair launches pad a group's last tile of at
+ *                               most 128 rows to a 256-row tile instead of one
+ *                               M = 128 pair MMA (64 rows per CTA)
+ *     MOE_TUNE_GEMM1_SPLIT      gate/up projection: whole 256-row blocks on CTA
+ *                               pairs, the remaining rows on single CTAs (two
+ *                               launches)
+ *     MOE_TUNE_FUSED_GATHER     moe_layer_forward / moe_ec_layer_forward: the
+ *                               gate/up projection gathers token rows itself
+ *                               (TMA 4-row gathers), no x_perm; not with
+ *                               gemm1_tile = 256
+ *     MOE_TUNE_GATE_IN_EPILOGUE moe_layer_forward / moe_ec_layer_forward: the
+ *                               down projection's epilogue scales each routed
+ *                               row by its gate (fp32, before rounding) and
+ *                               the combine only adds rows, in the same order
+ *   wait_timeout_ns limit of this call's bounded device waits; 0: the
+ *                   process-wide limit (moe_set_wait_timeout_ns)             */
+#define MOE_TUNE_NO_HALF_TILES 1u
+#define MOE_TUNE_GEMM1_SPLIT 2u
+#define MOE_TUNE_FUSED_GATHER 4u
+#define MOE_TUNE_GATE_IN_EPILOGUE 8u
+typedef struct moe_tuning {
+    int32_t gemm1_tile, gemm2_tile, tile_order, tail_max_n, n_block, block_min_rows;
+    uint32_t options;
+    uint32_t reserved;  /* must be 0 */
+    uint64_t wait_timeout_ns;
+} moe_tuning_t;
+
 /* Layer shape.
  *   T  tokens;  d  model width;  M  expert intermediate width;
  *   E  routed experts;  k  experts per token;  n_shared  shared experts,
@@ -99,12 +150,17 @@ extern "C" {
  *   capacity_factor  c; <= 0 means dropless, otherwise C = ceil(c*k*T/E)
  *      evaluated in double precision;
  *   balance_coef  lambda of the balance loss (0.01 is customary);
- *   flags  routing variants, a combination of the MOE_FLAG_* bits above.     */
+ *   flags  routing variants, a combination of the MOE_FLAG_* bits above;
+ *   tuning  scheduling choices (all zero: the defaults), see moe_tuning_t.
+ * A zero-initialised struct with the first eight fields set is a complete
+ * description; the library reads nothing from the environment.              */
 typedef struct moe_shape {
     int32_t T, d, M, E, k, n_shared;
     float capacity_factor;
     float balance_coef;
     uint32_t flags;
+    uint32_t reserved;  /* must be 0 */
+    moe_tuning_t tuning;
 } moe_shape_t;
 
 /* Error text for a MOE_* code (static string, never NULL). */
@@ -330,8 +386,9 @@ int moe_ec_layer_forward(const moe_shape_t *shape, const uint16_t *x, const uint
  * MOE_OK or MOE_ERR_TIMEOUT to *status (host).  Synchronises `stream`.        */
 int moe_check_status(void *ws, int *status, void *stream);
 
-/* Wait limit, in nanoseconds, for every bounded device wait launched after
- * this call (default 2e9).  Process-wide.                                    */
+/* Default wait limit, in nanoseconds, of the bounded device waits of every
+ * call launched after this one whose shape->tuning.wait_timeout_ns is 0
+ * (initially 2e9).  Process-wide.                                            */
 int moe_set_wait_timeout_ns(uint64_t ns);
 
 /* Launches one CTA that waits on a barrier nothing ever signals, bounded by
@@ -361,42 +418,6 @@ int moe_route_noalloc(const moe_shape_t *shape, const uint16_t *x, const uint16_
                       const float *logit_offset, const float *sel_bias, int32_t *ids,
                       float *gates, int32_t *counts, float *f, float *P, float *bal_loss,
                       float *z_loss, void *stream);
-
-/* Expert-GEMM variants, read from the environment at every grouped-FFN
- * launch (the defaults are the measured fastest; every variant gives
- * parity-tested results, most bit-identical to the default):
- *   MOE_GEMM_TILE=128|256    the gate/up projection on single-CTA 128 x 256 or
- *                            CTA-pair 256 x 256 tiles (256 also puts the down
- *                            projection on pairs; default: pairs when E <= 16,
- *                            experts average >= 512 rows and rows are not
- *                            gathered)
- *   MOE_GEMM_DYNAMIC=0|1     CTA-pair launches take tiles in a static
- *                            round-robin order (0) or from a tile counter in
- *                            the workspace (1; default when K >= 4096)
- *   MOE_GEMM_HALF=0          CTA-pair launches pad a group's last tile of at
- *                            most 128 rows to a 256-row tile instead of running
- *                            it as one M = 128 pair MMA (64 rows per CTA)
- *   MOE_GEMM2_TILE=128|256   the down projection on single-CTA 128 x BN or
- *                            CTA-pair 256 x 256 tiles (default: pairs when
- *                            d % 256 == 0 and experts average >= 512 rows)
- *   MOE_GEMM_MC=1            clusters of two single CTAs sharing each B tile
- *                            through TMA multicast
- *   MOE_GEMM1_SPLIT=1        gate/up projection: whole 256-row blocks on CTA
- *                            pairs, the remaining rows on single CTAs
- *   MOE_GEMM_TAIL_MAX_N=n    a group's last m-tile with r rows runs transposed
- *                            (weights as the MMA's M) when r rounded up to 16
- *                            is <= n (default 112; 0 never)
- *   MOE_GEMM_NBLOCK=b        tile order inside a group with more rows than
- *                            MOE_GEMM_BLOCK_MIN_ROWS (default 2048): blocks of
- *                            b n-tiles, m-tile major inside a block (default 8;
- *                            0 or 1: n-tile major, m-tile minor throughout)
- *   MOE_FUSED_GATHER=1       moe_layer_forward: the gate/up projection gathers
- *                            token rows itself (TMA 4-row gathers), no x_perm
- *   MOE_GATE_IN_EPILOGUE=1   moe_layer_forward / moe_ec_layer_forward: the down
- *                            projection's epilogue scales each routed row by
- *                            its gate (fp32, before rounding) and the combine
- *                            only adds rows, in the same fixed order
- * All are tuning switches, not part of the layer's definition.               */
 
 /* Kernel accounting for benchmarks (host-side, process-wide, not thread-safe).
  * Kernel ids reported by moe_profile_collect: */

@@ -5,6 +5,8 @@ mutated build) and raises AssertionError on mismatch.  The pins are:
 
 * the hand-worked 2-token / 4-expert example in ``golden/hand_2tok_4exp.json``
   (closed-form values, worked out by hand);
+* per-row experts (the reference of the grouped-FFN stage tests): a closed-form
+  hand case and rows through different random experts against numpy;
 * the second gating formula Softmax(TopK(W_g x, k)) of the aiattnstudio page
   (§2.2), which must give the same set and gates as softmax -> TopK ->
   renormalise when there is no selection bias;
@@ -592,6 +594,35 @@ def pin_expert_choice(lib):
     _close(ec.y, tc.y, 1e-12, "EC with r = T vs token choice k = E")
 
 
-ALL_PINS = [pin_priority_capacity, pin_expert_choice, pin_alf_bias_update, pin_routing_variants, pin_entropy_and_importance, pin_combine, pin_hand_routing, pin_hand_capacity, pin_hand_shared_k0, pin_two_gating_formulas,
+def pin_expert_rows(lib):
+    """oracle_expert_rows: each row goes through its own expert ("深入理解 MoE"
+    §10.2, the SwiGLU expert W2 (SiLU(W1 x) * W3 x)).
+    Hand case: W1 = W3 = I and W2_e = (e + 1) I give E_e(x)_i = (e + 1) x_i
+    SiLU(x_i), with SiLU(1), SiLU(2), SiLU(-1) from the closed form; random
+    case: experts with different weights, d != M, each row against a numpy
+    SwiGLU with that row's expert."""
+    w1, w3, w2, _ = _hand_weights()
+    x = bf16_bits(np.array([[1.0, 2.0, -1.0, 0.0]] * 4))
+    expert = np.array([2, 0, 3, 1], np.int32)
+    got = oracle.expert_rows(x, expert, w1, w3, w2, lib=lib)
+    s1, s2, sm1 = 1 / (1 + np.exp(-1.0)), 2 / (1 + np.exp(-2.0)), -1 / (1 + np.exp(1.0))
+    base = np.array([1.0 * s1, 2.0 * s2, -1.0 * sm1, 0.0])
+    _close(got, (expert[:, None] + 1.0) * base[None, :], 1e-12, "expert rows, hand case")
+    rng = np.random.default_rng(77)
+    n, d, M, E = 9, 12, 8, 4
+    xr = bf16_bits(rng.standard_normal((n, d)))
+    ww1 = bf16_bits(rng.standard_normal((E, M, d)) * 0.4)
+    ww3 = bf16_bits(rng.standard_normal((E, M, d)) * 0.4)
+    ww2 = bf16_bits(rng.standard_normal((E, d, M)) * 0.4)
+    ex = np.array([3, 0, 1, 2, 2, 0, 3, 1, 3], np.int32)
+    got = oracle.expert_rows(xr, ex, ww1, ww3, ww2, lib=lib)
+    for r in range(n):
+        e = ex[r]
+        want = np_swiglu(bf16_val(xr[r:r + 1]), bf16_val(ww1[e]), bf16_val(ww3[e]),
+                         bf16_val(ww2[e]))[0]
+        _close(got[r], want, 1e-12 * max(1.0, np.abs(want).max()), f"expert row {r} (expert {e})")
+
+
+ALL_PINS = [pin_expert_rows, pin_priority_capacity, pin_expert_choice, pin_alf_bias_update, pin_routing_variants, pin_entropy_and_importance, pin_combine, pin_hand_routing, pin_hand_capacity, pin_hand_shared_k0, pin_two_gating_formulas,
             pin_bruteforce_subsets, pin_dispatch_argsort, pin_capacity_formula, pin_invariants,
             pin_determinism, pin_gap_and_force]

@@ -37,9 +37,10 @@ LOSS_REL = 1e-4
 GATE_ABS = 1e-5
 
 
-def shape_of(w: synth.Workload) -> moe.Shape:
+def shape_of(w: synth.Workload, **tuning) -> moe.Shape:
+    """The workload's moe_shape_t; keyword arguments set moe_tuning_t fields."""
     return moe.Shape.of(w.T, w.d, w.M, w.E, w.k, w.n_shared, w.capacity_factor,
-                        w.balance_coef, w.flags)
+                        w.balance_coef, w.flags, **tuning)
 
 
 def np_of(t: Optional[torch.Tensor]):
@@ -68,10 +69,11 @@ class GpuOut:
     z: float
 
 
-def run_layer(inp: synth.Inputs, layer: Optional[moe.MoELayer] = None) -> GpuOut:
+def run_layer(inp: synth.Inputs, layer: Optional[moe.MoELayer] = None,
+              tuning: Optional[dict] = None) -> GpuOut:
     w = inp.w
     if layer is None:
-        layer = moe.MoELayer(shape_of(w), inp.wr, inp.w1, inp.w3, inp.w2, inp.ws1, inp.ws3,
+        layer = moe.MoELayer(shape_of(w, **(tuning or {})), inp.wr, inp.w1, inp.w3, inp.w2, inp.ws1, inp.ws3,
                              inp.ws2, inp.offset, inp.sel_bias, device=inp.x.device)
     layer.forward(inp.x)
     torch.cuda.synchronize()
@@ -81,28 +83,64 @@ def run_layer(inp: synth.Inputs, layer: Optional[moe.MoELayer] = None) -> GpuOut
                   float(layer.losses[0]), float(layer.losses[1]))
 
 
+def topk_choice_problems(key: np.ndarray, ids: np.ndarray, k: int, tol: float = TIE):
+    """Why ``ids`` is not a valid Top-k of one token's selection keys ``key``
+    (fp64, the oracle's) within ``tol``; an empty list when it is.
+
+    A valid choice names k distinct experts in [0, E); each selected key is at
+    least the k-th largest key minus tol, each unselected key at most the
+    (k+1)-th largest plus tol, and the selected keys descend up to tol.  With
+    a gap of at least tol between the k-th and (k+1)-th keys this leaves only
+    the oracle's set (in any order of keys closer than tol)."""
+    E = key.shape[0]
+    ids = np.asarray(ids)
+    out = []
+    if len(ids) != k or len(set(ids.tolist())) != k:
+        out.append(f"ids {ids.tolist()} are not {k} distinct experts")
+        return out
+    if ids.min() < 0 or ids.max() >= E:
+        out.append(f"ids {ids.tolist()} outside [0, {E})")
+        return out
+    srt = np.sort(key)[::-1]
+    kth = srt[k - 1]
+    nxt = srt[k] if k < E else -np.inf
+    sel = key[ids]
+    if np.any(sel < kth - tol):
+        out.append(f"selected key {sel.min():.9g} below the k-th key {kth:.9g} - {tol}")
+    rest = np.delete(key, ids)
+    if rest.size and np.any(rest > nxt + tol):
+        out.append(f"unselected key {rest.max():.9g} above the (k+1)-th key {nxt:.9g} + {tol}")
+    if np.any(np.diff(sel) > tol):
+        out.append(f"selected keys {sel.tolist()} not descending up to {tol}")
+    return out
+
+
 def routing_force_mask(free: oracle.Routing, gpu_ids: np.ndarray, bias) -> np.ndarray:
-    """Tokens whose GPU selection may be taken over by the oracle.
+    """Tokens whose GPU selection the oracle takes over, after checking it.
 
     The selected set is unique unless the k-th and (k+1)-th keys are within
-    1e-5 (near tie at the cut): such tokens are exempt.  Inside the set, the
-    order of two keys closer than 1e-5 is not unique either; there the GPU's
-    order is accepted after checking that it is descending in the oracle's
-    keys up to 1e-5.  Any other difference fails.  (Slot order inside one
-    token cannot change drops or rows: a token sends at most one pair to an
-    expert.)"""
+    1e-5 (a near tie at the cut: such tokens are exempt).  Inside the set, the
+    order of two keys closer than 1e-5 is not unique either.  Every token whose
+    GPU choice differs from the oracle's must be a valid Top-k of the oracle's
+    fp64 keys within 1e-5 (``topk_choice_problems``); a token outside the
+    near-tie band must in addition have the oracle's set.  Any other
+    difference fails.  (Slot order inside one token cannot change drops or
+    rows: a token sends at most one pair to an expert.)"""
     key = free.p + (0.0 if bias is None else np.asarray(bias, np.float64)[None, :])
+    k = free.ids.shape[1]
     exempt = free.gap < TIE
     diff = np.any(free.ids != gpu_ids, axis=1)
     bad = []
-    for t in np.nonzero(diff & ~exempt)[0]:
-        same_set = sorted(free.ids[t].tolist()) == sorted(gpu_ids[t].tolist())
-        kg = key[t, gpu_ids[t]]
-        if not (same_set and np.all(np.diff(kg) <= TIE)):
-            bad.append(t)
-    assert not bad, (f"{len(bad)} non-tie tokens routed differently, e.g. token {bad[0]}: "
-                     f"gpu {gpu_ids[bad[0]]} oracle {free.ids[bad[0]]} gap {free.gap[bad[0]]}")
-    return diff | exempt
+    for t in np.nonzero(diff)[0]:
+        why = topk_choice_problems(key[t], gpu_ids[t], k)
+        if not exempt[t] and sorted(free.ids[t].tolist()) != sorted(gpu_ids[t].tolist()):
+            why.append("a different set outside the near-tie band")
+        if why:
+            bad.append((t, why))
+    assert not bad, (f"{len(bad)} tokens routed to an invalid choice, e.g. token {bad[0][0]}: "
+                     f"gpu {gpu_ids[bad[0][0]]} oracle {free.ids[bad[0][0]]} gap "
+                     f"{free.gap[bad[0][0]]}: {'; '.join(bad[0][1])}")
+    return diff
 
 
 @dataclass
@@ -170,7 +208,7 @@ def oracle_routing(inp: synth.Inputs, gpu_ids: np.ndarray,
     if w.k > 0:
         force = routing_force_mask(free, gpu_ids, bias)
         r = oracle.route(logits, w.k, bias, force_ids=gpu_ids, force_mask=force, flags=rflags)
-        exempt = force
+        exempt = force | exempt
     else:
         r = free
     C = oracle.capacity(float(np.float32(w.capacity_factor)), w.k, w.T, w.E)
@@ -184,25 +222,31 @@ def oracle_routing(inp: synth.Inputs, gpu_ids: np.ndarray,
     return OracleRef(r, disp, ls, exempt, C)
 
 
-def oracle_y(inp: synth.Inputs, ref: OracleRef, sel: np.ndarray) -> np.ndarray:
+def oracle_y(inp: synth.Inputs, ref: OracleRef, sel: np.ndarray,
+             host_weights: Optional[tuple] = None) -> np.ndarray:
     """Oracle layer output for the tokens in ``sel``, copying to the host only
-    the expert weights those tokens use."""
+    the expert weights those tokens use (or using ``host_weights``, the full
+    (w1, w3, w2) as uint16 arrays, when given)."""
     w = inp.w
     sel = np.asarray(sel, np.int32)
     x = np_of(inp.x)
     ids = ref.routing.ids[sel]
-    used = sorted(set(ids.reshape(-1).tolist())) if w.k > 0 else []
-    remap = {e: i for i, e in enumerate(used)}
-    if used:
-        idx = torch.tensor(used, device=inp.w1.device)
-        w1 = np_of(inp.w1.index_select(0, idx))
-        w3 = np_of(inp.w3.index_select(0, idx))
-        w2 = np_of(inp.w2.index_select(0, idx))
-        ids_c = np.vectorize(remap.get)(ids).astype(np.int32).reshape(ids.shape)
+    if host_weights is not None:
+        w1, w3, w2 = host_weights
+        ids_c = np.ascontiguousarray(ids, np.int32)
     else:
-        w1 = w3 = np.zeros((1, w.M, w.d), np.uint16)
-        w2 = np.zeros((1, w.d, w.M), np.uint16)
-        ids_c = np.zeros((len(sel), w.k), np.int32)
+        used = sorted(set(ids.reshape(-1).tolist())) if w.k > 0 else []
+        remap = {e: i for i, e in enumerate(used)}
+        if used:
+            idx = torch.tensor(used, device=inp.w1.device)
+            w1 = np_of(inp.w1.index_select(0, idx))
+            w3 = np_of(inp.w3.index_select(0, idx))
+            w2 = np_of(inp.w2.index_select(0, idx))
+            ids_c = np.vectorize(remap.get)(ids).astype(np.int32).reshape(ids.shape)
+        else:
+            w1 = w3 = np.zeros((1, w.M, w.d), np.uint16)
+            w2 = np.zeros((1, w.d, w.M), np.uint16)
+            ids_c = np.zeros((len(sel), w.k), np.int32)
     xs = x[sel]
     loc = np.arange(len(sel), dtype=np.int32)
     return oracle.layer_tokens(xs, ids_c, ref.routing.gates[sel], ref.disp.dropped[sel], w1, w3,
@@ -240,9 +284,11 @@ def assert_routing_parity(g: GpuOut, ref: OracleRef, w: synth.Workload):
     rel_close(g.z, ref.loss.L_z, LOSS_REL, "z-loss")
 
 
-def check_layer(inp: synth.Inputs, sel: Optional[np.ndarray] = None, layer=None):
-    """Runs the GPU layer and checks it against the oracle.  Returns (gpu, ref)."""
-    g = run_layer(inp, layer)
+def check_layer(inp: synth.Inputs, sel: Optional[np.ndarray] = None, layer=None,
+                tuning: Optional[dict] = None):
+    """Runs the GPU layer (with the given moe_tuning_t fields) and checks it
+    against the oracle.  Returns (gpu, ref)."""
+    g = run_layer(inp, layer, tuning)
     ref = oracle_routing(inp, g.ids, g.drop)
     assert_routing_parity(g, ref, inp.w)
     if sel is None:
@@ -269,11 +315,12 @@ class EcGpuOut:
     r: int
 
 
-def run_ec_layer(inp: synth.Inputs, layer: Optional[moe.MoELayer] = None) -> EcGpuOut:
+def run_ec_layer(inp: synth.Inputs, layer: Optional[moe.MoELayer] = None,
+                 tuning: Optional[dict] = None) -> EcGpuOut:
     w = inp.w
     assert w.flags & moe.MOE_FLAG_EXPERT_CHOICE
     if layer is None:
-        layer = moe.MoELayer(shape_of(w), inp.wr, inp.w1, inp.w3, inp.w2, inp.ws1, inp.ws3,
+        layer = moe.MoELayer(shape_of(w, **(tuning or {})), inp.wr, inp.w1, inp.w3, inp.w2, inp.ws1, inp.ws3,
                              inp.ws2, inp.offset, None, device=inp.x.device)
     layer.forward(inp.x)
     torch.cuda.synchronize()
@@ -338,10 +385,11 @@ def oracle_ec_y(inp: synth.Inputs, ref: EcRef, sel: np.ndarray) -> np.ndarray:
                                   np_of(inp.ws3), np_of(inp.ws2), sel)
 
 
-def check_ec_layer(inp: synth.Inputs, sel: Optional[np.ndarray] = None, layer=None):
+def check_ec_layer(inp: synth.Inputs, sel: Optional[np.ndarray] = None, layer=None,
+                   tuning: Optional[dict] = None):
     """Runs the GPU expert-choice layer and checks it against the oracle."""
     w = inp.w
-    g = run_ec_layer(inp, layer)
+    g = run_ec_layer(inp, layer, tuning)
     ref = oracle_ec(inp, g.row_token)
     assert g.r == ref.ec.r
     np.testing.assert_array_equal(g.row_token, ref.ec.row_token)

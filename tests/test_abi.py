@@ -41,16 +41,48 @@ def test_every_declared_symbol_is_exported(lib):
         assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
 
 
-def test_every_tuning_switch_is_documented():
-    """Each environment switch the library reads is described in the header."""
+def test_library_reads_no_environment():
+    """Every scheduling choice comes through moe_shape_t.tuning: the sources
+    read no environment variable."""
     csrc = os.path.join(os.path.dirname(HEADER), "..", "top_routing_expert_lb_b300", "csrc")
-    names = set()
     for fn in os.listdir(csrc):
         if fn.endswith((".cu", ".cuh", ".h")):
-            names |= set(re.findall(r'getenv\("([A-Z0-9_]+)"\)', open(os.path.join(csrc, fn)).read()))
-    assert names, "no switches found"
-    header = open(HEADER).read()
-    assert not [n for n in sorted(names) if n not in header]
+            assert "getenv" not in open(os.path.join(csrc, fn)).read(), fn
+
+
+def test_shape_struct_layout_matches_the_header():
+    """moe_shape_t / moe_tuning_t as ctypes sees them: 80 and 40 bytes, the
+    tuning block after the flags word and its padding word."""
+    assert ctypes.sizeof(B.Tuning) == 40
+    assert ctypes.sizeof(B.Shape) == 80
+    assert B.Shape.tuning.offset == 40
+
+
+@pytest.mark.parametrize("tune,code", [
+    (dict(gemm1_tile=64), B.MOE_ERR_INVALID_ARG),
+    (dict(gemm2_tile=192), B.MOE_ERR_INVALID_ARG),
+    (dict(tile_order=3), B.MOE_ERR_INVALID_ARG),
+    (dict(tail_max_n=8), B.MOE_ERR_INVALID_ARG),
+    (dict(tail_max_n=129), B.MOE_ERR_INVALID_ARG),
+    (dict(n_block=-1), B.MOE_ERR_INVALID_ARG),
+    (dict(block_min_rows=-5), B.MOE_ERR_INVALID_ARG),
+    (dict(options=16), B.MOE_ERR_INVALID_ARG),
+    (dict(reserved=1), B.MOE_ERR_INVALID_ARG),
+    (dict(options=B.MOE_TUNE_FUSED_GATHER, gemm1_tile=256), B.MOE_ERR_INVALID_ARG),
+    (dict(gemm2_tile=256), B.MOE_ERR_UNSUPPORTED),   # d = 64 is not a multiple of 256
+])
+def test_tuning_fields_are_checked(lib, tune, code):
+    s = B.Shape.of(64, 64, 128, 8, 2, **tune)
+    v = ctypes.c_size_t()
+    assert lib.moe_workspace_size(ctypes.byref(s), ctypes.byref(v)) == code
+
+
+@pytest.mark.parametrize("tune", [dict(), dict(gemm1_tile=128, gemm2_tile=128, tile_order=1,
+                                               tail_max_n=-1, n_block=1, block_min_rows=1,
+                                               options=15, wait_timeout_ns=10**9)])
+def test_valid_tuning_leaves_the_workspace_size_unchanged(lib, tune):
+    base = B.Shape.of(4096, 256, 512, 8, 2, 1)
+    assert B.moe_workspace_size(base.tuned(**tune)) == B.moe_workspace_size(base)
 
 
 def test_error_strings(lib):

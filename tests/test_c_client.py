@@ -25,6 +25,12 @@ int main(void) {
   if (moe_max_rows(&s, &rows) != MOE_OK) return 3;
   s.k = 9;  /* k > E: refused */
   if (moe_workspace_size(&s, &ws) != MOE_ERR_INVALID_ARG) return 4;
+  s.k = 2;
+  s.tuning.gemm1_tile = 64;  /* not a tile height the library has: refused */
+  if (moe_workspace_size(&s, &ws) != MOE_ERR_INVALID_ARG) return 5;
+  s.tuning.gemm1_tile = 256;  /* CTA-pair gate/up tiles: accepted */
+  s.tuning.options = MOE_TUNE_NO_HALF_TILES;
+  if (moe_workspace_size(&s, &ws) != MOE_OK) return 6;
   printf("C=%lld rows=%lld err=%s\n", (long long)C, (long long)rows,
          moe_error_string(MOE_ERR_TIMEOUT));
   return 0;

@@ -53,13 +53,11 @@ def test_layer_parity(name):
 @pytest.mark.parametrize("dynamic", ["0", "1"])
 @pytest.mark.parametrize("name", ["ragged_shared", "capacity_k4", "fine_bias_shared",
                                   "k0_shared_only", "E1_k1_dense", "wide_E160"])
-def test_layer_parity_paired_tiles(name, dynamic, monkeypatch):
+def test_layer_parity_paired_tiles(name, dynamic):
     """The same cases with the expert GEMMs forced onto 256-row CTA-pair tiles,
     in the static and in the dynamic (tile counter) order."""
-    monkeypatch.setenv("MOE_GEMM_TILE", "256")
-    monkeypatch.setenv("MOE_GEMM_DYNAMIC", dynamic)
     inp = synth.make_inputs(CASES[name], "cuda")
-    g, ref = check_layer(inp)
+    g, ref = check_layer(inp, tuning=dict(gemm1_tile=256, tile_order=2 if dynamic == "1" else 1))
     if name == "k0_no_experts":
         assert torch.count_nonzero(g.y) == 0
     if CASES[name].capacity_factor > 0:
@@ -68,63 +66,41 @@ def test_layer_parity_paired_tiles(name, dynamic, monkeypatch):
 
 @pytest.mark.parametrize("name", ["ragged_shared", "capacity_k4", "fine_bias_shared",
                                   "top1_capacity", "wide_E160", "single_token"])
-def test_layer_parity_fused_gather(name, monkeypatch):
+def test_layer_parity_fused_gather(name):
     """The same cases with GEMM-1 gathering the token rows itself (TMA 4-row
     gathers by row_token) instead of reading the scatter's x_perm."""
-    monkeypatch.setenv("MOE_FUSED_GATHER", "1")
-    check_layer(synth.make_inputs(CASES[name], "cuda"))
-
-
-@pytest.mark.parametrize("name", ["ragged_shared", "capacity_k4", "fine_bias_shared",
-                                  "wide_E160", "single_token", "E1_k1_dense"])
-def test_layer_parity_multicast(name, monkeypatch):
-    """The same cases with the 256-column GEMM tiles on clusters of two CTAs
-    that share each B tile by TMA multicast."""
-    monkeypatch.setenv("MOE_GEMM_MC", "1")
-    check_layer(synth.make_inputs(CASES[name], "cuda"))
+    check_layer(synth.make_inputs(CASES[name], "cuda"),
+                tuning=dict(options=moe.MOE_TUNE_FUSED_GATHER))
 
 
 @pytest.mark.parametrize("name", ["ragged_shared", "capacity_k4", "fine_bias_shared",
                                   "top1_capacity", "E1_k1_dense", "k_equals_E"])
-def test_layer_parity_split_gate_up(name, monkeypatch):
+def test_layer_parity_split_gate_up(name):
     """The same cases with the gate/up projection split into CTA-pair tiles for
     whole 256-row blocks and single-CTA tiles for the rest."""
-    monkeypatch.setenv("MOE_GEMM1_SPLIT", "1")
-    check_layer(synth.make_inputs(CASES[name], "cuda"))
+    check_layer(synth.make_inputs(CASES[name], "cuda"),
+                tuning=dict(options=moe.MOE_TUNE_GEMM1_SPLIT))
 
 
 @pytest.mark.parametrize("name,tile2", [("ragged_shared", "128"), ("ragged_shared", "256"),
                                         ("capacity_k4", "128"), ("fine_bias_shared", "128"),
                                         ("wide_E160", "128"), ("k_equals_E", "128"),
                                         ("single_token", "128"), ("top1_capacity", "128")])
-def test_layer_parity_gate_in_epilogue(name, tile2, monkeypatch):
+def test_layer_parity_gate_in_epilogue(name, tile2):
     """The same cases with each routed row scaled by its gate in the down
     projection's epilogue and a combine that only adds rows."""
-    monkeypatch.setenv("MOE_GATE_IN_EPILOGUE", "1")
-    monkeypatch.setenv("MOE_GEMM2_TILE", tile2)
-    check_layer(synth.make_inputs(CASES[name], "cuda"))
+    check_layer(synth.make_inputs(CASES[name], "cuda"),
+                tuning=dict(options=moe.MOE_TUNE_GATE_IN_EPILOGUE, gemm2_tile=int(tile2)))
 
 
-def test_multicast_and_single_cta_agree_bitwise(monkeypatch):
-    """Sharing the B tiles changes only who loads them: outputs are bitwise equal."""
-    w = CASES["fine_bias_shared"]
-    inp = synth.make_inputs(w, "cuda")
-    outs = []
-    for flag in ("1", "0"):
-        monkeypatch.setenv("MOE_GEMM_MC", flag)
-        outs.append(run_layer(inp).y)
-    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
-
-
-def test_fused_and_materialised_rows_agree_bitwise(monkeypatch):
+def test_fused_and_materialised_rows_agree_bitwise():
     """Gathering the rows inside GEMM-1 stages the same bytes as the scatter's
     copy, so the two paths give bit-identical outputs."""
     w = CASES["fine_bias_shared"]
     inp = synth.make_inputs(w, "cuda")
     outs = []
-    for flag in ("1", "0"):
-        monkeypatch.setenv("MOE_FUSED_GATHER", flag)
-        outs.append(run_layer(inp).y)
+    for opts in (moe.MOE_TUNE_FUSED_GATHER, 0):
+        outs.append(run_layer(inp, tuning=dict(options=opts)).y)
     assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
 
 

@@ -146,26 +146,26 @@ def test_expert_choice_full_size(name):
 
 @pytest.mark.parametrize("w", [PRIO_CASES[0], PRIO_CASES[2], EC_CASES[1], EC_CASES[2]],
                          ids=lambda w: w.name)
-def test_select_paths_with_fused_gather(w, monkeypatch):
+def test_select_paths_with_fused_gather(w):
     """Priority capacity and expert choice with GEMM-1 gathering token rows by
     row_token instead of the gather kernel's x_perm."""
-    monkeypatch.setenv("MOE_FUSED_GATHER", "1")
+    tune = dict(options=moe.MOE_TUNE_FUSED_GATHER)
     if w.flags & EC:
-        check_ec_layer(synth.make_inputs(w, "cuda"))
+        check_ec_layer(synth.make_inputs(w, "cuda"), tuning=tune)
     else:
-        check_layer(synth.make_inputs(w, "cuda"))
+        check_layer(synth.make_inputs(w, "cuda"), tuning=tune)
 
 
 @pytest.mark.parametrize("w", [PRIO_CASES[0], PRIO_CASES[2], EC_CASES[0], EC_CASES[2]],
                          ids=lambda w: w.name)
-def test_select_paths_gate_in_epilogue(w, monkeypatch):
+def test_select_paths_gate_in_epilogue(w):
     """Priority capacity and expert choice with the gates applied in the down
     projection's epilogue."""
-    monkeypatch.setenv("MOE_GATE_IN_EPILOGUE", "1")
+    tune = dict(options=moe.MOE_TUNE_GATE_IN_EPILOGUE)
     if w.flags & EC:
-        check_ec_layer(synth.make_inputs(w, "cuda"))
+        check_ec_layer(synth.make_inputs(w, "cuda"), tuning=tune)
     else:
-        check_layer(synth.make_inputs(w, "cuda"))
+        check_layer(synth.make_inputs(w, "cuda"), tuning=tune)
 
 
 def test_deterministic_bitwise_select():

@@ -105,7 +105,25 @@ def test_permute(T, E, k, c, d):
 
 
 # --------------------------------------------------------------------------- grouped FFN
-@pytest.mark.parametrize("tile", ["128", "256", "256-static", "256-nohalf", "128-mc", "128-split",
+def _tuning_for(tile: str) -> dict:
+    """moe_tuning_t fields of a grouped-FFN variant name.
+    128: single-CTA 128-row tiles; 256: CTA-pair 256-row tiles; 128-split: the
+    gate/up projection's whole 256-row blocks on CTA pairs, the remaining rows
+    on single CTAs; *-block: every group of more than 100 rows in blocks of two
+    n-tiles, m-tile major inside a block (otherwise n-tile major throughout);
+    CTA pairs take their tiles from the workspace counter except with
+    256-static; a group's last pair tile of at most 128 rows runs as an M = 128
+    pair MMA except with 256-nohalf."""
+    opts = 0
+    if tile.endswith("nohalf"):
+        opts |= moe.MOE_TUNE_NO_HALF_TILES
+    if tile.endswith("split"):
+        opts |= moe.MOE_TUNE_GEMM1_SPLIT
+    return dict(gemm1_tile=int(tile.split("-")[0]), tile_order=1 if tile.endswith("static") else 2,
+                n_block=2 if tile.endswith("block") else 1, block_min_rows=100, options=opts)
+
+
+@pytest.mark.parametrize("tile", ["128", "256", "256-static", "256-nohalf", "128-split",
                                   "128-block", "256-block"])
 @pytest.mark.parametrize("rows,d,M,n_shared,T", [
     ([0, 1, 127, 128, 129, 300], 128, 256, 1, 200),    # empty, single, tile edges
@@ -118,22 +136,7 @@ def test_permute(T, E, k, c, d):
     ([16, 17, 111, 112, 113, 240, 33, 128], 256, 256, 1, 200),  # second projection N = 256
     ([48, 200, 97, 1], 384, 128, 0, 0),                # second projection N = 128
 ])
-def test_grouped_ffn(rows, d, M, n_shared, T, tile, monkeypatch):
-    # 128: single-CTA 128-row tiles; 128-mc: the same on clusters of two that
-    # share B tiles by multicast where N = 256; 256: CTA-pair 256-row tiles
-    # 128-split: the gate/up projection's whole 256-row blocks on CTA pairs,
-    # the remaining rows on single CTAs; *-block: every group of more than 100
-    # rows in blocks of two n-tiles, m-tile major inside a block; CTA pairs take
-    # their tiles from the workspace counter except with 256-static; a group's
-    # last pair tile of at most 128 rows runs as an M = 128 pair MMA except
-    # with 256-nohalf
-    monkeypatch.setenv("MOE_GEMM_TILE", tile.split("-")[0])
-    monkeypatch.setenv("MOE_GEMM_DYNAMIC", "0" if tile.endswith("static") else "1")
-    monkeypatch.setenv("MOE_GEMM_HALF", "0" if tile.endswith("nohalf") else "1")
-    monkeypatch.setenv("MOE_GEMM_NBLOCK", "2" if tile.endswith("block") else "0")
-    monkeypatch.setenv("MOE_GEMM_BLOCK_MIN_ROWS", "100")
-    monkeypatch.setenv("MOE_GEMM_MC", "1" if tile.endswith("mc") else "0")
-    monkeypatch.setenv("MOE_GEMM1_SPLIT", "1" if tile.endswith("split") else "0")
+def test_grouped_ffn(rows, d, M, n_shared, T, tile):
     E = len(rows)
     R = int(sum(rows))
     Ms = n_shared * M
@@ -141,7 +144,7 @@ def test_grouped_ffn(rows, d, M, n_shared, T, tile, monkeypatch):
     Tshape = T if n_shared else max(R, 1)
     k = max(1, -(-R // Tshape))
     assert k <= min(E, 8)
-    s_ffn = moe.Shape.of(Tshape, d, M, E, k, n_shared)
+    s_ffn = moe.Shape.of(Tshape, d, M, E, k, n_shared, **_tuning_for(tile))
     dev = "cuda"
     R_max = moe.moe_max_rows(s_ffn)
     assert R <= R_max
@@ -176,17 +179,15 @@ def test_grouped_ffn(rows, d, M, n_shared, T, tile, monkeypatch):
         assert_y_close(bf16_to_f64(y_s), ref_s, "y_shared")
 
 
-def test_grouped_ffn_dynamic_order_repeats(monkeypatch):
+def test_grouped_ffn_dynamic_order_repeats():
     """CTA-pair launches that take tiles from the workspace counter leave it at
     zero: back-to-back calls on one workspace (and a run of a different shape
     on it in between) give the same bits, and the oracle's values."""
-    monkeypatch.setenv("MOE_GEMM_TILE", "256")
-    monkeypatch.setenv("MOE_GEMM_DYNAMIC", "1")
     dev = "cuda"
     rows = [300, 0, 513, 77, 256, 129]
     E, d, M = len(rows), 256, 256
     R = sum(rows)
-    s_ffn = moe.Shape.of(R, d, M, E, 1, 0)
+    s_ffn = moe.Shape.of(R, d, M, E, 1, 0, gemm1_tile=256, tile_order=2)
     x_perm = synth.normal_bf16(7, synth.TID_X, (R, d), 1.0, dev)
     offsets = torch.tensor(np.concatenate([[0], np.cumsum(rows)]).astype(np.int32), device=dev)
     w1 = synth.normal_bf16(7, synth.TID_W1, (E, M, d), 0.05, dev)

@@ -63,6 +63,12 @@ MUTANTS = {
     "ec_default_c": ("double cc = (c > 0.0) ? c : 1.0;", "double cc = c;"),
     "ec_shared_missing": ("oracle_swiglu_row(d, Ms, x + (size_t)t * d, ws1, ws3, ws2, tmp);\n                for (int o = 0; o < d; ++o) yt[o] += tmp[o];",
                           "oracle_swiglu_row(d, Ms, x + (size_t)t * d, ws1, ws3, ws2, tmp);\n                for (int o = 0; o < d; ++o) yt[o] += 0.0;"),
+    "expert_rows_all_expert0": ("        size_t e = (size_t)expert[r];\n",
+                                "        size_t e = 0; (void)expert;\n"),
+    "expert_rows_w2_stride": ("w3 + e * M * d,\n                          w2 + e * d * M, out",
+                              "w3 + e * M * d,\n                          w2 + e * d * d, out"),
+    "expert_rows_w3_from_w1": ("x_rows + (size_t)r * d, w1 + e * M * d, w3 + e * M * d,",
+                               "x_rows + (size_t)r * d, w1 + e * M * d, w1 + e * M * d,"),
     "combine_shared_missing": ("yt[o] += bf16_val(y_shared[(size_t)t * d + o]);", "yt[o] += 0.0;"),
 }
 

@@ -1,8 +1,15 @@
-"""moe_route_noalloc — the router entry point for callers that cannot allocate
-device memory (no workspace; the library's static device scratch is used) —
-must give the same results as moe_route, the workspace entry point, on
-consecutive calls of different shapes.  This file is collected last so that a
-run stopping at the first failure has already run every other test."""
+"""moe_route_noalloc is the router for callers that cannot allocate device
+memory: code running under a host framework that owns all device memory
+through its own pool, plug-ins loaded into such a process, or paths where an
+allocation (and the synchronisation it may bring) is not allowed.  It takes no
+workspace; its scratch is a static device array inside the library.
+
+Checked here, through the C ABI: on consecutive calls of different shapes it
+gives the same results as moe_route (the workspace entry point) and the
+oracle's routing; it handles the largest shape its array allows and T = 0; it
+changes neither the device memory in use nor torch's allocations; shapes
+beyond its array are refused.  This file is collected last, so that a run
+stopping at the first failure has already run every other test."""
 import ctypes
 
 import numpy as np
@@ -11,7 +18,8 @@ import torch
 
 import synth
 import top_routing_expert_lb_b300 as moe
-from parity import GATE_ABS, LOSS_REL, shape_of
+from parity import GATE_ABS, LOSS_REL, assert_routing_parity, np_of, oracle_routing, shape_of, \
+    GpuOut
 from top_routing_expert_lb_b300 import _binding as B
 from top_routing_expert_lb_b300 import build as mbuild
 
@@ -26,11 +34,16 @@ def _lib():
 
 
 def _outs(w, dev="cuda"):
-    return dict(ids=torch.full((w.T, w.k), -5, dtype=torch.int32, device=dev),
-                gates=torch.full((w.T, w.k), -5.0, device=dev),
+    return dict(ids=torch.full((max(w.T, 1), max(w.k, 1)), -5, dtype=torch.int32, device=dev),
+                gates=torch.full((max(w.T, 1), max(w.k, 1)), -5.0, device=dev),
                 counts=torch.full((w.E,), -5, dtype=torch.int32, device=dev),
                 f=torch.full((w.E,), -5.0, device=dev), P=torch.full((w.E,), -5.0, device=dev),
                 lb=torch.full((1,), -5.0, device=dev), lz=torch.full((1,), -5.0, device=dev))
+
+
+def _noalloc(s, inp, o):
+    moe.moe_route_noalloc(s, inp.x, inp.wr, inp.offset, inp.sel_bias, o["ids"], o["gates"],
+                          o["counts"], o["f"], o["P"], o["lb"], o["lz"])
 
 
 def _route_both(w):
@@ -40,10 +53,9 @@ def _route_both(w):
     ws = B.alloc_workspace(s)
     moe.moe_route(s, inp.x, inp.wr, inp.offset, inp.sel_bias, ref["ids"], ref["gates"],
                   ref["counts"], ref["f"], ref["P"], ref["lb"], ref["lz"], ws)
-    moe.moe_route_noalloc(s, inp.x, inp.wr, inp.offset, inp.sel_bias, got["ids"], got["gates"],
-                          got["counts"], got["f"], got["P"], got["lb"], got["lz"])
+    _noalloc(s, inp, got)
     torch.cuda.synchronize()
-    return ref, got
+    return inp, ref, got
 
 
 def _assert_same(ref, got):
@@ -57,17 +69,72 @@ def _assert_same(ref, got):
         assert abs(a - b) <= LOSS_REL * max(abs(b), 1e-30), (key, a, b)
 
 
-def test_noalloc_router_matches_workspace_router_on_consecutive_calls():
+def _assert_oracle(inp, got):
+    """The no-allocation router's outputs against the oracle (dropless: the
+    drop mask is all zeros), with the near-tie protocol of the other tests."""
+    w = inp.w
+    g = GpuOut(None, np_of(got["ids"]), np_of(got["gates"]), np_of(got["counts"]),
+               np.zeros((w.T, w.k), np.uint8), np_of(got["f"]), np_of(got["P"]),
+               got["lb"].item(), got["lz"].item())
+    assert_routing_parity(g, oracle_routing(inp, g.ids), w)
+
+
+def test_noalloc_router_matches_workspace_router_and_oracle_on_consecutive_calls():
     shapes = [
         W("na_bias", T=700, d=1024, E=160, k=6, M=128, offsets="normal", sel_bias="uniform"),
         W("na_small", T=129, d=256, E=8, k=2, M=128),
         W("na_top1", T=3000, d=512, E=64, k=1, M=128, offsets="normal"),
     ]
     for w in shapes:           # consecutive calls reuse the same static scratch
-        ref, got = _route_both(w)
+        inp, ref, got = _route_both(w)
         _assert_same(ref, got)
-    ref, got = _route_both(shapes[0])  # and back to the first shape
+        _assert_oracle(inp, got)
+    inp, ref, got = _route_both(shapes[0])  # and back to the first shape
     _assert_same(ref, got)
+    _assert_oracle(inp, got)
+
+
+def test_noalloc_router_at_its_size_limit():
+    """T = 65536 tokens and E = 256 experts fill every per-tile and per-expert
+    region of the static array."""
+    w = W("na_limit", T=65536, d=64, E=256, k=8, M=128, offsets="normal")
+    inp, ref, got = _route_both(w)
+    _assert_same(ref, got)
+    _assert_oracle(inp, got)
+
+
+def test_noalloc_router_with_no_tokens():
+    """T = 0: no router launch, only the reduction, which writes zero counts,
+    f, P and losses."""
+    w = W("na_empty", T=0, d=128, E=16, k=2, M=128)
+    inp = synth.make_inputs(w, "cuda", experts=False)
+    got = _outs(w)
+    _noalloc(shape_of(w), inp, got)
+    torch.cuda.synchronize()
+    assert got["counts"].tolist() == [0] * w.E
+    assert got["f"].abs().max().item() == 0.0 and got["P"].abs().max().item() == 0.0
+    assert got["lb"].item() == 0.0 and got["lz"].item() == 0.0
+
+
+def test_noalloc_router_allocates_nothing():
+    """After a first call on the device (which may load the library's kernels
+    and its static array), further calls leave the device's free memory and
+    torch's allocations unchanged."""
+    w = W("na_mem", T=1000, d=256, E=32, k=4, M=128, offsets="normal")
+    inp = synth.make_inputs(w, "cuda", experts=False)
+    s = shape_of(w)
+    got = _outs(w)
+    _noalloc(s, inp, got)
+    torch.cuda.synchronize()
+    torch_before = torch.cuda.memory_allocated()
+    free_before, _ = torch.cuda.mem_get_info()
+    for _ in range(3):
+        _noalloc(s, inp, got)
+    torch.cuda.synchronize()
+    free_after, _ = torch.cuda.mem_get_info()
+    assert torch.cuda.memory_allocated() == torch_before
+    assert free_after == free_before
+    _assert_oracle(inp, got)
 
 
 def test_noalloc_router_rejects_shapes_beyond_its_scratch():

@@ -41,15 +41,45 @@ class RouteOut(ctypes.Structure):
                                                 "entropy_mean")]
 
 
+MOE_TUNE_NO_HALF_TILES = 1
+MOE_TUNE_GEMM1_SPLIT = 2
+MOE_TUNE_FUSED_GATHER = 4
+MOE_TUNE_GATE_IN_EPILOGUE = 8
+
+
+class Tuning(ctypes.Structure):
+    """moe_tuning_t: scheduling choices of the expert GEMMs (all zero: the
+    measured defaults)."""
+    _fields_ = [("gemm1_tile", ctypes.c_int32), ("gemm2_tile", ctypes.c_int32),
+                ("tile_order", ctypes.c_int32), ("tail_max_n", ctypes.c_int32),
+                ("n_block", ctypes.c_int32), ("block_min_rows", ctypes.c_int32),
+                ("options", ctypes.c_uint32), ("reserved", ctypes.c_uint32),
+                ("wait_timeout_ns", ctypes.c_uint64)]
+
+
 class Shape(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int32), ("d", ctypes.c_int32), ("M", ctypes.c_int32),
                 ("E", ctypes.c_int32), ("k", ctypes.c_int32), ("n_shared", ctypes.c_int32),
                 ("capacity_factor", ctypes.c_float), ("balance_coef", ctypes.c_float),
-                ("flags", ctypes.c_uint32)]
+                ("flags", ctypes.c_uint32), ("reserved", ctypes.c_uint32),
+                ("tuning", Tuning)]
 
     @classmethod
-    def of(cls, T, d, M, E, k, n_shared=0, capacity_factor=0.0, balance_coef=0.01, flags=0):
-        return cls(T, d, M, E, k, n_shared, capacity_factor, balance_coef, flags)
+    def of(cls, T, d, M, E, k, n_shared=0, capacity_factor=0.0, balance_coef=0.01, flags=0,
+           **tuning):
+        """Shape with the default tuning; keyword arguments set moe_tuning_t
+        fields (e.g. gemm1_tile=256, options=MOE_TUNE_FUSED_GATHER)."""
+        return cls(T, d, M, E, k, n_shared, capacity_factor, balance_coef, flags, 0,
+                   Tuning(**tuning))
+
+    def tuned(self, **tuning) -> "Shape":
+        """A copy of this shape with the given moe_tuning_t fields changed."""
+        t = Tuning()
+        ctypes.pointer(t)[0] = self.tuning
+        for key, v in tuning.items():
+            setattr(t, key, v)
+        return Shape(self.T, self.d, self.M, self.E, self.k, self.n_shared, self.capacity_factor,
+                     self.balance_coef, self.flags, 0, t)
 
     @property
     def Ms(self) -> int:

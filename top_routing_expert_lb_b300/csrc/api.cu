@@ -3,10 +3,9 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdint>
-#include <cstdlib>
-#include <cstring>
 #include <vector>
 
 #include "../../include/moe.h"
@@ -16,7 +15,7 @@ namespace moe {
 
 namespace {
 
-uint64_t g_timeout_ns = 2000000000ull;
+std::atomic<uint64_t> g_timeout_ns{2000000000ull};
 
 // ---------------------------------------------------------------- accounting
 uint64_t g_launches = 0;
@@ -99,7 +98,25 @@ int check_shape(const moe_shape_t* s) {
   if (s->d % 64 != 0 || s->d < 64 || s->d > 16384) return MOE_ERR_UNSUPPORTED;
   if (s->M % 128 != 0 || s->M < 128 || s->M > 32768) return MOE_ERR_UNSUPPORTED;
   if (s->n_shared > 8) return MOE_ERR_UNSUPPORTED;
+  if (s->reserved != 0) return MOE_ERR_INVALID_ARG;
+  const moe_tuning_t& t = s->tuning;
+  auto tile_ok = [](int32_t v) { return v == 0 || v == 128 || v == 256; };
+  if (!tile_ok(t.gemm1_tile) || !tile_ok(t.gemm2_tile)) return MOE_ERR_INVALID_ARG;
+  if (t.tile_order < 0 || t.tile_order > 2) return MOE_ERR_INVALID_ARG;
+  if (t.tail_max_n > 0 && (t.tail_max_n < 16 || t.tail_max_n > 128)) return MOE_ERR_INVALID_ARG;
+  if (t.n_block < 0 || t.n_block > 64 || t.block_min_rows < 0) return MOE_ERR_INVALID_ARG;
+  if ((t.options & ~(MOE_TUNE_NO_HALF_TILES | MOE_TUNE_GEMM1_SPLIT | MOE_TUNE_FUSED_GATHER |
+                     MOE_TUNE_GATE_IN_EPILOGUE)) != 0 || t.reserved != 0)
+    return MOE_ERR_INVALID_ARG;
+  if ((t.options & MOE_TUNE_FUSED_GATHER) && t.gemm1_tile == 256) return MOE_ERR_INVALID_ARG;
+  if (t.gemm2_tile == 256 && s->d % 256 != 0) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
+}
+
+// Limit of this call's bounded device waits.
+uint64_t timeout_of(const moe_shape_t* s) {
+  return s->tuning.wait_timeout_ns != 0 ? s->tuning.wait_timeout_ns
+                                          : g_timeout_ns.load(std::memory_order_relaxed);
 }
 
 int64_t capacity_of(const moe_shape_t* s) {
@@ -187,16 +204,16 @@ int check_ws(const moe_shape_t* s, void* ws, size_t ws_bytes, Layout* L) {
 }
 
 int sm_count_cached() {
-  static int cache[64] = {0};
+  static std::atomic<int> cache[64];  // 0 until looked up; racing writers store the same value
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-  if (cache[dev] == 0) {
-    int n = 0;
+  int n = cache[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
       n = 148;
-    cache[dev] = n;
+    cache[dev].store(n, std::memory_order_relaxed);
   }
-  return cache[dev];
+  return n;
 }
 
 inline int cuda_rc(int rc) {
@@ -242,7 +259,7 @@ int do_route(const moe_shape_t* s, const uint16_t* x, const uint16_t* wr, const 
     ra.tile_psum = at<float>(ws, L.tile_psum);
     ra.tile_lse2 = at<float>(ws, L.tile_lse2);
     ra.status = at<int>(ws, L.status);
-    ra.timeout_ns = g_timeout_ns;
+    ra.timeout_ns = timeout_of(s);
     ra.flags = s->flags & (kRouteSigmoid | kRouteNoRenorm);
     ra.tile_imp = want_imp ? at<float>(ws, L.tile_imp) : nullptr;
     ra.tile_ent = want_ent ? at<float>(ws, L.tile_ent) : nullptr;
@@ -383,36 +400,20 @@ int do_ec_route(const moe_shape_t* s, const uint16_t* x, const uint16_t* wr, con
   return cuda_rc(tracked(MOE_KERNEL_SELECT, st, [&] { return launch_ec_select(ea, st); }));
 }
 
-// Gate/up projection tile: MOE_GEMM_TILE=256 forces 256-row tiles on CTA
-// pairs, =128 single-CTA 128-row tiles; unset, the layer picks by the
-// average rows per expert (see do_ffn).  Returns 1, 0 or -1 (unset).
-int gemm_tile_env() {
-  const char* env = std::getenv("MOE_GEMM_TILE");
-  if (env == nullptr) return -1;
-  if (std::strcmp(env, "256") == 0) return 1;
-  if (std::strcmp(env, "128") == 0) return 0;
-  return -1;
-}
-
-// With MOE_FUSED_GATHER=1 the layer feeds GEMM-1 straight from the token
-// rows (TMA 4-row gathers by row_token, no x_perm); by default the scatter
-// materialises x_perm and GEMM-1 reads it with one box load per k-block.  The
-// gather issues 32 TMA instructions per k-block instead of one and measured
-// about 3.5x slower in GEMM-1, so it stays opt-in.  The paired GEMM always
-// reads x_perm.
-// MOE_GATE_IN_EPILOGUE=1: the down projection's epilogue multiplies each
+// The gate/up projection feeds from the token rows itself (TMA 4-row gathers by
+// row_token, no x_perm) only with MOE_TUNE_FUSED_GATHER: the gather issues 32
+// TMA instructions per k-block instead of one and measured about 3.5x slower
+// in GEMM-1, so the default materialises x_perm in the scatter.
+// MOE_TUNE_GATE_IN_EPILOGUE: the down projection's epilogue multiplies each
 // routed row by its gate (fp32, before rounding) and the combine only adds the
 // rows in slot order (or expert order).  Same bytes, one multiply moved; off
-// by default.
-bool gate_in_epilogue() {
-  const char* env = std::getenv("MOE_GATE_IN_EPILOGUE");
-  return env != nullptr && std::strcmp(env, "1") == 0;
+// by default (measured within noise).
+bool gate_in_epilogue(const moe_shape_t* s) {
+  return (s->tuning.options & MOE_TUNE_GATE_IN_EPILOGUE) != 0;
 }
 
-bool fused_gather() {
-  const char* env = std::getenv("MOE_FUSED_GATHER");
-  if (env == nullptr || std::strcmp(env, "1") != 0) return false;
-  return gemm_tile_env() != 1;
+bool fused_gather(const moe_shape_t* s) {
+  return (s->tuning.options & MOE_TUNE_FUSED_GATHER) != 0;
 }
 
 // x_perm: routed rows, or null with gather_rows (token row of every routed
@@ -441,27 +442,19 @@ int do_ffn(const moe_shape_t* s, const uint16_t* x_perm, const int32_t* offsets,
   // 256 rows.  With many experts of skewed sizes (DeepSeekMoE-16B) that
   // padding cost 13 % in this projection, so single-CTA tiles (transposed
   // tails) stay the default there.  Gathered rows need the single-CTA kernel.
-  const int tile_env = gemm_tile_env();
-  if (tile_env == 1 && gather_rows != nullptr) return MOE_ERR_INVALID_ARG;  // needs x_perm
+  const moe_tuning_t& tune = s->tuning;
+  if (tune.gemm1_tile == 256 && gather_rows != nullptr) return MOE_ERR_INVALID_ARG;  // needs x_perm
   const bool paired =
       gather_rows == nullptr &&
-      (tile_env == 1 || (tile_env < 0 && rows_per_expert >= 512 && E <= 16));
-  // MOE_GEMM_MC=1: clusters of two CTAs sharing each B tile through TMA
-  // multicast (half the B bytes from L2 per tile; measured slower than
-  // independent CTAs on every workload, so off by default); not with the
-  // paired tiles or gathered rows
-  bool mc = false;
-  if (const char* env = std::getenv("MOE_GEMM_MC")) mc = !paired && std::strcmp(env, "1") == 0;
-  const bool mc1 = mc && gather_rows == nullptr;
-  const uint32_t bbox = (paired || mc1) ? 128u : 256u;
-  // MOE_GEMM1_SPLIT=1: the first projection runs each group's whole 256-row
+      (tune.gemm1_tile == 256 || (tune.gemm1_tile == 0 && rows_per_expert >= 512 && E <= 16));
+  const uint32_t bbox = paired ? 128u : 256u;
+  // MOE_TUNE_GEMM1_SPLIT: the first projection runs each group's whole 256-row
   // blocks on CTA-pair tiles and only the remaining rows (< 256 per group) on
   // single-CTA tiles (two launches, both counted as the gate/up kernel).
   // Measured 9 % slower than single-CTA tiles throughout on Mixtral, so off
   // by default.
-  bool split1 = false;
-  if (const char* env = std::getenv("MOE_GEMM1_SPLIT")) split1 = std::strcmp(env, "1") == 0;
-  split1 = split1 && !paired && !mc1 && gather_rows == nullptr && nsm >= 2;
+  const bool split1 = (tune.options & MOE_TUNE_GEMM1_SPLIT) != 0 && !paired &&
+                      gather_rows == nullptr && nsm >= 2;
 
   // projection 1: [x_perm | x] -> h = SiLU(gate) * up
   CUtensorMap a0, a1, b0, b1;
@@ -508,40 +501,37 @@ int do_ffn(const moe_shape_t* s, const uint16_t* x_perm, const int32_t* offsets,
   g1.out_shared = h_s;
   g1.ld_shared = Ms;
   g1.status = at<int>(ws, L.status);
-  g1.timeout_ns = g_timeout_ns;
+  g1.timeout_ns = timeout_of(s);
   g1.gather_rows = routed ? gather_rows : nullptr;
-  if (const char* env = std::getenv("MOE_GEMM_TAIL_MAX_N")) g1.tail_max_n = std::atoi(env);
-  if (const char* env = std::getenv("MOE_GEMM_NBLOCK")) g1.n_block = std::atoi(env);
+  if (tune.tail_max_n != 0) g1.tail_max_n = tune.tail_max_n < 0 ? 0 : tune.tail_max_n;
+  if (tune.n_block != 0) g1.n_block = tune.n_block;
+  if (tune.block_min_rows != 0) g1.block_min_rows = tune.block_min_rows;
   // CTA-pair launches with long tiles (K >= 4096) take their tiles from a
   // counter in the workspace: the dynamic order keeps the pairs that share a
   // weight tile in step (Mixtral: DRAM bytes of the gate/up projection down
   // from 2.7 GB to the algorithmic 1.95 GB).  With short tiles on skewed
   // shapes (DeepSeekMoE-16B, K = 1408) the static round-robin order measured
-  // 3 % faster.  MOE_GEMM_DYNAMIC=0|1 forces either order.
-  int dyn_env = -1;
-  if (const char* env = std::getenv("MOE_GEMM_DYNAMIC")) dyn_env = std::atoi(env) != 0 ? 1 : 0;
+  // 3 % faster.  tile_order 1 / 2 forces either order.
   int* tile_counter = at<int>(ws, L.status + 128);
   auto dynamic_for = [&](int64_t K) {
-    return (dyn_env == 1 || (dyn_env < 0 && K >= 4096)) ? tile_counter : nullptr;
+    return (tune.tile_order == 2 || (tune.tile_order == 0 && K >= 4096)) ? tile_counter : nullptr;
   };
   g1.tile_counter = dynamic_for(d);
-  if (const char* env = std::getenv("MOE_GEMM_HALF")) g1.half_tiles = std::atoi(env) != 0 ? 1 : 0;
-  if (const char* env = std::getenv("MOE_GEMM_BLOCK_MIN_ROWS")) g1.block_min_rows = std::atoi(env);
+  g1.half_tiles = (tune.options & MOE_TUNE_NO_HALF_TILES) ? 0 : 1;
   int rc = 0;
   if (split1) {
     GroupedGemmArgs g1p = g1;
     g1p.row_split = 1;
     rc = tracked(MOE_KERNEL_GEMM_SWIGLU, st, [&] {
-      return launch_grouped_gemm(a0, a1, bp0, bp1, g1p, true, 256, true, nsm, st, false, &bh0,
-                                 &bh1);
+      return launch_grouped_gemm(a0, a1, bp0, bp1, g1p, true, 256, true, nsm, st, &bh0, &bh1);
     });
     if (rc != 0) return cuda_rc(rc);
     g1.row_split = 2;
   }
   rc = tracked(MOE_KERNEL_GEMM_SWIGLU, st,
                [&] {
-                 return launch_grouped_gemm(a0, a1, b0, b1, g1, true, 256, paired, nsm, st,
-                                            mc1, &bh0, &bh1);
+                 return launch_grouped_gemm(a0, a1, b0, b1, g1, true, 256, paired, nsm, st, &bh0,
+                                            &bh1);
                });
   if (rc != 0) return cuda_rc(rc);
   g1.row_split = 0;
@@ -551,15 +541,12 @@ int do_ffn(const moe_shape_t* s, const uint16_t* x_perm, const int32_t* offsets,
   // when experts average at least 512 rows: the pair halves the operand bytes
   // per FLOP and the 256-row padding stays small (measured 3 % faster steps on
   // Mixtral in the power-limited loop); with fewer rows per expert the padding
-  // costs more than the pair saves.  MOE_GEMM2_TILE=128|256 overrides.
+  // costs more than the pair saves.  gemm2_tile 128 / 256 overrides.
   bool paired2 = bn2 == 256 && (paired || rows_per_expert >= 512);
-  if (const char* env = std::getenv("MOE_GEMM2_TILE")) {
-    if (std::strcmp(env, "128") == 0) paired2 = false;
-    if (std::strcmp(env, "256") == 0) paired2 = bn2 == 256;
-  }
-  // the pair and multicast forms load B in 128-row halves
-  const bool mc2 = mc && bn2 == 256 && !paired2;
-  const uint32_t bbox2 = (paired2 || mc2) ? 128u : static_cast<uint32_t>(bn2);
+  if (tune.gemm2_tile == 128) paired2 = false;
+  if (tune.gemm2_tile == 256) paired2 = bn2 == 256;
+  // the pair form loads B in 128-row halves
+  const uint32_t bbox2 = paired2 ? 128u : static_cast<uint32_t>(bn2);
   if (routed) {
     if (!make_tmap_bf16(&a0, h, L.rmax, M, 128)) return MOE_ERR_CUDA;
     if (!make_tmap_bf16(&b0, w2, E * d, M, bbox2)) return MOE_ERR_CUDA;
@@ -584,13 +571,15 @@ int do_ffn(const moe_shape_t* s, const uint16_t* x_perm, const int32_t* offsets,
   g2.ld_shared = d;
   rc = tracked(MOE_KERNEL_GEMM_DOWN, st,
                [&] {
-                 return launch_grouped_gemm(a0, a1, b0, b1, g2, false, bn2, paired2, nsm, st,
-                                            mc2);
+                 return launch_grouped_gemm(a0, a1, b0, b1, g2, false, bn2, paired2, nsm, st);
                });
   return cuda_rc(rc);
 }
 
 }  // namespace
+
+uint64_t default_wait_timeout_ns() { return g_timeout_ns.load(std::memory_order_relaxed); }
+
 }  // namespace moe
 
 using namespace moe;
@@ -797,8 +786,8 @@ int moe_layer_forward(const moe_shape_t* s, const uint16_t* x, const uint16_t* w
   uint16_t* x_perm = at<uint16_t>(ws, L.x_perm);
   uint16_t* y_perm = at<uint16_t>(ws, L.y_perm);
   uint16_t* y_s = s->n_shared > 0 ? at<uint16_t>(ws, L.y_s) : nullptr;
-  const bool fused = fused_gather();
-  const bool gate_epi = gate_in_epilogue() && s->k > 0;
+  const bool fused = fused_gather(s);
+  const bool gate_epi = gate_in_epilogue(s) && s->k > 0;
   int32_t* row_token = at<int32_t>(ws, L.row_token);
   float* row_gate = gate_epi ? at<float>(ws, L.row_gate) : nullptr;
   if (s->k > 0) {
@@ -990,7 +979,7 @@ int moe_ec_layer_forward(const moe_shape_t* s, const uint16_t* x, const uint16_t
   uint16_t* x_perm = at<uint16_t>(ws, L.x_perm);
   uint16_t* y_perm = at<uint16_t>(ws, L.y_perm);
   uint16_t* y_s = s->n_shared > 0 ? at<uint16_t>(ws, L.y_s) : nullptr;
-  const bool fused = fused_gather();
+  const bool fused = fused_gather(s);
   if (L.rmax > 0 && !fused) {
     rc = cuda_rc(tracked(MOE_KERNEL_GATHER, st, [&] {
       return launch_gather_rows(x, row_token, offsets, s->E, s->d, L.rmax, x_perm,
@@ -998,7 +987,7 @@ int moe_ec_layer_forward(const moe_shape_t* s, const uint16_t* x, const uint16_t
     }));
     if (rc != MOE_OK) return rc;
   }
-  const bool gate_epi = gate_in_epilogue() && L.rmax > 0;
+  const bool gate_epi = gate_in_epilogue(s) && L.rmax > 0;
   rc = do_ffn(s, fused ? nullptr : x_perm, offsets, w13, w2, y_perm, x, w13_shared, w2_shared,
               y_s, ws, L, st, fused ? row_token : nullptr, gate_epi ? row_gate : nullptr);
   if (rc != MOE_OK) return rc;
@@ -1023,7 +1012,7 @@ int moe_check_status(void* ws, int* status, void* stream) {
 
 int moe_set_wait_timeout_ns(uint64_t ns) {
   if (ns == 0) return MOE_ERR_INVALID_ARG;
-  g_timeout_ns = ns;
+  g_timeout_ns.store(ns, std::memory_order_relaxed);
   return MOE_OK;
 }
 
@@ -1032,7 +1021,7 @@ int moe_debug_timeout_probe(void* ws, size_t ws_bytes, void* stream) {
     return MOE_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   return cuda_rc(tracked(MOE_KERNEL_OTHER, st, [&] {
-    return launch_timeout_probe(static_cast<int*>(ws), g_timeout_ns, st);
+    return launch_timeout_probe(static_cast<int*>(ws), default_wait_timeout_ns(), st);
   }));
 }
 

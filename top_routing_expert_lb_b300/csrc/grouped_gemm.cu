@@ -128,44 +128,9 @@ __device__ __forceinline__ TileInfo decode_tile(const Tail* st, const GroupedGem
   return ti;
 }
 
-// Cluster-multicast variant (kMC): the two CTAs of a cluster compute m-tiles
-// 2j and 2j+1 of the same group and n-tile, so they need the same B tile.
-// Each CTA loads its own A rows and one half of the B tile, multicast into
-// both CTAs: every B byte crosses from L2 once per two tiles.  Work items are
-// numbered per pair; a group with an odd m-tile count ends with a pair whose
-// second CTA repeats the first one's tile without storing it (rows_left = 0).
-template <typename Tail>
-__device__ __forceinline__ TileInfo decode_mc_tile(const Tail* st, const GroupedGemmArgs& p,
-                                                   int G, int pair, int bn, uint32_t rank) {
-  int lo = 0, hi = G;  // largest g with prefix[g] <= pair
-  while (hi - lo > 1) {
-    int mid = (lo + hi) >> 1;
-    if (st->prefix[mid] <= pair) lo = mid; else hi = mid;
-  }
-  TileInfo ti;
-  ti.g = lo;
-  const int has_shared = p.shared_rows > 0 ? 1 : 0;
-  ti.shared = (has_shared && lo == 0) ? 1 : 0;
-  const int rows = st->rows[lo];
-  const int mt = (rows + kBM - 1) / kBM;
-  const int mp = (mt + 1) / 2;
-  const int local = pair - st->prefix[lo];
-  ti.n = local / mp;
-  int m = 2 * (local - ti.n * mp) + static_cast<int>(rank);
-  const bool dup = m >= mt;
-  if (dup) m = mt - 1;
-  ti.a_row = st->row0[lo] + m * kBM;
-  ti.rows_left = dup ? 0 : rows - m * kBM;
-  const int ncols = ti.shared ? p.n_cols_shared : p.n_cols_routed;
-  const int e = lo - has_shared;
-  ti.b_row = (ti.shared ? 0 : e * ncols) + ti.n * bn;
-  ti.nk = (ti.shared ? p.k_shared : p.k_routed) / kBK;
-  return ti;
-}
-
 // kRowScale (plain projections only): every routed output row r is multiplied
 // by p.row_scale[r] in fp32 before rounding (the combine's gate, applied here).
-template <int BN, bool kSwiGLU, int kStages, bool kMC = false, bool kRowScale = false>
+template <int BN, bool kSwiGLU, int kStages, bool kRowScale = false>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
                         const __grid_constant__ CUtensorMap tmA1,
@@ -177,7 +142,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kStageBytes = kABytes + kBBytes;
   constexpr uint32_t kTmemCols = 2 * BN;
   constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, BN);
-  static_assert(!kMC || BN == 256, "multicast halves a 256-row B tile");
   static_assert(!(kRowScale && kSwiGLU), "row scaling applies to the plain projection");
 
   extern __shared__ uint8_t smem_raw[];
@@ -190,15 +154,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
   const int has_shared = p.shared_rows > 0 ? 1 : 0;
   const int G = p.n_routed + has_shared;
-  // multicast: cluster rank, first work item and stride (pairs of tiles)
-  const uint32_t rank = kMC ? cluster_ctarank() : 0u;
-  const int item0 = kMC ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
-  const int stride = kMC ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+  const int item0 = static_cast<int>(blockIdx.x);
+  const int stride = static_cast<int>(gridDim.x);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&st->full[s], 1);
-      mbar_init(&st->empty[s], kMC ? 2 : 1);  // multicast: both CTAs release a stage
+      mbar_init(&st->empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&st->tfull[a], 1);
@@ -233,7 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       st->rows[g] = rows;
       const int ncols = sh ? p.n_cols_shared : p.n_cols_routed;
       const int mt = (rows + kBM - 1) / kBM;
-      acc += (kMC ? (mt + 1) / 2 : mt) * (ncols / BN);
+      acc += mt * (ncols / BN);
       st->prefix[g + 1] = acc;
     }
     fence_barrier_init();
@@ -247,14 +209,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_alloc(&st->tmem_base, kTmemCols);
   tc_fence_before();
   __syncthreads();
-  if constexpr (kMC) cluster_arrive_wait();  // the peer's barriers exist before any remote signal
   tc_fence_after();
   const uint32_t tmem_base = st->tmem_base;
   const int total = st->prefix[G];
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (kMC || p.gather_rows == nullptr) {
+    if (p.gather_rows == nullptr) {
       // box loads: lane 0 alone runs the ring
       if (lane == 0) {
         int stage = 0;
@@ -263,31 +224,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int s = 0; s < kStages; ++s) uses[s] = 0;
         for (int tile = item0; tile < total && !*abort_flag; tile += stride) {
-          const TileInfo ti = kMC ? decode_mc_tile(st, p, G, tile, BN, rank)
-                                  : decode_tile(st, p, G, tile, BN);
+          const TileInfo ti = decode_tile(st, p, G, tile, BN);
           const CUtensorMap* am = ti.shared ? &tmA1 : &tmA0;
           const CUtensorMap* bm = ti.shared ? &tmB1 : &tmB0;
           bool ok = true;
           for (int kb = 0; kb < ti.nk; ++kb) {
-            if (!mbar_wait_bounded<kMC>(&st->empty[stage], phase ^ 1u, p.timeout_ns, p.status,
-                                        abort_flag)) {
+            if (!mbar_wait_bounded(&st->empty[stage], phase ^ 1u, p.timeout_ns, p.status,
+                                   abort_flag)) {
               ok = false;
               break;
             }
             uint8_t* sa = smem + stage * kStageBytes;
-            // a repeated tile (second CTA of a group's last odd m-tile) only
-            // supplies its half of B to the other CTA
-            const bool dup = kMC && ti.rows_left == 0;
-            mbar_arrive_expect_tx(&st->full[stage], dup ? kBBytes : kStageBytes);
-            if (!dup) tma_load_2d(sa, am, &st->full[stage], kb * kBK, ti.a_row);
-            if constexpr (kMC) {
-              // this CTA's half of the B tile, into both CTAs of the cluster
-              const int half = static_cast<int>(rank) * (BN / 2);
-              tma_load_2d_mc(sa + kABytes + half * (kBK * 2), bm, &st->full[stage], kb * kBK,
-                             ti.b_row + half, 0x3);
-            } else {
-              tma_load_2d(sa + kABytes, bm, &st->full[stage], kb * kBK, ti.b_row);
-            }
+            mbar_arrive_expect_tx(&st->full[stage], kStageBytes);
+            tma_load_2d(sa, am, &st->full[stage], kb * kBK, ti.a_row);
+            tma_load_2d(sa + kABytes, bm, &st->full[stage], kb * kBK, ti.b_row);
             uses[stage] += 1;
             if (++stage == kStages) {
               stage = 0;
@@ -301,17 +251,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int s = 0; s < kStages; ++s)
           if (uses[s] > 0)
-            mbar_wait_bounded<kMC>(&st->full[s], (uses[s] - 1u) & 1u, p.timeout_ns, p.status,
-                                   nullptr);
-        if constexpr (kMC) {
-          // and both CTAs' releases of each stage's last use: every arrival
-          // the peer sends to this CTA has landed before either CTA exits
-#pragma unroll
-          for (int s = 0; s < kStages; ++s)
-            if (uses[s] > 0)
-              mbar_wait_bounded<true>(&st->empty[s], (uses[s] - 1u) & 1u, p.timeout_ns,
-                                      p.status, nullptr);
-        }
+            mbar_wait_bounded(&st->full[s], (uses[s] - 1u) & 1u, p.timeout_ns, p.status,
+                              nullptr);
       }
       __syncwarp();
     } else {
@@ -389,8 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       int local = 0;
       for (int tile = item0; tile < total && !*abort_flag; tile += stride, ++local) {
-        const TileInfo ti = kMC ? decode_mc_tile(st, p, G, tile, BN, rank)
-                                : decode_tile(st, p, G, tile, BN);
+        const TileInfo ti = decode_tile(st, p, G, tile, BN);
         const int a = local & 1;
         const uint32_t q = static_cast<uint32_t>(local >> 1);
         if (!mbar_wait_bounded(&st->tempty[a], (q & 1u) ^ 1u, p.timeout_ns, p.status,
@@ -402,17 +342,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t idesc_sw = idesc_bf16_f32(kBM, static_cast<uint32_t>(nsw > 0 ? nsw : 16));
         bool ok = true;
         for (int kb = 0; kb < ti.nk; ++kb) {
-          if (!mbar_wait_bounded<kMC>(&st->full[stage], phase, p.timeout_ns, p.status,
-                                      abort_flag)) {
+          if (!mbar_wait_bounded(&st->full[stage], phase, p.timeout_ns, p.status,
+                                 abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + stage * kStageBytes);
           const uint32_t sb = sa + kABytes;
-          if (kMC && ti.rows_left == 0) {
-            // repeated tile: nothing to compute, the stage is only released
-          } else if (nsw == 0) {
+          if (nsw == 0) {
 #pragma unroll
             for (int kk = 0; kk < kBK / 16; ++kk) {
               tc_mma_bf16(d_tmem, smem_desc_sw128(sa + kk * 32), smem_desc_sw128(sb + kk * 32),
@@ -431,10 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             smem_desc_sw128(sa + kk * 32), idesc_sw, (kb | kk) != 0 ? 1u : 0u);
             }
           }
-          if constexpr (kMC)
-            tc_commit_mc(&st->empty[stage], 0x3);  // both CTAs wrote into this stage
-          else
-            tc_commit(&st->empty[stage]);
+          tc_commit(&st->empty[stage]);
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
@@ -453,8 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r_in_tile = quarter * 32 + lane;
     int local = 0;
     for (int tile = item0; tile < total && !*abort_flag; tile += stride, ++local) {
-      const TileInfo ti = kMC ? decode_mc_tile(st, p, G, tile, BN, rank)
-                              : decode_tile(st, p, G, tile, BN);
+      const TileInfo ti = decode_tile(st, p, G, tile, BN);
       const int a = local & 1;
       const uint32_t q = static_cast<uint32_t>(local >> 1);
       if (!mbar_wait_bounded(&st->tfull[a], q & 1u, p.timeout_ns, p.status, abort_flag)) break;
@@ -558,7 +492,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if constexpr (kMC) cluster_arrive_wait();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
 }
@@ -569,8 +502,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // tcgen05 cta_group::2.  Each CTA stages its 128 rows of A and its 128 rows of
 // B (half of N) per k-block, so one SM moves 32 KB per 64-deep k-block instead
 // of 48 KB and the ring holds 6 stages.  The even CTA issues the MMAs; its
-// full barrier collects the TMA bytes of both CTAs; MMA completion is
-// multicast to the empty / accumulator-full barriers of both CTAs; both CTAs'
+// full barrier collects the TMA bytes of both CTAs; each MMA completion
+// arrives on the empty / accumulator-full barriers of both CTAs; both CTAs'
 // epilogue warps release an accumulator buffer on the even CTA's barrier.
 // ---------------------------------------------------------------------------
 constexpr int kPairBM = 256;
@@ -1010,7 +943,7 @@ int launch_impl(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap&
                 cudaStream_t stream) {
   constexpr size_t smem = gemm_smem_bytes<BN, kStages>();
   static_assert(smem <= 227 * 1024, "shared memory budget");
-  auto kern = grouped_gemm_kernel<BN, kSwiGLU, kStages, false, kRowScale>;
+  auto kern = grouped_gemm_kernel<BN, kSwiGLU, kStages, kRowScale>;
   static bool attr_set = false;
   if (!attr_set) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1019,42 +952,6 @@ int launch_impl(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap&
     attr_set = true;
   }
   kern<<<num_sms, kThreads, smem, stream>>>(a0, a1, b0, b1, args);
-  return cudaGetLastError() == cudaSuccess ? 0 : -3;
-}
-
-// Cluster-multicast launch: clusters of two CTAs, as many as can be resident
-// at once (one CTA per SM), so the persistent loop never waits for a second
-// wave.
-template <int BN, bool kSwiGLU, int kStages>
-int launch_mc_impl(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b0,
-                   const CUtensorMap& b1, const GroupedGemmArgs& args, int num_sms,
-                   cudaStream_t stream) {
-  constexpr size_t smem = gemm_smem_bytes<BN, kStages>();
-  auto kern = grouped_gemm_kernel<BN, kSwiGLU, kStages, true>;
-  static int max_clusters = 0;
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attrs[1];
-  attrs[0].id = cudaLaunchAttributeClusterDimension;
-  attrs[0].val.clusterDim.x = 2;
-  attrs[0].val.clusterDim.y = 1;
-  attrs[0].val.clusterDim.z = 1;
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cfg.attrs = attrs;
-  cfg.numAttrs = 1;
-  if (max_clusters == 0) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess)
-      return -3;
-    cfg.gridDim = dim3(static_cast<unsigned>(num_sms & ~1));
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) return -3;
-    max_clusters = n;
-  }
-  int clusters = max_clusters < num_sms / 2 ? max_clusters : num_sms / 2;
-  cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters));
-  if (cudaLaunchKernelEx(&cfg, kern, a0, a1, b0, b1, args) != cudaSuccess) return -3;
   return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }
 
@@ -1090,16 +987,11 @@ bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t 
 
 int launch_grouped_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b0,
                         const CUtensorMap& b1, const GroupedGemmArgs& args, bool swiglu, int bn,
-                        bool paired, int num_sms, cudaStream_t stream, bool multicast,
-                        const CUtensorMap* b0h, const CUtensorMap* b1h) {
+                        bool paired, int num_sms, cudaStream_t stream, const CUtensorMap* b0h,
+                        const CUtensorMap* b1h) {
   if (args.n_routed + (args.shared_rows > 0 ? 1 : 0) > kMaxGroups) return -2;
   const bool scale = args.row_scale != nullptr;
-  if (scale && (swiglu || multicast)) return -2;
-  if (multicast) {
-    if (paired || bn != 256 || args.gather_rows != nullptr || num_sms < 2) return -2;
-    return swiglu ? launch_mc_impl<256, true, 4>(a0, a1, b0, b1, args, num_sms, stream)
-                  : launch_mc_impl<256, false, 4>(a0, a1, b0, b1, args, num_sms, stream);
-  }
+  if (scale && swiglu) return -2;
   if (paired) {
     if (bn != 256 || num_sms < 2) return -2;
     if (scale) return launch_pair_impl<false, true>(a0, a1, b0, b1, b0, b1, args, num_sms, stream);

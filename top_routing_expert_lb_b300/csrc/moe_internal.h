@@ -47,7 +47,7 @@ struct GroupedGemmArgs {
   const float* row_scale = nullptr;
   // Tile order inside a group with more than block_min_rows rows: blocks of
   // n_block n-tiles, m-tile major inside a block (n_block <= 1: n-tile major
-  // throughout).  Not with multicast.
+  // throughout).
   int32_t n_block = 8;
   int32_t block_min_rows = 2048;
   // Pair kernel: when set, tiles are taken dynamically from this counter
@@ -64,14 +64,11 @@ struct GroupedGemmArgs {
 // tile (packed gate/up weights); else writes acc as bf16.
 // paired: 256 x 256 tiles on CTA pairs (tcgen05 cta_group::2; bn must be 256;
 // the B tensor maps then use 128-row boxes); else 128 x bn tiles per CTA.
-// multicast: single-CTA 128 x 256 tiles on clusters of two CTAs that share
-// each B tile (each loads one 128-row half, multicast to both; the B maps
-// then use 128-row boxes); not with paired or gathered rows.
 // b0h / b1h (paired SwiGLU only): the same B tensors with 64-row boxes, for
 // the half-height tiles that end a group with at most 128 rows.
 int launch_grouped_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b0,
                         const CUtensorMap& b1, const GroupedGemmArgs& args, bool swiglu, int bn,
-                        bool paired, int num_sms, cudaStream_t stream, bool multicast = false,
+                        bool paired, int num_sms, cudaStream_t stream,
                         const CUtensorMap* b0h = nullptr, const CUtensorMap* b1h = nullptr);
 
 // Encodes a 2-D bf16 tensor map over a row-major [rows][cols] tensor with a
@@ -211,6 +208,7 @@ int launch_timeout_probe(int* status, uint64_t timeout_ns, cudaStream_t stream);
 int launch_alf_bias_update(int32_t E, int32_t T, int32_t k, const int32_t* counts, float gamma,
                            float* bias, cudaStream_t stream);
 
-int device_sm_count();
+// The process-wide limit of bounded device waits (moe_set_wait_timeout_ns).
+uint64_t default_wait_timeout_ns();
 
 }  // namespace moe

@@ -19,8 +19,10 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdint>
+#include <mutex>
 
 #include "../../include/moe.h"
 #include "moe_internal.h"
@@ -45,8 +47,12 @@ constexpr size_t kScratchBytes = kOffExpPsum + kNoAllocMaxExperts * 8;
 static __device__ __align__(256) unsigned char g_route_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 64;
-unsigned char* g_scratch_dev[kMaxDevices] = {nullptr};  // device address, per device
-int g_sm_count[kMaxDevices] = {0};
+// Device address of the array and SM count, per device.  The address is
+// published (release) after the SM count is stored, so a reader that sees it
+// also sees the count; the set-up itself runs under a mutex, once per device.
+std::atomic<unsigned char*> g_scratch_dev[kMaxDevices];
+std::atomic<int> g_sm_count[kMaxDevices];
+std::mutex g_setup_mutex;
 
 // Per-device set-up: the device address of the static array (host code may
 // not use the symbol itself as a device pointer) and the SM count.
@@ -54,18 +60,25 @@ int scratch_for_current_device(unsigned char** ptr, int* num_sms) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
     return MOE_ERR_CUDA;
-  if (g_scratch_dev[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess || p == nullptr)
-      return MOE_ERR_CUDA;
-    int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-      return MOE_ERR_CUDA;
-    g_sm_count[dev] = n;
-    g_scratch_dev[dev] = static_cast<unsigned char*>(p);
+  unsigned char* base = g_scratch_dev[dev].load(std::memory_order_acquire);
+  if (base == nullptr) {
+    std::lock_guard<std::mutex> lock(g_setup_mutex);
+    base = g_scratch_dev[dev].load(std::memory_order_acquire);
+    if (base == nullptr) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess || p == nullptr)
+        return MOE_ERR_CUDA;
+      int n = 0;
+      if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+          n <= 0)
+        return MOE_ERR_CUDA;
+      g_sm_count[dev].store(n, std::memory_order_relaxed);
+      base = static_cast<unsigned char*>(p);
+      g_scratch_dev[dev].store(base, std::memory_order_release);
+    }
   }
-  *ptr = g_scratch_dev[dev];
-  *num_sms = g_sm_count[dev];
+  *ptr = base;
+  *num_sms = g_sm_count[dev].load(std::memory_order_relaxed);
   return MOE_OK;
 }
 
@@ -120,8 +133,11 @@ extern "C" int moe_route_noalloc(const moe_shape_t* s, const uint16_t* x,
     ra.tile_psum = tile_psum;
     ra.tile_lse2 = tile_lse2;
     ra.status = status;
-    ra.timeout_ns = 2000000000ull;
-    ra.flags = s->flags;
+    // the same wait limit as the workspace entry points, and only the router's
+    // own variant bits (capacity and expert-choice bits do not concern it)
+    ra.timeout_ns = s->tuning.wait_timeout_ns != 0 ? s->tuning.wait_timeout_ns
+                                                    : default_wait_timeout_ns();
+    ra.flags = s->flags & (kRouteSigmoid | kRouteNoRenorm);
     rc = launch_router(mx, mw, ra, num_sms, st);
     if (rc != 0) return rc == -2 ? MOE_ERR_UNSUPPORTED : MOE_ERR_CUDA;
   }
