@@ -52,6 +52,8 @@ def parse_args(argv=None):
                     help="token: token-choice top-k (the headline); priority: capacity "
                          "keeps each expert's highest scores; expert-choice: every expert "
                          "takes its top-r tokens (secondary lines: no e2e or CPU leg)")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the other workloads' lines (per_config)")
     ap.add_argument("--no-graph", action="store_true",
                     help="launch every timed step directly instead of replaying CUDA graphs")
     ap.add_argument("--stage", choices=["layer", "router"], default="layer",
@@ -454,6 +456,144 @@ def job_tokens_per_s(world: int, tokens_per_rank: int, ms: float) -> float:
 
 
 # --------------------------------------------------------------------------- #
+# per-kernel stage times and the other workloads                               #
+# --------------------------------------------------------------------------- #
+WORKLOAD_ORDER = ["tiny", "mixtral", "deepseekmoe16b", "deepseekv2", "switch"]
+
+
+def stage_pass(layer, inp, w, flush, dev, n: int, graph: bool = True):
+    """Per-kernel device time of one layer forward, every kernel bracketed by
+    events.  With ``graph`` the n forwards are captured as CUDA graphs first
+    (the events become event nodes of the graphs) and replayed with an L2
+    flush before each, so the brackets hold only device time, as in the timed
+    loop; otherwise they are launched directly (host launch gaps included)."""
+    import torch
+    import top_routing_expert_lb_b300 as moe
+    stream = torch.cuda.current_stream(dev)
+    moe.moe_profile_collect()
+    moe.moe_profile_enable(True)
+    if graph:
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        graphs = []
+        with torch.cuda.stream(side):
+            for _ in range(n):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=side):
+                    layer.forward(inp.x)
+                graphs.append(g)
+        stream.wait_stream(side)
+        torch.cuda.synchronize(dev)
+        for g in graphs:
+            flush.zero_()
+            g.replay()
+    else:
+        for _ in range(n):
+            flush.zero_()
+            layer.forward(inp.x)
+    torch.cuda.synchronize(dev)
+    moe.moe_profile_enable(False)
+    per_kernel = {}
+    for name, t in moe.moe_profile_collect():
+        per_kernel.setdefault(name, []).append(t)
+    kern_ms = {k: sum(v) / n for k, v in per_kernel.items()}
+    if layer.expert_choice:
+        R = w.E * layer.r
+    else:
+        R = int(w.T * w.k - int(layer.drop_mask.sum().item())) if w.k else 0
+    flops, bytes_ = algorithmic_work(w, R)
+    peaks, _ = load_peaks()
+    kept = kept_rows_per_expert(layer, w)
+    ffn_ms = kern_ms.get("gemm_swiglu", 0.0) + kern_ms.get("gemm_down", 0.0)
+    ffn_flops = flops["gemm_swiglu"] + flops["gemm_down"]
+    return {"kernel_ms": kern_ms, "kernel_launches": {k: len(v) for k, v in per_kernel.items()},
+            "rows": R, "kept": kept, "ffn_ms": ffn_ms,
+            "ffn_tflops": ffn_flops / (ffn_ms * 1e-3) / 1e12 if ffn_ms > 0 else 0.0,
+            "ffn_attainable_ms": attainable_ffn_ms(w, kept, peaks),
+            "stage_gbs": {k: bytes_[k] / (kern_ms[k] * 1e-3) / 1e9
+                          for k in bytes_ if k in kern_ms},
+            "how": (f"{n} CUDA-graph replays of one forward, every kernel bracketed by event "
+                    "nodes, L2 flushed before each" if graph else
+                    f"{n} direct forwards, every launch bracketed by events, L2 flushed "
+                    "before each")}
+
+
+def st_summary(st, w, step_ms: float, peaks):
+    """The per-workload figures of one stage pass and timed loop."""
+    kept = st["kept"]
+    tot = sum(kept)
+    return {"workload": workload_desc(w), "tokens_per_s": w.T / (step_ms * 1e-3),
+            "ms_per_step": step_ms, "ffn_ms": st["ffn_ms"], "ffn_tflops": st["ffn_tflops"],
+            "ffn_frac_of_bf16_peak": st["ffn_tflops"] / peaks["bf16_tflops"],
+            "ffn_attainable_ms": st["ffn_attainable_ms"],
+            "ffn_frac_of_attainable": (st["ffn_attainable_ms"] / st["ffn_ms"]
+                                       if st["ffn_ms"] > 0 else None),
+            "kernel_ms": st["kernel_ms"],
+            "stage_gbs": st["stage_gbs"],
+            "stage_frac_of_hbm": {k: v / peaks["hbm_gbs"] for k, v in st["stage_gbs"].items()},
+            "load": {"max_over_mean": float(max(kept) / (tot / len(kept))) if tot else None,
+                     "empty_experts": int(sum(1 for v in kept if v == 0)),
+                     "rows_computed": st["rows"],
+                     "dropped_pairs": int(w.T * w.k - st["rows"])}}
+
+
+def measure_other(w, args, dev, flush, steps: int = 20, warmup: int = 3):
+    """One more workload in this process: graph-replayed timed steps (L2
+    flushed before each) and a stage pass; inputs released afterwards."""
+    import torch
+
+    import synth
+    import top_routing_expert_lb_b300 as moe
+    inp = synth.make_inputs(w, dev)
+    shape = moe.Shape.of(w.T, w.d, w.M, w.E, w.k, w.n_shared, w.capacity_factor,
+                         w.balance_coef, w.flags)
+    layer = moe.MoELayer(shape, inp.wr, inp.w1, inp.w3, inp.w2, inp.ws1, inp.ws3, inp.ws2,
+                         inp.offset, inp.sel_bias, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(warmup):
+        layer.forward(inp.x)
+    torch.cuda.synchronize(dev)
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(stream)
+    graphs = []
+    moe.moe_profile_collect()
+    moe.moe_profile_enable(True, kernels=["gemm_swiglu", "gemm_down"])
+    with torch.cuda.stream(side):
+        for _ in range(steps):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=side):
+                layer.forward(inp.x)
+            graphs.append(g)
+    stream.wait_stream(side)
+    torch.cuda.synchronize(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for g, (a, b) in zip(graphs, ev):
+        flush.zero_()
+        a.record(stream)
+        g.replay()
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    moe.moe_profile_enable(False)
+    gemm = moe.moe_profile_collect()
+    if moe.moe_check_status(layer.ws) != 0:
+        raise RuntimeError(f"device wait timed out ({w.name})")
+    step_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    st = stage_pass(layer, inp, w, flush, dev, 5)
+    peaks, _ = load_peaks()
+    if gemm:
+        # the expert FFN as timed inside the timed replays
+        R = st["rows"]
+        flops, _ = algorithmic_work(w, R)
+        st["ffn_ms"] = sum(t for _, t in gemm) / steps
+        st["ffn_tflops"] = (flops["gemm_swiglu"] + flops["gemm_down"]) / (st["ffn_ms"] * 1e-3) / 1e12
+    out = dict(st_summary(st, w, step_ms, peaks), steps=steps, warmup=warmup)
+    del graphs, layer, inp
+    torch.cuda.empty_cache()
+    return out
+
+
+# --------------------------------------------------------------------------- #
 # our arm                                                                      #
 # --------------------------------------------------------------------------- #
 def run_ours(args, w):
@@ -501,7 +641,7 @@ def run_ours(args, w):
     # launch work from the step; --no-graph launches every step directly.
     graphs = None
     per_forward = 0
-    moe.moe_profile_enable(True, kernels=["gemm_swiglu"])
+    moe.moe_profile_enable(True, kernels=["gemm_swiglu", "gemm_down"])
     if not args.no_graph:
         graphs = []
         side = torch.cuda.Stream(dev)
@@ -543,39 +683,29 @@ def run_ours(args, w):
     ms = max_over_ranks(statistics.mean(step_ms), dev)
 
     dom_times = [t for name, t in prof if name == "gemm_swiglu"]
-
-    # stage breakdown: a separate short pass with every kernel bracketed
-    n_stage = max(3, min(args.steps, 10))
-    moe.moe_profile_enable(True)
-    for _ in range(n_stage):
-        flush.zero_()
-        layer.forward(inp.x)
-    torch.cuda.synchronize(dev)
-    moe.moe_profile_enable(False)
-    per_kernel = {}
-    for name, t in moe.moe_profile_collect():
-        per_kernel.setdefault(name, []).append(t)
-    # time per step of each kernel (a stage may take more than one launch)
-    kern_ms = {k: sum(v) / n_stage for k, v in per_kernel.items()}
-    kern_n = {k: len(v) for k, v in per_kernel.items()}
-
-    if layer.expert_choice:
-        R = w.E * layer.r
-    else:
-        R = int(w.T * w.k - int(layer.drop_mask.sum().item())) if w.k else 0
+    down_times = [t for name, t in prof if name == "gemm_down"]
+    used_graph = graphs is not None
+    expert_choice = layer.expert_choice
+    st = stage_pass(layer, inp, w, flush, dev, max(3, min(args.steps, 10)),
+                    graph=not args.no_graph)
+    kern_ms, kern_n = st["kernel_ms"], st["kernel_launches"]
+    R = st["rows"]
     flops, bytes_ = algorithmic_work(w, R)
     peaks, peak_src = load_peaks()
-    kept = kept_rows_per_expert(layer, w)
-    attainable_ms = attainable_ffn_ms(w, kept, peaks)
-    ffn_ms = kern_ms.get("gemm_swiglu", 0.0) + kern_ms.get("gemm_down", 0.0)
+    kept = st["kept"]
+    attainable_ms = st["ffn_attainable_ms"]
+    # the expert FFN as timed inside the timed steps (event nodes around both
+    # projections), not from the stage pass
+    ffn_ms = (sum(dom_times) + sum(down_times)) / args.steps if dom_times else st["ffn_ms"]
     ffn_tflops = (flops["gemm_swiglu"] + flops["gemm_down"]) / (ffn_ms * 1e-3) / 1e12
+    st["ffn_ms"], st["ffn_tflops"] = ffn_ms, ffn_tflops
     dom = "gemm_swiglu"
     # the gate/up projection may take two launches per step (pair tiles for
     # whole 256-row blocks, single-CTA tiles for the rest): time per step
     dom_per_step = len(dom_times) // max(1, args.steps)
     dom_ms = sum(dom_times) / args.steps if dom_times else kern_ms[dom]
     ach = flops[dom] / (dom_ms * 1e-3) / 1e12
-    stage_gbs = {k: bytes_[k] / (kern_ms[k] * 1e-3) / 1e9 for k in bytes_ if k in kern_ms}
+    stage_gbs = st["stage_gbs"]
 
     # end to end: host tokens in, host output and losses out, through the C ABI.
     # Headline: a stream of batches through moe_layer_forward_host_batches
@@ -656,6 +786,22 @@ def run_ours(args, w):
     if rank == 0 and not args.no_cpu_baseline and args.routing == "token":
         cpu = cpu_baseline(w, inp, args.cpu_budget_s)
 
+    per_config = None
+    if not args.no_per_config and args.routing == "token" and world == 1:
+        # every other workload of the layer, measured the same way in this
+        # process (fewer steps; no e2e or CPU leg), after the headline's
+        # graphs, inputs and layer are released
+        graphs = None
+        layer = inp = None
+        torch.cuda.empty_cache()
+        per_config = {w.name: dict(st_summary(st, w, ms, peaks), steps=args.steps,
+                                   warmup=args.warmup)}
+        for name in WORKLOAD_ORDER:
+            if name == w.name:
+                continue
+            per_config[name] = measure_other(synth.WORKLOADS[name], args, dev, flush)
+        per_config = {k: per_config[k] for k in WORKLOAD_ORDER if k in per_config}
+
     if rank != 0:
         return 0
     line = {
@@ -668,7 +814,7 @@ def run_ours(args, w):
                    "rows_computed": R,
                    "l2": f"flushed: {FLUSH_BYTES >> 20} MiB written before every timed step",
                    "parallelism": "replicas" if world > 1 else "single GPU",
-                   "cuda_graph": graphs is not None},
+                   "cuda_graph": used_graph},
         "ffn_tflops": ffn_tflops,
         "ffn_frac_of_bf16_peak": ffn_tflops / peaks["bf16_tflops"],
         "ffn_attainable_ms": attainable_ms,
@@ -676,8 +822,9 @@ def run_ours(args, w):
         "routing": args.routing,
         "load": {"max_over_mean": float(max(kept) / (sum(kept) / len(kept))) if sum(kept) else None,
                  "empty_experts": int(sum(1 for v in kept if v == 0)),
-                 "dropped_pairs": int(w.T * w.k - R) if not layer.expert_choice else None},
+                 "dropped_pairs": int(w.T * w.k - R) if not expert_choice else None},
         "kernel_ms": kern_ms, "kernel_launches_stage_pass": kern_n,
+        "stage_pass": st["how"],
         "stage_gbs": stage_gbs,
         "stage_frac_of_hbm": {k: v / peaks["hbm_gbs"] for k, v in stage_gbs.items()},
         "roofline": {"bound": "tensor", "kernel": dom, "achieved": ach,
@@ -695,6 +842,7 @@ def run_ours(args, w):
                      if len(dom_times) >= 5 * max(1, dom_per_step) else None},
         "cpu_baseline": cpu,
         "e2e": e2e,
+        "per_config": per_config,
         "gpu_launches": launches,
         "clocks": clk.summary(),
     }

@@ -50,6 +50,10 @@ extern "C" {
 #define MOE_ERR_CUDA (-3)         /* a CUDA runtime/driver call failed              */
 #define MOE_ERR_TIMEOUT (-4)      /* a bounded device wait ran out                  */
 #define MOE_ERR_WORKSPACE (-5)    /* workspace smaller than moe_workspace_size      */
+#define MOE_ERR_BOUNDS (-6)       /* a device index out of range; reported only by a
+                                     library built with -DMOE_BOUNDS_CHECK, which
+                                     checks every data-dependent index and skips
+                                     the access instead of faulting               */
 
 /* Supported limits (MOE_ERR_UNSUPPORTED outside them):
  *   1 <= E <= 256;  0 <= k <= min(E, 8);  0 <= T <= 2^24;  d % 64 == 0,
@@ -383,7 +387,9 @@ int moe_ec_layer_forward(const moe_shape_t *shape, const uint16_t *x, const uint
                          void *stream);
 
 /* Reads (and clears) the device status word kept in the workspace; writes
- * MOE_OK or MOE_ERR_TIMEOUT to *status (host).  Synchronises `stream`.        */
+ * MOE_OK, MOE_ERR_TIMEOUT or (bounds-checked builds) MOE_ERR_BOUNDS to *status
+ * (host).  Synchronises `stream`.  After MOE_ERR_TIMEOUT the workspace's
+ * counters may be left nonzero: zero the workspace again before reusing it.  */
 int moe_check_status(void *ws, int *status, void *stream);
 
 /* Default wait limit, in nanoseconds, of the bounded device waits of every

@@ -12,3 +12,15 @@ if TESTS not in sys.path:
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (B300, sm_103a)")
     config.addinivalue_line("markers", "slow: long-running")
+
+
+import pytest  # noqa: E402
+
+
+@pytest.fixture(autouse=True)
+def _canary_guards():
+    """After every test: the guard bytes around every canary-guarded device
+    buffer (tests/guard.py) are intact."""
+    yield
+    import guard
+    guard.check_guards()

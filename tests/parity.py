@@ -28,6 +28,7 @@ import torch
 import oracle
 import synth
 import top_routing_expert_lb_b300 as moe
+from guard import guarded, guarded_like
 
 TIE = 1e-5
 CUT_REL = 1e-5   # near-cut band of score-ordered selections, relative to the cut score
@@ -41,6 +42,23 @@ def shape_of(w: synth.Workload, **tuning) -> moe.Shape:
     """The workload's moe_shape_t; keyword arguments set moe_tuning_t fields."""
     return moe.Shape.of(w.T, w.d, w.M, w.E, w.k, w.n_shared, w.capacity_factor,
                         w.balance_coef, w.flags, **tuning)
+
+
+def guarded_workspace(shape: moe.Shape, device="cuda") -> torch.Tensor:
+    """A zeroed workspace with canary guards on both sides."""
+    n = max(moe.moe_workspace_size(shape), 256)
+    return guarded((n,), torch.uint8, device, fill=0, label="workspace")
+
+
+def guard_layer(layer: moe.MoELayer) -> moe.MoELayer:
+    """Replaces the layer's outputs and workspace by canary-guarded buffers."""
+    names = ["y", "ids", "gates", "drop_mask", "counts", "f", "P", "losses"]
+    if layer.expert_choice:
+        names += ["row_token", "row_gate"]
+    for name in names:
+        setattr(layer, name, guarded_like(getattr(layer, name), label=f"layer.{name}"))
+    layer.ws = guarded_workspace(layer.shape, layer.ws.device)
+    return layer
 
 
 def np_of(t: Optional[torch.Tensor]):
@@ -73,8 +91,9 @@ def run_layer(inp: synth.Inputs, layer: Optional[moe.MoELayer] = None,
               tuning: Optional[dict] = None) -> GpuOut:
     w = inp.w
     if layer is None:
-        layer = moe.MoELayer(shape_of(w, **(tuning or {})), inp.wr, inp.w1, inp.w3, inp.w2, inp.ws1, inp.ws3,
-                             inp.ws2, inp.offset, inp.sel_bias, device=inp.x.device)
+        layer = guard_layer(moe.MoELayer(shape_of(w, **(tuning or {})), inp.wr, inp.w1, inp.w3,
+                                         inp.w2, inp.ws1, inp.ws3, inp.ws2, inp.offset,
+                                         inp.sel_bias, device=inp.x.device))
     layer.forward(inp.x)
     torch.cuda.synchronize()
     assert moe.moe_check_status(layer.ws) == 0
@@ -320,8 +339,9 @@ def run_ec_layer(inp: synth.Inputs, layer: Optional[moe.MoELayer] = None,
     w = inp.w
     assert w.flags & moe.MOE_FLAG_EXPERT_CHOICE
     if layer is None:
-        layer = moe.MoELayer(shape_of(w, **(tuning or {})), inp.wr, inp.w1, inp.w3, inp.w2, inp.ws1, inp.ws3,
-                             inp.ws2, inp.offset, None, device=inp.x.device)
+        layer = guard_layer(moe.MoELayer(shape_of(w, **(tuning or {})), inp.wr, inp.w1, inp.w3,
+                                         inp.w2, inp.ws1, inp.ws3, inp.ws2, inp.offset, None,
+                                         device=inp.x.device))
     layer.forward(inp.x)
     torch.cuda.synchronize()
     assert moe.moe_check_status(layer.ws) == 0

@@ -248,3 +248,14 @@ def test_entry_points_check_the_routing_mode(lib):
                            need, None) == B.MOE_ERR_UNSUPPORTED
     # the extra scratch is sized only when a mode needs it
     assert B.moe_workspace_size(shape(capacity_factor=1.0)) < B.moe_workspace_size(prio)
+
+
+def test_bounds_checked_build_compiles(tmp_path):
+    """The debug build with every data-dependent device index range-checked
+    (-DMOE_BOUNDS_CHECK) compiles and exports the same entry points."""
+    out = str(tmp_path / "libmoe_bounds.so")
+    mbuild.build(extra=("-DMOE_BOUNDS_CHECK",), out=out)
+    L = ctypes.CDLL(out)
+    for name in declared_functions():
+        assert hasattr(L, name), name
+    assert L.moe_error_string.restype is not None

@@ -8,7 +8,8 @@ import torch
 import oracle
 import synth
 import top_routing_expert_lb_b300 as moe
-from parity import (GATE_ABS, LOSS_REL, assert_y_close, bf16_to_f64, np_of, oracle_routing,
+from guard import guarded
+from parity import (guarded_workspace, GATE_ABS, LOSS_REL, assert_y_close, bf16_to_f64, np_of, oracle_routing,
                     rel_close, shape_of)
 from top_routing_expert_lb_b300 import build as mbuild
 
@@ -23,7 +24,7 @@ def _lib():
 
 
 def _ws(s):
-    return moe._binding.alloc_workspace(s)
+    return guarded_workspace(s)
 
 
 # --------------------------------------------------------------------------- route
@@ -39,13 +40,13 @@ def test_route(w):
     inp = synth.make_inputs(w, "cuda", experts=False)
     s = shape_of(w)
     dev = "cuda"
-    ids = torch.empty((w.T, w.k), dtype=torch.int32, device=dev)
-    gates = torch.empty((w.T, w.k), dtype=torch.float32, device=dev)
-    counts = torch.empty(w.E, dtype=torch.int32, device=dev)
-    f = torch.empty(w.E, device=dev)
-    P = torch.empty(w.E, device=dev)
-    lb = torch.empty(1, device=dev)
-    lz = torch.empty(1, device=dev)
+    ids = guarded((w.T, w.k), torch.int32, dev, label="ids")
+    gates = guarded((w.T, w.k), torch.float32, dev, label="gates")
+    counts = guarded(w.E, torch.int32, dev, label="counts")
+    f = guarded(w.E, torch.float32, dev, label="f")
+    P = guarded(w.E, torch.float32, dev, label="P")
+    lb = guarded(1, torch.float32, dev, label="bal_loss")
+    lz = guarded(1, torch.float32, dev, label="z_loss")
     ws = _ws(s)
     moe.moe_route(s, inp.x, inp.wr, inp.offset, inp.sel_bias, ids, gates, counts, f, P, lb, lz,
                   ws)
@@ -85,11 +86,11 @@ def test_permute(T, E, k, c, d):
     x = synth.normal_bf16(3, synth.TID_X, (T, d), 1.0, "cuda")
     ids = torch.from_numpy(ids_np).cuda()
     R_max = moe.moe_max_rows(s)
-    offsets = torch.full((E + 1,), -7, dtype=torch.int32, device="cuda")
-    slot_row = torch.empty((T, k), dtype=torch.int32, device="cuda")
-    row_token = torch.full((max(R_max, 1),), -7, dtype=torch.int32, device="cuda")
-    drop = torch.empty((T, k), dtype=torch.uint8, device="cuda")
-    x_perm = torch.zeros((max(R_max, 1), d), dtype=torch.bfloat16, device="cuda")
+    offsets = guarded(E + 1, torch.int32, fill=-7, label="offsets")
+    slot_row = guarded((T, k), torch.int32, label="slot_row")
+    row_token = guarded(max(R_max, 1), torch.int32, fill=-7, label="row_token")
+    drop = guarded((T, k), torch.uint8, label="drop_mask")
+    x_perm = guarded((max(R_max, 1), d), torch.bfloat16, fill=0, label="x_perm")
     ws = _ws(s)
     moe.moe_permute(s, x, ids, offsets, slot_row, row_token, drop, x_perm, ws)
     torch.cuda.synchronize()
@@ -156,7 +157,7 @@ def test_grouped_ffn(rows, d, M, n_shared, T, tile):
     w3 = synth.normal_bf16(5, synth.TID_W3, (E, M, d), 0.05, dev)
     w2 = synth.normal_bf16(5, synth.TID_W2, (E, d, M), 0.05, dev)
     w13 = moe.moe_pack_w13(w1, w3)
-    y_perm = torch.zeros((max(R_max, 1), d), dtype=torch.bfloat16, device=dev)
+    y_perm = guarded((max(R_max, 1), d), torch.bfloat16, dev, fill=0, label="y_perm")
     x = ws1 = ws3 = ws2 = w13s = y_s = None
     if n_shared:
         x = synth.normal_bf16(6, synth.TID_X, (T, d), 1.0, dev)
@@ -164,7 +165,7 @@ def test_grouped_ffn(rows, d, M, n_shared, T, tile):
         ws3 = synth.normal_bf16(5, synth.TID_WS3, (Ms, d), 0.05, dev)
         ws2 = synth.normal_bf16(5, synth.TID_WS2, (d, Ms), 0.05, dev)
         w13s = moe.moe_pack_w13(ws1, ws3)
-        y_s = torch.zeros((T, d), dtype=torch.bfloat16, device=dev)
+        y_s = guarded((T, d), torch.bfloat16, dev, fill=0, label="y_shared")
     ws = _ws(s_ffn)
     moe.moe_grouped_ffn(s_ffn, x_perm, offsets, w13, w2, y_perm, x, w13s, ws2, y_s, ws)
     torch.cuda.synchronize()
@@ -197,7 +198,7 @@ def test_grouped_ffn_dynamic_order_repeats():
     ws = _ws(s_ffn)
     outs = []
     for i in range(3):
-        y = torch.zeros((R, d), dtype=torch.bfloat16, device=dev)
+        y = guarded((R, d), torch.bfloat16, dev, fill=0, label="y_perm")
         moe.moe_grouped_ffn(s_ffn, x_perm, offsets, w13, w2, y, None, None, None, None, ws)
         if i == 1:   # another grouping on the same workspace in between
             off2 = torch.tensor([0, R // 2, R, R, R, R, R], dtype=torch.int32, device=dev)
@@ -228,7 +229,7 @@ def test_combine(T, d, E, k, c, shared):
     g /= g.sum(1, keepdims=True)
     y_perm = synth.normal_bf16(9, synth.TID_X, (R, d), 1.0, "cuda")
     y_s = synth.normal_bf16(10, synth.TID_X, (T, d), 1.0, "cuda") if shared else None
-    y = torch.empty((T, d), dtype=torch.bfloat16, device="cuda")
+    y = guarded((T, d), torch.bfloat16, label="y")
     s = moe.Shape.of(T, d, 128, E, k, 1 if shared else 0, c)
     moe.moe_combine(s, y_perm, torch.from_numpy(disp.slot_row).cuda(), torch.from_numpy(g).cuda(),
                     y_s, y)

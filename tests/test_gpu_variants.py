@@ -8,7 +8,9 @@ import torch
 import oracle
 import synth
 import top_routing_expert_lb_b300 as moe
-from parity import GATE_ABS, LOSS_REL, check_layer, np_of, oracle_routing, rel_close, shape_of
+from guard import guarded
+from parity import GATE_ABS, LOSS_REL, check_layer, guarded_workspace, np_of, oracle_routing, rel_close, \
+    shape_of
 from top_routing_expert_lb_b300 import build as mbuild
 
 pytestmark = pytest.mark.gpu
@@ -38,14 +40,17 @@ def test_route_ex_variants_and_side_outputs(w):
     inp = synth.make_inputs(w, "cuda", experts=False)
     s = shape_of(w)
     dev = "cuda"
-    out = dict(ids=torch.empty((w.T, w.k), dtype=torch.int32, device=dev),
-               gates=torch.empty((w.T, w.k), device=dev),
-               counts=torch.empty(w.E, dtype=torch.int32, device=dev),
-               f=torch.empty(w.E, device=dev), P=torch.empty(w.E, device=dev),
-               bal_loss=torch.empty(1, device=dev), z_loss=torch.empty(1, device=dev),
-               importance=torch.empty(w.E, device=dev), importance_cv2=torch.empty(1, device=dev),
-               entropy_mean=torch.empty(1, device=dev))
-    ws = moe.alloc_workspace(s)
+    out = dict(ids=guarded((w.T, w.k), torch.int32, dev, label="ids"),
+               gates=guarded((w.T, w.k), torch.float32, dev, label="gates"),
+               counts=guarded(w.E, torch.int32, dev, label="counts"),
+               f=guarded(w.E, torch.float32, dev, label="f"),
+               P=guarded(w.E, torch.float32, dev, label="P"),
+               bal_loss=guarded(1, torch.float32, dev, label="bal_loss"),
+               z_loss=guarded(1, torch.float32, dev, label="z_loss"),
+               importance=guarded(w.E, torch.float32, dev, label="importance"),
+               importance_cv2=guarded(1, torch.float32, dev, label="importance_cv2"),
+               entropy_mean=guarded(1, torch.float32, dev, label="entropy_mean"))
+    ws = guarded_workspace(s)
     moe.moe_route_ex(s, inp.x, inp.wr, inp.offset, inp.sel_bias, ws, **out)
     torch.cuda.synchronize()
     assert moe.moe_check_status(ws) == 0

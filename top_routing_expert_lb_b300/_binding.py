@@ -21,6 +21,7 @@ MOE_ERR_UNSUPPORTED = -2
 MOE_ERR_CUDA = -3
 MOE_ERR_TIMEOUT = -4
 MOE_ERR_WORKSPACE = -5
+MOE_ERR_BOUNDS = -6
 
 
 class MoeError(RuntimeError):

@@ -1,4 +1,11 @@
-"""Builds libmoe_b300.so in-tree with nvcc for sm_103a."""
+"""Builds libmoe_b300.so in-tree with nvcc for sm_103a.
+
+With MOE_BUILD_BOUNDS_CHECK=1 in the environment of the build, the library is
+compiled with -DMOE_BOUNDS_CHECK: every data-dependent index in the kernels is
+range-checked, a failed check is reported as MOE_ERR_BOUNDS by
+moe_check_status and the access is skipped (a debug build that stands in for a
+device memory checker).  The recorded source hash covers the flags, so
+switching the variable rebuilds the library."""
 from __future__ import annotations
 
 import glob
@@ -18,6 +25,11 @@ NVCC_FLAGS = [
 ]
 
 
+def flags():
+    extra = ["-DMOE_BOUNDS_CHECK"] if os.environ.get("MOE_BUILD_BOUNDS_CHECK") == "1" else []
+    return NVCC_FLAGS + extra
+
+
 def sources():
     return sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cuh"))
                   + glob.glob(os.path.join(CSRC, "*.h")) + [HEADER])
@@ -29,7 +41,7 @@ def source_hash() -> str:
         h.update(os.path.basename(s).encode())
         with open(s, "rb") as fh:
             h.update(fh.read())
-    h.update(" ".join(NVCC_FLAGS).encode())
+    h.update(" ".join(flags()).encode())
     return h.hexdigest()
 
 
@@ -42,21 +54,25 @@ def is_stale() -> bool:
         return fh.read().strip() != source_hash()
 
 
-def build(verbose: bool = False, extra=()) -> str:
+def build(verbose: bool = False, extra=(), out: str | None = None) -> str:
+    """Compiles the library into the package (or into `out`, without touching
+    the in-tree copy); `extra` adds nvcc flags."""
     os.makedirs(LIB_DIR, exist_ok=True)
     nvcc = os.environ.get("NVCC", "nvcc")
     if not os.path.exists(nvcc) and os.path.exists("/usr/local/cuda/bin/nvcc"):
         nvcc = "/usr/local/cuda/bin/nvcc"
     cus = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
-    tmp = LIB + ".tmp"
-    cmd = [nvcc, *NVCC_FLAGS, *extra, "-o", tmp, *cus]
+    target = out or LIB
+    tmp = target + ".tmp"
+    cmd = [nvcc, *flags(), *extra, "-o", tmp, *cus]
     if verbose:
         print(" ".join(cmd))
     subprocess.run(cmd, check=True)
-    os.replace(tmp, LIB)
-    with open(LIB + ".srchash", "w") as fh:
-        fh.write(source_hash() + "\n")
-    return LIB
+    os.replace(tmp, target)
+    if out is None:
+        with open(LIB + ".srchash", "w") as fh:
+            fh.write(source_hash() + "\n")
+    return target
 
 
 def ensure_built() -> str:

@@ -6,9 +6,11 @@
 #include <atomic>
 #include <cmath>
 #include <cstdint>
+#include <cstring>
 #include <vector>
 
 #include "../../include/moe.h"
+#include "bounds.cuh"
 #include "moe_internal.h"
 
 namespace moe {
@@ -67,6 +69,11 @@ int tracked(int32_t kernel, cudaStream_t st, F&& launch) {
 }
 
 constexpr size_t kAlign = 256;
+// router accumulator block: counts [256] int32 at 0, P sums [256] u64 at 1024,
+// importance sums [256] u64 at 3072, entropy sum u64 at 5120, finished tiles
+// int32 at 5128
+constexpr size_t kRaccBytes = 5376;
+constexpr int64_t kPartUnits = 256;  // K-split units whose partial logits the workspace holds
 inline size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -74,6 +81,8 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 struct Layout {
   size_t status, tile_hist, tile_psum, tile_lse2, tile_base, exp_count, exp_psum, offsets;
   size_t tile_imp, tile_ent, exp_imp;
+  size_t racc, tile_arrive, chunk_acc, part;  // router accumulators and K-split partials
+  int32_t max_split, chunk_tiles, n_chunks;
   size_t slot_row, row_token;
   size_t pair_score, stage_q, stage_key, all_offsets;  // priority capacity
   size_t scores_t, sel_t, row_gate;                    // expert choice
@@ -172,6 +181,20 @@ Layout layout_of(const moe_shape_t* s) {
   L.tile_ent = take(L.ntiles * 4);
   L.exp_imp = take(E * 8);
   L.offsets = take((E + 1) * 4);
+  // router: [E] counts (int32), [E] P and [E] importance sums (fixed point,
+  // 64-bit), the entropy sum and the finished-tile counter; per-tile arrival
+  // counters of K-split slices; per-chunk expert counts; partial logits of
+  // K-split units (at most kPartUnits units of E x 128 fp32)
+  L.racc = take(kRaccBytes);
+  L.tile_arrive = take(L.ntiles * 4);
+  L.chunk_tiles = L.ntiles <= 1024 ? 32 : 1;
+  while (static_cast<int64_t>(L.chunk_tiles) * 32 < L.ntiles) L.chunk_tiles *= 2;
+  L.n_chunks = static_cast<int32_t>((L.ntiles + L.chunk_tiles - 1) / L.chunk_tiles);
+  L.chunk_acc = take(static_cast<size_t>(L.n_chunks) * E * 4);
+  L.max_split = 1;
+  while (L.max_split < kMaxSplitUnits && L.ntiles * 2 * L.max_split <= kPartUnits)
+    L.max_split *= 2;
+  L.part = take(L.max_split > 1 ? static_cast<size_t>(L.ntiles) * L.max_split * E * 128 * 4 : 0);
   L.slot_row = take(T * k * 4);
   L.row_token = take(L.rmax * 4);
   L.pair_score = take(prio ? T * k * 4 : 0);
@@ -233,84 +256,91 @@ struct RouteExtras {
   double n_pairs = -1.0;            // expert choice: E r
 };
 
+// Points the router's scratch fields at the accumulator block `racc` and the
+// given per-tile / partial regions.
+void set_router_scratch(RouterArgs* ra, uint8_t* racc, float* tile_lse2, int* tile_arrive,
+                        float* part, int max_split) {
+  ra->acc_count = reinterpret_cast<int*>(racc);
+  ra->acc_psum = reinterpret_cast<unsigned long long*>(racc + 1024);
+  ra->acc_ent = reinterpret_cast<unsigned long long*>(racc + 5120);
+  ra->tiles_done = reinterpret_cast<int*>(racc + 5128);
+  ra->tile_lse2 = tile_lse2;
+  ra->tile_arrive = tile_arrive;
+  ra->part_logits = part;
+  ra->max_split = max_split;
+}
+
 int do_route(const moe_shape_t* s, const uint16_t* x, const uint16_t* wr, const float* off,
              const float* bias, int32_t* ids, float* gates, int32_t* counts, float* f, float* P,
-             float* bal, float* z, void* ws, const Layout& L, int32_t* tile_base,
+             float* bal, float* z, void* ws, const Layout& L, bool for_layer,
              int32_t* offsets, cudaStream_t st, float* importance = nullptr,
              float* importance_cv2 = nullptr, float* entropy_mean = nullptr,
              const RouteExtras& ex = RouteExtras()) {
   const bool want_imp = (importance != nullptr || importance_cv2 != nullptr) && s->k > 0;
-  const bool want_ent = entropy_mean != nullptr;
+  RouterArgs ra{};
+  ra.T = s->T;
+  ra.d = s->d;
+  ra.E = s->E;
+  ra.k = ex.scores_t ? 0 : s->k;  // expert choice: no per-token Top-k
+  ra.logit_offset = off;
+  ra.sel_bias = bias;
+  ra.ids = ids;
+  ra.gates = gates;
+  ra.status = at<int>(ws, L.status);
+  ra.timeout_ns = timeout_of(s);
+  ra.flags = s->flags & (kRouteSigmoid | kRouteNoRenorm);
+  ra.pair_score = ex.pair_score;
+  ra.scores_t = ex.scores_t;
+  uint8_t* racc = at<uint8_t>(ws, L.racc);
+  set_router_scratch(&ra, racc, at<float>(ws, L.tile_lse2), at<int>(ws, L.tile_arrive),
+                     L.max_split > 1 ? at<float>(ws, L.part) : nullptr, L.max_split);
+  if (want_imp) ra.acc_imp = reinterpret_cast<unsigned long long*>(racc + 3072);
+  if (entropy_mean == nullptr) ra.acc_ent = nullptr;
+  if (for_layer) {
+    // the permutation's inputs: per-tile counts and per-chunk bases
+    ra.tile_hist = at<int32_t>(ws, L.tile_hist);
+    ra.chunk_acc = at<int32_t>(ws, L.chunk_acc);
+    ra.chunk_base = at<int32_t>(ws, L.tile_base);
+    ra.chunk_tiles = L.chunk_tiles;
+    ra.n_chunks = L.n_chunks;
+  }
+  ra.C = L.C;
+  ra.balance_coef = s->balance_coef;
+  ra.counts = counts;
+  ra.f = f;
+  ra.P = P;
+  ra.bal_loss = bal;
+  ra.z_loss = z;
+  ra.offsets = offsets;
+  ra.all_offsets = ex.all_offsets;
+  ra.importance = want_imp ? importance : nullptr;
+  ra.importance_cv2 = want_imp ? importance_cv2 : nullptr;
+  ra.entropy_mean = entropy_mean;
+  ra.fixed_count = ex.fixed_count;
+  ra.n_pairs = ex.n_pairs;
+  CUtensorMap mx, mw;
+  std::memset(&mx, 0, sizeof(mx));
+  std::memset(&mw, 0, sizeof(mw));
   if (s->T > 0) {
-    CUtensorMap mx, mw;
     const uint32_t nr = static_cast<uint32_t>((s->E + 15) / 16 * 16);
     if (!make_tmap_bf16(&mx, x, s->T, s->d, 128)) return MOE_ERR_CUDA;
     if (!make_tmap_bf16(&mw, wr, s->E, s->d, nr)) return MOE_ERR_CUDA;
-    RouterArgs ra{};
-    ra.T = s->T;
-    ra.d = s->d;
-    ra.E = s->E;
-    ra.k = ex.scores_t ? 0 : s->k;  // expert choice: no per-token Top-k
-    ra.logit_offset = off;
-    ra.sel_bias = bias;
-    ra.ids = ids;
-    ra.gates = gates;
-    ra.tile_hist = at<int32_t>(ws, L.tile_hist);
-    ra.tile_psum = at<float>(ws, L.tile_psum);
-    ra.tile_lse2 = at<float>(ws, L.tile_lse2);
-    ra.status = at<int>(ws, L.status);
-    ra.timeout_ns = timeout_of(s);
-    ra.flags = s->flags & (kRouteSigmoid | kRouteNoRenorm);
-    ra.tile_imp = want_imp ? at<float>(ws, L.tile_imp) : nullptr;
-    ra.tile_ent = want_ent ? at<float>(ws, L.tile_ent) : nullptr;
-    ra.pair_score = ex.pair_score;
-    ra.scores_t = ex.scores_t;
-    const int rc = tracked(MOE_KERNEL_ROUTER, st, [&] { return launch_router(mx, mw, ra, sm_count_cached(), st); });
-    if (rc != 0) return cuda_rc(rc);
   }
-  FinalizeArgs fa{};
-  fa.T = s->T;
-  fa.E = s->E;
-  fa.k = s->k;
-  fa.C = L.C;
-  fa.balance_coef = s->balance_coef;
-  fa.tile_hist = at<int32_t>(ws, L.tile_hist);
-  fa.tile_psum = at<float>(ws, L.tile_psum);
-  fa.tile_lse2 = at<float>(ws, L.tile_lse2);
-  fa.counts = counts;
-  fa.f = f;
-  fa.P = P;
-  fa.bal_loss = bal;
-  fa.z_loss = z;
-  fa.tile_base = tile_base;
-  fa.offsets = offsets;
-  fa.exp_count = at<int32_t>(ws, L.exp_count);
-  fa.exp_psum = at<double>(ws, L.exp_psum);
-  fa.done_counter = at<int>(ws, L.status + 64);
-  fa.fixed_count = ex.fixed_count;
-  fa.n_pairs = ex.n_pairs;
-  fa.all_offsets = ex.all_offsets;
-  if (want_imp) {
-    fa.tile_imp = at<float>(ws, L.tile_imp);
-    fa.exp_imp = at<double>(ws, L.exp_imp);
-    fa.importance = importance;
-    fa.importance_cv2 = importance_cv2;
-    if (s->T == 0) {  // no router launch wrote the partials
-      if (importance) cudaMemsetAsync(importance, 0, sizeof(float) * s->E, st);
-      if (importance_cv2) cudaMemsetAsync(importance_cv2, 0, sizeof(float), st);
-      fa.tile_imp = nullptr;
-    }
+  if (s->k == 0 || ex.scores_t) {
+    // no Top-k: zero importance (its definition has no selected experts)
+    if (importance) cudaMemsetAsync(importance, 0, sizeof(float) * s->E, st);
+    if (importance_cv2) cudaMemsetAsync(importance_cv2, 0, sizeof(float), st);
   }
-  if (want_ent) {
-    fa.tile_ent = at<float>(ws, L.tile_ent);
-    fa.entropy_mean = entropy_mean;
-  }
-  return cuda_rc(tracked(MOE_KERNEL_FINALIZE, st, [&] { return launch_finalize(fa, st); }));
+  return cuda_rc(tracked(MOE_KERNEL_ROUTER, st, [&] {
+    return launch_router(mx, mw, ra, sm_count_cached(), st);
+  }));
 }
 
+// chunk_tiles: tiles per base in the workspace's tile_base region (the
+// router's chunks in the layer, 1 after finalize_kernel in moe_permute)
 int do_scatter(const moe_shape_t* s, const uint16_t* x, const int32_t* ids, const Layout& L,
                void* ws, const int32_t* offsets, int32_t* slot_row, int32_t* row_token,
-               uint8_t* drop_mask, uint16_t* x_perm, cudaStream_t st,
+               uint8_t* drop_mask, uint16_t* x_perm, cudaStream_t st, int32_t chunk_tiles,
                const float* gates = nullptr, float* row_gate = nullptr) {
   ScatterArgs sa{};
   sa.T = s->T;
@@ -320,6 +350,8 @@ int do_scatter(const moe_shape_t* s, const uint16_t* x, const int32_t* ids, cons
   sa.C = L.C;
   sa.ids = ids;
   sa.tile_base = at<int32_t>(ws, L.tile_base);
+  sa.tile_hist = at<int32_t>(ws, L.tile_hist);
+  sa.chunk_tiles = chunk_tiles;
   sa.offsets = offsets;
   sa.x = x;
   sa.slot_row = slot_row;
@@ -329,6 +361,8 @@ int do_scatter(const moe_shape_t* s, const uint16_t* x, const int32_t* ids, cons
   sa.num_sms = sm_count_cached();
   sa.gates = gates;
   sa.row_gate = row_gate;
+  sa.rmax = L.rmax;
+  sa.status = at<int>(ws, L.status);
   return cuda_rc(tracked(MOE_KERNEL_SCATTER, st, [&] { return launch_scatter(sa, st); }));
 }
 
@@ -347,6 +381,8 @@ int do_priority_dispatch(const moe_shape_t* s, const uint16_t* x, const int32_t*
   sa.C = L.C;
   sa.ids = ids;
   sa.tile_base = at<int32_t>(ws, L.tile_base);
+  sa.tile_hist = at<int32_t>(ws, L.tile_hist);
+  sa.chunk_tiles = L.chunk_tiles;
   sa.offsets = offsets;
   sa.x = x;
   sa.num_sms = sm_count_cached();
@@ -354,6 +390,8 @@ int do_priority_dispatch(const moe_shape_t* s, const uint16_t* x, const int32_t*
   sa.stage_key = at<float>(ws, L.stage_key);
   sa.pair_score = at<float>(ws, L.pair_score);
   sa.all_offsets = at<int32_t>(ws, L.all_offsets);
+  sa.rmax = static_cast<int64_t>(s->T) * s->k;  // staging rows: every pair
+  sa.status = at<int>(ws, L.status);
   int rc = cuda_rc(tracked(MOE_KERNEL_SCATTER, st, [&] { return launch_scatter(sa, st); }));
   if (rc != MOE_OK) return rc;
   PrioritySelectArgs pa{};
@@ -369,11 +407,14 @@ int do_priority_dispatch(const moe_shape_t* s, const uint16_t* x, const int32_t*
   pa.row_token = row_token;
   pa.gates = gates;
   pa.row_gate = row_gate;
+  pa.rmax = L.rmax;
+  pa.n_pairs = static_cast<int64_t>(s->T) * s->k;
+  pa.status = at<int>(ws, L.status);
   rc = cuda_rc(tracked(MOE_KERNEL_SELECT, st, [&] { return launch_priority_select(pa, st); }));
   if (rc != MOE_OK || x_perm == nullptr) return rc;  // no x_perm: GEMM-1 gathers the rows
   return cuda_rc(tracked(MOE_KERNEL_GATHER, st, [&] {
     return launch_gather_rows(x, row_token, offsets, s->E, s->d, L.rmax, x_perm,
-                              sm_count_cached(), st);
+                              sm_count_cached(), s->T, at<int>(ws, L.status), st);
   }));
 }
 
@@ -387,7 +428,7 @@ int do_ec_route(const moe_shape_t* s, const uint16_t* x, const uint16_t* wr, con
   ex.fixed_count = static_cast<int32_t>(L.r);
   ex.n_pairs = static_cast<double>(s->E) * static_cast<double>(L.r);
   int rc = do_route(s, x, wr, off, nullptr, nullptr, nullptr, counts, f, P, bal, z, ws, L,
-                    nullptr, at<int32_t>(ws, L.offsets), st, nullptr, nullptr, nullptr, ex);
+                    false, at<int32_t>(ws, L.offsets), st, nullptr, nullptr, nullptr, ex);
   if (rc != MOE_OK || s->T == 0) return rc;
   EcSelectArgs ea{};
   ea.T = s->T;
@@ -503,6 +544,9 @@ int do_ffn(const moe_shape_t* s, const uint16_t* x_perm, const int32_t* offsets,
   g1.status = at<int>(ws, L.status);
   g1.timeout_ns = timeout_of(s);
   g1.gather_rows = routed ? gather_rows : nullptr;
+  g1.out_rows_routed = L.rmax;
+  g1.out_rows_shared = T;
+  g1.gather_limit = T;
   if (tune.tail_max_n != 0) g1.tail_max_n = tune.tail_max_n < 0 ? 0 : tune.tail_max_n;
   if (tune.n_block != 0) g1.n_block = tune.n_block;
   if (tune.block_min_rows != 0) g1.block_min_rows = tune.block_min_rows;
@@ -567,6 +611,8 @@ int do_ffn(const moe_shape_t* s, const uint16_t* x_perm, const int32_t* offsets,
   g2.k_shared = static_cast<int32_t>(Ms > 0 ? Ms : 64);
   g2.out_routed = y_perm;
   g2.ld_routed = d;
+  g2.out_rows_routed = L.rmax;
+  g2.out_rows_shared = T;
   g2.out_shared = y_s;
   g2.ld_shared = d;
   rc = tracked(MOE_KERNEL_GEMM_DOWN, st,
@@ -594,6 +640,7 @@ const char* moe_error_string(int code) {
     case MOE_ERR_CUDA: return "CUDA call failed";
     case MOE_ERR_TIMEOUT: return "bounded device wait timed out";
     case MOE_ERR_WORKSPACE: return "workspace too small";
+    case MOE_ERR_BOUNDS: return "device index out of range (bounds-checked build)";
     default: return "unknown error";
   }
 }
@@ -648,7 +695,7 @@ int moe_route(const moe_shape_t* s, const uint16_t* x, const uint16_t* w_router,
     if (s->k > 0 && (!ids || !gates)) return MOE_ERR_INVALID_ARG;
   }
   return do_route(s, x, w_router, logit_offset, sel_bias, ids, gates, counts, f, P, bal_loss,
-                  z_loss, ws, L, nullptr, nullptr, static_cast<cudaStream_t>(stream));
+                  z_loss, ws, L, false, nullptr, static_cast<cudaStream_t>(stream));
 }
 
 int moe_route_ex(const moe_shape_t* s, const uint16_t* x, const uint16_t* w_router,
@@ -665,7 +712,7 @@ int moe_route_ex(const moe_shape_t* s, const uint16_t* x, const uint16_t* w_rout
     if (s->k > 0 && (!o->ids || !o->gates)) return MOE_ERR_INVALID_ARG;
   }
   return do_route(s, x, w_router, logit_offset, sel_bias, o->ids, o->gates, o->counts, o->f,
-                  o->P, o->bal_loss, o->z_loss, ws, L, nullptr, nullptr,
+                  o->P, o->bal_loss, o->z_loss, ws, L, false, nullptr,
                   static_cast<cudaStream_t>(stream), o->importance, o->importance_cv2,
                   o->entropy_mean);
 }
@@ -688,7 +735,7 @@ int moe_permute(const moe_shape_t* s, const uint16_t* x, const int32_t* ids, int
   int32_t* tile_hist = at<int32_t>(ws, L.tile_hist);
   if (work) {
     if ((rc = cuda_rc(tracked(MOE_KERNEL_TILE_HIST, st, [&] {
-           return launch_tile_hist(ids, s->T, s->k, s->E, tile_hist, st);
+           return launch_tile_hist(ids, s->T, s->k, s->E, tile_hist, at<int>(ws, L.status), st);
          }))) != MOE_OK)
       return rc;
   }
@@ -707,7 +754,7 @@ int moe_permute(const moe_shape_t* s, const uint16_t* x, const int32_t* ids, int
       MOE_OK)
     return rc;
   if (!work) return MOE_OK;
-  return do_scatter(s, x, ids, L, ws, offsets, slot_row, row_token, drop_mask, x_perm, st);
+  return do_scatter(s, x, ids, L, ws, offsets, slot_row, row_token, drop_mask, x_perm, st, 1);
 }
 
 int moe_grouped_ffn(const moe_shape_t* s, const uint16_t* x_perm, const int32_t* offsets,
@@ -744,7 +791,10 @@ int moe_combine(const moe_shape_t* s, const uint16_t* y_perm, const int32_t* slo
   if (y_shared && !aligned16(y_shared)) return MOE_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   return cuda_rc(tracked(MOE_KERNEL_COMBINE, st, [&] {
-    return launch_combine(s->T, s->d, s->k, y_perm, slot_row, gates, y_shared, y, st);
+    // no workspace: a failed index check (bounds-checked builds) skips the row
+    // without recording it
+    return launch_combine(s->T, s->d, s->k, y_perm, slot_row, gates, y_shared, y,
+                          layout_of(s).rmax, nullptr, st);
   }));
 }
 
@@ -779,8 +829,7 @@ int moe_layer_forward(const moe_shape_t* s, const uint16_t* x, const uint16_t* w
     ex.all_offsets = at<int32_t>(ws, L.all_offsets);
   }
   rc = do_route(s, x, w_router, logit_offset, sel_bias, ids, gates, counts, f, P, bal_loss,
-                z_loss, ws, L, at<int32_t>(ws, L.tile_base), offsets, st, nullptr, nullptr,
-                nullptr, ex);
+                z_loss, ws, L, true, offsets, st, nullptr, nullptr, nullptr, ex);
   if (rc != MOE_OK || s->T == 0) return rc;
   int32_t* slot_row = at<int32_t>(ws, L.slot_row);
   uint16_t* x_perm = at<uint16_t>(ws, L.x_perm);
@@ -796,8 +845,8 @@ int moe_layer_forward(const moe_shape_t* s, const uint16_t* x, const uint16_t* w
       rc = do_priority_dispatch(s, x, ids, L, ws, offsets, slot_row, row_token, drop_mask, xp,
                                 st, gates, row_gate);
     else
-      rc = do_scatter(s, x, ids, L, ws, offsets, slot_row, row_token, drop_mask, xp, st, gates,
-                      row_gate);
+      rc = do_scatter(s, x, ids, L, ws, offsets, slot_row, row_token, drop_mask, xp, st,
+                      L.chunk_tiles, gates, row_gate);
     if (rc != MOE_OK) return rc;
   }
   rc = do_ffn(s, fused ? nullptr : x_perm, offsets, w13, w2, y_perm, x, w13_shared, w2_shared,
@@ -805,7 +854,8 @@ int moe_layer_forward(const moe_shape_t* s, const uint16_t* x, const uint16_t* w
   if (rc != MOE_OK) return rc;
   const float* combine_gates = gate_epi ? nullptr : gates;
   return cuda_rc(tracked(MOE_KERNEL_COMBINE, st, [&] {
-    return launch_combine(s->T, s->d, s->k, y_perm, slot_row, combine_gates, y_s, y, st);
+    return launch_combine(s->T, s->d, s->k, y_perm, slot_row, combine_gates, y_s, y, L.rmax,
+                          at<int>(ws, L.status), st);
   }));
 }
 
@@ -983,7 +1033,7 @@ int moe_ec_layer_forward(const moe_shape_t* s, const uint16_t* x, const uint16_t
   if (L.rmax > 0 && !fused) {
     rc = cuda_rc(tracked(MOE_KERNEL_GATHER, st, [&] {
       return launch_gather_rows(x, row_token, offsets, s->E, s->d, L.rmax, x_perm,
-                                sm_count_cached(), st);
+                                sm_count_cached(), s->T, at<int>(ws, L.status), st);
     }));
     if (rc != MOE_OK) return rc;
   }
@@ -994,7 +1044,7 @@ int moe_ec_layer_forward(const moe_shape_t* s, const uint16_t* x, const uint16_t
   const float* combine_gates = gate_epi ? nullptr : row_gate;
   return cuda_rc(tracked(MOE_KERNEL_COMBINE, st, [&] {
     return launch_ec_combine(s->T, s->d, s->E, at<int32_t>(ws, L.sel_t), combine_gates, y_perm,
-                             y_s, y, st);
+                             y_s, y, L.rmax, at<int>(ws, L.status), st);
   }));
 }
 
@@ -1006,7 +1056,7 @@ int moe_check_status(void* ws, int* status, void* stream) {
     return MOE_ERR_CUDA;
   if (cudaMemsetAsync(ws, 0, sizeof(int), st) != cudaSuccess) return MOE_ERR_CUDA;
   if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
-  *status = (v == 0) ? MOE_OK : MOE_ERR_TIMEOUT;
+  *status = (v == 0) ? MOE_OK : (v == kStatusBounds ? MOE_ERR_BOUNDS : MOE_ERR_TIMEOUT);
   return MOE_OK;
 }
 

@@ -12,6 +12,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include "bounds.cuh"
 #include "moe_internal.h"
 #include "sm100_primitives.cuh"
 
@@ -45,7 +46,8 @@ template <int K>
 __global__ void __launch_bounds__(kCombineWarps * 32)
     combine_kernel(int32_t T, int32_t d, const uint16_t* __restrict__ y_perm,
                    const int32_t* __restrict__ slot_row, const float* __restrict__ gates,
-                   const uint16_t* __restrict__ y_shared, uint16_t* __restrict__ y) {
+                   const uint16_t* __restrict__ y_shared, uint16_t* __restrict__ y, int64_t rmax,
+                   int* status) {
   // vectors per lane per iteration: about 8 loads of 16 bytes in flight
   constexpr int U = (K + 1) >= 8 ? 1 : 8 / (K + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -56,6 +58,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
 #pragma unroll
   for (int s = 0; s < K; ++s) {
     rows[s] = slot_row[static_cast<int64_t>(t) * K + s];
+    if (rows[s] >= 0 && !idx_ok(rows[s], rmax, status)) rows[s] = -1;
     g[s] = gates ? gates[static_cast<int64_t>(t) * K + s] : 1.0f;  // null: rows pre-scaled
   }
   const int nvec = d / 8;
@@ -139,20 +142,20 @@ __global__ void timeout_probe_kernel(int* status, uint64_t timeout_ns) {
 
 int launch_combine(int32_t T, int32_t d, int32_t k, const uint16_t* y_perm,
                    const int32_t* slot_row, const float* gates, const uint16_t* y_shared,
-                   uint16_t* y, cudaStream_t stream) {
+                   uint16_t* y, int64_t rmax, int* status, cudaStream_t stream) {
   if (T == 0) return 0;
   const int grid = (T + kCombineWarps - 1) / kCombineWarps;
   const dim3 b(kCombineWarps * 32);
   switch (k) {
-    case 0: combine_kernel<0><<<grid, b, 0, stream>>>(T, d, y_perm, slot_row, gates, y_shared, y); break;
-    case 1: combine_kernel<1><<<grid, b, 0, stream>>>(T, d, y_perm, slot_row, gates, y_shared, y); break;
-    case 2: combine_kernel<2><<<grid, b, 0, stream>>>(T, d, y_perm, slot_row, gates, y_shared, y); break;
-    case 3: combine_kernel<3><<<grid, b, 0, stream>>>(T, d, y_perm, slot_row, gates, y_shared, y); break;
-    case 4: combine_kernel<4><<<grid, b, 0, stream>>>(T, d, y_perm, slot_row, gates, y_shared, y); break;
-    case 5: combine_kernel<5><<<grid, b, 0, stream>>>(T, d, y_perm, slot_row, gates, y_shared, y); break;
-    case 6: combine_kernel<6><<<grid, b, 0, stream>>>(T, d, y_perm, slot_row, gates, y_shared, y); break;
-    case 7: combine_kernel<7><<<grid, b, 0, stream>>>(T, d, y_perm, slot_row, gates, y_shared, y); break;
-    case 8: combine_kernel<8><<<grid, b, 0, stream>>>(T, d, y_perm, slot_row, gates, y_shared, y); break;
+    case 0: combine_kernel<0><<<grid, b, 0, stream>>>(T, d, y_perm, slot_row, gates, y_shared, y, rmax, status); break;
+    case 1: combine_kernel<1><<<grid, b, 0, stream>>>(T, d, y_perm, slot_row, gates, y_shared, y, rmax, status); break;
+    case 2: combine_kernel<2><<<grid, b, 0, stream>>>(T, d, y_perm, slot_row, gates, y_shared, y, rmax, status); break;
+    case 3: combine_kernel<3><<<grid, b, 0, stream>>>(T, d, y_perm, slot_row, gates, y_shared, y, rmax, status); break;
+    case 4: combine_kernel<4><<<grid, b, 0, stream>>>(T, d, y_perm, slot_row, gates, y_shared, y, rmax, status); break;
+    case 5: combine_kernel<5><<<grid, b, 0, stream>>>(T, d, y_perm, slot_row, gates, y_shared, y, rmax, status); break;
+    case 6: combine_kernel<6><<<grid, b, 0, stream>>>(T, d, y_perm, slot_row, gates, y_shared, y, rmax, status); break;
+    case 7: combine_kernel<7><<<grid, b, 0, stream>>>(T, d, y_perm, slot_row, gates, y_shared, y, rmax, status); break;
+    case 8: combine_kernel<8><<<grid, b, 0, stream>>>(T, d, y_perm, slot_row, gates, y_shared, y, rmax, status); break;
     default: return -2;
   }
   return cudaGetLastError() == cudaSuccess ? 0 : -3;

@@ -31,6 +31,7 @@
 
 #include <cstdio>
 
+#include "bounds.cuh"
 #include "moe_internal.h"
 #include "sm100_primitives.cuh"
 
@@ -282,6 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < 4; ++j) {
             const int i = 4 * lane + j;
             rr[j] = __ldg(p.gather_rows + ti.a_row + (i < nvalid ? i : nvalid - 1));
+            if (!idx_ok(rr[j], p.gather_limit, p.status)) rr[j] = 0;
           }
         }
         bool ok = true;
@@ -393,8 +395,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t q = static_cast<uint32_t>(local >> 1);
       if (!mbar_wait_bounded(&st->tfull[a], q & 1u, p.timeout_ns, p.status, abort_flag)) break;
       tc_fence_after();
-      const bool valid = r_in_tile < ti.rows_left;
+      const int64_t out_rows = ti.shared ? p.out_rows_shared : p.out_rows_routed;
       const int64_t row = static_cast<int64_t>(ti.a_row) + r_in_tile;
+      const bool valid = r_in_tile < ti.rows_left && idx_ok(row, out_rows, p.status);
       const uint32_t taddr =
           tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(a * BN);
       __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(ti.shared ? p.out_shared
@@ -415,7 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_ld_wait();
 #pragma unroll
             for (int j = 0; j < 32; ++j)
-              if (c + j < ti.rows_left)
+              if (c + j < ti.rows_left && idx_ok(ti.a_row + c + j, out_rows, p.status))
                 dst[static_cast<int64_t>(c + j) * ld] = __float2bfloat16_rn(silu_f32(g[j]) * u[j]);
           }
         } else {
@@ -429,7 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               tmem_ld_wait();
 #pragma unroll
               for (int j = 0; j < 32; ++j)
-                if (c + j < ti.rows_left) {
+                if (c + j < ti.rows_left && idx_ok(ti.a_row + c + j, out_rows, p.status)) {
                   float o = v[j];
                   if constexpr (kRowScale)
                     if (!ti.shared) o *= __ldg(p.row_scale + ti.a_row + c + j);
@@ -824,8 +827,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int r_in_tile = static_cast<int>(rank) * (half ? 64 : 128) +
                             (half ? (r_in_half & 63) : r_in_half);
       const int col_half = half ? (r_in_half >> 6) : 0;
-      const bool valid = r_in_tile < ti.rows_left;
       const int64_t row = static_cast<int64_t>(ti.a_row) + r_in_tile;
+      const bool valid = r_in_tile < ti.rows_left &&
+                         idx_ok(row, ti.shared ? p.out_rows_shared : p.out_rows_routed, p.status);
       const uint32_t taddr =
           tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(a * BN);
       __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(ti.shared ? p.out_shared

@@ -9,6 +9,7 @@ namespace moe {
 
 constexpr int kTileTokens = 128;  // tokens per router / permute tile (= MMA M)
 constexpr int kMaxTopK = 8;
+constexpr int kMaxSplitUnits = 8;  // largest K split of a router tile
 // routing variants (the values of MOE_FLAG_SIGMOID / MOE_FLAG_NO_RENORM)
 constexpr uint32_t kRouteSigmoid = 1u;
 constexpr uint32_t kRouteNoRenorm = 2u;
@@ -57,6 +58,10 @@ struct GroupedGemmArgs {
   // Pair kernel: a group's last tile with at most 128 rows runs as one M = 128
   // pair MMA (half the padding) instead of a 256-row tile.
   int32_t half_tiles = 1;
+  // Bounds-checked builds: rows of the two outputs and of the gathered tensor
+  int64_t out_rows_routed = INT64_MAX;
+  int64_t out_rows_shared = INT64_MAX;
+  int64_t gather_limit = INT64_MAX;
 };
 
 // A0/A1: activations [rows][K] (routed / shared), B0/B1: weights [rows][K].
@@ -76,33 +81,62 @@ int launch_grouped_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUte
 bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                     uint32_t box_rows);
 
-// Router: logits tile GEMM + softmax / bias / Top-k epilogue (one CTA per
-// 128 tokens).  Writes ids, gates and per-tile partials.
+// Router: logits tile GEMM + softmax / bias / Top-k epilogue on a persistent
+// grid, and the reduction of the side outputs by the CTA that completes the
+// last tile.  Accumulators (acc_*, tiles_done, tile_arrive, chunk_acc) must be
+// zero before the launch; the kernel leaves them at zero.
 struct RouterArgs {
   int32_t T, d, E, k;
   const float* logit_offset;  // [E] or null
   const float* sel_bias;      // [E] or null
   int32_t* ids;               // [T][k]
   float* gates;               // [T][k]
-  int32_t* tile_hist;         // [ntiles][E]
-  float* tile_psum;           // [ntiles][E]
-  float* tile_lse2;           // [ntiles]
   int* status;
   uint64_t timeout_ns;
-  int32_t split;              // CTAs of a cluster sharing one tile (set by the launcher)
-  int32_t stages;             // pipeline depth (set by the launcher)
   uint32_t flags;             // kRouteSigmoid | kRouteNoRenorm
-  float* tile_imp;            // [ntiles][E] importance partials, or null
-  float* tile_ent;            // [ntiles] entropy partials, or null
+  int32_t max_split = kMaxSplitUnits;  // largest K split the caller's scratch allows
+  int32_t split = 1;          // set by the launcher
+  int32_t stages = 1;         // set by the launcher
   float* pair_score = nullptr;  // [T][k] unbiased score of each selected pair, or null
   float* scores_t = nullptr;    // [E][T] every score, expert-major, or null
+  // scratch
+  float* part_logits = nullptr;         // [S][ntiles][E][128] partial logits (K split)
+  int* tile_arrive = nullptr;           // [ntiles] slices stored per tile (K split)
+  float* tile_lse2 = nullptr;           // [ntiles] sum of lse^2 over each tile's rows
+  int* tiles_done = nullptr;            // [1]
+  int* acc_count = nullptr;             // [E] pairs per expert
+  unsigned long long* acc_psum = nullptr;  // [E] sum of scores, fixed point 2^-32
+  unsigned long long* acc_imp = nullptr;   // [E] importance, fixed point, or null
+  unsigned long long* acc_ent = nullptr;   // [1] entropy sum, fixed point, or null
+  int32_t* tile_hist = nullptr;         // [ntiles][E] per-tile counts, or null
+  int32_t* chunk_acc = nullptr;         // [n_chunks][E] counts per chunk of tiles, or null
+  int32_t* chunk_base = nullptr;        // [n_chunks][E] exclusive scan of chunk_acc over chunks
+  int32_t chunk_tiles = 1;              // tiles per chunk
+  int32_t n_chunks = 0;
+  // outputs of the reduction
+  int64_t C = -1;                       // capacity or -1
+  float balance_coef = 0.0f;
+  int32_t* counts = nullptr;            // [E]
+  float* f = nullptr;                   // [E]
+  float* P = nullptr;                   // [E]
+  float* bal_loss = nullptr;            // [1]
+  float* z_loss = nullptr;              // [1]
+  int32_t* offsets = nullptr;           // [E+1] kept-row offsets, or null
+  int32_t* all_offsets = nullptr;       // [E+1] offsets before capacity, or null
+  float* importance = nullptr;          // [E] or null
+  float* importance_cv2 = nullptr;      // [1] or null
+  float* entropy_mean = nullptr;        // [1] or null
+  int32_t fixed_count = -1;             // >= 0: every expert's count (expert choice)
+  double n_pairs = -1.0;                // denominator of f; < 0: k T
 };
 int launch_router(const CUtensorMap& x_map, const CUtensorMap& wr_map, RouterArgs args,
                   int num_sms, cudaStream_t stream);
+// K split the router takes for this shape (1 = none).
+int router_split(int T, int d, int num_sms, int max_split);
 
 // Per-tile expert histogram of ids (when the router did not produce it).
 int launch_tile_hist(const int32_t* ids, int32_t T, int32_t k, int32_t E, int32_t* tile_hist,
-                     cudaStream_t stream);
+                     int* status, cudaStream_t stream);
 
 // Reduces the per-tile partials: counts, f, P, losses (optional) and the
 // permutation scan (offsets of kept rows, per-tile bases).
@@ -140,7 +174,11 @@ struct ScatterArgs {
   int32_t T, d, E, k;
   int64_t C;
   const int32_t* ids;        // [T][k]
-  const int32_t* tile_base;  // [ntiles][E]
+  // base of tile t for expert e: tile_base[(t / chunk_tiles) E + e] plus the
+  // counts of the chunk's earlier tiles, tile_hist[t' E + e]
+  const int32_t* tile_base;  // [ceil(ntiles / chunk_tiles)][E]
+  const int32_t* tile_hist = nullptr;  // [ntiles][E] (chunk_tiles > 1)
+  int32_t chunk_tiles = 1;
   const int32_t* offsets;    // [E+1]
   const uint16_t* x;         // [T][d]
   int32_t* slot_row;         // [T][k]
@@ -158,6 +196,8 @@ struct ScatterArgs {
   float* stage_key = nullptr;          // [T*k]
   const float* pair_score = nullptr;   // [T][k]
   const int32_t* all_offsets = nullptr;  // [E+1]
+  int64_t rmax = 0;                    // rows of x_perm / row_token / row_gate (staging: T k)
+  int* status = nullptr;               // bounds-checked builds: where a failed check is recorded
 };
 int launch_scatter(const ScatterArgs& args, cudaStream_t stream);
 
@@ -174,6 +214,9 @@ struct PrioritySelectArgs {
   int32_t* row_token;          // [R]
   const float* gates = nullptr;  // [T][k]; with row_gate, each kept row gets its gate
   float* row_gate = nullptr;     // [R] or null
+  int64_t rmax = 0;              // rows of row_token / row_gate
+  int64_t n_pairs = 0;           // T k: pair numbers in stage_q lie below
+  int* status = nullptr;         // bounds-checked builds
 };
 int launch_priority_select(const PrioritySelectArgs& args, cudaStream_t stream);
 
@@ -188,17 +231,20 @@ struct EcSelectArgs {
 int launch_ec_select(const EcSelectArgs& args, cudaStream_t stream);
 
 // x_perm[row] = x[row_token[row]] for row < offsets[E] (read on the device).
+// x_rows: rows of x (row_token values must lie below); status: bounds-checked
+// builds record a failed index check there (null: not recorded).
 int launch_gather_rows(const uint16_t* x, const int32_t* row_token, const int32_t* offsets,
                        int32_t E, int32_t d, int64_t max_rows, uint16_t* x_perm, int num_sms,
-                       cudaStream_t stream);
+                       int64_t x_rows, int* status, cudaStream_t stream);
 
+// rmax: rows of y_perm (every row index read must lie below).
 int launch_ec_combine(int32_t T, int32_t d, int32_t E, const int32_t* sel_t,
                       const float* row_gate, const uint16_t* y_perm, const uint16_t* y_shared,
-                      uint16_t* y, cudaStream_t stream);
+                      uint16_t* y, int64_t rmax, int* status, cudaStream_t stream);
 
 int launch_combine(int32_t T, int32_t d, int32_t k, const uint16_t* y_perm,
                    const int32_t* slot_row, const float* gates, const uint16_t* y_shared,
-                   uint16_t* y, cudaStream_t stream);
+                   uint16_t* y, int64_t rmax, int* status, cudaStream_t stream);
 
 int launch_pack_w13(int32_t G, int32_t Mw, int32_t d, const uint16_t* w1, const uint16_t* w3,
                     uint16_t* w13, cudaStream_t stream);

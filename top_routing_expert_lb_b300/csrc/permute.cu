@@ -7,11 +7,13 @@
 // order.  Here the same result comes from integer work only:
 //   1. per 128-token tile, an expert histogram (from the router, or
 //      tile_hist_kernel);
-//   2. finalize_kernel: counts n_e, kept_e = min(n_e, C)
-//      (C = ceil(c k T / E), "MoE：条件计算与路由" §3), offsets = exclusive scan
-//      of kept_e, and per-tile exclusive bases tile_base[tile][e];
+//   2. counts n_e, kept_e = min(n_e, C) (C = ceil(c k T / E),
+//      "MoE：条件计算与路由" §3), offsets = exclusive scan of kept_e, and
+//      exclusive bases per chunk of tiles (the router's last CTA, chunks of up
+//      to 32 tiles) or per tile (finalize_kernel, for ids given by the caller);
 //   3. scatter_kernel: the rank of pair (t, s) among its expert's pairs in
-//      token-major order is tile_base + rank inside the tile (warp match +
+//      token-major order is the tile's base (its chunk's base plus the counts
+//      of the chunk's earlier tiles) + rank inside the tile (warp match +
 //      per-warp counts); the pair is kept iff rank < C and lands on row
 //      offsets[e] + rank.  Each token row is read once and written to each of
 //      its kept rows.  With probability-priority capacity the same ranks
@@ -25,6 +27,7 @@
 // L_z = (1/T) sum_t lse_t^2 ("MOE大模型对比篇" §2.2).
 #include <cuda_runtime.h>
 
+#include "bounds.cuh"
 #include "moe_internal.h"
 
 namespace moe {
@@ -32,7 +35,7 @@ namespace moe {
 namespace {
 
 __global__ void tile_hist_kernel(const int32_t* __restrict__ ids, int32_t T, int32_t k,
-                                 int32_t E, int32_t* __restrict__ tile_hist) {
+                                 int32_t E, int32_t* __restrict__ tile_hist, int* status) {
   __shared__ int hist[256];
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
   __syncthreads();
@@ -40,7 +43,10 @@ __global__ void tile_hist_kernel(const int32_t* __restrict__ ids, int32_t T, int
   const int t0 = tile * kTileTokens;
   const int pairs = min(kTileTokens, T - t0) * k;
   const int32_t* tid = ids + static_cast<int64_t>(t0) * k;
-  for (int q = threadIdx.x; q < pairs; q += blockDim.x) atomicAdd(&hist[tid[q]], 1);
+  for (int q = threadIdx.x; q < pairs; q += blockDim.x) {
+    const int e = tid[q];
+    if (idx_ok(e, E, status)) atomicAdd(&hist[e], 1);
+  }
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x)
     tile_hist[static_cast<int64_t>(tile) * E + e] = hist[e];
@@ -199,9 +205,15 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_kernel(const ScatterA
   const int ntok = min(kTileTokens, a.T - t0);
   const int pairs = ntok * k;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // this tile's base per expert: its chunk's base plus the counts of the
+  // chunk's earlier tiles (chunk_tiles = 1: a per-tile base)
+  const int chunk = tile / a.chunk_tiles;
+  const int first = chunk * a.chunk_tiles;
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     run[e] = 0;
-    base[e] = a.tile_base[static_cast<int64_t>(tile) * E + e];
+    int b = a.tile_base[static_cast<int64_t>(chunk) * E + e];
+    for (int tt = first; tt < tile; ++tt) b += __ldg(a.tile_hist + static_cast<int64_t>(tt) * E + e);
+    base[e] = b;
 #pragma unroll
     for (int w = 0; w < kScatterWarps; ++w) wcnt[w][e] = 0;
   }
@@ -211,8 +223,13 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_kernel(const ScatterA
   const bool staging = a.stage_q != nullptr;
   for (int q0 = 0; q0 < pairs; q0 += kScatterThreads) {
     const int q = q0 + threadIdx.x;
-    const bool active = q < pairs;
-    const int e = active ? tid[q] : -1;
+    bool active = q < pairs;
+    int e = active ? tid[q] : -1;
+    if (kBoundsChecked && active && !idx_ok(e, E, a.status)) {
+      active = false;  // an expert id outside [0, E): the pair is left unplaced
+      e = -1;
+      rows[q] = -1;
+    }
     const unsigned peers = __match_any_sync(0xffffffffu, e);
     const int rank_w = __popc(peers & lt_mask);
     if (active && rank_w == 0) wcnt[warp][e] = __popc(peers);
@@ -243,6 +260,7 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_kernel(const ScatterA
   if (staging) {
     for (int q = threadIdx.x; q < pairs; q += blockDim.x) {
       const int64_t gq = static_cast<int64_t>(t0) * k + q;
+      if (!idx_ok(rows[q], a.rmax, a.status)) continue;
       a.stage_q[rows[q]] = static_cast<int32_t>(gq);
       a.stage_key[rows[q]] = __ldg(a.pair_score + gq);
     }
@@ -254,7 +272,7 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_kernel(const ScatterA
       const int64_t gq = static_cast<int64_t>(t0) * k + q;
       a.slot_row[gq] = row;
       if (a.drop_mask) a.drop_mask[gq] = row < 0 ? 1 : 0;
-      if (row >= 0) {
+      if (row >= 0 && idx_ok(row, a.rmax, a.status)) {
         a.row_token[row] = t0 + q / k;
         if (a.row_gate) a.row_gate[row] = a.gates[gq];
       }
@@ -271,7 +289,10 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_kernel(const ScatterA
     const int t = t0 + tl;
     int dst[kMaxTopK];
 #pragma unroll
-    for (int s = 0; s < kMaxTopK; ++s) dst[s] = (s < k) ? rows[tl * k + s] : -1;
+    for (int s = 0; s < kMaxTopK; ++s) {
+      dst[s] = (s < k) ? rows[tl * k + s] : -1;
+      if (dst[s] >= 0 && !idx_ok(dst[s], a.rmax, a.status)) dst[s] = -1;
+    }
     const uint4* src = reinterpret_cast<const uint4*>(a.x + static_cast<int64_t>(t) * a.d);
     for (int v0 = lane; v0 < nvec; v0 += 32 * kGatherUnroll) {
       uint4 val[kGatherUnroll];
@@ -295,10 +316,10 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_kernel(const ScatterA
 }  // namespace
 
 int launch_tile_hist(const int32_t* ids, int32_t T, int32_t k, int32_t E, int32_t* tile_hist,
-                     cudaStream_t stream) {
+                     int* status, cudaStream_t stream) {
   const int ntiles = (T + kTileTokens - 1) / kTileTokens;
   if (ntiles == 0) return 0;
-  tile_hist_kernel<<<ntiles, 256, 0, stream>>>(ids, T, k, E, tile_hist);
+  tile_hist_kernel<<<ntiles, 256, 0, stream>>>(ids, T, k, E, tile_hist, status);
   return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }
 

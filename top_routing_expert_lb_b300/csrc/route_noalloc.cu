@@ -4,15 +4,19 @@
 // inside a host framework owning every byte of device memory through its own
 // pool, plug-ins loaded into such a process, or code paths where allocating
 // (and the device synchronisation it may imply) is not allowed.  For them this
-// entry point runs the same router and reduction kernels as moe_route, with
-// the scratch those kernels need (per-tile partial sums, per-expert totals,
-// the status word and the reduction's completion counter) placed in one
-// file-scope device array instead of a caller workspace.
+// entry point runs the same router kernel as moe_route (logits, Top-k and the
+// reduction of the side outputs in one launch), with the scratch it needs
+// (the status word, per-expert accumulators, per-tile lse^2 sums and the
+// finished-tile counter) placed in one file-scope device array instead of a
+// caller workspace.  It never splits a tile's d dimension across CTAs (that
+// would need partial logits of up to tens of MB), so shapes with few tokens
+// use fewer SMs than through moe_route.
 //
 // That array is part of the library image: every GPU that loads the library
 // holds it until the process exits.  All calls share it and it keeps the
 // contents of the last call, so each call clears the words that must start at
-// zero; two calls that overlap on the GPU (different streams, no ordering)
+// zero (and the router leaves its accumulators at zero); two calls that
+// overlap on the GPU (different streams, no ordering)
 // race on it.  The first call on a device looks up the array's device address
 // (cudaGetSymbolAddress, with that device current) and caches it; make that
 // first call before any stream capture.
@@ -22,6 +26,7 @@
 #include <atomic>
 #include <cmath>
 #include <cstdint>
+#include <cstring>
 #include <mutex>
 
 #include "../../include/moe.h"
@@ -34,15 +39,15 @@ constexpr int kNoAllocMaxTokens = MOE_NOALLOC_MAX_TOKENS;
 constexpr int kNoAllocMaxTiles = kNoAllocMaxTokens / kTileTokens;
 constexpr int kNoAllocMaxExperts = MOE_MAX_EXPERTS;
 
-// Byte offsets inside the static scratch.
-constexpr size_t kOffStatus = 0;    // int status word
-constexpr size_t kOffCounter = 64;  // int completion counter of the reduction
-constexpr size_t kOffHist = 256;
-constexpr size_t kOffPsum = kOffHist + static_cast<size_t>(kNoAllocMaxTiles) * kNoAllocMaxExperts * 4;
-constexpr size_t kOffLse2 = kOffPsum + static_cast<size_t>(kNoAllocMaxTiles) * kNoAllocMaxExperts * 4;
-constexpr size_t kOffExpCount = kOffLse2 + static_cast<size_t>(kNoAllocMaxTiles) * 4;
-constexpr size_t kOffExpPsum = kOffExpCount + kNoAllocMaxExperts * 4;
-constexpr size_t kScratchBytes = kOffExpPsum + kNoAllocMaxExperts * 8;
+// Byte offsets inside the static scratch (about 8 KB).
+constexpr size_t kOffStatus = 0;   // int status word
+constexpr size_t kOffAcc = 256;    // router accumulators: counts [256] int32 at +0, P sums
+                                   // [256] u64 at +1024, entropy u64 at +5120, finished
+                                   // tiles int32 at +5128 (5376 bytes)
+constexpr size_t kAccBytes = 5376;
+constexpr size_t kOffLse2 = kOffAcc + kAccBytes;  // [tiles] sums of lse^2
+constexpr size_t kScratchBytes = kOffLse2 + static_cast<size_t>(kNoAllocMaxTiles) * 4;
+static_assert(kNoAllocMaxExperts <= 256, "accumulator block holds 256 experts");
 
 static __device__ __align__(256) unsigned char g_route_scratch[kScratchBytes];
 
@@ -108,57 +113,46 @@ extern "C" int moe_route_noalloc(const moe_shape_t* s, const uint16_t* x,
   int num_sms = 0;
   if ((rc = scratch_for_current_device(&scratch, &num_sms)) != MOE_OK) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // status word and completion counter start at zero on every call
-  if (cudaMemsetAsync(scratch, 0, kOffHist, st) != cudaSuccess) return MOE_ERR_CUDA;
-
-  int* status = reinterpret_cast<int*>(scratch + kOffStatus);
-  int32_t* tile_hist = reinterpret_cast<int32_t*>(scratch + kOffHist);
-  float* tile_psum = reinterpret_cast<float*>(scratch + kOffPsum);
-  float* tile_lse2 = reinterpret_cast<float*>(scratch + kOffLse2);
+  // the status word and the accumulators start at zero on every call (the
+  // router also leaves them at zero, unless a bounded wait ran out)
+  if (cudaMemsetAsync(scratch, 0, kOffLse2, st) != cudaSuccess) return MOE_ERR_CUDA;
+  uint8_t* acc = scratch + kOffAcc;
+  RouterArgs ra{};
+  ra.T = s->T;
+  ra.d = s->d;
+  ra.E = s->E;
+  ra.k = s->k;
+  ra.logit_offset = logit_offset;
+  ra.sel_bias = sel_bias;
+  ra.ids = ids;
+  ra.gates = gates;
+  ra.status = reinterpret_cast<int*>(scratch + kOffStatus);
+  // the same wait limit as the workspace entry points, and only the router's
+  // own variant bits (capacity and expert-choice bits do not concern it)
+  ra.timeout_ns = s->tuning.wait_timeout_ns != 0 ? s->tuning.wait_timeout_ns
+                                                  : default_wait_timeout_ns();
+  ra.flags = s->flags & (kRouteSigmoid | kRouteNoRenorm);
+  ra.max_split = 1;
+  ra.acc_count = reinterpret_cast<int*>(acc);
+  ra.acc_psum = reinterpret_cast<unsigned long long*>(acc + 1024);
+  ra.tiles_done = reinterpret_cast<int*>(acc + 5128);
+  ra.tile_lse2 = reinterpret_cast<float*>(scratch + kOffLse2);
+  ra.C = -1;
+  ra.balance_coef = s->balance_coef;
+  ra.counts = counts;
+  ra.f = f;
+  ra.P = P;
+  ra.bal_loss = bal_loss;
+  ra.z_loss = z_loss;
+  CUtensorMap mx, mw;
+  std::memset(&mx, 0, sizeof(mx));
+  std::memset(&mw, 0, sizeof(mw));
   if (s->T > 0) {
-    CUtensorMap mx, mw;
     const uint32_t nr = static_cast<uint32_t>((s->E + 15) / 16 * 16);
     if (!make_tmap_bf16(&mx, x, s->T, s->d, 128)) return MOE_ERR_CUDA;
     if (!make_tmap_bf16(&mw, w_router, s->E, s->d, nr)) return MOE_ERR_CUDA;
-    RouterArgs ra{};
-    ra.T = s->T;
-    ra.d = s->d;
-    ra.E = s->E;
-    ra.k = s->k;
-    ra.logit_offset = logit_offset;
-    ra.sel_bias = sel_bias;
-    ra.ids = ids;
-    ra.gates = gates;
-    ra.tile_hist = tile_hist;
-    ra.tile_psum = tile_psum;
-    ra.tile_lse2 = tile_lse2;
-    ra.status = status;
-    // the same wait limit as the workspace entry points, and only the router's
-    // own variant bits (capacity and expert-choice bits do not concern it)
-    ra.timeout_ns = s->tuning.wait_timeout_ns != 0 ? s->tuning.wait_timeout_ns
-                                                    : default_wait_timeout_ns();
-    ra.flags = s->flags & (kRouteSigmoid | kRouteNoRenorm);
-    rc = launch_router(mx, mw, ra, num_sms, st);
-    if (rc != 0) return rc == -2 ? MOE_ERR_UNSUPPORTED : MOE_ERR_CUDA;
   }
-  FinalizeArgs fa{};
-  fa.T = s->T;
-  fa.E = s->E;
-  fa.k = s->k;
-  fa.C = -1;
-  fa.balance_coef = s->balance_coef;
-  fa.tile_hist = tile_hist;
-  fa.tile_psum = tile_psum;
-  fa.tile_lse2 = tile_lse2;
-  fa.counts = counts;
-  fa.f = f;
-  fa.P = P;
-  fa.bal_loss = bal_loss;
-  fa.z_loss = z_loss;
-  fa.exp_count = reinterpret_cast<int32_t*>(scratch + kOffExpCount);
-  fa.exp_psum = reinterpret_cast<double*>(scratch + kOffExpPsum);
-  fa.done_counter = reinterpret_cast<int*>(scratch + kOffCounter);
-  rc = launch_finalize(fa, st);
+  rc = launch_router(mx, mw, ra, num_sms, st);
   if (rc != 0) return rc == -2 ? MOE_ERR_UNSUPPORTED : MOE_ERR_CUDA;
   return MOE_OK;
 }

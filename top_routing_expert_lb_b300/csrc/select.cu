@@ -25,6 +25,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include "bounds.cuh"
 #include "moe_internal.h"
 #include "sm100_primitives.cuh"
 
@@ -181,12 +182,16 @@ __global__ void __launch_bounds__(kSelThreads) priority_select_kernel(const Prio
     const bool keep = gt || (eq && eq_before < ties);
     if (in) {
       const int q = __ldg(list + i);
-      if (keep) {
+      if (!idx_ok(q, a.n_pairs, a.status)) {
+        // a staged pair number outside [0, T k): nothing to place
+      } else if (keep) {
         const int row = out0 + carry_gt + ex_gt + min(eq_before, ties);
         a.slot_row[q] = row;
         if (a.drop_mask) a.drop_mask[q] = 0;
-        a.row_token[row] = q / k;
-        if (a.row_gate) a.row_gate[row] = a.gates[q];
+        if (idx_ok(row, a.rmax, a.status)) {
+          a.row_token[row] = q / k;
+          if (a.row_gate) a.row_gate[row] = a.gates[q];
+        }
       } else {
         a.slot_row[q] = -1;
         if (a.drop_mask) a.drop_mask[q] = 1;
@@ -250,12 +255,18 @@ constexpr int kGatherU = 4;
 __global__ void __launch_bounds__(kGatherWarps * 32)
     gather_rows_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ row_token,
                        const int32_t* __restrict__ offsets, int32_t E, int32_t d,
-                       uint16_t* __restrict__ x_perm) {
-  const int R = __ldg(offsets + E);
+                       uint16_t* __restrict__ x_perm, int64_t max_rows, int64_t x_rows,
+                       int* status) {
+  int R = __ldg(offsets + E);
+  if (kBoundsChecked && R > max_rows) {
+    idx_ok(R - 1, max_rows, status);  // records the overflow
+    R = static_cast<int>(max_rows);
+  }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nvec = d / 8;
   for (int row = blockIdx.x * kGatherWarps + warp; row < R; row += gridDim.x * kGatherWarps) {
     const int t = __ldg(row_token + row);
+    if (!idx_ok(t, x_rows, status)) continue;
     const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<int64_t>(t) * d);
     uint4* dst = reinterpret_cast<uint4*>(x_perm + static_cast<int64_t>(row) * d);
     for (int v0 = lane; v0 < nvec; v0 += 32 * kGatherU) {
@@ -289,7 +300,8 @@ __device__ __forceinline__ void fma_bf16x8(float (&acc)[8], const uint4 v, float
 __global__ void __launch_bounds__(kEcCombineWarps * 32)
     ec_combine_kernel(int32_t T, int32_t d, int32_t E, const int32_t* __restrict__ sel_t,
                       const float* __restrict__ row_gate, const uint16_t* __restrict__ y_perm,
-                      const uint16_t* __restrict__ y_shared, uint16_t* __restrict__ y) {
+                      const uint16_t* __restrict__ y_shared, uint16_t* __restrict__ y,
+                      int64_t rmax, int* status) {
   __shared__ int lrow[kEcCombineWarps][256];
   __shared__ float lgate[kEcCombineWarps][256];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -298,7 +310,8 @@ __global__ void __launch_bounds__(kEcCombineWarps * 32)
   int n = 0;
   for (int e0 = 0; e0 < E; e0 += 32) {
     const int e = e0 + lane;
-    const int row = e < E ? __ldg(sel_t + static_cast<int64_t>(e) * T + t) : -1;
+    int row = e < E ? __ldg(sel_t + static_cast<int64_t>(e) * T + t) : -1;
+    if (row >= 0 && !idx_ok(row, rmax, status)) row = -1;
     const unsigned m = __ballot_sync(0xffffffffu, row >= 0);
     if (row >= 0) {
       const int pos = n + __popc(m & ((1u << lane) - 1u));
@@ -360,24 +373,24 @@ int launch_ec_select(const EcSelectArgs& args, cudaStream_t stream) {
 
 int launch_gather_rows(const uint16_t* x, const int32_t* row_token, const int32_t* offsets,
                        int32_t E, int32_t d, int64_t max_rows, uint16_t* x_perm, int num_sms,
-                       cudaStream_t stream) {
+                       int64_t x_rows, int* status, cudaStream_t stream) {
   if (max_rows <= 0) return 0;
   int64_t grid = (max_rows + kGatherWarps - 1) / kGatherWarps;
   const int64_t cap = static_cast<int64_t>(num_sms) * 8;
   if (grid > cap) grid = cap;
   gather_rows_kernel<<<static_cast<unsigned>(grid), kGatherWarps * 32, 0, stream>>>(
-      x, row_token, offsets, E, d, x_perm);
+      x, row_token, offsets, E, d, x_perm, max_rows, x_rows, status);
   return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }
 
 int launch_ec_combine(int32_t T, int32_t d, int32_t E, const int32_t* sel_t,
                       const float* row_gate, const uint16_t* y_perm, const uint16_t* y_shared,
-                      uint16_t* y, cudaStream_t stream) {
+                      uint16_t* y, int64_t rmax, int* status, cudaStream_t stream) {
   if (T == 0) return 0;
   if (E > 256) return -2;
   const int grid = (T + kEcCombineWarps - 1) / kEcCombineWarps;
   ec_combine_kernel<<<grid, kEcCombineWarps * 32, 0, stream>>>(T, d, E, sel_t, row_gate, y_perm,
-                                                             y_shared, y);
+                                                             y_shared, y, rmax, status);
   return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }
 
