@@ -56,9 +56,15 @@ def parse_args(argv=None):
                     help="skip the other workloads' lines (per_config)")
     ap.add_argument("--no-graph", action="store_true",
                     help="launch every timed step directly instead of replaying CUDA graphs")
-    ap.add_argument("--stage", choices=["layer", "router"], default="layer",
+    ap.add_argument("--stage", choices=["layer", "router", "ffn"], default="layer",
                     help="router: time moe_route alone (no expert weights are drawn); "
-                         "for profiling, not the headline number")
+                         "ffn: time moe_grouped_ffn on a slice of the workload's realised "
+                         "expert loads (--experts of them); for profiling, not the headline")
+    ap.add_argument("--experts", type=int, default=0,
+                    help="--stage ffn: experts in the slice (0: all)")
+    ap.add_argument("--tune", action="append", default=[],
+                    help="moe_tuning_t field=value for --stage ffn (repeatable), "
+                         "e.g. --tune interleave_rows=256")
     return ap.parse_args(argv)
 
 
@@ -899,6 +905,101 @@ def run_router_stage(args, w):
     return 0
 
 
+def run_ffn_stage(args, w):
+    """moe_grouped_ffn alone on a slice of the workload's realised loads: the
+    router runs on the full workload (no expert weights), the experts are
+    sorted by load and every (E / n)-th of them is kept in index order, and
+    the shared group (if any) gets T n / E rows.  Device time per projection
+    (L2 flushed before each call), FFN TFLOP/s and the attainable bound of the
+    slice.  For profiling the expert GEMMs on small footprints."""
+    import torch
+
+    import synth
+    import top_routing_expert_lb_b300 as moe
+    from top_routing_expert_lb_b300 import build as mbuild
+
+    mbuild.ensure_built()
+    dev = torch.device("cuda", 0)
+    inp = synth.make_inputs(w, dev, experts=False)
+    s = moe.Shape.of(w.T, w.d, w.M, w.E, w.k, w.n_shared, w.capacity_factor, w.balance_coef)
+    ws = moe.alloc_workspace(s, dev)
+    ids = torch.empty((w.T, max(w.k, 1)), dtype=torch.int32, device=dev)
+    gates = torch.empty((w.T, max(w.k, 1)), dtype=torch.float32, device=dev)
+    counts = torch.empty(w.E, dtype=torch.int32, device=dev)
+    f, P = torch.empty(w.E, device=dev), torch.empty(w.E, device=dev)
+    lb, lz = torch.empty(1, device=dev), torch.empty(1, device=dev)
+    moe.moe_route(s, inp.x, inp.wr, inp.offset, inp.sel_bias, ids, gates, counts, f, P, lb, lz, ws)
+    C = moe.moe_capacity(s)
+    n = counts.cpu().tolist()
+    if C >= 0:
+        n = [min(v, C) for v in n]
+    del inp, ws, ids, gates
+    n_sel = args.experts if 0 < args.experts < w.E else w.E
+    order = sorted(range(w.E), key=lambda e: (-n[e], e))
+    picked = sorted(order[int(i * w.E / n_sel)] for i in range(n_sel))
+    rows = [n[e] for e in picked]
+    R = sum(rows)
+    T_sh = max(1, round(w.T * n_sel / w.E), -(-R // min(8, n_sel))) if w.n_shared else 0
+    Tshape = T_sh if w.n_shared else max(R, 1)
+    k = max(1, -(-R // Tshape))
+    tune = {kv.split("=")[0]: int(kv.split("=")[1]) for kv in args.tune}
+    sf = moe.Shape.of(Tshape, w.d, w.M, n_sel, min(k, n_sel), w.n_shared, **tune)
+    assert R <= moe.moe_max_rows(sf), "slice rows exceed the shape's row bound"
+    x_perm = synth.normal_bf16(5, synth.TID_X, (max(R, 1), w.d), 1.0, dev)
+    offsets = torch.tensor([0] + list(__import__("itertools").accumulate(rows)), dtype=torch.int32,
+                           device=dev)
+    w1 = synth.normal_bf16(5, synth.TID_W1, (n_sel, w.M, w.d), w.w_std, dev)
+    w3 = synth.normal_bf16(5, synth.TID_W3, (n_sel, w.M, w.d), w.w_std, dev)
+    w13 = moe.moe_pack_w13(w1, w3)
+    del w1, w3
+    w2 = synth.normal_bf16(5, synth.TID_W2, (n_sel, w.d, w.M), w.w_std, dev)
+    y_perm = torch.empty((max(moe.moe_max_rows(sf), 1), w.d), dtype=torch.bfloat16, device=dev)
+    xs = w13s = w2s = ys = None
+    if w.n_shared:
+        Ms = w.n_shared * w.M
+        xs = synth.normal_bf16(6, synth.TID_X, (T_sh, w.d), 1.0, dev)
+        w13s = moe.moe_pack_w13(synth.normal_bf16(5, synth.TID_WS1, (Ms, w.d), w.w_std, dev),
+                                synth.normal_bf16(5, synth.TID_WS3, (Ms, w.d), w.w_std, dev))
+        w2s = synth.normal_bf16(5, synth.TID_WS2, (w.d, Ms), w.w_std, dev)
+        ys = torch.empty((T_sh, w.d), dtype=torch.bfloat16, device=dev)
+    xp = torch.zeros((max(moe.moe_max_rows(sf), 1), w.d), dtype=torch.bfloat16, device=dev)
+    xp[:R] = x_perm[:R]
+    del x_perm
+    ws = moe.alloc_workspace(sf, dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def call():
+        moe.moe_grouped_ffn(sf, xp, offsets, w13, w2, y_perm, xs, w13s, w2s, ys, ws)
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize(dev)
+    moe.moe_profile_collect()
+    moe.moe_profile_enable(True)
+    for _ in range(args.steps):
+        flush.zero_()
+        call()
+    torch.cuda.synchronize(dev)
+    moe.moe_profile_enable(False)
+    if moe.moe_check_status(ws) != 0:
+        raise RuntimeError("device wait timed out")
+    per = {}
+    for name, t in moe.moe_profile_collect():
+        per.setdefault(name, []).append(t)
+    kern = {k2: sum(v) / args.steps for k2, v in per.items()}
+    peaks, _ = load_peaks()
+    ws2 = w.replace(T=T_sh if w.n_shared else w.T, E=n_sel)
+    flops, _ = algorithmic_work(ws2, R)
+    ffn_ms = kern.get("gemm_swiglu", 0.0) + kern.get("gemm_down", 0.0)
+    att = attainable_ffn_ms(ws2, rows, peaks)
+    print(json.dumps({"stage": "ffn", "workload": workload_desc(w), "experts": n_sel, "tune": tune,
+                      "rows": rows, "shared_rows": T_sh, "kernel_ms": kern,
+                      "gemm_swiglu_tflops": flops["gemm_swiglu"] / (kern["gemm_swiglu"] * 1e-3) / 1e12,
+                      "ffn_tflops": (flops["gemm_swiglu"] + flops["gemm_down"]) / (ffn_ms * 1e-3) / 1e12,
+                      "ffn_attainable_ms": att, "ffn_frac_of_attainable": att / ffn_ms,
+                      "weight_bytes": 2 * 3 * w.M * w.d * (n_sel + w.n_shared)}), flush=True)
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     import synth
@@ -915,6 +1016,8 @@ def main(argv=None):
         return run_reference(args, w)
     if args.stage == "router":
         return run_router_stage(args, w)
+    if args.stage == "ffn":
+        return run_ffn_stage(args, w)
     return run_ours(args, w)
 
 

@@ -48,5 +48,6 @@ def test_alf_bias_update_balances_load_over_steps():
             inp = synth.Inputs(w.replace(sel_bias="given"), x, wr, None, None, None,
                                offset=off, sel_bias=torch.from_numpy(before).to(dev))
             oracle_routing(inp, np_of(ids))
+    assert moe.moe_check_status(ws) == 0
     # coefficient of variation of the loads: ~1.8 at the start, a few tenths after
     assert cvs[0] > 1.0 and np.mean(cvs[-10:]) < 0.25 * cvs[0], cvs[::10]

@@ -94,6 +94,7 @@ def test_permute(T, E, k, c, d):
     ws = _ws(s)
     moe.moe_permute(s, x, ids, offsets, slot_row, row_token, drop, x_perm, ws)
     torch.cuda.synchronize()
+    assert moe.moe_check_status(ws) == 0
     C = oracle.capacity(float(np.float32(c)), k, T, E)
     ref = oracle.dispatch(ids_np, E, C)
     R = int(ref.offsets[-1])
