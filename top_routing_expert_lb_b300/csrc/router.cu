@@ -25,12 +25,14 @@
 // CTA that stores a tile's last slice sums the S partials in slice order,
 // writes the sums back into its TMEM buffer and runs the tile's epilogue.
 //
-// The epilogue reads the logits straight from TMEM: thread (row r, half h)
-// owns 32-column chunks h, h+2, ... of row r.  Three passes over the chunks:
-// row max, sum of exponentials, then the scores, the keys and a per-thread
-// Top-k list; the two halves exchange max, sum and lists through shared
-// memory.  Column sums over the tile's rows (P, importance) go through a
-// transposition buffer in a fixed order.  Every cross-tile total is either a
+// The epilogue reads the logits straight from TMEM.  Sixteen warps share a
+// tile: thread (row r, part c) owns the 16-column groups c, c+4, c+8, ... of
+// row r.  Two passes over the groups: an online max and sum of exponentials
+// (rescaled whenever a group raises the running max), then the scores, the
+// keys and a per-thread Top-k list; the four parts of a row combine max, sum
+// and lists through shared memory in part order.  Column sums over the
+// tile's rows (P, importance) are reduced inside each warp by a fixed shuffle
+// tree and then over the four row quarters in order.  Every cross-tile total is either a
 // 64-bit integer atomic on fixed-point values (P and importance at 2^-32,
 // entropy at 2^-32, counts exact) or a per-tile value summed in tile order
 // (lse^2), so all results are bitwise reproducible whichever CTA runs which
@@ -50,14 +52,13 @@ namespace {
 
 constexpr int kBK = 64;
 constexpr int kMaxStages = 8;
-constexpr int kEpiWarps = 8;
+constexpr int kEpiWarps = 16;
 constexpr int kEpiThreads = kEpiWarps * 32;
-constexpr int kThreads = 64 + kEpiThreads;  // TMA warp, MMA warp, 8 epilogue warps
+constexpr int kThreads = 64 + kEpiThreads;  // TMA warp, MMA warp, 16 epilogue warps
+constexpr int kParts = kEpiWarps / 4;       // threads per row (TMEM lane quarters x parts)
 constexpr int kMaxSplit = 8;
-constexpr int kTbPitch = 129;               // transposition buffer row pitch (floats)
 constexpr double kFix = 4294967296.0;       // 2^32: fixed-point scale of P, importance, entropy
-constexpr int kBarEpi = 1;                  // named barrier of the 8 epilogue warps
-constexpr int kBarHalf = 2;                 // + h: named barrier of epilogue half h
+constexpr int kBarEpi = 1;                  // named barrier of the epilogue warps
 
 struct RouterSmem {
   uint64_t full[kMaxStages];
@@ -70,24 +71,23 @@ struct RouterSmem {
   int flag;                 // broadcast of a last-arrival decision
   int go;                   // broadcast: the unit's accumulator is ready (0: stop)
   int hist[256];            // this tile's expert counts
-  float off[256];
-  float bias[256];
-  float xm[2][128];         // per-half row max
-  float xs[2][128];         // per-half sum of exponentials
-  float xh[2][128];         // per-half entropy partial (softmax: sum ex (l - m); sigmoid: sum s)
-  float xq[2][128];         // sigmoid: per-half sum s
-  float xg[2][128];         // sigmoid: per-half sum s log s
-  // half 1's Top-k list per row; after the merge (by the same row's half-0
-  // thread) the merged selection: ids in tk_id, gates in tk_p
-  float tk_key[kMaxTopK][128];
-  int tk_id[kMaxTopK][128];
-  float tk_p[kMaxTopK][128];
+  alignas(16) float off[256];
+  alignas(16) float bias[256];
+  float xm[kParts][128];    // per-part running row max
+  float xs[kParts][128];    // per-part sum of exponentials relative to it
+  float xh[kParts][128];    // per-part sum ex (l - m) (softmax entropy)
+  float xq[kParts][128];    // sigmoid: per-part sum s
+  float xg[kParts][128];    // sigmoid: per-part sum s log s
+  // the Top-k lists of parts 1..3 per row (score and id; the key is
+  // recomputed as score + bias); after the merge by the row's part-0 thread,
+  // list 0 holds the merged selection (ids, gates)
+  float tk_p[kParts - 1][kMaxTopK][128];
+  int tk_id[kParts - 1][kMaxTopK][128];
   float rowv[2][128];       // per-row lse^2 and entropy, for the tile sums
-  float red[2][4][16];      // column-sum partials: [half][row quarter][column]
-  double dred[kEpiWarps];   // finalize: per-warp sums
-  double dred2[kEpiWarps];
+  float colsum[4][256];     // [row quarter][expert]: column sums over 32 rows
+  float fred[kEpiWarps];    // finalize: per-warp sums
+  float fred2[kEpiWarps];
   int wtot[kEpiWarps];
-  float tb[2][16 * kTbPitch];  // transposition buffers (16 columns), one per half
 };
 
 struct RouterGeom {
@@ -203,27 +203,59 @@ __device__ int epi_exclusive_scan(RouterSmem* st, int eidx, int v, int* total) {
   return before_w + x - v;
 }
 
-// Sums of two doubles per epilogue thread in a fixed order (xor tree in each
+// Sums of two floats per epilogue thread in a fixed order (xor tree in each
 // warp, then the warps in order); every thread gets both.
-__device__ double2 epi_sum2(RouterSmem* st, int eidx, double a, double b) {
+__device__ float2 epi_sum2(RouterSmem* st, int eidx, float a, float b) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     a += __shfl_xor_sync(0xffffffffu, a, o);
     b += __shfl_xor_sync(0xffffffffu, b, o);
   }
   if ((eidx & 31) == 0) {
-    st->dred[eidx >> 5] = a;
-    st->dred2[eidx >> 5] = b;
+    st->fred[eidx >> 5] = a;
+    st->fred2[eidx >> 5] = b;
   }
   named_bar_sync(kBarEpi, kEpiThreads);
-  double ra = 0.0, rb = 0.0;
+  float ra = 0.0f, rb = 0.0f;
 #pragma unroll
   for (int w = 0; w < kEpiWarps; ++w) {
-    ra += st->dred[w];
-    rb += st->dred2[w];
+    ra += st->fred[w];
+    rb += st->fred2[w];
   }
   named_bar_sync(kBarEpi, kEpiThreads);
-  return make_double2(ra, rb);
+  return make_float2(ra, rb);
+}
+
+// Column sums of a warp's 32 rows: lane l holds 16 values (columns 0..15 of
+// its row); afterwards lanes 2c and 2c+1 hold the total of column c.  Four
+// halving exchanges (xor 16, 8, 4, 2) then a pair sum (xor 1), all in a fixed
+// order.
+__device__ __forceinline__ float warp_column_sums16(const float (&a)[16], int lane) {
+  float b8[8], b4[4], b2[2];
+  const bool u16 = (lane & 16) != 0, u8 = (lane & 8) != 0, u4 = (lane & 4) != 0,
+             u2 = (lane & 2) != 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float send = u16 ? a[i] : a[i + 8];
+    const float keep = u16 ? a[i + 8] : a[i];
+    b8[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float send = u8 ? b8[i] : b8[i + 4];
+    const float keep = u8 ? b8[i + 4] : b8[i];
+    b4[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const float send = u4 ? b4[i] : b4[i + 2];
+    const float keep = u4 ? b4[i + 2] : b4[i];
+    b2[i] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+  }
+  const float send = u2 ? b2[0] : b2[1];
+  const float keep = u2 ? b2[1] : b2[0];
+  const float c = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+  return c + __shfl_xor_sync(0xffffffffu, c, 1);
 }
 
 // The reductions across tiles, run by the epilogue warps of the CTA that
@@ -290,18 +322,17 @@ __device__ void finalize_all(const RouterArgs& p, RouterSmem* st, int eidx, int 
     if (in) p.all_offsets[e] = off;
     if (e == 0) p.all_offsets[E] = n_all;
   }
-  // ---- losses
-  const double imp = static_cast<double>(is) * (1.0 / kFix);
-  const double2 s1 = epi_sum2(st, eidx, fe * Pe, static_cast<double>(zf));
+  // ---- losses (fixed-order float sums)
+  const float imp = static_cast<float>(static_cast<double>(is) * (1.0 / kFix));
+  const float2 s1 = epi_sum2(st, eidx, static_cast<float>(fe * Pe), zf);
   if (want_imp) {
-    if (in && p.importance) p.importance[e] = static_cast<float>(imp);
-    const double mean = epi_sum2(st, eidx, imp, 0.0).x / E;
-    const double var = epi_sum2(st, eidx, in ? (imp - mean) * (imp - mean) : 0.0, 0.0).x / E;
-    if (e == 0 && p.importance_cv2)
-      *p.importance_cv2 = static_cast<float>(mean != 0.0 ? var / (mean * mean) : 0.0);
+    if (in && p.importance) p.importance[e] = imp;
+    const float mean = epi_sum2(st, eidx, imp, 0.0f).x / E;
+    const float var = epi_sum2(st, eidx, in ? (imp - mean) * (imp - mean) : 0.0f, 0.0f).x / E;
+    if (e == 0 && p.importance_cv2) *p.importance_cv2 = mean != 0.0f ? var / (mean * mean) : 0.0f;
   }
   if (e == 0) {
-    if (p.bal_loss) *p.bal_loss = static_cast<float>(static_cast<double>(p.balance_coef) * E * s1.x);
+    if (p.bal_loss) *p.bal_loss = p.balance_coef * static_cast<float>(E) * s1.x;
     if (p.z_loss) *p.z_loss = (p.T > 0) ? static_cast<float>(s1.y * inv_T) : 0.0f;
     if (p.entropy_mean)
       *p.entropy_mean =
@@ -442,33 +473,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ---------------------------------------------------------------- epilogue
-    const int eidx = static_cast<int>(threadIdx.x) - 64;  // 0..255
-    const int h = eidx >> 7;                             // column half
+    const int eidx = static_cast<int>(threadIdx.x) - 64;  // 0..511
+    const int c = eidx >> 7;                             // column part
     const int quarter = warp & 3;                        // TMEM lanes 32*quarter .. +31
     const int r = quarter * 32 + lane;                   // this thread's tile row
-    const int ng = (E + 15) / 16;  // 16-column groups; half h owns groups h, h+2, ...
+    const int ng = (E + 15) / 16;  // 16-column groups; part c owns groups c, c+4, ...
+    const int nparts = ng < kParts ? ng : kParts;  // parts that own a group
     const bool sigmoid = (p.flags & kRouteSigmoid) != 0;
     const bool renorm = (p.flags & kRouteNoRenorm) == 0;
     const bool want_imp = p.acc_imp != nullptr && K > 0;
     const bool want_ent = p.acc_ent != nullptr;
-    float* tb = st->tb[h];
-    // Column sums of the 16 values per row this half staged in tb: the warp of
-    // each row quarter sums its 32 rows (lane = column), then the quarters in
-    // order; the total of column j goes to acc[g*16 + j] (fixed point).
-    auto column_sums = [&](int g, unsigned long long* acc) {
-      named_bar_sync(kBarHalf + h, 128);
-      if (lane < 16) {
-        float x = 0.0f;
-#pragma unroll 8
-        for (int i = 0; i < 32; ++i) x += tb[lane * kTbPitch + quarter * 32 + i];
-        st->red[h][quarter][lane] = x;
-      }
-      named_bar_sync(kBarHalf + h, 128);
-      if (quarter == 0 && lane < 16 && g * 16 + lane < E) {
+    // hands the TMEM buffer back to the MMA warp (one arrival per warp)
+    auto release = [&](int b) {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&st->tempty[b]);
+    };
+    // totals of colsum[0..3][e] in quarter order, added to acc[e] (fixed point)
+    auto add_column_totals = [&](unsigned long long* acc, int e) {
+      if (e < E) {
         const float tot =
-            ((st->red[h][0][lane] + st->red[h][1][lane]) + st->red[h][2][lane]) + st->red[h][3][lane];
-        add_fixed(acc + g * 16 + lane, static_cast<double>(tot));
+            ((st->colsum[0][e] + st->colsum[1][e]) + st->colsum[2][e]) + st->colsum[3][e];
+        add_fixed(acc + e, static_cast<double>(tot));
       }
+    };
+    // this warp's 32-row column sums of group g (lanes 2j, 2j+1 hold column j)
+    auto stage_columns = [&](int g, const float (&a)[16]) {
+      const float s = warp_column_sums16(a, lane);
+      const int e = g * 16 + (lane >> 1);
+      if ((lane & 1) == 0 && e < E) st->colsum[quarter][e] = s;
     };
     int local = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x, ++local) {
@@ -490,7 +523,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // partial logits of slice s, [slice][tile][expert][row] (coalesced per expert)
         float* part = p.part_logits + ((static_cast<size_t>(s) * ntiles + t) * E) * 128 + r;
 #pragma unroll 1
-        for (int g = h; g < ng; g += 2) {
+        for (int g = c; g < ng; g += kParts) {
           float v[16];
           tmem_ld16(taddr + g * 16, v);
           tmem_ld_wait();
@@ -512,7 +545,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float* part0 = p.part_logits + (static_cast<size_t>(t) * E) * 128 + r;
           const size_t slice = static_cast<size_t>(ntiles) * E * 128;
 #pragma unroll 1
-          for (int g = h; g < ng; g += 2) {
+          for (int g = c; g < ng; g += kParts) {
             const float* src = part0 + static_cast<size_t>(g * 16) * 128;
             float v[16];
 #pragma unroll
@@ -532,54 +565,67 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st16(taddr + g * 16, v);
           }
           tmem_st_wait();
+        } else {
+          release(b);
         }
       }
       if (run_tile) {
         // ------------------------------------------------ the tile's epilogue
         const int tok = t * 128 + r;
         const bool valid = tok < p.T;
-        // pass 1: row max (four independent maxima)
-        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        // pass 1: running max m and, relative to it, the sum of exponentials
+        // and sum ex (l - m); a group that raises m rescales both first
+        float m = -INFINITY, sx = 0.0f, hs = 0.0f;
 #pragma unroll 1
-        for (int g = h; g < ng; g += 2) {
+        for (int g = c; g < ng; g += kParts) {
           float v[16];
           tmem_ld16(taddr + g * 16, v);
           tmem_ld_wait();
+          float gm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-          for (int j = 0; j < 16; ++j)
-            if (g * 16 + j < E) mx[j & 3] = fmaxf(mx[j & 3], v[j] + st->off[g * 16 + j]);
-        }
-        float m = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-        st->xm[h][r] = m;
-        named_bar_sync(kBarEpi, kEpiThreads);
-        m = fmaxf(st->xm[0][r], st->xm[1][r]);
-        // pass 2: sum of exponentials (and sum ex (l - m) for the entropy)
-        // (four independent partial sums per thread, combined in a fixed order)
-        float sp[4] = {0.0f, 0.0f, 0.0f, 0.0f}, hp[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll 1
-        for (int g = h; g < ng; g += 2) {
-          float v[16];
-          tmem_ld16(taddr + g * 16, v);
-          tmem_ld_wait();
+          for (int j = 0; j < 16; ++j) {
+            v[j] += st->off[g * 16 + j];
+            if (g * 16 + j < E) gm[j & 3] = fmaxf(gm[j & 3], v[j]);
+          }
+          const float mg = fmaxf(fmaxf(gm[0], gm[1]), fmaxf(gm[2], gm[3]));
+          if (mg > m) {
+            if (m != -INFINITY) {
+              const float a = __expf(m - mg);
+              hs = a * fmaf(m - mg, sx, hs);
+              sx *= a;
+            }
+            m = mg;
+          }
+          float sp[4] = {0.0f, 0.0f, 0.0f, 0.0f}, hp[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
           for (int j = 0; j < 16; ++j)
             if (g * 16 + j < E) {
-              const float l = v[j] + st->off[g * 16 + j] - m;
+              const float l = v[j] - m;
               const float ex = __expf(l);
               sp[j & 3] += ex;
               hp[j & 3] = fmaf(ex, l, hp[j & 3]);
             }
+          sx += (sp[0] + sp[1]) + (sp[2] + sp[3]);
+          hs += (hp[0] + hp[1]) + (hp[2] + hp[3]);
         }
-        float sx = (sp[0] + sp[1]) + (sp[2] + sp[3]);
-        float hs = (hp[0] + hp[1]) + (hp[2] + hp[3]);
-        st->xs[h][r] = sx;
-        st->xh[h][r] = hs;
+        st->xm[c][r] = m;
+        st->xs[c][r] = sx;
+        st->xh[c][r] = hs;
         named_bar_sync(kBarEpi, kEpiThreads);
-        sx = st->xs[0][r] + st->xs[1][r];
-        hs = st->xh[0][r] + st->xh[1][r];
+        // the parts in order: row max, then the sums moved to it
+        m = st->xm[0][r];
+        for (int i = 1; i < nparts; ++i) m = fmaxf(m, st->xm[i][r]);
+        sx = 0.0f;
+        hs = 0.0f;
+        for (int i = 0; i < nparts; ++i) {
+          const float mi = st->xm[i][r], si = st->xs[i][r];
+          const float a = __expf(mi - m);
+          sx = fmaf(a, si, sx);
+          hs = fmaf(a, fmaf(mi - m, si, st->xh[i][r]), hs);
+        }
         const float inv_s = 1.0f / sx;
         const float lse = m + logf(sx);
-        // pass 3: scores, keys, this thread's Top-k list, column sums of P
+        // pass 2: scores, keys, this thread's Top-k list, column sums of P
         float top_key[K > 0 ? K : 1];
         int top_id[K > 0 ? K : 1];
         float top_p[K > 0 ? K : 1];
@@ -592,84 +638,89 @@ __global__ void __launch_bounds__(kThreads, 1)
         float thresh = -INFINITY;
         float ssum = 0.0f, slog = 0.0f;  // sigmoid: sum s, sum s log s
 #pragma unroll 1
-        for (int g = h; g < ng; g += 2) {
+        for (int g = c; g < ng; g += kParts) {
           float v[16];
           tmem_ld16(taddr + g * 16, v);
           tmem_ld_wait();
-          // scores into the transposition buffer (0 for rows past T) and a
-          // mask of the experts whose key beats the list's current last entry
-          uint32_t cand = 0u;
-          if (sigmoid) {
+          float pe[16];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const int e = g * 16 + j;
-              float pe = 0.0f;
-              if (e < E) {
-                const float en = __expf(-(v[j] + st->off[e]));
-                pe = 1.0f / (1.0f + en);
-                ssum += pe;
-                if (pe > 0.0f) slog -= pe * log1pf(en);  // s log s = -s log(1 + e^-l)
-                if (pe + st->bias[e] > thresh) cand |= 1u << j;
+          for (int j = 0; j < 16; ++j) {
+            const int e = g * 16 + j;
+            pe[j] = 0.0f;
+            if (e < E) {
+              const float l = v[j] + st->off[e];
+              if (sigmoid) {
+                const float en = __expf(-l);
+                pe[j] = 1.0f / (1.0f + en);
+                ssum += pe[j];
+                if (pe[j] > 0.0f) slog -= pe[j] * log1pf(en);  // s log s = -s log(1 + e^-l)
+              } else {
+                pe[j] = __expf(l - m) * inv_s;
               }
-              tb[j * kTbPitch + r] = valid ? pe : 0.0f;
-            }
-          } else {
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const int e = g * 16 + j;
-              float pe = 0.0f;
-              if (e < E) {
-                pe = __expf(v[j] + st->off[e] - m) * inv_s;
-                if (pe + st->bias[e] > thresh) cand |= 1u << j;
-              }
-              tb[j * kTbPitch + r] = valid ? pe : 0.0f;
             }
           }
           // candidates in ascending expert order (equal keys keep the lower
           // index first); the threshold rises as entries go in
           if (K > 0) {
-            while (cand != 0u) {
-              const int j = __ffs(cand) - 1;
-              cand &= cand - 1u;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
               const int e = g * 16 + j;
-              const float pe = tb[j * kTbPitch + r];
-              const float key = pe + st->bias[e];
-              if (key > thresh) {
-                topk_push_ascending<K>(top_key, top_id, top_p, key, e, pe);
+              const float key = pe[j] + st->bias[e];
+              if (e < E && key > thresh) {
+                topk_push_ascending<K>(top_key, top_id, top_p, key, e, pe[j]);
                 thresh = top_key[K > 0 ? K - 1 : 0];
               }
             }
           }
           if (p.scores_t != nullptr && valid) {
-#pragma unroll 1
-            for (int j = 0; j < 16 && g * 16 + j < E; ++j)
-              p.scores_t[static_cast<size_t>(g * 16 + j) * p.T + tok] = tb[j * kTbPitch + r];
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              if (g * 16 + j < E) p.scores_t[static_cast<size_t>(g * 16 + j) * p.T + tok] = pe[j];
           }
-          column_sums(g, p.acc_psum);
+          if (!valid) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) pe[j] = 0.0f;
+          }
+          stage_columns(g, pe);
         }
-        // merge the two halves' Top-k lists (half 0 keeps the result)
-        if (h == 1) {
+        // the logits are no longer needed: the next unit may use the buffer
+        release(b);
+        if (c > 0 && c < nparts) {
 #pragma unroll
           for (int j = 0; j < K; ++j) {
-            st->tk_key[j][r] = top_key[j];
-            st->tk_id[j][r] = top_id[j];
-            st->tk_p[j][r] = top_p[j];
+            st->tk_p[c - 1][j][r] = top_p[j];
+            st->tk_id[c - 1][j][r] = top_id[j];
           }
         }
-        st->xq[h][r] = ssum;
-        st->xg[h][r] = slog;
+        st->xq[c][r] = ssum;
+        st->xg[c][r] = slog;
         named_bar_sync(kBarEpi, kEpiThreads);
-        if (h == 0) {
+        if (c >= 2) {
+          add_column_totals(p.acc_psum, eidx - 256);  // parts 2, 3: expert eidx - 256
+        } else if (c == 0) {
+          // merge the other parts' lists (each descending: stop at the first
+          // entry that does not make it)
 #pragma unroll 1
-          for (int i = 0; i < K; ++i)
-            topk_insert<K>(top_key, top_id, top_p, st->tk_key[i][r], st->tk_id[i][r],
-                           st->tk_p[i][r]);
+          for (int i = 1; i < nparts; ++i) {
+#pragma unroll 1
+            for (int j = 0; j < K; ++j) {
+              const int id = st->tk_id[i - 1][j][r];
+              if (id >= E) break;
+              const float pv = st->tk_p[i - 1][j][r];
+              const float key = pv + st->bias[id];
+              if (!before(key, id, top_key[K > 0 ? K - 1 : 0], top_id[K > 0 ? K - 1 : 0])) break;
+              topk_insert<K>(top_key, top_id, top_p, key, id, pv);
+            }
+          }
           // entropy of the router distribution: softmax log s - sum ex (l-m) / s;
           // sigmoid q = s / sum s: log sum s - sum s log s / sum s
           float ent = 0.0f;
           if (sigmoid) {
-            const float ss = st->xq[0][r] + st->xq[1][r];
-            const float sl = st->xg[0][r] + st->xg[1][r];
+            float ss = 0.0f, sl = 0.0f;
+            for (int i = 0; i < nparts; ++i) {
+              ss += st->xq[i][r];
+              sl += st->xg[i][r];
+            }
             ent = logf(ss) - sl / ss;
           } else {
             ent = logf(sx) - hs * inv_s;
@@ -684,8 +735,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int j = 0; j < K; ++j) {
               const float gj = top_p[j] * inv_d;
-              st->tk_id[j][r] = valid ? top_id[j] : -1;  // the merged selection
-              st->tk_p[j][r] = gj;
+              st->tk_id[0][j][r] = valid ? top_id[j] : -1;  // the merged selection
+              st->tk_p[0][j][r] = gj;
               if (valid) {
                 p.ids[static_cast<int64_t>(tok) * K + j] = top_id[j];
                 p.gates[static_cast<int64_t>(tok) * K + j] = gj;
@@ -707,7 +758,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             atomicAdd(p.chunk_acc + (t / p.chunk_tiles) * E + e, hcount);
           st->hist[e] = 0;
         }
-        if (warp == 2 + 4) {  // one warp (eidx 128..159): the two row sums in a fixed order
+        if (warp == 2 + 8) {  // one warp (eidx 256..287): the two row sums in a fixed order
           float z = 0.0f, hsum = 0.0f;
 #pragma unroll
           for (int x = 0; x < 4; ++x) {
@@ -728,17 +779,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           // importance: each row's sparse gate vector (gates on the selected
           // experts, 0 elsewhere), column sums as for P
 #pragma unroll 1
-          for (int g = h; g < ng; g += 2) {
+          for (int g = c; g < ng; g += kParts) {
+            float gv[16];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) tb[j * kTbPitch + r] = 0.0f;
+            for (int j = 0; j < 16; ++j) gv[j] = 0.0f;
 #pragma unroll
             for (int j = 0; j < K; ++j) {
-              const int id = st->tk_id[j][r];
-              if (id >= g * 16 && id < g * 16 + 16 && id < E)
-                tb[(id - g * 16) * kTbPitch + r] = st->tk_p[j][r];
+              const int id = st->tk_id[0][j][r];
+              const float gate = st->tk_p[0][j][r];
+#pragma unroll
+              for (int i = 0; i < 16; ++i)
+                if (id == g * 16 + i) gv[i] = gate;
             }
-            column_sums(g, p.acc_imp);
+            stage_columns(g, gv);
           }
+          named_bar_sync(kBarEpi, kEpiThreads);
+          if (c >= 2) add_column_totals(p.acc_imp, eidx - 256);
         }
         // this tile is done: the CTA that completes the last tile reduces
         named_bar_sync(kBarEpi, kEpiThreads);
@@ -746,10 +802,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         named_bar_sync(kBarEpi, kEpiThreads);
         if (st->flag) finalize_all(p, st, eidx, ntiles);
       }
-      // release the TMEM buffer to the MMA warp
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&st->tempty[b]);
     }
     if (ntiles == 0 && blockIdx.x == 0) finalize_all(p, st, eidx, 0);
   }
