@@ -57,7 +57,7 @@ constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr int kThreads = 64 + kEpiThreads;  // TMA warp, MMA warp, 16 epilogue warps
 constexpr int kParts = kEpiWarps / 4;       // threads per row (TMEM lane quarters x parts)
 constexpr int kMaxSplit = 8;
-constexpr double kFix = 4294967296.0;       // 2^32: fixed-point scale of P, importance, entropy
+constexpr float kFix = 4294967296.0f;       // 2^32: fixed-point scale of P, importance, entropy
 constexpr int kBarEpi = 1;                  // named barrier of the epilogue warps
 
 struct RouterSmem {
@@ -175,8 +175,12 @@ __device__ __forceinline__ int atom_add_acq_rel(int* ptr, int v) {
   return old;
 }
 
-__device__ __forceinline__ void add_fixed(unsigned long long* acc, double v) {
-  atomicAdd(acc, static_cast<unsigned long long>(__double2ll_rn(v * kFix)));
+// v * 2^32 is exact in float (a power-of-two scale), so the integer added is
+// v's value to 2^-32 with nothing rounded but v itself.  The router does no
+// FP64 arithmetic: this part's FP64 units are few, and a few dozen FP64
+// operations per thread cost microseconds.
+__device__ __forceinline__ void add_fixed(unsigned long long* acc, float v) {
+  atomicAdd(acc, static_cast<unsigned long long>(__float2ll_rn(v * kFix)));
 }
 
 
@@ -279,16 +283,16 @@ __device__ void finalize_all(const RouterArgs& p, RouterSmem* st, int eidx, int 
 #pragma unroll
   for (int i = 0; i < 8; ++i) cv[i] = (chunks && i < p.n_chunks) ? __ldcg(p.chunk_acc + i * E + e) : 0;
   // ---- per-expert outputs
-  const double n_pairs = p.n_pairs >= 0.0 ? p.n_pairs
-                                          : static_cast<double>(p.k) * static_cast<double>(p.T);
-  const double inv_pairs = n_pairs > 0.0 ? 1.0 / n_pairs : 0.0;
-  const double inv_T = p.T > 0 ? 1.0 / p.T : 0.0;
-  const double fe = (in && p.T > 0) ? static_cast<double>(n) * inv_pairs : 0.0;
-  const double Pe = (in && p.T > 0) ? static_cast<double>(ps) * (1.0 / kFix) * inv_T : 0.0;
+  // pair and token counts stay below 2^24, exact in float
+  const float n_pairs = p.n_pairs >= 0.0 ? static_cast<float>(p.n_pairs)
+                                         : static_cast<float>(p.k) * static_cast<float>(p.T);
+  const float inv_T = p.T > 0 ? 1.0f / static_cast<float>(p.T) : 0.0f;
+  const float fe = (in && p.T > 0 && n_pairs > 0.0f) ? static_cast<float>(n) / n_pairs : 0.0f;
+  const float Pe = (in && p.T > 0) ? static_cast<float>(ps) * (1.0f / kFix) * inv_T : 0.0f;
   if (in) {
     if (p.counts) p.counts[e] = n;
-    if (p.f) p.f[e] = static_cast<float>(fe);
-    if (p.P) p.P[e] = static_cast<float>(Pe);
+    if (p.f) p.f[e] = fe;
+    if (p.P) p.P[e] = Pe;
   }
   // ---- per-chunk bases of the permutation: exclusive scan over chunks
   if (chunks) {
@@ -323,8 +327,8 @@ __device__ void finalize_all(const RouterArgs& p, RouterSmem* st, int eidx, int 
     if (e == 0) p.all_offsets[E] = n_all;
   }
   // ---- losses (fixed-order float sums)
-  const float imp = static_cast<float>(static_cast<double>(is) * (1.0 / kFix));
-  const float2 s1 = epi_sum2(st, eidx, static_cast<float>(fe * Pe), zf);
+  const float imp = static_cast<float>(is) * (1.0f / kFix);
+  const float2 s1 = epi_sum2(st, eidx, fe * Pe, zf);
   if (want_imp) {
     if (in && p.importance) p.importance[e] = imp;
     const float mean = epi_sum2(st, eidx, imp, 0.0f).x / E;
@@ -336,7 +340,7 @@ __device__ void finalize_all(const RouterArgs& p, RouterSmem* st, int eidx, int 
     if (p.z_loss) *p.z_loss = (p.T > 0) ? static_cast<float>(s1.y * inv_T) : 0.0f;
     if (p.entropy_mean)
       *p.entropy_mean =
-          (p.T > 0) ? static_cast<float>(static_cast<double>(es) * (1.0 / kFix) * inv_T) : 0.0f;
+          (p.T > 0) ? static_cast<float>(es) * (1.0f / kFix) * inv_T : 0.0f;
   }
   // ---- every accumulator back to zero (all of them were read above)
   if (in) {
@@ -494,7 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (e < E) {
         const float tot =
             ((st->colsum[0][e] + st->colsum[1][e]) + st->colsum[2][e]) + st->colsum[3][e];
-        add_fixed(acc + e, static_cast<double>(tot));
+        add_fixed(acc + e, tot);
       }
     };
     // this warp's 32-row column sums of group g (lanes 2j, 2j+1 hold column j)
@@ -772,7 +776,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (lane == 0) {
             p.tile_lse2[t] = z;
-            if (want_ent) add_fixed(p.acc_ent, static_cast<double>(hsum));
+            if (want_ent) add_fixed(p.acc_ent, hsum);
           }
         }
         if (want_imp) {
