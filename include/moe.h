@@ -100,11 +100,9 @@ extern "C" {
  * of the layer's definition.  Every field at zero selects the measured-
  * fastest default; every choice gives parity-tested results (most of them
  * bit-identical to the default).  Invalid values -> MOE_ERR_INVALID_ARG.
- *   gemm1_tile      gate/up projection tiles.  0: CTA-pair 256 x 256 tiles
- *                   when E <= 16, experts average >= 512 rows and rows are not
- *                   gathered, else single-CTA 128 x 256 tiles; 128: single-CTA
- *                   tiles; 256: CTA-pair tiles (then the down projection too,
- *                   unless gemm2_tile is 128)
+ *   gemm1_tile      gate/up projection tiles.  0 or 128: single-CTA 128 x 256
+ *                   tiles; 256: CTA-pair 256 x 256 tiles (then the down
+ *                   projection too, unless gemm2_tile is 128)
  *   gemm2_tile      down projection tiles.  0: CTA pairs when d % 256 == 0 and
  *                   experts average >= 512 rows (or gemm1_tile is 256), else
  *                   single-CTA 128 x BN (BN = 256, 128 or 64 by d); 128:
@@ -117,8 +115,10 @@ extern "C" {
  *                   this.  0: 112; < 0: never; 16..112 in steps of 16
  *   n_block         tile order inside a group with more than block_min_rows
  *                   rows: blocks of n_block n-tiles, m-tile major inside a
- *                   block.  0: 8; 1: n-tile major, m-tile minor throughout
- *   block_min_rows  0: 2048
+ *                   block.  0: 8, or 4 for a single-CTA gate/up projection
+ *                   of at least 64 n-tiles (2M >= 16384); 1: n-tile major,
+ *                   m-tile minor throughout
+ *   block_min_rows  0: 2048, or 512 for such a gate/up projection
  *   options         MOE_TUNE_* bits:
  *     MOE_TUNE_NO_HALF_TILES    CTA-pair launches pad a group's last tile of at
  *                               most 128 rows to a 256-row tile instead of one

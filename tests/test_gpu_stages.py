@@ -63,6 +63,49 @@ def test_route(w):
     rel_close(lz.item(), ref.loss.L_z, LOSS_REL, "z-loss")
 
 
+@pytest.mark.parametrize("d", [256, 4096])
+def test_route_exact_expert_ties_break_to_lower_index(d):
+    """Pairs of experts with identical router rows and offsets tie exactly in
+    every token; the lower index must be chosen first (listed before the
+    higher one with the same gate, and never left out while the higher one is
+    in).  The pairs sit in the same and in different 16-column groups, so the
+    tie is decided inside one thread's list and in the merge of the four
+    per-row lists; d = 4096 splits each tile's K across CTAs."""
+    w = W("r_ties", T=1000, d=d, E=80, k=6, M=128, offsets="normal")
+    inp = synth.make_inputs(w, "cuda", experts=False)
+    pairs = [(3, 20), (17, 50), (5, 37), (2, 10), (64, 79)]
+    wr = inp.wr.clone()
+    off = inp.offset.clone()
+    for lo, hi in pairs:
+        wr[hi] = wr[lo]
+        off[lo] = off[hi] = 2.5   # popular, so both members are often selected
+    inp.wr, inp.offset = wr, off
+    s = shape_of(w)
+    dev = "cuda"
+    ids = guarded((w.T, w.k), torch.int32, dev, label="ids")
+    gates = guarded((w.T, w.k), torch.float32, dev, label="gates")
+    counts = guarded(w.E, torch.int32, dev, label="counts")
+    f, P = torch.empty(w.E, device=dev), torch.empty(w.E, device=dev)
+    lb, lz = torch.empty(1, device=dev), torch.empty(1, device=dev)
+    ws = _ws(s)
+    moe.moe_route(s, inp.x, inp.wr, inp.offset, inp.sel_bias, ids, gates, counts, f, P, lb, lz,
+                  ws)
+    torch.cuda.synchronize()
+    assert moe.moe_check_status(ws) == 0
+    g_ids, g_gates = np_of(ids), np_of(gates)
+    for lo, hi in pairs:
+        has_lo, has_hi = (g_ids == lo).any(1), (g_ids == hi).any(1)
+        assert has_hi.sum() > 0 and (has_lo & ~has_hi).sum() > 0, "the tie is not exercised"
+        assert not (has_hi & ~has_lo).any(), f"expert {hi} chosen without its tie partner {lo}"
+        for t in np.nonzero(has_hi)[0]:
+            jl, jh = int(np.nonzero(g_ids[t] == lo)[0][0]), int(np.nonzero(g_ids[t] == hi)[0][0])
+            assert jl < jh, f"token {t}: {hi} listed before its tie partner {lo}"
+            assert g_gates[t, jl] == g_gates[t, jh]
+    ref = oracle_routing(inp, g_ids)
+    np.testing.assert_array_equal(g_ids, ref.routing.ids)
+    np.testing.assert_array_equal(np_of(counts), ref.disp.counts)
+
+
 # --------------------------------------------------------------------------- permute
 def _synthetic_ids(T, E, k, seed, hot_frac=0.4):
     rng = np.random.default_rng(seed)
@@ -115,7 +158,8 @@ def _tuning_for(tile: str) -> dict:
     n-tiles, m-tile major inside a block (otherwise n-tile major throughout);
     CTA pairs take their tiles from the workspace counter except with
     256-static; a group's last pair tile of at most 128 rows runs as an M = 128
-    pair MMA except with 256-nohalf."""
+    pair MMA except with 256-nohalf.  With 256* and d % 256 == 0 the down
+    projection runs on CTA pairs too."""
     opts = 0
     if tile.endswith("nohalf"):
         opts |= moe.MOE_TUNE_NO_HALF_TILES
@@ -146,7 +190,10 @@ def test_grouped_ffn(rows, d, M, n_shared, T, tile):
     Tshape = T if n_shared else max(R, 1)
     k = max(1, -(-R // Tshape))
     assert k <= min(E, 8)
-    s_ffn = moe.Shape.of(Tshape, d, M, E, k, n_shared, **_tuning_for(tile))
+    tune = _tuning_for(tile)
+    if tile.startswith("256") and d % 256 == 0:
+        tune["gemm2_tile"] = 256   # the down projection on CTA pairs as well
+    s_ffn = moe.Shape.of(Tshape, d, M, E, k, n_shared, **tune)
     dev = "cuda"
     R_max = moe.moe_max_rows(s_ffn)
     assert R <= R_max

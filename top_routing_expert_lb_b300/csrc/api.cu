@@ -475,19 +475,17 @@ int do_ffn(const moe_shape_t* s, const uint16_t* x_perm, const int32_t* offsets,
   const int nsm = sm_count_cached();
   const int64_t rows_per_expert =
       L.r >= 0 ? L.r : (E > 0 ? (static_cast<int64_t>(T) * s->k) / E : 0);
-  // The gate/up projection runs on 256 x 256 CTA-pair tiles for a few large
-  // experts (at most 16, averaging at least 512 rows): the pair halves the
-  // weight bytes each SM stages per FLOP, and with the dynamic tile order its
-  // DRAM traffic is the algorithmic one; it measured 1.7 % faster steps than
-  // single-CTA tiles on Mixtral although each expert's last tile is padded to
-  // 256 rows.  With many experts of skewed sizes (DeepSeekMoE-16B) that
-  // padding cost 13 % in this projection, so single-CTA tiles (transposed
-  // tails) stay the default there.  Gathered rows need the single-CTA kernel.
+  // The gate/up projection runs on single-CTA 128 x 256 tiles (transposed
+  // tails) unless gemm1_tile asks for 256 x 256 CTA-pair tiles.  Timed against
+  // each other call by call in one process (200 alternating layer calls, L2
+  // flushed before each), single-CTA tiles made the Mixtral layer 4.3 %
+  // faster (2.51 against 2.63 ms median), early and late in the power-capped
+  // run alike, and the pair tiles cost DeepSeekMoE-16B 11 % (the 256-row
+  // padding of its many small experts).  Gathered rows need the single-CTA
+  // kernel.
   const moe_tuning_t& tune = s->tuning;
   if (tune.gemm1_tile == 256 && gather_rows != nullptr) return MOE_ERR_INVALID_ARG;  // needs x_perm
-  const bool paired =
-      gather_rows == nullptr &&
-      (tune.gemm1_tile == 256 || (tune.gemm1_tile == 0 && rows_per_expert >= 512 && E <= 16));
+  const bool paired = gather_rows == nullptr && tune.gemm1_tile == 256;
   const uint32_t bbox = paired ? 128u : 256u;
   // MOE_TUNE_GEMM1_SPLIT: the first projection runs each group's whole 256-row
   // blocks on CTA-pair tiles and only the remaining rows (< 256 per group) on
@@ -548,8 +546,19 @@ int do_ffn(const moe_shape_t* s, const uint16_t* x_perm, const int32_t* offsets,
   g1.out_rows_shared = T;
   g1.gather_limit = T;
   if (tune.tail_max_n != 0) g1.tail_max_n = tune.tail_max_n < 0 ? 0 : tune.tail_max_n;
-  if (tune.n_block != 0) g1.n_block = tune.n_block;
-  if (tune.block_min_rows != 0) g1.block_min_rows = tune.block_min_rows;
+  // A wide single-CTA gate/up projection (at least 64 n-tiles, 2M >= 16384)
+  // takes every group of more than 512 rows in blocks of 4 n-tiles: 5.4 %
+  // faster on the Mixtral shape (1577 against 1667 us, 80 alternating layer
+  // calls), while the narrow projections of DeepSeek-V2 keep blocks of 8 for
+  // groups of more than 2048 rows (blocks of 4 there: +1 %).
+  const bool wide1 = !paired && 2 * M / 256 >= 64;
+  const int32_t n_block1 = tune.n_block != 0 ? tune.n_block : (wide1 ? 4 : g1.n_block);
+  const int32_t min_rows1 =
+      tune.block_min_rows != 0 ? tune.block_min_rows : (wide1 ? 512 : g1.block_min_rows);
+  const int32_t n_block2 = tune.n_block != 0 ? tune.n_block : g1.n_block;
+  const int32_t min_rows2 = tune.block_min_rows != 0 ? tune.block_min_rows : g1.block_min_rows;
+  g1.n_block = n_block1;
+  g1.block_min_rows = min_rows1;
   // CTA-pair launches with long tiles (K >= 4096) take their tiles from a
   // counter in the workspace: the dynamic order keeps the pairs that share a
   // weight tile in step (Mixtral: DRAM bytes of the gate/up projection down
@@ -602,6 +611,8 @@ int do_ffn(const moe_shape_t* s, const uint16_t* x_perm, const int32_t* offsets,
   if (!routed) { a0 = a1; b0 = b1; }
   if (!shared) { a1 = a0; b1 = b0; }
   GroupedGemmArgs g2 = g1;
+  g2.n_block = n_block2;
+  g2.block_min_rows = min_rows2;
   g2.tile_counter = dynamic_for(M);
   g2.gather_rows = nullptr;
   g2.row_scale = routed ? row_scale : nullptr;
