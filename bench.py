@@ -56,16 +56,24 @@ def parse_args(argv=None):
                     help="skip the other workloads' lines (per_config)")
     ap.add_argument("--no-graph", action="store_true",
                     help="launch every timed step directly instead of replaying CUDA graphs")
-    ap.add_argument("--stage", choices=["layer", "router", "ffn"], default="layer",
+    ap.add_argument("--stage", choices=["layer", "router", "ffn", "ab"], default="layer",
                     help="router: time moe_route alone (no expert weights are drawn); "
                          "ffn: time moe_grouped_ffn on a slice of the workload's realised "
-                         "expert loads (--experts of them); for profiling, not the headline")
+                         "expert loads (--experts of them); ab: two layers that differ only "
+                         "in moe_tuning_t (--tune for A, --tune-b for B) called alternately "
+                         "--steps times each; for profiling, not the headline")
     ap.add_argument("--experts", type=int, default=0,
                     help="--stage ffn: experts in the slice (0: all)")
     ap.add_argument("--tune", action="append", default=[],
-                    help="moe_tuning_t field=value for --stage ffn (repeatable), "
-                         "e.g. --tune interleave_rows=256")
+                    help="moe_tuning_t field=value for --stage ffn / ab (repeatable), "
+                         "e.g. --tune gemm1_tile=256")
+    ap.add_argument("--tune-b", action="append", default=[],
+                    help="--stage ab: moe_tuning_t field=value of layer B (repeatable)")
     return ap.parse_args(argv)
+
+
+def parse_tune(items):
+    return {kv.split("=")[0]: int(kv.split("=")[1]) for kv in items}
 
 
 def recorded_traffic(workload: str, kernel: str):
@@ -942,7 +950,7 @@ def run_ffn_stage(args, w):
     T_sh = max(1, round(w.T * n_sel / w.E), -(-R // min(8, n_sel))) if w.n_shared else 0
     Tshape = T_sh if w.n_shared else max(R, 1)
     k = max(1, -(-R // Tshape))
-    tune = {kv.split("=")[0]: int(kv.split("=")[1]) for kv in args.tune}
+    tune = parse_tune(args.tune)
     sf = moe.Shape.of(Tshape, w.d, w.M, n_sel, min(k, n_sel), w.n_shared, **tune)
     assert R <= moe.moe_max_rows(sf), "slice rows exceed the shape's row bound"
     x_perm = synth.normal_bf16(5, synth.TID_X, (max(R, 1), w.d), 1.0, dev)
@@ -1000,6 +1008,66 @@ def run_ffn_stage(args, w):
     return 0
 
 
+def run_ab_stage(args, w):
+    """Two layers of the workload that differ only in their moe_tuning_t
+    fields, built once and called alternately (A B B A ...), the L2 flushed
+    before every call and each call bracketed by events, and with every
+    kernel bracketed too.  Prints the medians of both and of the paired
+    differences: the power cap makes separate runs drift by several percent,
+    while alternating calls see the same clock."""
+    import statistics
+
+    import torch
+
+    import synth
+    import top_routing_expert_lb_b300 as moe
+    from top_routing_expert_lb_b300 import build as mbuild
+
+    mbuild.ensure_built()
+    dev = torch.device("cuda", 0)
+    inp = synth.make_inputs(w, dev)
+    tunes = (parse_tune(args.tune), parse_tune(args.tune_b))
+    layers = [moe.MoELayer(moe.Shape.of(w.T, w.d, w.M, w.E, w.k, w.n_shared, w.capacity_factor,
+                                        w.balance_coef, w.flags, **t),
+                           inp.wr, inp.w1, inp.w3, inp.w2, inp.ws1, inp.ws3, inp.ws2, inp.offset,
+                           inp.sel_bias, device=dev) for t in tunes]
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    for _ in range(max(args.warmup, 1)):
+        for L in layers:
+            L.forward(inp.x)
+    torch.cuda.synchronize(dev)
+    times = ([], [])
+    kern = ({}, {})
+    moe.moe_profile_collect()
+    moe.moe_profile_enable(True)
+    for i in range(args.steps):
+        for v in ((0, 1) if i % 2 == 0 else (1, 0)):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            layers[v].forward(inp.x)
+            b.record()
+            torch.cuda.synchronize(dev)
+            times[v].append(a.elapsed_time(b))
+            for name, ms in moe.moe_profile_collect():
+                kern[v].setdefault(name, []).append(ms)
+    moe.moe_profile_enable(False)
+    for L in layers:
+        if moe.moe_check_status(L.ws) != 0:
+            raise RuntimeError("device wait timed out")
+    med = lambda xs: statistics.median(xs)
+    print(json.dumps({
+        "stage": "ab", "workload": workload_desc(w), "calls_each": args.steps,
+        "A": tunes[0], "B": tunes[1],
+        "layer_ms": [med(times[0]), med(times[1])],
+        "median_diff_a_minus_b_us": 1000.0 * med([x - y for x, y in zip(*times)]),
+        "kernel_us": [{k: 1000.0 * med(v) for k, v in kern[0].items()},
+                      {k: 1000.0 * med(v) for k, v in kern[1].items()}],
+        "same_y": bool(torch.equal(layers[0].y.view(torch.int16), layers[1].y.view(torch.int16))),
+    }), flush=True)
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     import synth
@@ -1018,6 +1086,8 @@ def main(argv=None):
         return run_router_stage(args, w)
     if args.stage == "ffn":
         return run_ffn_stage(args, w)
+    if args.stage == "ab":
+        return run_ab_stage(args, w)
     return run_ours(args, w)
 
 
