@@ -103,8 +103,9 @@ extern "C" {
  *   gemm1_tile      gate/up projection tiles.  0 or 128: single-CTA 128 x 256
  *                   tiles; 256: CTA-pair 256 x 256 tiles (then the down
  *                   projection too, unless gemm2_tile is 128)
- *   gemm2_tile      down projection tiles.  0: CTA pairs when d % 256 == 0 and
- *                   experts average >= 512 rows (or gemm1_tile is 256), else
+ *   gemm2_tile      down projection tiles.  0: CTA pairs when d % 256 == 0,
+ *                   E <= 16 and experts average >= 512 rows (or gemm1_tile is
+ *                   256), else
  *                   single-CTA 128 x BN (BN = 256, 128 or 64 by d); 128:
  *                   single-CTA tiles; 256: CTA pairs (needs d % 256 == 0)
  *   tile_order      CTA-pair launches.  0: tiles from a counter in the

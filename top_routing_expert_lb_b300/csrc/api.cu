@@ -591,11 +591,13 @@ int do_ffn(const moe_shape_t* s, const uint16_t* x_perm, const int32_t* offsets,
 
   // projection 2: [h | h_s] -> [y_perm | y_s]
   // The down projection (K = M, long tiles) runs on 256 x 256 CTA-pair tiles
-  // when experts average at least 512 rows: the pair halves the operand bytes
-  // per FLOP and the 256-row padding stays small (measured 3 % faster steps on
-  // Mixtral in the power-limited loop); with fewer rows per expert the padding
-  // costs more than the pair saves.  gemm2_tile 128 / 256 overrides.
-  bool paired2 = bn2 == 256 && (paired || rows_per_expert >= 512);
+  // for a few large experts (at most 16, averaging at least 512 rows): the
+  // pair halves the operand bytes per FLOP and the 256-row padding stays
+  // small (Mixtral: single-CTA tiles +119 us per layer in alternating calls).
+  // With many experts of skewed sizes the padding costs more than the pair
+  // saves (DeepSeekMoE-16B, 64 experts averaging 768 rows: pair tiles +10 us
+  // in this projection).  gemm2_tile 128 / 256 overrides.
+  bool paired2 = bn2 == 256 && (paired || (rows_per_expert >= 512 && E <= 16));
   if (tune.gemm2_tile == 128) paired2 = false;
   if (tune.gemm2_tile == 256) paired2 = bn2 == 256;
   // the pair form loads B in 128-row halves
