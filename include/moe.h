@@ -111,9 +111,9 @@ extern "C" {
  *   tile_order      CTA-pair launches.  0: tiles from a counter in the
  *                   workspace when K >= 4096, else round-robin; 1: round-robin
  *                   throughout; 2: counter throughout
- *   tail_max_n      a group's last m-tile with r valid rows runs transposed
- *                   (weights as the MMA's M) when r rounded up to 16 is at most
- *                   this.  0: 112; < 0: never; 16..112 in steps of 16
+ *   tail_max_n      single-CTA tiles: a group's only m-tile with r valid rows
+ *                   runs transposed (weights as the MMA's M) when r rounded up
+ *                   to 16 is at most this.  0: 112; < 0: never; 16..128
  *   n_block         tile order inside a group with more than block_min_rows
  *                   rows: blocks of n_block n-tiles, m-tile major inside a
  *                   block.  0: 8, or 4 for a single-CTA gate/up projection
@@ -135,12 +135,17 @@ extern "C" {
  *                               down projection's epilogue scales each routed
  *                               row by its gate (fp32, before rounding) and
  *                               the combine only adds rows, in the same order
+ *     MOE_TUNE_SWAP_ALL_TAILS   single-CTA tiles: the last m-tile of every
+ *                               group may run transposed (by tail_max_n), not
+ *                               only a group's only m-tile (the default for a
+ *                               projection with K <= 1024)
  *   wait_timeout_ns limit of this call's bounded device waits; 0: the
  *                   process-wide limit (moe_set_wait_timeout_ns)             */
 #define MOE_TUNE_NO_HALF_TILES 1u
 #define MOE_TUNE_GEMM1_SPLIT 2u
 #define MOE_TUNE_FUSED_GATHER 4u
 #define MOE_TUNE_GATE_IN_EPILOGUE 8u
+#define MOE_TUNE_SWAP_ALL_TAILS 16u
 typedef struct moe_tuning {
     int32_t gemm1_tile, gemm2_tile, tile_order, tail_max_n, n_block, block_min_rows;
     uint32_t options;

@@ -159,8 +159,11 @@ def _tuning_for(tile: str) -> dict:
     CTA pairs take their tiles from the workspace counter except with
     256-static; a group's last pair tile of at most 128 rows runs as an M = 128
     pair MMA except with 256-nohalf.  With 256* and d % 256 == 0 the down
-    projection runs on CTA pairs too."""
+    projection runs on CTA pairs too.  Single-CTA tiles transpose the tail of
+    a group of one m-tile; with 128-swapall the tail of every group."""
     opts = 0
+    if tile.endswith("swapall"):
+        opts |= moe.MOE_TUNE_SWAP_ALL_TAILS
     if tile.endswith("nohalf"):
         opts |= moe.MOE_TUNE_NO_HALF_TILES
     if tile.endswith("split"):
@@ -169,8 +172,8 @@ def _tuning_for(tile: str) -> dict:
                 n_block=2 if tile.endswith("block") else 1, block_min_rows=100, options=opts)
 
 
-@pytest.mark.parametrize("tile", ["128", "256", "256-static", "256-nohalf", "128-split",
-                                  "128-block", "256-block"])
+@pytest.mark.parametrize("tile", ["128", "128-swapall", "256", "256-static", "256-nohalf",
+                                  "128-split", "128-block", "256-block"])
 @pytest.mark.parametrize("rows,d,M,n_shared,T", [
     ([0, 1, 127, 128, 129, 300], 128, 256, 1, 200),    # empty, single, tile edges
     ([5, 0, 0, 260], 64, 128, 0, 0),                   # d = 64 (second projection N = 64)
@@ -178,7 +181,8 @@ def _tuning_for(tile: str) -> dict:
     ([0, 0, 0], 192, 128, 1, 77),                      # routed rows all empty, shared only
     ([400], 320, 384, 0, 0),                           # one group, d = 320 (N tile 64)
     ([255, 256, 257, 511, 1], 512, 256, 1, 300),       # 256-row tile edges, d = 512
-    # tails of 1..112 rows run transposed (weights as the MMA's M); 113..127 do not
+    # tails of 1..112 rows run transposed (weights as the MMA's M) in groups of
+    # one m-tile (every group with 128-swapall); 113..127 never
     ([16, 17, 111, 112, 113, 240, 33, 128], 256, 256, 1, 200),  # second projection N = 256
     ([48, 200, 97, 1], 384, 128, 0, 0),                # second projection N = 128
 ])

@@ -46,6 +46,7 @@ MOE_TUNE_NO_HALF_TILES = 1
 MOE_TUNE_GEMM1_SPLIT = 2
 MOE_TUNE_FUSED_GATHER = 4
 MOE_TUNE_GATE_IN_EPILOGUE = 8
+MOE_TUNE_SWAP_ALL_TAILS = 16
 
 
 class Tuning(ctypes.Structure):

@@ -88,6 +88,18 @@ __device__ __forceinline__ int swapped_n(int rows_left, int max_n) {
   return n <= max_n ? n : 0;
 }
 
+// Which tails may run transposed.  The tail of a group that also has full
+// m-tiles finds its weight tile in L2 (its full tiles read it) and is bound by
+// the MMA, where two M = 128 MMAs of N = r cost more than one padded 128-row
+// MMA: transposing those tails made the Mixtral layer 33 us slower (1.4 %),
+// DeepSeek-V2 9 us.  A group of one m-tile streams its weights and gains, and
+// so does every tail of a short reduction (swap_all_tails, set for K <= 1024).
+template <typename Tail>
+__device__ __forceinline__ bool swap_tail(const Tail* st, const GroupedGemmArgs& p,
+                                          const TileInfo& ti) {
+  return p.swap_all_tails || ti.rows_left == st->rows[ti.g];
+}
+
 template <typename Tail>
 __device__ __forceinline__ TileInfo decode_tile(const Tail* st, const GroupedGemmArgs& p, int G,
                                                 int tile, int bn, int bm = kBM) {
@@ -340,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(a * BN);
-        const int nsw = swapped_n<BN>(ti.rows_left, p.tail_max_n);
+        const int nsw = swap_tail(st, p, ti) ? swapped_n<BN>(ti.rows_left, p.tail_max_n) : 0;
         const uint32_t idesc_sw = idesc_bf16_f32(kBM, static_cast<uint32_t>(nsw > 0 ? nsw : 16));
         bool ok = true;
         for (int kb = 0; kb < ti.nk; ++kb) {
@@ -403,7 +415,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(ti.shared ? p.out_shared
                                                                       : p.out_routed);
       const int64_t ld = ti.shared ? p.ld_shared : p.ld_routed;
-      const int nsw = swapped_n<BN>(ti.rows_left, p.tail_max_n);
+      const int nsw = swap_tail(st, p, ti) ? swapped_n<BN>(ti.rows_left, p.tail_max_n) : 0;
       if (nsw > 0) {
         // transposed tail: this thread's TMEM lane is output column r_in_tile
         // of each 128-wide half; TMEM column j of a half is token row j

@@ -41,8 +41,10 @@ struct GroupedGemmArgs {
   // blocks on CTA pairs and the remainders on single CTAs.
   int32_t row_split = 0;
   // A group's last m-tile with r valid rows runs transposed when r rounded up
-  // to 16 is at most tail_max_n (0: never).
+  // to 16 is at most tail_max_n (0: never), and, unless swap_all_tails, only
+  // when it is the group's only m-tile.
   int32_t tail_max_n = 112;
+  int32_t swap_all_tails = 0;
   // Plain projection only: routed output row r is scaled by row_scale[r]
   // (fp32, before rounding); the shared group is never scaled.
   const float* row_scale = nullptr;
