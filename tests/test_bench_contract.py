@@ -48,3 +48,20 @@ def test_defaults_follow_the_timing_rules():
     a = bench.parse_args([])
     assert a.gpus == 1 and a.warmup >= 3 and a.steps >= 1
     assert bench.FLUSH_BYTES > 126 * 2**20    # larger than the L2
+
+
+def test_ab_stage_arguments():
+    """`--stage ab` takes the tuning of each layer as field=value pairs; the
+    fields are moe_tuning_t's and unknown ones fail when the shape is built."""
+    import top_routing_expert_lb_b300 as moe
+    args = bench.parse_args(["--stage", "ab", "--tune", "n_block=8", "--tune", "block_min_rows=2048",
+                             "--tune-b", "gemm1_tile=256"])
+    assert args.stage == "ab"
+    a, b = bench.parse_tune(args.tune), bench.parse_tune(args.tune_b)
+    assert a == {"n_block": 8, "block_min_rows": 2048} and b == {"gemm1_tile": 256}
+    s = moe.Shape.of(64, 64, 128, 8, 2, **a)
+    assert s.tuning.n_block == 8 and s.tuning.block_min_rows == 2048
+    with pytest.raises(TypeError):
+        moe.Shape.of(64, 64, 128, 8, 2, no_such_field=1)
+    with pytest.raises(TypeError):
+        s.tuned(gemm_tile=128)

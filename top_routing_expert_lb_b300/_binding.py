@@ -49,6 +49,15 @@ MOE_TUNE_GATE_IN_EPILOGUE = 8
 MOE_TUNE_SWAP_ALL_TAILS = 16
 
 
+def _check_tuning_names(tuning):
+    # ctypes would store an unknown keyword as a plain attribute and pass
+    # nothing to the library
+    known = {name for name, _ in Tuning._fields_}
+    unknown = sorted(set(tuning) - known)
+    if unknown:
+        raise TypeError(f"unknown moe_tuning_t fields {unknown}; known: {sorted(known)}")
+
+
 class Tuning(ctypes.Structure):
     """moe_tuning_t: scheduling choices of the expert GEMMs (all zero: the
     measured defaults)."""
@@ -71,11 +80,13 @@ class Shape(ctypes.Structure):
            **tuning):
         """Shape with the default tuning; keyword arguments set moe_tuning_t
         fields (e.g. gemm1_tile=256, options=MOE_TUNE_FUSED_GATHER)."""
+        _check_tuning_names(tuning)
         return cls(T, d, M, E, k, n_shared, capacity_factor, balance_coef, flags, 0,
                    Tuning(**tuning))
 
     def tuned(self, **tuning) -> "Shape":
         """A copy of this shape with the given moe_tuning_t fields changed."""
+        _check_tuning_names(tuning)
         t = Tuning()
         ctypes.pointer(t)[0] = self.tuning
         for key, v in tuning.items():
