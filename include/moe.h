@@ -139,6 +139,11 @@ extern "C" {
  *                               group may run transposed (by tail_max_n), not
  *                               only a group's only m-tile (the default for a
  *                               projection with K <= 1024)
+ *     MOE_TUNE_TWO_CTAS_PER_SM  single-CTA expert GEMMs with 256-column tiles run
+ *                               two CTAs per SM, each with a 2-stage ring and
+ *                               one TMEM accumulator (the default only for a
+ *                               down projection with M <= 2048 over experts
+ *                               averaging fewer than 512 rows)
  *   wait_timeout_ns limit of this call's bounded device waits; 0: the
  *                   process-wide limit (moe_set_wait_timeout_ns)             */
 #define MOE_TUNE_NO_HALF_TILES 1u
@@ -146,6 +151,7 @@ extern "C" {
 #define MOE_TUNE_FUSED_GATHER 4u
 #define MOE_TUNE_GATE_IN_EPILOGUE 8u
 #define MOE_TUNE_SWAP_ALL_TAILS 16u
+#define MOE_TUNE_TWO_CTAS_PER_SM 32u
 typedef struct moe_tuning {
     int32_t gemm1_tile, gemm2_tile, tile_order, tail_max_n, n_block, block_min_rows;
     uint32_t options;

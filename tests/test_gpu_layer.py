@@ -96,6 +96,17 @@ def test_layer_parity_gate_in_epilogue(name, tile2):
                 tuning=dict(options=moe.MOE_TUNE_GATE_IN_EPILOGUE, gemm2_tile=int(tile2)))
 
 
+@pytest.mark.parametrize("name", ["ragged_shared", "capacity_k4", "fine_bias_shared", "wide_E160"])
+def test_two_ctas_per_sm_gives_the_same_bits(name):
+    """The single-CTA GEMMs run two CTAs per SM (MOE_TUNE_TWO_CTAS_PER_SM): the
+    oracle's results, and the bits of the default launch (the same tiles, run
+    by other CTAs)."""
+    inp = synth.make_inputs(CASES[name], "cuda")
+    g, _ = check_layer(inp, tuning=dict(options=moe.MOE_TUNE_TWO_CTAS_PER_SM))
+    plain = run_layer(inp)
+    assert torch.equal(g.y.view(torch.int16), plain.y.view(torch.int16))
+
+
 def test_fused_and_materialised_rows_agree_bitwise():
     """Gathering the rows inside GEMM-1 stages the same bytes as the scatter's
     copy, so the two paths give bit-identical outputs."""

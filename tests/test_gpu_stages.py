@@ -160,10 +160,13 @@ def _tuning_for(tile: str) -> dict:
     256-static; a group's last pair tile of at most 128 rows runs as an M = 128
     pair MMA except with 256-nohalf.  With 256* and d % 256 == 0 the down
     projection runs on CTA pairs too.  Single-CTA tiles transpose the tail of
-    a group of one m-tile; with 128-swapall the tail of every group."""
+    a group of one m-tile; with 128-swapall the tail of every group.  128-twosm
+    runs two CTAs per SM (one accumulator, 2-stage ring each) where BN = 256."""
     opts = 0
     if tile.endswith("swapall"):
         opts |= moe.MOE_TUNE_SWAP_ALL_TAILS
+    if tile.endswith("twosm"):
+        opts |= moe.MOE_TUNE_TWO_CTAS_PER_SM
     if tile.endswith("nohalf"):
         opts |= moe.MOE_TUNE_NO_HALF_TILES
     if tile.endswith("split"):
@@ -172,7 +175,8 @@ def _tuning_for(tile: str) -> dict:
                 n_block=2 if tile.endswith("block") else 1, block_min_rows=100, options=opts)
 
 
-@pytest.mark.parametrize("tile", ["128", "128-swapall", "256", "256-static", "256-nohalf",
+@pytest.mark.parametrize("tile", ["128", "128-swapall", "128-twosm", "256", "256-static",
+                                  "256-nohalf",
                                   "128-split", "128-block", "256-block"])
 @pytest.mark.parametrize("rows,d,M,n_shared,T", [
     ([0, 1, 127, 128, 129, 300], 128, 256, 1, 200),    # empty, single, tile edges

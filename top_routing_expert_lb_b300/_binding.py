@@ -47,6 +47,7 @@ MOE_TUNE_GEMM1_SPLIT = 2
 MOE_TUNE_FUSED_GATHER = 4
 MOE_TUNE_GATE_IN_EPILOGUE = 8
 MOE_TUNE_SWAP_ALL_TAILS = 16
+MOE_TUNE_TWO_CTAS_PER_SM = 32
 
 
 def _check_tuning_names(tuning):

@@ -115,7 +115,8 @@ int check_shape(const moe_shape_t* s) {
   if (t.tail_max_n > 0 && (t.tail_max_n < 16 || t.tail_max_n > 128)) return MOE_ERR_INVALID_ARG;
   if (t.n_block < 0 || t.n_block > 64 || t.block_min_rows < 0) return MOE_ERR_INVALID_ARG;
   if ((t.options & ~(MOE_TUNE_NO_HALF_TILES | MOE_TUNE_GEMM1_SPLIT | MOE_TUNE_FUSED_GATHER |
-                     MOE_TUNE_GATE_IN_EPILOGUE | MOE_TUNE_SWAP_ALL_TAILS)) != 0 || t.reserved != 0)
+                     MOE_TUNE_GATE_IN_EPILOGUE | MOE_TUNE_SWAP_ALL_TAILS |
+                     MOE_TUNE_TWO_CTAS_PER_SM)) != 0 || t.reserved != 0)
     return MOE_ERR_INVALID_ARG;
   if ((t.options & MOE_TUNE_FUSED_GATHER) && t.gemm1_tile == 256) return MOE_ERR_INVALID_ARG;
   if (t.gemm2_tile == 256 && s->d % 256 != 0) return MOE_ERR_UNSUPPORTED;
@@ -575,6 +576,7 @@ int do_ffn(const moe_shape_t* s, const uint16_t* x_perm, const int32_t* offsets,
   // projection, 12 us per layer faster), else only a group's only m-tile
   const bool swap_all = (tune.options & MOE_TUNE_SWAP_ALL_TAILS) != 0;
   g1.swap_all_tails = (swap_all || d <= 1024) ? 1 : 0;
+  g1.two_per_sm = (tune.options & MOE_TUNE_TWO_CTAS_PER_SM) ? 1 : 0;
   int rc = 0;
   if (split1) {
     GroupedGemmArgs g1p = g1;
@@ -618,6 +620,11 @@ int do_ffn(const moe_shape_t* s, const uint16_t* x_perm, const int32_t* offsets,
   if (!shared) { a1 = a0; b1 = b0; }
   GroupedGemmArgs g2 = g1;
   g2.swap_all_tails = (swap_all || M <= 1024) ? 1 : 0;
+  // A short down projection (K = M <= 2048) over many small experts (fewer
+  // than 512 rows on average) runs two CTAs per SM: DeepSeek-V2's took 1190
+  // against 1242 us in alternating calls; the gate/up projections and longer
+  // reductions ran slower that way (DeepSeekMoE-16B, Switch, Mixtral).
+  g2.two_per_sm = (g1.two_per_sm || (M <= 2048 && rows_per_expert < 512)) ? 1 : 0;
   g2.n_block = n_block2;
   g2.block_min_rows = min_rows2;
   g2.tile_counter = dynamic_for(M);

@@ -143,8 +143,12 @@ __device__ __forceinline__ TileInfo decode_tile(const Tail* st, const GroupedGem
 
 // kRowScale (plain projections only): every routed output row r is multiplied
 // by p.row_scale[r] in fp32 before rounding (the combine's gate, applied here).
-template <int BN, bool kSwiGLU, int kStages, bool kRowScale = false>
-__global__ void __launch_bounds__(kThreads, 1)
+// kAcc = 2: one CTA per SM, two TMEM accumulators (a tile's epilogue runs
+// under the next tile's MMAs).  kAcc = 1: two CTAs per SM with one accumulator
+// and a shorter ring each, so that one CTA's MMAs run while the other waits
+// for its operands or drains its accumulator.
+template <int BN, bool kSwiGLU, int kStages, bool kRowScale = false, int kAcc = 2>
+__global__ void __launch_bounds__(kThreads, 3 - kAcc)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
                         const __grid_constant__ CUtensorMap tmA1,
                         const __grid_constant__ CUtensorMap tmB0,
@@ -153,9 +157,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kABytes = kBM * kBK * 2;
   constexpr int kBBytes = BN * kBK * 2;
   constexpr int kStageBytes = kABytes + kBBytes;
-  constexpr uint32_t kTmemCols = 2 * BN;
+  constexpr uint32_t kTmemCols = kAcc * BN;
   constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, BN);
   static_assert(!(kRowScale && kSwiGLU), "row scaling applies to the plain projection");
+  static_assert(kAcc == 1 || kAcc == 2, "one or two accumulators");
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
@@ -345,8 +350,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       int local = 0;
       for (int tile = item0; tile < total && !*abort_flag; tile += stride, ++local) {
         const TileInfo ti = decode_tile(st, p, G, tile, BN);
-        const int a = local & 1;
-        const uint32_t q = static_cast<uint32_t>(local >> 1);
+        const int a = local % kAcc;
+        const uint32_t q = static_cast<uint32_t>(local / kAcc);
         if (!mbar_wait_bounded(&st->tempty[a], (q & 1u) ^ 1u, p.timeout_ns, p.status,
                                abort_flag))
           break;
@@ -403,8 +408,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     int local = 0;
     for (int tile = item0; tile < total && !*abort_flag; tile += stride, ++local) {
       const TileInfo ti = decode_tile(st, p, G, tile, BN);
-      const int a = local & 1;
-      const uint32_t q = static_cast<uint32_t>(local >> 1);
+      const int a = local % kAcc;
+      const uint32_t q = static_cast<uint32_t>(local / kAcc);
       if (!mbar_wait_bounded(&st->tfull[a], q & 1u, p.timeout_ns, p.status, abort_flag)) break;
       tc_fence_after();
       const int64_t out_rows = ti.shared ? p.out_rows_shared : p.out_rows_routed;
@@ -953,13 +958,13 @@ int launch_pair_impl(const CUtensorMap& a0, const CUtensorMap& a1, const CUtenso
   return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }
 
-template <int BN, bool kSwiGLU, int kStages, bool kRowScale = false>
+template <int BN, bool kSwiGLU, int kStages, bool kRowScale = false, int kAcc = 2>
 int launch_impl(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b0,
                 const CUtensorMap& b1, const GroupedGemmArgs& args, int num_sms,
                 cudaStream_t stream) {
   constexpr size_t smem = gemm_smem_bytes<BN, kStages>();
   static_assert(smem <= 227 * 1024, "shared memory budget");
-  auto kern = grouped_gemm_kernel<BN, kSwiGLU, kStages, kRowScale>;
+  auto kern = grouped_gemm_kernel<BN, kSwiGLU, kStages, kRowScale, kAcc>;
   static bool attr_set = false;
   if (!attr_set) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -967,7 +972,7 @@ int launch_impl(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap&
       return -3;
     attr_set = true;
   }
-  kern<<<num_sms, kThreads, smem, stream>>>(a0, a1, b0, b1, args);
+  kern<<<num_sms * (3 - kAcc), kThreads, smem, stream>>>(a0, a1, b0, b1, args);
   return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }
 
@@ -1014,6 +1019,10 @@ int launch_grouped_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUte
     if (!swiglu) return launch_pair_impl<false>(a0, a1, b0, b1, b0, b1, args, num_sms, stream);
     if (b0h == nullptr || b1h == nullptr) return -2;  // half tiles need 64-row B boxes
     return launch_pair_impl<true>(a0, a1, b0, b1, *b0h, *b1h, args, num_sms, stream);
+  }
+  if (args.two_per_sm && bn == 256 && !scale) {
+    if (swiglu) return launch_impl<256, true, 2, false, 1>(a0, a1, b0, b1, args, num_sms, stream);
+    return launch_impl<256, false, 2, false, 1>(a0, a1, b0, b1, args, num_sms, stream);
   }
   if (swiglu) {
     if (bn != 256) return -2;

@@ -45,6 +45,9 @@ struct GroupedGemmArgs {
   // when it is the group's only m-tile.
   int32_t tail_max_n = 112;
   int32_t swap_all_tails = 0;
+  // Single-CTA kernel with BN = 256 (no row scaling): two CTAs per SM, each
+  // with a 2-stage ring and one TMEM accumulator.
+  int32_t two_per_sm = 0;
   // Plain projection only: routed output row r is scaled by row_scale[r]
   // (fp32, before rounding); the shared group is never scaled.
   const float* row_scale = nullptr;
