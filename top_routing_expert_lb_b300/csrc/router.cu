@@ -19,8 +19,9 @@
 // d dimension of each tile is split into S slices so that every SM streams.
 // A persistent grid (one CTA per SM) takes units round-robin; per CTA a TMA
 // warp fills a ring of (x, W_r) stages, an MMA warp accumulates each unit into
-// one of two TMEM buffers, and eight epilogue warps drain the other buffer, so
-// a unit's epilogue overlaps the next unit's loads.  A K-split unit stores its
+// one of two TMEM buffers, and sixteen epilogue warps drain the other buffer
+// (handing it back right after their last TMEM read), so a unit's epilogue
+// overlaps the next unit's loads.  A K-split unit stores its
 // partial logits to the workspace (coalesced, [expert][row] per tile); the
 // CTA that stores a tile's last slice sums the S partials in slice order,
 // writes the sums back into its TMEM buffer and runs the tile's epilogue.
@@ -32,8 +33,8 @@
 // keys and a per-thread Top-k list; the four parts of a row combine max, sum
 // and lists through shared memory in part order.  Column sums over the
 // tile's rows (P, importance) are reduced inside each warp by a fixed shuffle
-// tree and then over the four row quarters in order.  Every cross-tile total is either a
-// 64-bit integer atomic on fixed-point values (P and importance at 2^-32,
+// tree and then over the four row quarters in order.  Every cross-tile total
+// is either a 64-bit integer atomic on fixed-point values (P and importance at 2^-32,
 // entropy at 2^-32, counts exact) or a per-tile value summed in tile order
 // (lse^2), so all results are bitwise reproducible whichever CTA runs which
 // tile.  The CTA that completes the last tile reduces the totals (f, P, both
