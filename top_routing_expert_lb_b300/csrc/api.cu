@@ -521,6 +521,12 @@ int do_ffn(const moe_shape_t* s, const uint16_t* x_perm, const int32_t* offsets,
     if (!routed) bh0 = bh1;
     if (!shared) bh1 = bh0;
   }
+  // the outputs h / h_s as tensor maps (the epilogue's block stores)
+  CUtensorMap o0, o1;
+  if (routed && !make_tmap_out_bf16(&o0, h, L.rmax, M)) return MOE_ERR_CUDA;
+  if (shared && !make_tmap_out_bf16(&o1, h_s, T, Ms)) return MOE_ERR_CUDA;
+  if (!routed) o0 = o1;
+  if (!shared) o1 = o0;
   CUtensorMap bp0 = b0, bp1 = b1;  // 128-row boxes for the pair launch
   if (split1) {
     if (routed && !make_tmap_bf16(&bp0, w13, E * 2 * M, d, 128)) return MOE_ERR_CUDA;
@@ -582,15 +588,16 @@ int do_ffn(const moe_shape_t* s, const uint16_t* x_perm, const int32_t* offsets,
     GroupedGemmArgs g1p = g1;
     g1p.row_split = 1;
     rc = tracked(MOE_KERNEL_GEMM_SWIGLU, st, [&] {
-      return launch_grouped_gemm(a0, a1, bp0, bp1, g1p, true, 256, true, nsm, st, &bh0, &bh1);
+      return launch_grouped_gemm(a0, a1, bp0, bp1, o0, o1, g1p, true, 256, true, nsm, st, &bh0,
+                                 &bh1);
     });
     if (rc != 0) return cuda_rc(rc);
     g1.row_split = 2;
   }
   rc = tracked(MOE_KERNEL_GEMM_SWIGLU, st,
                [&] {
-                 return launch_grouped_gemm(a0, a1, b0, b1, g1, true, 256, paired, nsm, st, &bh0,
-                                            &bh1);
+                 return launch_grouped_gemm(a0, a1, b0, b1, o0, o1, g1, true, 256, paired, nsm,
+                                            st, &bh0, &bh1);
                });
   if (rc != 0) return cuda_rc(rc);
   g1.row_split = 0;
@@ -618,6 +625,10 @@ int do_ffn(const moe_shape_t* s, const uint16_t* x_perm, const int32_t* offsets,
   }
   if (!routed) { a0 = a1; b0 = b1; }
   if (!shared) { a1 = a0; b1 = b0; }
+  if (routed && !make_tmap_out_bf16(&o0, y_perm, L.rmax, d)) return MOE_ERR_CUDA;
+  if (shared && !make_tmap_out_bf16(&o1, y_s, T, d)) return MOE_ERR_CUDA;
+  if (!routed) o0 = o1;
+  if (!shared) o1 = o0;
   GroupedGemmArgs g2 = g1;
   g2.swap_all_tails = (swap_all || M <= 1024) ? 1 : 0;
   // A short down projection (K = M <= 2048) over many small experts (fewer
@@ -642,7 +653,8 @@ int do_ffn(const moe_shape_t* s, const uint16_t* x_perm, const int32_t* offsets,
   g2.ld_shared = d;
   rc = tracked(MOE_KERNEL_GEMM_DOWN, st,
                [&] {
-                 return launch_grouped_gemm(a0, a1, b0, b1, g2, false, bn2, paired2, nsm, st);
+                 return launch_grouped_gemm(a0, a1, b0, b1, o0, o1, g2, false, bn2, paired2, nsm,
+                                            st);
                });
   return cuda_rc(rc);
 }

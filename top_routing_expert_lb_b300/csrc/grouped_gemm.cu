@@ -57,10 +57,51 @@ struct GemmSmemTail {
   int rows[kMaxGroups];
 };
 
-template <int BN, int kStages>
+// Epilogue output staging.  Each of the four epilogue warps owns two 2 KB
+// buffers, each holding one block of 32 rows x 32 bf16 columns in the
+// 64-byte-swizzled layout of the output tensor maps, and writes a block with
+// one TMA tile store: the block reaches L2 as whole 64-byte row segments,
+// where direct stores send 32 scattered 16-byte pieces per instruction.  On the
+// dense 8192 x 4096 x 28672 gate/up shape the direct stores alone cost 8 % of
+// the launch.
+constexpr int kOutBlockBytes = 32 * 32 * 2;
+constexpr int kOutStageBytes = 4 * 2 * kOutBlockBytes;
+
+template <int BN, int kStages, bool kTmaOut = true>
 constexpr size_t gemm_smem_bytes() {
   return 1024 + static_cast<size_t>(kStages) * (kBM * kBK * 2 + BN * kBK * 2) +
-         sizeof(GemmSmemTail);
+         (kTmaOut ? kOutStageBytes : 0) + sizeof(GemmSmemTail);
+}
+
+struct OutStage {
+  uint32_t buf0;  // shared address of this warp's first buffer (1024-byte aligned)
+  uint32_t n;     // blocks issued so far; block n uses buffer n & 1
+};
+
+// Writes one 32 x 32 output block whose top-left element is (row, col) of the
+// tensor behind `map`; lane l holds row l's 32 values as packed bf16 pairs.
+// Row l's 16-byte piece i goes to piece i ^ ((l >> 1) & 3) of the row's 64
+// bytes in the buffer (the 64-byte swizzle), so each quarter-warp's writes
+// cover all 32 banks.
+__device__ __forceinline__ void store_block_tma(OutStage& o, const uint32_t (&packed)[16],
+                                                const CUtensorMap* map, int col, int64_t row,
+                                                int lane) {
+  const uint32_t buf = o.buf0 + (o.n & 1u) * static_cast<uint32_t>(kOutBlockBytes);
+  if (lane == 0) bulk_wait_read<1>();  // the store that used this buffer has read it
+  __syncwarp();
+  const uint32_t r = buf + static_cast<uint32_t>(lane) * 64u;
+  const uint32_t sw = (static_cast<uint32_t>(lane) >> 1) & 3u;
+#pragma unroll
+  for (uint32_t i = 0; i < 4; ++i)
+    st_shared_v4(r + ((i ^ sw) << 4), packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
+                 packed[4 * i + 3]);
+  fence_proxy_async_shared();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_2d(map, buf, col, static_cast<int32_t>(row));
+    bulk_commit_group();
+  }
+  ++o.n;
 }
 
 struct TileInfo {
@@ -152,7 +193,9 @@ __global__ void __launch_bounds__(kThreads, 3 - kAcc)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
                         const __grid_constant__ CUtensorMap tmA1,
                         const __grid_constant__ CUtensorMap tmB0,
-                        const __grid_constant__ CUtensorMap tmB1, const GroupedGemmArgs p) {
+                        const __grid_constant__ CUtensorMap tmB1,
+                        const __grid_constant__ CUtensorMap tmO0,
+                        const __grid_constant__ CUtensorMap tmO1, const GroupedGemmArgs p) {
   static_assert(!kSwiGLU || BN == 256, "SwiGLU tiles pair 128 gate with 128 up columns");
   constexpr int kABytes = kBM * kBK * 2;
   constexpr int kBBytes = BN * kBK * 2;
@@ -161,11 +204,14 @@ __global__ void __launch_bounds__(kThreads, 3 - kAcc)
   constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, BN);
   static_assert(!(kRowScale && kSwiGLU), "row scaling applies to the plain projection");
   static_assert(kAcc == 1 || kAcc == 2, "one or two accumulators");
+  // two CTAs per SM have no shared memory to spare for output staging
+  constexpr bool kTmaOut = kAcc == 2;
+  constexpr int kOutBytes = kTmaOut ? kOutStageBytes : 0;
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* smem = smem_raw + pad;
-  GemmSmemTail* st = reinterpret_cast<GemmSmemTail*>(smem + kStages * kStageBytes);
+  GemmSmemTail* st = reinterpret_cast<GemmSmemTail*>(smem + kStages * kStageBytes + kOutBytes);
   volatile int* abort_flag = &st->abort_flag;
 
   const int warp = threadIdx.x >> 5;
@@ -405,6 +451,9 @@ __global__ void __launch_bounds__(kThreads, 3 - kAcc)
     // ------------------------------------------------------------ epilogue
     const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
     const int r_in_tile = quarter * 32 + lane;
+    OutStage ostage{smem_u32(smem + kStages * kStageBytes) +
+                        static_cast<uint32_t>(quarter * 2 * kOutBlockBytes),
+                    0u};
     int local = 0;
     for (int tile = item0; tile < total && !*abort_flag; tile += stride, ++local) {
       const TileInfo ti = decode_tile(st, p, G, tile, BN);
@@ -460,6 +509,9 @@ __global__ void __launch_bounds__(kThreads, 3 - kAcc)
         }
       } else if constexpr (kSwiGLU) {
         __nv_bfloat16* dst = out + row * ld + static_cast<int64_t>(ti.n) * 128;
+        // a warp whose 32 rows are all stored writes through the tensor map
+        const bool via_tma = kTmaOut && __all_sync(0xffffffffu, valid);
+        const CUtensorMap* om = ti.shared ? &tmO1 : &tmO0;
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           float g[32], u[32];
@@ -471,7 +523,9 @@ __global__ void __launch_bounds__(kThreads, 3 - kAcc)
           for (int i = 0; i < 16; ++i)
             packed[i] = pack_bf16x2(silu_f32(g[2 * i]) * u[2 * i],
                                     silu_f32(g[2 * i + 1]) * u[2 * i + 1]);
-          if (valid) {
+          if (via_tma) {
+            store_block_tma(ostage, packed, om, ti.n * 128 + c * 32, row - lane, lane);
+          } else if (valid) {
             uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
 #pragma unroll
             for (int i = 0; i < 4; ++i)
@@ -483,6 +537,8 @@ __global__ void __launch_bounds__(kThreads, 3 - kAcc)
         __nv_bfloat16* dst = out + row * ld + static_cast<int64_t>(ti.n) * BN;
         float sc = 1.0f;
         if constexpr (kRowScale) sc = (valid && !ti.shared) ? __ldg(p.row_scale + row) : 1.0f;
+        const bool via_tma = kTmaOut && __all_sync(0xffffffffu, valid);
+        const CUtensorMap* om = ti.shared ? &tmO1 : &tmO0;
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
           float v[32];
@@ -495,7 +551,9 @@ __global__ void __launch_bounds__(kThreads, 3 - kAcc)
           uint32_t packed[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) packed[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
-          if (valid) {
+          if (via_tma) {
+            store_block_tma(ostage, packed, om, ti.n * BN + c * 32, row - lane, lane);
+          } else if (valid) {
             uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
 #pragma unroll
             for (int i = 0; i < 4; ++i)
@@ -508,6 +566,8 @@ __global__ void __launch_bounds__(kThreads, 3 - kAcc)
       __syncwarp();
       if (lane == 0) mbar_arrive(&st->tempty[a]);
     }
+    // every output block written before the CTA (and its buffers) goes away
+    if (kTmaOut && lane == 0) bulk_wait_all();
   }
 
   tc_fence_before();
@@ -551,7 +611,7 @@ struct PairSmemTail {
 
 constexpr size_t pair_smem_bytes() {
   return 1024 + static_cast<size_t>(kPairStages) * (128 * kBK * 2 + 128 * kBK * 2) +
-         sizeof(PairSmemTail);
+         kOutStageBytes + sizeof(PairSmemTail);
 }
 
 // Dynamic schedule of the pair kernel.  The even CTA's producer takes the
@@ -580,7 +640,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                              const __grid_constant__ CUtensorMap tmB0,
                              const __grid_constant__ CUtensorMap tmB1,
                              const __grid_constant__ CUtensorMap tmB0h,
-                             const __grid_constant__ CUtensorMap tmB1h, const GroupedGemmArgs p) {
+                             const __grid_constant__ CUtensorMap tmB1h,
+                             const __grid_constant__ CUtensorMap tmO0,
+                             const __grid_constant__ CUtensorMap tmO1, const GroupedGemmArgs p) {
   constexpr int BN = 256;                 // N of the pair tile
   constexpr int kABytes = 128 * kBK * 2;  // this CTA's A rows
   constexpr int kBBytes = 128 * kBK * 2;  // this CTA's half of B
@@ -599,7 +661,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* smem = smem_raw + pad;
-  PairSmemTail* st = reinterpret_cast<PairSmemTail*>(smem + kPairStages * kStageBytes);
+  PairSmemTail* st =
+      reinterpret_cast<PairSmemTail*>(smem + kPairStages * kStageBytes + kOutStageBytes);
   volatile int* abort_flag = &st->abort_flag;
 
   const int warp = threadIdx.x >> 5;
@@ -823,6 +886,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r_in_half = quarter * 32 + lane;
     const uint32_t tempty_leader0 = mapa_shared(smem_u32(&st->tempty[0]), 0);
     const uint32_t tempty_leader1 = mapa_shared(smem_u32(&st->tempty[1]), 0);
+    OutStage ostage{smem_u32(smem + kPairStages * kStageBytes) +
+                        static_cast<uint32_t>(quarter * 2 * kOutBlockBytes),
+                    0u};
     int local = 0;
     const bool dyn = p.tile_counter != nullptr;
     for (int tile = pair; !*abort_flag; tile += npairs, ++local) {
@@ -852,6 +918,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(ti.shared ? p.out_shared
                                                                       : p.out_routed);
       const int64_t ld = ti.shared ? p.ld_shared : p.ld_routed;
+      // a warp's 32 lanes hold 32 consecutive rows of one column range; when
+      // all of them are stored the warp writes through the tensor map
+      const bool via_tma = __all_sync(0xffffffffu, valid);
+      const CUtensorMap* om = ti.shared ? &tmO1 : &tmO0;
       if constexpr (kSwiGLU) {
         // full: gate in TMEM columns [0, 128), up in [128, 256); half: this
         // lane's 64 output columns, gate in [0, 64), up in [64, 128)
@@ -870,7 +940,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 16; ++i)
             packed[i] = pack_bf16x2(silu_f32(g[2 * i]) * u[2 * i],
                                     silu_f32(g[2 * i + 1]) * u[2 * i + 1]);
-          if (valid) {
+          if (via_tma) {
+            store_block_tma(ostage, packed, om, ti.n * 128 + col_half * 64 + c * 32, row - lane,
+                            lane);
+          } else if (valid) {
             uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
 #pragma unroll
             for (int i = 0; i < 4; ++i)
@@ -896,7 +969,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t packed[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) packed[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
-          if (valid) {
+          if (via_tma) {
+            store_block_tma(ostage, packed, om, ti.n * BN + col_half * 128 + c * 32, row - lane,
+                            lane);
+          } else if (valid) {
             uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
 #pragma unroll
             for (int i = 0; i < 4; ++i)
@@ -909,6 +985,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(a ? tempty_leader1 : tempty_leader0);
     }
+    // every output block written before the CTA (and its buffers) goes away
+    if (lane == 0) bulk_wait_all();
   }
 
   // Both CTAs stay until the even CTA's MMAs and the odd CTA's copies are done.
@@ -931,7 +1009,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <bool kSwiGLU, bool kRowScale = false>
 int launch_pair_impl(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b0,
                      const CUtensorMap& b1, const CUtensorMap& b0h, const CUtensorMap& b1h,
-                     const GroupedGemmArgs& args, int num_sms, cudaStream_t stream) {
+                     const CUtensorMap& o0, const CUtensorMap& o1, const GroupedGemmArgs& args,
+                     int num_sms, cudaStream_t stream) {
   constexpr size_t smem = pair_smem_bytes();
   static_assert(smem <= 227 * 1024, "shared memory budget");
   auto kern = grouped_gemm_pair_kernel<kSwiGLU, kRowScale>;
@@ -954,15 +1033,16 @@ int launch_pair_impl(const CUtensorMap& a0, const CUtensorMap& a1, const CUtenso
   attrs[0].val.clusterDim.z = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, kern, a0, a1, b0, b1, b0h, b1h, args) != cudaSuccess) return -3;
+  if (cudaLaunchKernelEx(&cfg, kern, a0, a1, b0, b1, b0h, b1h, o0, o1, args) != cudaSuccess)
+    return -3;
   return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }
 
 template <int BN, bool kSwiGLU, int kStages, bool kRowScale = false, int kAcc = 2>
 int launch_impl(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b0,
-                const CUtensorMap& b1, const GroupedGemmArgs& args, int num_sms,
-                cudaStream_t stream) {
-  constexpr size_t smem = gemm_smem_bytes<BN, kStages>();
+                const CUtensorMap& b1, const CUtensorMap& o0, const CUtensorMap& o1,
+                const GroupedGemmArgs& args, int num_sms, cudaStream_t stream) {
+  constexpr size_t smem = gemm_smem_bytes<BN, kStages, kAcc == 2>();
   static_assert(smem <= 227 * 1024, "shared memory budget");
   auto kern = grouped_gemm_kernel<BN, kSwiGLU, kStages, kRowScale, kAcc>;
   static bool attr_set = false;
@@ -972,7 +1052,7 @@ int launch_impl(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap&
       return -3;
     attr_set = true;
   }
-  kern<<<num_sms * (3 - kAcc), kThreads, smem, stream>>>(a0, a1, b0, b1, args);
+  kern<<<num_sms * (3 - kAcc), kThreads, smem, stream>>>(a0, a1, b0, b1, o0, o1, args);
   return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }
 
@@ -1006,40 +1086,55 @@ bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t 
   return r == CUDA_SUCCESS;
 }
 
+bool make_tmap_out_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols) {
+  auto encode = get_encode_fn();
+  if (encode == nullptr || rows == 0 || cols == 0 || cols % 8 != 0) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                      CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 int launch_grouped_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b0,
-                        const CUtensorMap& b1, const GroupedGemmArgs& args, bool swiglu, int bn,
-                        bool paired, int num_sms, cudaStream_t stream, const CUtensorMap* b0h,
+                        const CUtensorMap& b1, const CUtensorMap& o0, const CUtensorMap& o1,
+                        const GroupedGemmArgs& args, bool swiglu, int bn, bool paired,
+                        int num_sms, cudaStream_t stream, const CUtensorMap* b0h,
                         const CUtensorMap* b1h) {
   if (args.n_routed + (args.shared_rows > 0 ? 1 : 0) > kMaxGroups) return -2;
   const bool scale = args.row_scale != nullptr;
   if (scale && swiglu) return -2;
   if (paired) {
     if (bn != 256 || num_sms < 2) return -2;
-    if (scale) return launch_pair_impl<false, true>(a0, a1, b0, b1, b0, b1, args, num_sms, stream);
-    if (!swiglu) return launch_pair_impl<false>(a0, a1, b0, b1, b0, b1, args, num_sms, stream);
+    if (scale) return launch_pair_impl<false, true>(a0, a1, b0, b1, b0, b1, o0, o1, args, num_sms, stream);
+    if (!swiglu) return launch_pair_impl<false>(a0, a1, b0, b1, b0, b1, o0, o1, args, num_sms, stream);
     if (b0h == nullptr || b1h == nullptr) return -2;  // half tiles need 64-row B boxes
-    return launch_pair_impl<true>(a0, a1, b0, b1, *b0h, *b1h, args, num_sms, stream);
+    return launch_pair_impl<true>(a0, a1, b0, b1, *b0h, *b1h, o0, o1, args, num_sms, stream);
   }
   if (args.two_per_sm && bn == 256 && !scale) {
-    if (swiglu) return launch_impl<256, true, 2, false, 1>(a0, a1, b0, b1, args, num_sms, stream);
-    return launch_impl<256, false, 2, false, 1>(a0, a1, b0, b1, args, num_sms, stream);
+    if (swiglu) return launch_impl<256, true, 2, false, 1>(a0, a1, b0, b1, o0, o1, args, num_sms, stream);
+    return launch_impl<256, false, 2, false, 1>(a0, a1, b0, b1, o0, o1, args, num_sms, stream);
   }
   if (swiglu) {
     if (bn != 256) return -2;
-    return launch_impl<256, true, 4>(a0, a1, b0, b1, args, num_sms, stream);
+    return launch_impl<256, true, 4>(a0, a1, b0, b1, o0, o1, args, num_sms, stream);
   }
   if (scale) {
     switch (bn) {
-      case 256: return launch_impl<256, false, 4, true>(a0, a1, b0, b1, args, num_sms, stream);
-      case 128: return launch_impl<128, false, 6, true>(a0, a1, b0, b1, args, num_sms, stream);
-      case 64: return launch_impl<64, false, 8, true>(a0, a1, b0, b1, args, num_sms, stream);
+      case 256: return launch_impl<256, false, 4, true>(a0, a1, b0, b1, o0, o1, args, num_sms, stream);
+      case 128: return launch_impl<128, false, 6, true>(a0, a1, b0, b1, o0, o1, args, num_sms, stream);
+      case 64: return launch_impl<64, false, 8, true>(a0, a1, b0, b1, o0, o1, args, num_sms, stream);
       default: return -2;
     }
   }
   switch (bn) {
-    case 256: return launch_impl<256, false, 4>(a0, a1, b0, b1, args, num_sms, stream);
-    case 128: return launch_impl<128, false, 6>(a0, a1, b0, b1, args, num_sms, stream);
-    case 64: return launch_impl<64, false, 8>(a0, a1, b0, b1, args, num_sms, stream);
+    case 256: return launch_impl<256, false, 4>(a0, a1, b0, b1, o0, o1, args, num_sms, stream);
+    case 128: return launch_impl<128, false, 6>(a0, a1, b0, b1, o0, o1, args, num_sms, stream);
+    case 64: return launch_impl<64, false, 8>(a0, a1, b0, b1, o0, o1, args, num_sms, stream);
     default: return -2;
   }
 }

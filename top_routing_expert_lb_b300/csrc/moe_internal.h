@@ -76,15 +76,24 @@ struct GroupedGemmArgs {
 // the B tensor maps then use 128-row boxes); else 128 x bn tiles per CTA.
 // b0h / b1h (paired SwiGLU only): the same B tensors with 64-row boxes, for
 // the half-height tiles that end a group with at most 128 rows.
+// o0 / o1: the routed / shared outputs (out_routed, out_shared) as tensor maps
+// from make_tmap_out_bf16; the epilogue writes every 32-row block of a tile
+// whose rows are all valid through them.
 int launch_grouped_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b0,
-                        const CUtensorMap& b1, const GroupedGemmArgs& args, bool swiglu, int bn,
-                        bool paired, int num_sms, cudaStream_t stream,
-                        const CUtensorMap* b0h = nullptr, const CUtensorMap* b1h = nullptr);
+                        const CUtensorMap& b1, const CUtensorMap& o0, const CUtensorMap& o1,
+                        const GroupedGemmArgs& args, bool swiglu, int bn, bool paired,
+                        int num_sms, cudaStream_t stream, const CUtensorMap* b0h = nullptr,
+                        const CUtensorMap* b1h = nullptr);
 
 // Encodes a 2-D bf16 tensor map over a row-major [rows][cols] tensor with a
 // 64-column x box_rows box and 128-byte swizzle.  Returns false on failure.
 bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                     uint32_t box_rows);
+
+// The GEMM outputs' tensor maps: bf16 [rows][cols] row-major, 32 x 32 boxes
+// with 64-byte swizzle (the epilogue's staging layout).  cols must be a
+// multiple of 8.  Returns false on failure.
+bool make_tmap_out_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols);
 
 // Router: logits tile GEMM + softmax / bias / Top-k epilogue on a persistent
 // grid, and the reduction of the side outputs by the CTA that completes the
