@@ -57,25 +57,26 @@ struct GemmSmemTail {
   int rows[kMaxGroups];
 };
 
-// Epilogue output staging.  Each of the four epilogue warps owns two 2 KB
-// buffers, each holding one block of 32 rows x 32 bf16 columns in the
-// 64-byte-swizzled layout of the output tensor maps, and writes a block with
-// one TMA tile store: the block reaches L2 as whole 64-byte row segments,
-// where direct stores send 32 scattered 16-byte pieces per instruction.  On the
-// dense 8192 x 4096 x 28672 gate/up shape the direct stores alone cost 8 % of
-// the launch.
+// Epilogue output staging.  Each of the four epilogue warps owns kBufs 2 KB
+// buffers (two with one CTA per SM, one with two CTAs per SM), each holding one
+// block of 32 rows x 32 bf16 columns in the 64-byte-swizzled layout of the
+// output tensor maps, and writes a block with one TMA tile store: the block
+// reaches L2 as whole 64-byte row segments, where direct stores send 32
+// scattered 16-byte pieces per instruction.  On the dense 8192 x 4096 x 28672
+// gate/up shape the direct stores alone cost 8 % of the launch.
 constexpr int kOutBlockBytes = 32 * 32 * 2;
-constexpr int kOutStageBytes = 4 * 2 * kOutBlockBytes;
+__host__ __device__ constexpr int out_stage_bytes(int bufs) { return 4 * bufs * kOutBlockBytes; }
+constexpr int kOutStageBytes = out_stage_bytes(2);
 
-template <int BN, int kStages, bool kTmaOut = true>
+template <int BN, int kStages, int kOutBufs = 2>
 constexpr size_t gemm_smem_bytes() {
   return 1024 + static_cast<size_t>(kStages) * (kBM * kBK * 2 + BN * kBK * 2) +
-         (kTmaOut ? kOutStageBytes : 0) + sizeof(GemmSmemTail);
+         out_stage_bytes(kOutBufs) + sizeof(GemmSmemTail);
 }
 
 struct OutStage {
   uint32_t buf0;  // shared address of this warp's first buffer (1024-byte aligned)
-  uint32_t n;     // blocks issued so far; block n uses buffer n & 1
+  uint32_t n;     // blocks issued so far; block n uses buffer n % kBufs
 };
 
 // Writes one 32 x 32 output block whose top-left element is (row, col) of the
@@ -83,11 +84,14 @@ struct OutStage {
 // Row l's 16-byte piece i goes to piece i ^ ((l >> 1) & 3) of the row's 64
 // bytes in the buffer (the 64-byte swizzle), so each quarter-warp's writes
 // cover all 32 banks.
+template <int kBufs>
 __device__ __forceinline__ void store_block_tma(OutStage& o, const uint32_t (&packed)[16],
                                                 const CUtensorMap* map, int col, int64_t row,
                                                 int lane) {
-  const uint32_t buf = o.buf0 + (o.n & 1u) * static_cast<uint32_t>(kOutBlockBytes);
-  if (lane == 0) bulk_wait_read<1>();  // the store that used this buffer has read it
+  static_assert(kBufs == 1 || kBufs == 2, "one or two buffers per warp");
+  const uint32_t buf = o.buf0 + (o.n & static_cast<uint32_t>(kBufs - 1)) *
+                                    static_cast<uint32_t>(kOutBlockBytes);
+  if (lane == 0) bulk_wait_read<kBufs - 1>();  // the store that used this buffer has read it
   __syncwarp();
   const uint32_t r = buf + static_cast<uint32_t>(lane) * 64u;
   const uint32_t sw = (static_cast<uint32_t>(lane) >> 1) & 3u;
@@ -204,9 +208,9 @@ __global__ void __launch_bounds__(kThreads, 3 - kAcc)
   constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, BN);
   static_assert(!(kRowScale && kSwiGLU), "row scaling applies to the plain projection");
   static_assert(kAcc == 1 || kAcc == 2, "one or two accumulators");
-  // two CTAs per SM have no shared memory to spare for output staging
-  constexpr bool kTmaOut = kAcc == 2;
-  constexpr int kOutBytes = kTmaOut ? kOutStageBytes : 0;
+  // two CTAs per SM fit one output buffer per epilogue warp each
+  constexpr int kOutBufs = kAcc == 2 ? 2 : 1;
+  constexpr int kOutBytes = out_stage_bytes(kOutBufs);
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
@@ -452,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 3 - kAcc)
     const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
     const int r_in_tile = quarter * 32 + lane;
     OutStage ostage{smem_u32(smem + kStages * kStageBytes) +
-                        static_cast<uint32_t>(quarter * 2 * kOutBlockBytes),
+                        static_cast<uint32_t>(quarter * kOutBufs * kOutBlockBytes),
                     0u};
     int local = 0;
     for (int tile = item0; tile < total && !*abort_flag; tile += stride, ++local) {
@@ -510,7 +514,7 @@ __global__ void __launch_bounds__(kThreads, 3 - kAcc)
       } else if constexpr (kSwiGLU) {
         __nv_bfloat16* dst = out + row * ld + static_cast<int64_t>(ti.n) * 128;
         // a warp whose 32 rows are all stored writes through the tensor map
-        const bool via_tma = kTmaOut && __all_sync(0xffffffffu, valid);
+        const bool via_tma = __all_sync(0xffffffffu, valid);
         const CUtensorMap* om = ti.shared ? &tmO1 : &tmO0;
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
@@ -524,7 +528,7 @@ __global__ void __launch_bounds__(kThreads, 3 - kAcc)
             packed[i] = pack_bf16x2(silu_f32(g[2 * i]) * u[2 * i],
                                     silu_f32(g[2 * i + 1]) * u[2 * i + 1]);
           if (via_tma) {
-            store_block_tma(ostage, packed, om, ti.n * 128 + c * 32, row - lane, lane);
+            store_block_tma<kOutBufs>(ostage, packed, om, ti.n * 128 + c * 32, row - lane, lane);
           } else if (valid) {
             uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
 #pragma unroll
@@ -537,7 +541,7 @@ __global__ void __launch_bounds__(kThreads, 3 - kAcc)
         __nv_bfloat16* dst = out + row * ld + static_cast<int64_t>(ti.n) * BN;
         float sc = 1.0f;
         if constexpr (kRowScale) sc = (valid && !ti.shared) ? __ldg(p.row_scale + row) : 1.0f;
-        const bool via_tma = kTmaOut && __all_sync(0xffffffffu, valid);
+        const bool via_tma = __all_sync(0xffffffffu, valid);
         const CUtensorMap* om = ti.shared ? &tmO1 : &tmO0;
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
@@ -552,7 +556,7 @@ __global__ void __launch_bounds__(kThreads, 3 - kAcc)
 #pragma unroll
           for (int i = 0; i < 16; ++i) packed[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
           if (via_tma) {
-            store_block_tma(ostage, packed, om, ti.n * BN + c * 32, row - lane, lane);
+            store_block_tma<kOutBufs>(ostage, packed, om, ti.n * BN + c * 32, row - lane, lane);
           } else if (valid) {
             uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
 #pragma unroll
@@ -567,7 +571,7 @@ __global__ void __launch_bounds__(kThreads, 3 - kAcc)
       if (lane == 0) mbar_arrive(&st->tempty[a]);
     }
     // every output block written before the CTA (and its buffers) goes away
-    if (kTmaOut && lane == 0) bulk_wait_all();
+    if (lane == 0) bulk_wait_all();
   }
 
   tc_fence_before();
@@ -941,8 +945,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             packed[i] = pack_bf16x2(silu_f32(g[2 * i]) * u[2 * i],
                                     silu_f32(g[2 * i + 1]) * u[2 * i + 1]);
           if (via_tma) {
-            store_block_tma(ostage, packed, om, ti.n * 128 + col_half * 64 + c * 32, row - lane,
-                            lane);
+            store_block_tma<2>(ostage, packed, om, ti.n * 128 + col_half * 64 + c * 32,
+                               row - lane, lane);
           } else if (valid) {
             uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
 #pragma unroll
@@ -970,8 +974,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 16; ++i) packed[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
           if (via_tma) {
-            store_block_tma(ostage, packed, om, ti.n * BN + col_half * 128 + c * 32, row - lane,
-                            lane);
+            store_block_tma<2>(ostage, packed, om, ti.n * BN + col_half * 128 + c * 32,
+                               row - lane, lane);
           } else if (valid) {
             uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
 #pragma unroll
@@ -1042,8 +1046,10 @@ template <int BN, bool kSwiGLU, int kStages, bool kRowScale = false, int kAcc = 
 int launch_impl(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b0,
                 const CUtensorMap& b1, const CUtensorMap& o0, const CUtensorMap& o1,
                 const GroupedGemmArgs& args, int num_sms, cudaStream_t stream) {
-  constexpr size_t smem = gemm_smem_bytes<BN, kStages, kAcc == 2>();
+  constexpr size_t smem = gemm_smem_bytes<BN, kStages, kAcc == 2 ? 2 : 1>();
   static_assert(smem <= 227 * 1024, "shared memory budget");
+  // two CTAs per SM: both blocks and the 1 KB each reserves fit the SM's 228 KB
+  static_assert(kAcc == 2 || 2 * (smem + 1024) <= 228 * 1024, "two CTAs per SM");
   auto kern = grouped_gemm_kernel<BN, kSwiGLU, kStages, kRowScale, kAcc>;
   static bool attr_set = false;
   if (!attr_set) {
