@@ -56,12 +56,17 @@ def parse_args(argv=None):
                     help="skip the other workloads' lines (per_config)")
     ap.add_argument("--no-graph", action="store_true",
                     help="launch every timed step directly instead of replaying CUDA graphs")
-    ap.add_argument("--stage", choices=["layer", "router", "ffn", "ab"], default="layer",
+    ap.add_argument("--stage", choices=["layer", "router", "ffn", "ab", "dense"], default="layer",
                     help="router: time moe_route alone (no expert weights are drawn); "
                          "ffn: time moe_grouped_ffn on a slice of the workload's realised "
                          "expert loads (--experts of them); ab: two layers that differ only "
                          "in moe_tuning_t (--tune for A, --tune-b for B) called alternately "
-                         "--steps times each; for profiling, not the headline")
+                         "--steps times each; dense: the gate/up projection of one expert "
+                         "holding --rows rows, on single-CTA and on CTA-pair tiles, called "
+                         "alternately with torch's (cuBLAS) GEMM of the same shape; for "
+                         "profiling, not the headline")
+    ap.add_argument("--rows", type=int, default=8192,
+                    help="--stage dense: rows of the one expert")
     ap.add_argument("--experts", type=int, default=0,
                     help="--stage ffn: experts in the slice (0: all)")
     ap.add_argument("--tune", action="append", default=[],
@@ -1068,6 +1073,77 @@ def run_ab_stage(args, w):
     return 0
 
 
+def run_dense_stage(args, w):
+    """The gate/up projection of one expert holding all --rows rows (a dense
+    rows x d x 2M GEMM with the SwiGLU epilogue) through moe_grouped_ffn on
+    single-CTA and on CTA-pair tiles, called alternately with torch.matmul of
+    the same operands (cuBLAS, no epilogue), the L2 flushed before every call.
+    Prints the median gate/up kernel time of each (events around the kernel)."""
+    import statistics
+
+    import torch
+
+    import synth
+    import top_routing_expert_lb_b300 as moe
+    from top_routing_expert_lb_b300 import build as mbuild
+
+    mbuild.ensure_built()
+    dev = torch.device("cuda", 0)
+    rows, d, M = args.rows, w.d, w.M
+    x = synth.normal_bf16(5, synth.TID_X, (rows, d), 1.0, dev)
+    w13 = moe.moe_pack_w13(synth.normal_bf16(5, synth.TID_W1, (1, M, d), w.w_std, dev),
+                           synth.normal_bf16(5, synth.TID_W3, (1, M, d), w.w_std, dev))
+    w2 = synth.normal_bf16(5, synth.TID_W2, (1, d, M), w.w_std, dev)
+    w13_t = w13.view(2 * M, d).t()
+    offsets = torch.tensor([0, rows], dtype=torch.int32, device=dev)
+    # the down projection follows the gate/up tiles where d allows 256-wide tiles
+    pair = dict(gemm1_tile=256, **({"gemm2_tile": 256} if d % 256 == 0 else {}))
+    tiles = {"single_cta": dict(gemm1_tile=128), "cta_pair": pair}
+    runs = {}
+    for name, tu in tiles.items():
+        s = moe.Shape.of(rows, d, M, 1, 1, 0, **tu)
+        xp = torch.zeros((moe.moe_max_rows(s), d), dtype=torch.bfloat16, device=dev)
+        xp[:rows] = x
+        y = torch.empty((moe.moe_max_rows(s), d), dtype=torch.bfloat16, device=dev)
+        ws = moe.alloc_workspace(s, dev)
+        runs[name] = (lambda s=s, xp=xp, y=y, ws=ws:
+                      moe.moe_grouped_ffn(s, xp, offsets, w13, w2, y, None, None, None, None, ws))
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    for _ in range(max(args.warmup, 1)):
+        for f in runs.values():
+            f()
+        x @ w13_t
+    torch.cuda.synchronize(dev)
+    times = {k: [] for k in list(runs) + ["cublas"]}
+    moe.moe_profile_collect()
+    moe.moe_profile_enable(True)
+    order = list(runs) + ["cublas"]
+    for i in range(args.steps):
+        for name in (order if i % 2 == 0 else order[::-1]):
+            flush.zero_()
+            torch.cuda.synchronize(dev)
+            if name == "cublas":
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                x @ w13_t
+                b.record()
+                torch.cuda.synchronize(dev)
+                times[name].append(a.elapsed_time(b))
+            else:
+                runs[name]()
+                torch.cuda.synchronize(dev)
+                times[name] += [ms for k, ms in moe.moe_profile_collect() if k == "gemm_swiglu"]
+    moe.moe_profile_enable(False)
+    flops = 2.0 * rows * d * 2 * M
+    med = {k: statistics.median(v) for k, v in times.items()}
+    print(json.dumps({
+        "stage": "dense", "shape": {"rows": rows, "d": d, "two_M": 2 * M}, "calls_each": args.steps,
+        "gate_up_ms": med, "tflops": {k: flops / v / 1e9 for k, v in med.items()},
+        "vs_cublas": {k: med[k] / med["cublas"] for k in runs},
+    }), flush=True)
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     import synth
@@ -1088,6 +1164,8 @@ def main(argv=None):
         return run_ffn_stage(args, w)
     if args.stage == "ab":
         return run_ab_stage(args, w)
+    if args.stage == "dense":
+        return run_dense_stage(args, w)
     return run_ours(args, w)
 
 

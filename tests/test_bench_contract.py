@@ -65,3 +65,10 @@ def test_ab_stage_arguments():
         moe.Shape.of(64, 64, 128, 8, 2, no_such_field=1)
     with pytest.raises(TypeError):
         s.tuned(gemm_tile=128)
+
+
+def test_dense_stage_arguments():
+    """`--stage dense` takes the expert's row count; it defaults to 8192."""
+    assert bench.parse_args(["--stage", "dense"]).rows == 8192
+    args = bench.parse_args(["--stage", "dense", "--rows", "1024", "--workload", "mixtral"])
+    assert args.stage == "dense" and args.rows == 1024

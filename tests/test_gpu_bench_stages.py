@@ -44,3 +44,14 @@ def test_ab_stage_same_bits_for_a_pure_scheduling_change(capsys):
     assert set(j["kernel_us"][0]) >= {"router", "scatter", "gemm_swiglu", "gemm_down", "combine"}
     assert j["same_y"] is True
     torch.cuda.synchronize()
+
+
+def test_dense_stage(capsys):
+    """The dense gate/up comparison runs both tile shapes and the library GEMM
+    of torch and reports a time for each."""
+    j = _run(capsys, ["--stage", "dense", "--workload", "tiny", "--rows", "256", "--steps", "3",
+                      "--warmup", "1", "--no-clocks"])
+    assert j["stage"] == "dense" and j["shape"] == {"rows": 256, "d": 64, "two_M": 256}
+    assert set(j["gate_up_ms"]) == {"single_cta", "cta_pair", "cublas"}
+    assert all(t > 0.0 for t in j["gate_up_ms"].values())
+    torch.cuda.synchronize()
