@@ -144,6 +144,12 @@ extern "C" {
  *                               one TMEM accumulator (the default only for a
  *                               down projection with M <= 2048 over experts
  *                               averaging fewer than 512 rows)
+ *     MOE_TUNE_NO_PDL           launch the router, scatter, expert GEMMs and
+ *                               combine without programmatic dependent launch
+ *                               (by default each of them may start while the
+ *                               kernel before it in the stream finishes, and
+ *                               waits for that kernel before reading its
+ *                               outputs; results are the same either way)
  *   wait_timeout_ns limit of this call's bounded device waits; 0: the
  *                   process-wide limit (moe_set_wait_timeout_ns)             */
 #define MOE_TUNE_NO_HALF_TILES 1u
@@ -152,6 +158,7 @@ extern "C" {
 #define MOE_TUNE_GATE_IN_EPILOGUE 8u
 #define MOE_TUNE_SWAP_ALL_TAILS 16u
 #define MOE_TUNE_TWO_CTAS_PER_SM 32u
+#define MOE_TUNE_NO_PDL 64u
 typedef struct moe_tuning {
     int32_t gemm1_tile, gemm2_tile, tile_order, tail_max_n, n_block, block_min_rows;
     uint32_t options;

@@ -66,7 +66,7 @@ def test_shape_struct_layout_matches_the_header():
     (dict(tail_max_n=129), B.MOE_ERR_INVALID_ARG),
     (dict(n_block=-1), B.MOE_ERR_INVALID_ARG),
     (dict(block_min_rows=-5), B.MOE_ERR_INVALID_ARG),
-    (dict(options=64), B.MOE_ERR_INVALID_ARG),
+    (dict(options=128), B.MOE_ERR_INVALID_ARG),
     (dict(reserved=1), B.MOE_ERR_INVALID_ARG),
     (dict(options=B.MOE_TUNE_FUSED_GATHER, gemm1_tile=256), B.MOE_ERR_INVALID_ARG),
     (dict(gemm2_tile=256), B.MOE_ERR_UNSUPPORTED),   # d = 64 is not a multiple of 256
@@ -79,7 +79,7 @@ def test_tuning_fields_are_checked(lib, tune, code):
 
 @pytest.mark.parametrize("tune", [dict(), dict(gemm1_tile=128, gemm2_tile=128, tile_order=1,
                                                tail_max_n=-1, n_block=1, block_min_rows=1,
-                                               options=63, wait_timeout_ns=10**9)])
+                                               options=127, wait_timeout_ns=10**9)])
 def test_valid_tuning_leaves_the_workspace_size_unchanged(lib, tune):
     base = B.Shape.of(4096, 256, 512, 8, 2, 1)
     assert B.moe_workspace_size(base.tuned(**tune)) == B.moe_workspace_size(base)

@@ -7,7 +7,7 @@ import torch
 
 import synth
 import top_routing_expert_lb_b300 as moe
-from parity import check_layer, run_layer, shape_of, np_of
+from parity import check_layer, guard_layer, run_layer, shape_of, np_of
 from top_routing_expert_lb_b300 import build as mbuild
 
 pytestmark = pytest.mark.gpu
@@ -270,3 +270,23 @@ def test_cuda_graph_capture_and_replay():
     assert moe.moe_check_status(layer.ws) == 0
     assert torch.equal(layer.y.view(torch.int16), direct.view(torch.int16))
     check_layer(inp, layer=None)
+
+
+@pytest.mark.parametrize("name", ["ragged_shared", "capacity_k4", "wide_E160"])
+def test_programmatic_dependent_launch_gives_the_same_bits(name):
+    """Each kernel of the layer may start while the one before it finishes
+    (the default) or only after it (MOE_TUNE_NO_PDL): the same bits either way,
+    also when calls follow each other on the stream with no host sync between."""
+    inp = synth.make_inputs(CASES[name], "cuda")
+    layer = guard_layer(moe.MoELayer(shape_of(inp.w), inp.wr, inp.w1, inp.w3, inp.w2, inp.ws1,
+                                     inp.ws3, inp.ws2, inp.offset, inp.sel_bias,
+                                     device=inp.x.device))
+    g, _ = check_layer(inp, layer=layer)
+    serial = run_layer(inp, tuning=dict(options=moe.MOE_TUNE_NO_PDL))
+    assert torch.equal(g.y.view(torch.int16), serial.y.view(torch.int16))
+    for _ in range(5):
+        layer.forward(inp.x)
+    torch.cuda.synchronize()
+    assert torch.equal(layer.y.view(torch.int16), serial.y.view(torch.int16))
+    assert np.array_equal(np_of(layer.ids), serial.ids)
+    assert moe.moe_check_status(layer.ws) == 0

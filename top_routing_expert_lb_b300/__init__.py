@@ -15,4 +15,5 @@ from ._binding import (  # noqa: F401
     moe_alf_bias_update, MOE_FLAG_PRIORITY_CAPACITY, MOE_FLAG_EXPERT_CHOICE, moe_ec_capacity,
     moe_ec_route, moe_ec_layer_forward, Tuning, MOE_TUNE_NO_HALF_TILES, MOE_TUNE_GEMM1_SPLIT,
     MOE_TUNE_FUSED_GATHER, MOE_TUNE_GATE_IN_EPILOGUE, MOE_TUNE_SWAP_ALL_TAILS, MOE_TUNE_TWO_CTAS_PER_SM,
+    MOE_TUNE_NO_PDL,
 )

@@ -48,6 +48,7 @@ MOE_TUNE_FUSED_GATHER = 4
 MOE_TUNE_GATE_IN_EPILOGUE = 8
 MOE_TUNE_SWAP_ALL_TAILS = 16
 MOE_TUNE_TWO_CTAS_PER_SM = 32
+MOE_TUNE_NO_PDL = 64
 
 
 def _check_tuning_names(tuning):

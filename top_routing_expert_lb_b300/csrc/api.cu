@@ -116,7 +116,8 @@ int check_shape(const moe_shape_t* s) {
   if (t.n_block < 0 || t.n_block > 64 || t.block_min_rows < 0) return MOE_ERR_INVALID_ARG;
   if ((t.options & ~(MOE_TUNE_NO_HALF_TILES | MOE_TUNE_GEMM1_SPLIT | MOE_TUNE_FUSED_GATHER |
                      MOE_TUNE_GATE_IN_EPILOGUE | MOE_TUNE_SWAP_ALL_TAILS |
-                     MOE_TUNE_TWO_CTAS_PER_SM)) != 0 || t.reserved != 0)
+                     MOE_TUNE_TWO_CTAS_PER_SM | MOE_TUNE_NO_PDL)) != 0 ||
+      t.reserved != 0)
     return MOE_ERR_INVALID_ARG;
   if ((t.options & MOE_TUNE_FUSED_GATHER) && t.gemm1_tile == 256) return MOE_ERR_INVALID_ARG;
   if (t.gemm2_tile == 256 && s->d % 256 != 0) return MOE_ERR_UNSUPPORTED;
@@ -128,6 +129,11 @@ uint64_t timeout_of(const moe_shape_t* s) {
   return s->tuning.wait_timeout_ns != 0 ? s->tuning.wait_timeout_ns
                                           : g_timeout_ns.load(std::memory_order_relaxed);
 }
+
+// Whether this call's router, scatter, GEMM and combine launches use
+// programmatic dependent launch (each may start while the kernel before it
+// finishes; each waits for it before reading what it wrote).
+bool use_pdl(const moe_shape_t* s) { return (s->tuning.options & MOE_TUNE_NO_PDL) == 0; }
 
 int64_t capacity_of(const moe_shape_t* s) {
   if (!(s->capacity_factor > 0.0f)) return -1;
@@ -319,6 +325,7 @@ int do_route(const moe_shape_t* s, const uint16_t* x, const uint16_t* wr, const 
   ra.entropy_mean = entropy_mean;
   ra.fixed_count = ex.fixed_count;
   ra.n_pairs = ex.n_pairs;
+  ra.pdl = use_pdl(s) ? 1 : 0;
   CUtensorMap mx, mw;
   std::memset(&mx, 0, sizeof(mx));
   std::memset(&mw, 0, sizeof(mw));
@@ -364,6 +371,7 @@ int do_scatter(const moe_shape_t* s, const uint16_t* x, const int32_t* ids, cons
   sa.row_gate = row_gate;
   sa.rmax = L.rmax;
   sa.status = at<int>(ws, L.status);
+  sa.pdl = use_pdl(s) ? 1 : 0;
   return cuda_rc(tracked(MOE_KERNEL_SCATTER, st, [&] { return launch_scatter(sa, st); }));
 }
 
@@ -583,6 +591,7 @@ int do_ffn(const moe_shape_t* s, const uint16_t* x_perm, const int32_t* offsets,
   const bool swap_all = (tune.options & MOE_TUNE_SWAP_ALL_TAILS) != 0;
   g1.swap_all_tails = (swap_all || d <= 1024) ? 1 : 0;
   g1.two_per_sm = (tune.options & MOE_TUNE_TWO_CTAS_PER_SM) ? 1 : 0;
+  g1.pdl = use_pdl(s) ? 1 : 0;
   int rc = 0;
   if (split1) {
     GroupedGemmArgs g1p = g1;
@@ -831,7 +840,7 @@ int moe_combine(const moe_shape_t* s, const uint16_t* y_perm, const int32_t* slo
     // no workspace: a failed index check (bounds-checked builds) skips the row
     // without recording it
     return launch_combine(s->T, s->d, s->k, y_perm, slot_row, gates, y_shared, y,
-                          layout_of(s).rmax, nullptr, st);
+                          layout_of(s).rmax, nullptr, st, use_pdl(s));
   }));
 }
 
@@ -892,7 +901,7 @@ int moe_layer_forward(const moe_shape_t* s, const uint16_t* x, const uint16_t* w
   const float* combine_gates = gate_epi ? nullptr : gates;
   return cuda_rc(tracked(MOE_KERNEL_COMBINE, st, [&] {
     return launch_combine(s->T, s->d, s->k, y_perm, slot_row, combine_gates, y_s, y, L.rmax,
-                          at<int>(ws, L.status), st);
+                          at<int>(ws, L.status), st, use_pdl(s));
   }));
 }
 

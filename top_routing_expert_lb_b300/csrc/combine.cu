@@ -50,6 +50,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
                    int* status) {
   // vectors per lane per iteration: about 8 loads of 16 bytes in flight
   constexpr int U = (K + 1) >= 8 ? 1 : 8 / (K + 1);
+  pdl_wait();  // y_perm (and y_shared) come from the down projection
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * kCombineWarps + warp;
   if (t >= T) return;
@@ -142,22 +143,26 @@ __global__ void timeout_probe_kernel(int* status, uint64_t timeout_ns) {
 
 int launch_combine(int32_t T, int32_t d, int32_t k, const uint16_t* y_perm,
                    const int32_t* slot_row, const float* gates, const uint16_t* y_shared,
-                   uint16_t* y, int64_t rmax, int* status, cudaStream_t stream) {
+                   uint16_t* y, int64_t rmax, int* status, cudaStream_t stream, bool pdl) {
   if (T == 0) return 0;
   const int grid = (T + kCombineWarps - 1) / kCombineWarps;
-  const dim3 b(kCombineWarps * 32);
+  void (*kern)(int32_t, int32_t, const uint16_t*, const int32_t*, const float*, const uint16_t*,
+               uint16_t*, int64_t, int*) = nullptr;
   switch (k) {
-    case 0: combine_kernel<0><<<grid, b, 0, stream>>>(T, d, y_perm, slot_row, gates, y_shared, y, rmax, status); break;
-    case 1: combine_kernel<1><<<grid, b, 0, stream>>>(T, d, y_perm, slot_row, gates, y_shared, y, rmax, status); break;
-    case 2: combine_kernel<2><<<grid, b, 0, stream>>>(T, d, y_perm, slot_row, gates, y_shared, y, rmax, status); break;
-    case 3: combine_kernel<3><<<grid, b, 0, stream>>>(T, d, y_perm, slot_row, gates, y_shared, y, rmax, status); break;
-    case 4: combine_kernel<4><<<grid, b, 0, stream>>>(T, d, y_perm, slot_row, gates, y_shared, y, rmax, status); break;
-    case 5: combine_kernel<5><<<grid, b, 0, stream>>>(T, d, y_perm, slot_row, gates, y_shared, y, rmax, status); break;
-    case 6: combine_kernel<6><<<grid, b, 0, stream>>>(T, d, y_perm, slot_row, gates, y_shared, y, rmax, status); break;
-    case 7: combine_kernel<7><<<grid, b, 0, stream>>>(T, d, y_perm, slot_row, gates, y_shared, y, rmax, status); break;
-    case 8: combine_kernel<8><<<grid, b, 0, stream>>>(T, d, y_perm, slot_row, gates, y_shared, y, rmax, status); break;
+    case 0: kern = combine_kernel<0>; break;
+    case 1: kern = combine_kernel<1>; break;
+    case 2: kern = combine_kernel<2>; break;
+    case 3: kern = combine_kernel<3>; break;
+    case 4: kern = combine_kernel<4>; break;
+    case 5: kern = combine_kernel<5>; break;
+    case 6: kern = combine_kernel<6>; break;
+    case 7: kern = combine_kernel<7>; break;
+    case 8: kern = combine_kernel<8>; break;
     default: return -2;
   }
+  if (launch_kernel(kern, dim3(grid), dim3(kCombineWarps * 32), 0, stream, pdl, 1u, T, d, y_perm,
+                    slot_row, gates, y_shared, y, rmax, status) != cudaSuccess)
+    return -3;
   return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }
 

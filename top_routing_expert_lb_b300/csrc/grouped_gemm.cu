@@ -236,6 +236,18 @@ __global__ void __launch_bounds__(kThreads, 3 - kAcc)
     }
     mbar_init(&st->fin, 1);
     st->abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA0);
+    tma_prefetch_desc(&tmA1);
+    tma_prefetch_desc(&tmB0);
+    tma_prefetch_desc(&tmB1);
+  }
+  if (warp == 1) tmem_alloc(&st->tmem_base, kTmemCols);
+  // the row offsets and the A rows come from earlier kernels in the stream
+  pdl_wait();
+  if (threadIdx.x == 0) {
     int acc = 0;
     st->prefix[0] = 0;
     for (int g = 0; g < G; ++g) {
@@ -266,15 +278,7 @@ __global__ void __launch_bounds__(kThreads, 3 - kAcc)
       acc += mt * (ncols / BN);
       st->prefix[g + 1] = acc;
     }
-    fence_barrier_init();
   }
-  if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&tmA0);
-    tma_prefetch_desc(&tmA1);
-    tma_prefetch_desc(&tmB0);
-    tma_prefetch_desc(&tmB1);
-  }
-  if (warp == 1) tmem_alloc(&st->tmem_base, kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -576,6 +580,7 @@ __global__ void __launch_bounds__(kThreads, 3 - kAcc)
 
   tc_fence_before();
   __syncthreads();
+  pdl_trigger();  // this CTA's tiles are done: the next kernel's CTAs may come up
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
 }
@@ -693,6 +698,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&st->q_empty[q], kTileQConsumers);
     }
     st->abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA0);
+    tma_prefetch_desc(&tmA1);
+    tma_prefetch_desc(&tmB0);
+    tma_prefetch_desc(&tmB1);
+  }
+  if (warp == 1) tmem_alloc_pair(&st->tmem_base, kTmemCols);
+  // the row offsets and the A rows come from earlier kernels in the stream
+  pdl_wait();
+  if (threadIdx.x == 0) {
     int acc = 0;
     st->prefix[0] = 0;
     for (int g = 0; g < G; ++g) {
@@ -722,15 +739,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       acc += ((rows + kPairBM - 1) / kPairBM) * (ncols / BN);
       st->prefix[g + 1] = acc;
     }
-    fence_barrier_init();
   }
-  if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&tmA0);
-    tma_prefetch_desc(&tmA1);
-    tma_prefetch_desc(&tmB0);
-    tma_prefetch_desc(&tmB1);
-  }
-  if (warp == 1) tmem_alloc_pair(&st->tmem_base, kTmemCols);
   tc_fence_before();
   __syncthreads();
   cluster_arrive_wait();  // both CTAs' barriers initialised before any remote signal
@@ -997,6 +1006,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   cluster_arrive_wait();
+  pdl_trigger();  // this pair's tiles are done: the next kernel's CTAs may come up
   tc_fence_after();
   if (warp == 1) tmem_dealloc_pair(tmem_base, kTmemCols);
   // The last CTA out puts the tile counter back to zero for the next launch
@@ -1025,19 +1035,8 @@ int launch_pair_impl(const CUtensorMap& a0, const CUtensorMap& a1, const CUtenso
       return -3;
     attr_set = true;
   }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(num_sms & ~1));
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attrs[1];
-  attrs[0].id = cudaLaunchAttributeClusterDimension;
-  attrs[0].val.clusterDim.x = 2;
-  attrs[0].val.clusterDim.y = 1;
-  attrs[0].val.clusterDim.z = 1;
-  cfg.attrs = attrs;
-  cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, kern, a0, a1, b0, b1, b0h, b1h, o0, o1, args) != cudaSuccess)
+  if (launch_kernel(kern, dim3(static_cast<unsigned>(num_sms & ~1)), dim3(kThreads), smem, stream,
+                    args.pdl != 0, 2u, a0, a1, b0, b1, b0h, b1h, o0, o1, args) != cudaSuccess)
     return -3;
   return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }
@@ -1058,7 +1057,9 @@ int launch_impl(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap&
       return -3;
     attr_set = true;
   }
-  kern<<<num_sms * (3 - kAcc), kThreads, smem, stream>>>(a0, a1, b0, b1, o0, o1, args);
+  if (launch_kernel(kern, dim3(static_cast<unsigned>(num_sms * (3 - kAcc))), dim3(kThreads), smem,
+                    stream, args.pdl != 0, 1u, a0, a1, b0, b1, o0, o1, args) != cudaSuccess)
+    return -3;
   return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }
 

@@ -16,6 +16,40 @@ constexpr uint32_t kRouteNoRenorm = 2u;
 constexpr uint32_t kRoutePriority = 4u;      // capacity keeps the highest scores
 constexpr uint32_t kRouteExpertChoice = 8u;  // experts pick tokens
 
+// Launches `kern` on `stream`.  With pdl, the launch allows programmatic
+// dependent launch: the kernel's CTAs may start while the previous kernel in
+// the stream is still running (after every CTA of that kernel has started),
+// so launch latency and the prologue (barrier set-up, TMEM allocation,
+// descriptor prefetch) overlap its tail; the kernel waits (pdl_wait) before
+// it touches memory that earlier work wrote.  cluster_x > 1 launches clusters
+// of that many CTAs along x.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t stream, bool pdl, unsigned cluster_x, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attrs[2];
+  unsigned n = 0;
+  if (pdl) {
+    attrs[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (cluster_x > 1) {
+    attrs[n].id = cudaLaunchAttributeClusterDimension;
+    attrs[n].val.clusterDim.x = cluster_x;
+    attrs[n].val.clusterDim.y = 1;
+    attrs[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = attrs;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
 // Ragged grouped GEMM  out[g] = A[g] * B[g]^T  over E routed groups (rows from
 // device offsets) and an optional shared group (fixed row count).
 struct GroupedGemmArgs {
@@ -67,6 +101,7 @@ struct GroupedGemmArgs {
   int64_t out_rows_routed = INT64_MAX;
   int64_t out_rows_shared = INT64_MAX;
   int64_t gather_limit = INT64_MAX;
+  int32_t pdl = 0;  // launch with programmatic dependent launch (see launch_kernel)
 };
 
 // A0/A1: activations [rows][K] (routed / shared), B0/B1: weights [rows][K].
@@ -142,6 +177,7 @@ struct RouterArgs {
   float* entropy_mean = nullptr;        // [1] or null
   int32_t fixed_count = -1;             // >= 0: every expert's count (expert choice)
   double n_pairs = -1.0;                // denominator of f; < 0: k T
+  int32_t pdl = 0;                      // programmatic dependent launch (see launch_kernel)
 };
 int launch_router(const CUtensorMap& x_map, const CUtensorMap& wr_map, RouterArgs args,
                   int num_sms, cudaStream_t stream);
@@ -212,6 +248,7 @@ struct ScatterArgs {
   const int32_t* all_offsets = nullptr;  // [E+1]
   int64_t rmax = 0;                    // rows of x_perm / row_token / row_gate (staging: T k)
   int* status = nullptr;               // bounds-checked builds: where a failed check is recorded
+  int32_t pdl = 0;                     // programmatic dependent launch (see launch_kernel)
 };
 int launch_scatter(const ScatterArgs& args, cudaStream_t stream);
 
@@ -258,7 +295,8 @@ int launch_ec_combine(int32_t T, int32_t d, int32_t E, const int32_t* sel_t,
 
 int launch_combine(int32_t T, int32_t d, int32_t k, const uint16_t* y_perm,
                    const int32_t* slot_row, const float* gates, const uint16_t* y_shared,
-                   uint16_t* y, int64_t rmax, int* status, cudaStream_t stream);
+                   uint16_t* y, int64_t rmax, int* status, cudaStream_t stream,
+                   bool pdl = false);
 
 int launch_pack_w13(int32_t G, int32_t Mw, int32_t d, const uint16_t* w1, const uint16_t* w3,
                     uint16_t* w13, cudaStream_t stream);

@@ -29,6 +29,7 @@
 
 #include "bounds.cuh"
 #include "moe_internal.h"
+#include "sm100_primitives.cuh"
 
 namespace moe {
 
@@ -199,6 +200,7 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_kernel(const ScatterA
   __shared__ int wcnt[kScatterWarps][256];      // pairs of e per warp, this round
   __shared__ int base[256];                     // tile_base
   __shared__ int rows[kTileTokens * kMaxTopK];  // destination row per pair (-1 dropped)
+  pdl_wait();  // ids, offsets and bases come from the router
   const int E = a.E, k = a.k;
   const int tile = blockIdx.x;
   const int t0 = tile * kTileTokens;
@@ -336,7 +338,9 @@ int launch_scatter(const ScatterArgs& args, cudaStream_t stream) {
   int G = (4 * args.num_sms + ntiles - 1) / ntiles;
   G = G < 1 ? 1 : (G > 16 ? 16 : G);
   if (args.stage_q || args.x_perm == nullptr) G = 1;  // indices only, no row copies
-  scatter_kernel<<<dim3(ntiles, G), kScatterThreads, 0, stream>>>(args);
+  if (launch_kernel(scatter_kernel, dim3(ntiles, G), dim3(kScatterThreads), 0, stream,
+                    args.pdl != 0, 1u, args) != cudaSuccess)
+    return -3;
   return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }
 

@@ -390,6 +390,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     st->abort_flag = 0;
     fence_barrier_init();
   }
+  // x, the offsets and the bias may come from the previous kernel in the stream
+  pdl_wait();
   for (int e = threadIdx.x; e < 256; e += blockDim.x) {
     st->hist[e] = 0;
     st->off[e] = (e < E && p.logit_offset) ? p.logit_offset[e] : 0.0f;
@@ -813,6 +815,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  pdl_trigger();  // this CTA's work is done: the next kernel's CTAs may come up
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem_base, tmem_cols);
 }
@@ -878,7 +881,9 @@ int launch_router(const CUtensorMap& x_map, const CUtensorMap& wr_map, RouterArg
       return -3;
     attr[args.k] = true;
   }
-  kern<<<grid, kThreads, smem, stream>>>(x_map, wr_map, args);
+  if (launch_kernel(kern, dim3(grid), dim3(kThreads), smem, stream, args.pdl != 0, 1u, x_map,
+                    wr_map, args) != cudaSuccess)
+    return -3;
   return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }
 

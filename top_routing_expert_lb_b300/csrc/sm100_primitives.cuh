@@ -23,6 +23,25 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 }
 
 // ---------------------------------------------------------------------------
+// Programmatic dependent launch
+// ---------------------------------------------------------------------------
+// Waits until the grids this one depends on programmatically (the previous
+// kernel in the stream, when this one was launched with programmatic stream
+// serialization) have completed and their memory operations are visible.
+// Returns at once for a grid launched without that attribute.  Every thread
+// that reads memory written by earlier work in the stream executes it first.
+__device__ __forceinline__ void pdl_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+// Lets the next kernel in the stream (if launched with programmatic stream
+// serialization) start its CTAs once every CTA of this grid has executed this
+// or exited; the next kernel still waits for this grid's completion in its
+// own pdl_wait before it reads what this grid writes.
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
 // mbarrier
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
