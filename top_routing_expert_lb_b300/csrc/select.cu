@@ -297,6 +297,12 @@ __device__ __forceinline__ void fma_bf16x8(float (&acc)[8], const uint4 v, float
   }
 }
 
+// kU vectors of the row per lane and kR rows at a time: kU * kR 16-byte loads
+// in flight before the first FMA.  Tokens with few rows (about E r / T) take
+// kU = 4, kR = 2, so that the vectors supply the parallelism; tokens with
+// many rows take kU = 1, kR = 8 (fewer registers, more resident warps).  Rows
+// are accumulated in ascending expert order either way.
+template <int kU, int kR>
 __global__ void __launch_bounds__(kEcCombineWarps * 32)
     ec_combine_kernel(int32_t T, int32_t d, int32_t E, const int32_t* __restrict__ sel_t,
                       const float* __restrict__ row_gate, const uint16_t* __restrict__ y_perm,
@@ -325,35 +331,52 @@ __global__ void __launch_bounds__(kEcCombineWarps * 32)
   const uint4* ys =
       y_shared ? reinterpret_cast<const uint4*>(y_shared + static_cast<int64_t>(t) * d) : nullptr;
   uint4* out = reinterpret_cast<uint4*>(y + static_cast<int64_t>(t) * d);
-  constexpr int kInFlight = 8;  // row loads issued before the first FMA
-  for (int v = lane; v < nvec; v += 32) {
-    float acc[8];
+  for (int v0 = lane; v0 < nvec; v0 += 32 * kU) {
+    float acc[kU][8];
+    uint4 sv[kU];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-    uint4 sv = make_uint4(0u, 0u, 0u, 0u);
-    if (ys) sv = __ldg(ys + v);
-    for (int j0 = 0; j0 < n; j0 += kInFlight) {
-      uint4 val[kInFlight];
+    for (int u = 0; u < kU; ++u) {
 #pragma unroll
-      for (int u = 0; u < kInFlight; ++u)
-        if (j0 + u < n)
-          val[u] = __ldg(reinterpret_cast<const uint4*>(
-                             y_perm + static_cast<int64_t>(lrow[warp][j0 + u]) * d) + v);
-#pragma unroll
-      for (int u = 0; u < kInFlight; ++u)  // experts in ascending order
-        if (j0 + u < n) fma_bf16x8(acc, val[u], lgate[warp][j0 + u]);
+      for (int i = 0; i < 8; ++i) acc[u][i] = 0.0f;
+      sv[u] = make_uint4(0u, 0u, 0u, 0u);
+      if (ys && v0 + 32 * u < nvec) sv[u] = __ldg(ys + v0 + 32 * u);
     }
-    if (ys) {
-      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&sv);
+    for (int j0 = 0; j0 < n; j0 += kR) {
+      uint4 val[kU][kR];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 f = __bfloat1622float2(h[i]);
-        acc[2 * i] += f.x;
-        acc[2 * i + 1] += f.y;
+      for (int rr = 0; rr < kR; ++rr) {
+        if (j0 + rr >= n) continue;
+        const uint4* src =
+            reinterpret_cast<const uint4*>(y_perm + static_cast<int64_t>(lrow[warp][j0 + rr]) * d);
+#pragma unroll
+        for (int u = 0; u < kU; ++u)
+          if (v0 + 32 * u < nvec) val[u][rr] = __ldg(src + v0 + 32 * u);
+      }
+#pragma unroll
+      for (int rr = 0; rr < kR; ++rr) {  // experts in ascending order
+        if (j0 + rr >= n) continue;
+        const float gate = lgate[warp][j0 + rr];
+#pragma unroll
+        for (int u = 0; u < kU; ++u)
+          if (v0 + 32 * u < nvec) fma_bf16x8(acc[u], val[u][rr], gate);
       }
     }
-    out[v] = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
-                        pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int v = v0 + 32 * u;
+      if (v >= nvec) continue;
+      if (ys) {
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&sv[u]);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 f = __bfloat1622float2(h[i]);
+          acc[u][2 * i] += f.x;
+          acc[u][2 * i + 1] += f.y;
+        }
+      }
+      out[v] = make_uint4(pack_bf16x2(acc[u][0], acc[u][1]), pack_bf16x2(acc[u][2], acc[u][3]),
+                          pack_bf16x2(acc[u][4], acc[u][5]), pack_bf16x2(acc[u][6], acc[u][7]));
+    }
   }
 }
 
@@ -389,8 +412,13 @@ int launch_ec_combine(int32_t T, int32_t d, int32_t E, const int32_t* sel_t,
   if (T == 0) return 0;
   if (E > 256) return -2;
   const int grid = (T + kEcCombineWarps - 1) / kEcCombineWarps;
-  ec_combine_kernel<<<grid, kEcCombineWarps * 32, 0, stream>>>(T, d, E, sel_t, row_gate, y_perm,
-                                                             y_shared, y, rmax, status);
+  // rmax = E r rows: tokens average rmax / T of them
+  if (rmax <= 3 * static_cast<int64_t>(T))
+    ec_combine_kernel<4, 2><<<grid, kEcCombineWarps * 32, 0, stream>>>(
+        T, d, E, sel_t, row_gate, y_perm, y_shared, y, rmax, status);
+  else
+    ec_combine_kernel<1, 8><<<grid, kEcCombineWarps * 32, 0, stream>>>(
+        T, d, E, sel_t, row_gate, y_perm, y_shared, y, rmax, status);
   return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }
 
