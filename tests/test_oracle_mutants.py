@@ -70,6 +70,13 @@ MUTANTS = {
     "expert_rows_w3_from_w1": ("x_rows + (size_t)r * d, w1 + e * M * d, w3 + e * M * d,",
                                "x_rows + (size_t)r * d, w1 + e * M * d, w1 + e * M * d,"),
     "combine_shared_missing": ("yt[o] += bf16_val(y_shared[(size_t)t * d + o]);", "yt[o] += 0.0;"),
+    "router_wr_transposed": ("acc += bf16_val(wr[(size_t)e * d + i]) * bf16_val(x[(size_t)t * d + i]);",
+                             "acc += bf16_val(wr[(size_t)i * E + e]) * bf16_val(x[(size_t)t * d + i]);"),
+    "dispatch_rows_reversed": ("int r = offsets[e] + rank[q];", "int r = offsets[e + 1] - 1 - rank[q];"),
+    "combine_gate_of_slot0": ("double g = gates[(size_t)t * k + s];", "double g = gates[(size_t)t * k];"),
+    "P_over_E": ("P[e] = (T > 0) ? acc / (double)T : 0.0;", "P[e] = (T > 0) ? acc / (double)E : 0.0;"),
+    "counts_after_capacity": ("            counts[e] += 1;\n            if (C < 0 || kept_counts[e] < C) {",
+                              "            counts[e] += (C < 0 || kept_counts[e] < C);\n            if (C < 0 || kept_counts[e] < C) {"),
 }
 
 
