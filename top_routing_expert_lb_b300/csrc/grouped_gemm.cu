@@ -15,7 +15,8 @@
 //   * 128 x BN x 64 tiles per stage, TMA with 128-byte swizzle, kStages-deep
 //     mbarrier ring (full: TMA bytes landed; empty: MMAs reading it retired).
 //   * Accumulators in TMEM, two buffers of BN fp32 columns so the epilogue of
-//     one tile overlaps the main loop of the next.
+//     one tile overlaps the main loop of the next.  The epilogue writes 32 x 32
+//     output blocks through shared memory with TMA tile stores.
 //   * Persistent grid (one CTA per SM).  Tiles are numbered group by group,
 //     n-tile major / m-tile minor inside a group, so CTAs running at the same
 //     time share a weight tile through L2 (groups with many rows go in blocks
@@ -25,6 +26,9 @@
 //     epilogue, and rows past a group's end are computed but never stored.
 //   * Every wait is bounded; on expiry the kernel records a timeout in the
 //     status word, drains its copies and MMAs, frees TMEM and returns.
+//   * Launched with programmatic dependent launch: the prologue (barriers,
+//     descriptor prefetch, TMEM) runs while the previous kernel finishes, and
+//     griddepcontrol.wait precedes the first read of the row offsets.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
